@@ -1,0 +1,135 @@
+"""CPU oracle of the fused input projection — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product library does not, and shares
+no code with it. ``fp_oracle.c`` holds the definition (fp64, one token at a
+time, following the pages' steps); this module builds it with gcc and calls it
+through ctypes.
+
+Parity pins: every function of the oracle is pinned by ``tests/test_oracle_pins.py``
+(library cross-checks, closed forms, invariants, brute force, planted mistakes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
+
+MUTATIONS = {
+    "drop_bias": 1, "rope_sign": 2, "w_transposed": 3, "tanh_const": 4, "scatter_order": 5,
+    "rope_interleaved": 6, "rope_freq": 7, "view_not_permute": 8, "act_on_q": 9,
+    "pos_global": 10, "rope_on_v": 11, "qk_swapped": 12, "gelu_scale": 13,
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile fp_oracle.c into liboracle.so (plain C, no CUDA)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        f = lib.oracle_forward
+        f.restype = ctypes.c_int
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        I64 = ctypes.c_int64
+        f.argtypes = [P, I, I, P, P, I, I, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+                      P, I64, P, P, P, P, I, I]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_dim: int,
+            n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
+            rope_base: float, dtype: str, pos: Optional[np.ndarray] = None,
+            groups: int = 0, rope_n_elem: int = 0, rows: Optional[Sequence[int]] = None,
+            threads: Optional[int] = None, mutate: int = 0,
+            x_strides: Optional[Sequence[int]] = None, x_base: Optional[np.ndarray] = None
+            ) -> Dict[str, np.ndarray]:
+    """Evaluate the projection in fp64.
+
+    ``x`` holds stored values (uint16 bf16 bits or float32) with logical shape
+    ``x.shape``; by default it is addressed through its own (element) strides.
+    To describe a strided view, pass the backing buffer as ``x_base`` and the
+    element strides as ``x_strides``.
+
+    Returns ``ff`` [M, F], ``q`` [B*heads, T, hd], ``k``/``v`` [B*kv, T, hd]
+    when ``rows`` is None, else per-row arrays ``ff`` [R, F], ``q`` [R, heads*hd],
+    ``k``/``v`` [R, kv*hd] for the requested token indices.
+    """
+    lib = _load()
+    is_bf16 = dtype == "bf16"
+    want = np.uint16 if is_bf16 else np.float32
+    sizes = np.array(x.shape, dtype=np.int64)
+    if x_base is None:
+        xb = np.ascontiguousarray(x)
+        if xb.dtype != want:
+            raise TypeError(f"x must be {want}")
+        strides = np.array([s // xb.itemsize for s in xb.strides], dtype=np.int64)
+    else:
+        xb = x_base
+        if xb.dtype != want:
+            raise TypeError(f"x_base must be {want}")
+        strides = np.array(x_strides, dtype=np.int64)
+    Wc = np.ascontiguousarray(W, dtype=want)
+    bc = None if b is None else np.ascontiguousarray(b, dtype=want)
+    posc = None if pos is None else np.ascontiguousarray(pos, dtype=np.int32)
+    nkv = groups if groups else heads
+    tok = [s for a, s in enumerate(x.shape) if a != channel_dim]
+    Bb = int(np.prod(tok[:n_batch_dims], dtype=np.int64))
+    T = int(np.prod(tok[n_batch_dims:], dtype=np.int64))
+    M = Bb * T
+    if rows is None:
+        out = {"ff": np.zeros((M, F)), "q": np.zeros((Bb * heads, T, head_dim)),
+               "k": np.zeros((Bb * nkv, T, head_dim)), "v": np.zeros((Bb * nkv, T, head_dim))}
+        rr = None
+        R = 0
+    else:
+        rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        R = len(rr)
+        out = {"ff": np.zeros((R, F)), "q": np.zeros((R, heads * head_dim)),
+               "k": np.zeros((R, nkv * head_dim)), "v": np.zeros((R, nkv * head_dim))}
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.oracle_forward(_ptr(xb), int(is_bf16), x.ndim, _ptr(sizes), _ptr(strides), channel_dim,
+                            n_batch_dims, _ptr(Wc), _ptr(bc), _ptr(posc), C, F, heads, head_dim,
+                            groups, rope_n_elem, act, float(rope_base), _ptr(rr), R,
+                            _ptr(out["ff"]), _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]),
+                            int(threads), int(mutate))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
+
+
+def forward_workload(w, inputs: Dict[str, np.ndarray], **kw) -> Dict[str, np.ndarray]:
+    """``forward`` with the shape parameters of an ``fpsynth.Workload``."""
+    return forward(inputs["x"], inputs["W"], inputs["b"], channel_dim=w.channel_dim,
+                   n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
+                   head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, dtype=w.dtype,
+                   pos=inputs.get("pos"), groups=w.n_query_groups, rope_n_elem=w.rope_n_elem,
+                   **kw)

@@ -1,0 +1,82 @@
+"""An independent float64 restatement of the projection with PyTorch CPU library ops.
+
+Used only to pin the oracle. Each step is a library routine or textbook
+identity rather than the oracle's own loops:
+
+* gather: ``torch.permute`` + ``reshape`` (the rearrange of "Make fused_ff_qkv
+  contiguous", Walrus PR #12);
+* fused linear: ``torch.addmm``;
+* activations: ``torch.nn.functional.gelu`` (erf / tanh) and ``silu``;
+* rotary embedding: multiplication of the complex number u[i] + i*u[i+half]
+  by exp(i*theta) in complex128 (the rotate-half form of "Improve performance
+  on RoPE", nvFuser issue #1597, written as a complex rotation);
+* split: ``transpose(1, 2)`` then flattening batch and heads, the conversion to
+  the [batch*heads, tokens, head_dim] layout of "Improve performance via
+  batched-matmul and fused multiplies" (memory-efficient-attention issue #7);
+  grouped-query heads follow the view/permute/split of the split_qkv listing.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+import torch.nn.functional as Fn
+
+
+def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, channel_dim: int,
+              n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
+              rope_base: float, pos: Optional[np.ndarray] = None, groups: int = 0,
+              rope_n_elem: int = 0) -> Dict[str, np.ndarray]:
+    x = torch.from_numpy(np.asarray(x64, dtype=np.float64))
+    nd = x.dim()
+    perm = [a for a in range(nd) if a != channel_dim] + [channel_dim]
+    tok = [x.shape[a] for a in range(nd) if a != channel_dim]
+    Bb = int(np.prod(tok[:n_batch_dims], dtype=np.int64))
+    T = int(np.prod(tok[n_batch_dims:], dtype=np.int64))
+    M = Bb * T
+    X = x.permute(*perm).reshape(M, C)
+    Wt = torch.from_numpy(np.asarray(W64, dtype=np.float64))
+    bt = torch.zeros(Wt.shape[1], dtype=torch.float64) if b64 is None else torch.from_numpy(
+        np.asarray(b64, dtype=np.float64))
+    Y = torch.addmm(bt, X, Wt)
+    ff = Y[:, :F]
+    if act == 1:
+        ff = Fn.gelu(ff, approximate="none")
+    elif act == 2:
+        ff = Fn.gelu(ff, approximate="tanh")
+    elif act == 3:
+        ff = Fn.silu(ff)
+    hd = head_dim
+    rest = Y[:, F:]
+    if groups:
+        qpk = heads // groups
+        qkv = rest.reshape(Bb, T, groups, qpk + 2, hd).permute(0, 2, 3, 1, 4)
+        q, k, v = qkv.split((qpk, 1, 1), dim=2)
+        q = q.reshape(Bb, heads, T, hd)
+        k = k.reshape(Bb, groups, T, hd)
+        v = v.reshape(Bb, groups, T, hd)
+    else:
+        q = rest[:, :C].reshape(Bb, T, heads, hd).transpose(1, 2)
+        k = rest[:, C:2 * C].reshape(Bb, T, heads, hd).transpose(1, 2)
+        v = rest[:, 2 * C:3 * C].reshape(Bb, T, heads, hd).transpose(1, 2)
+    if rope_base > 0 and heads > 0:
+        n = rope_n_elem or hd
+        half = n // 2
+        p = torch.arange(T, dtype=torch.float64) if pos is None else torch.from_numpy(
+            np.asarray(pos, dtype=np.float64))
+        inv = torch.tensor([rope_base ** (-2.0 * i / n) for i in range(half)], dtype=torch.float64)
+        rot = torch.polar(torch.ones(T, half, dtype=torch.float64), p[:, None] * inv[None, :])
+
+        def rope(u):
+            z = torch.complex(u[..., :half], u[..., half:n]) * rot
+            return torch.cat([z.real, z.imag, u[..., n:]], dim=-1)
+
+        q, k = rope(q), rope(k)
+    out = {
+        "ff": ff.contiguous().numpy(),
+        "q": q.flatten(end_dim=1).contiguous().numpy(),
+        "k": k.flatten(end_dim=1).contiguous().numpy(),
+        "v": v.flatten(end_dim=1).contiguous().numpy(),
+    }
+    return out
