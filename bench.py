@@ -1,0 +1,373 @@
+"""Benchmark of the fused input projection on GB300.
+
+One step = one fp_forward over one batch of synthetic input: the whole path
+(strided load, fused GEMM, bias, activation, rotary embedding, head-major
+split) on the Walrus-shaped channels-first workload by default.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank projects its own copy
+of the workload (weak scaling, no data-path collective); the step time is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import fpsynth  # noqa: E402
+
+METRIC = "fused-proj TFLOP/s & tokens/s on 1 GB300; % of min(TC peak, HBM) roofline"
+DEFAULT_WORKLOAD = "walrus_bf16"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["ff_input_projection_gb300/csrc/gemm_tc.cu",
+                  "ff_input_projection_gb300/csrc/epilogue.cuh",
+                  "ff_input_projection_gb300/csrc/gemm_simt.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fpsynth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def algorithmic(w: fpsynth.Workload):
+    esz = 2 if w.dtype == "bf16" else 4
+    n_out = w.M * w.N
+    bytes_ = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0) + n_out) * esz
+    return w.flops, bytes_
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"tc_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    mh = re.search(r"kernel_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_hash():
+        return None
+    return float(mt.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid: str):
+        self.uuid = device_uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags)
+                          if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_baseline(w: fpsynth.Workload, inp, seconds: float):
+    """The oracle, as it stands, on a bounded sample of token rows."""
+    import oracle
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    n = 8
+    t0 = time.perf_counter()
+    done_rows = 0
+    elapsed = 0.0
+    while True:
+        rows = np.sort(rng.choice(w.M, size=min(n, w.M), replace=False))
+        t = time.perf_counter()
+        oracle.forward_workload(w, inp, rows=rows, threads=cores)
+        dt = time.perf_counter() - t
+        done_rows += len(rows)
+        elapsed += dt
+        if elapsed >= seconds or time.perf_counter() - t0 > 3 * seconds:
+            break
+        rate = len(rows) / max(dt, 1e-6)
+        n = int(max(8, min(rate * (seconds - elapsed), 4 * n, w.M)))
+    flops = 2.0 * done_rows * w.C * w.N
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "tokens_per_s": done_rows / elapsed,
+            "sample": f"{done_rows} of {w.M} token rows of {w.name} (all {w.N} fused columns), "
+                      f"fp64, {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = fpsynth.WORKLOADS[args.workload]
+    inp = fpsynth.make_inputs(w)
+    import oracle
+    cores = os.cpu_count() or 1
+    # per step: a fixed sample of rows sized so the whole run takes a few minutes
+    per_step_rows = max(1, min(w.M, int(os.environ.get("FP_REF_ROWS", "64"))))
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(w.M, size=per_step_rows, replace=False))
+    for _ in range(args.warmup):
+        oracle.forward_workload(w, inp, rows=rows[:8], threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.forward_workload(w, inp, rows=rows, threads=cores)
+        times.append(time.perf_counter() - t)
+        if sum(times) > 150:
+            break
+    total = sum(times)
+    flops = 2.0 * per_step_rows * len(times) * w.C * w.N
+    value = flops / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "x": list(w.x_shape), "C": w.C, "F": w.F,
+                       "heads": w.heads, "head_dim": w.head_dim, "N": w.N, "tokens": w.M},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step_rows} token rows of {w.M} per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import ff_input_projection_gb300 as fpx
+    from ff_input_projection_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = fpsynth.WORKLOADS[args.workload]
+    inp = fpsynth.make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
+            if w.dtype == "bf16" else torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(dev)
+
+    flops, alg_bytes = algorithmic(w)
+    in_bytes = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0)) * (2 if w.dtype == "bf16" else 4)
+    n_sets = max(2, int(np.ceil(2 * L2_BYTES / in_bytes)))
+    xs = [to_dev(inp["x"]) for _ in range(n_sets)]
+    Ws = [to_dev(inp["W"]) for _ in range(n_sets)]
+    bs = [to_dev(inp["b"]) for _ in range(n_sets)]
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    proj.reserve(w.T)
+    stream = torch.cuda.Stream(device=dev)
+    outs = None
+
+    def step(i):
+        nonlocal outs
+        j = i % n_sets
+        outs = proj.forward(xs[j], Ws[j], bs[j], None, channel_dim=w.channel_dim,
+                            n_batch_dims=w.n_batch_dims, out=outs, stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    launches_per_step = proj.last_launch_count
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    fpx.check(proj.device_status(stream.cuda_stream))
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    total_flops = flops * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    tokens_per_s = w.M * world / (ms * 1e-3)
+
+    # ---- end to end through the public API with pinned host buffers
+    hx = torch.empty(xs[0].shape, dtype=tdt, pin_memory=True)
+    hx.copy_(xs[0].cpu())
+    host_outs = [None if o is None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+                 for o in outs]
+    dx = torch.empty_like(xs[0])
+    h2d = hx.numel() * hx.element_size()
+    d2h = sum(o.numel() * o.element_size() for o in host_outs if o is not None)
+    e2e_steps = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        o = proj.forward(dx, Ws[0], bs[0], None, channel_dim=w.channel_dim,
+                         n_batch_dims=w.n_batch_dims, out=outs, stream=stream.cuda_stream)
+        for h, d in zip(host_outs, o):
+            if h is not None:
+                h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    pk, pk_src = peaks()
+    tensor_time = flops / (pk["bf16_tflops"] * 1e12)
+    hbm_time = alg_bytes / (pk["hbm_gbs"] * 1e9)
+    if w.dtype == "bf16" and tensor_time >= hbm_time:
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg_bytes / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["peak_source"] = f"{pk_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})"
+    roof["kernel_hash"] = kernel_hash()
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "tokens_per_s": tokens_per_s,
+        "config": {"workload": w.name, "x": list(w.x_shape), "channel_dim": w.channel_dim,
+                   "C": w.C, "F": w.F, "heads": w.heads, "head_dim": w.head_dim, "N": w.N,
+                   "tokens": w.M, "act": fpsynth.ACT_NAMES[w.act], "rope_base": w.rope_base,
+                   "bias": w.bias, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs rotate over {n_sets} copies ({n_sets * in_bytes / 1e6:.0f} MB) "
+                         f"> L2 129 MB; each step also writes {w.M * w.N * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""Fused input projection on one GB300 — Python binding of ``libfp.so``.
+
+Argument marshalling only: every step of the projection runs in the library's
+CUDA kernels. The functions below carry the names of the C ABI declared in
+``include/fp.h``; ``FusedProjection`` wraps them for torch tensors (torch is
+used for device memory and streams only).
+
+If the library has not been built, ``load()`` raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+from . import _build
+
+FP_OK = 0
+FP_ERR_INVALID_ARG = 1
+FP_ERR_UNSUPPORTED_LAYOUT = 2
+FP_ERR_MISALIGNED = 3
+FP_ERR_CUDA = 4
+FP_ERR_OUT_OF_MEMORY = 5
+FP_ERR_TIMEOUT = 6
+FP_ERR_DEVICE_BOUNDS = 7
+
+FP_ACT_NONE, FP_ACT_GELU_ERF, FP_ACT_GELU_TANH, FP_ACT_SILU = 0, 1, 2, 3
+ACTS = {"none": 0, "gelu": 1, "gelu_erf": 1, "gelu_tanh": 2, "silu": 3}
+FP_BF16, FP_F32 = 0, 1
+FP_MAX_DIMS = 8
+
+FP_OPT_WAIT_LIMIT_NS = 1
+FP_OPT_INJECT_STALL = 2
+FP_OPT_GROUP_M = 3
+FP_OPT_MAX_CTAS = 4
+
+# the C ABI's entry points, as declared in include/fp.h
+EXPORTS = ("fp_create", "fp_forward", "fp_reserve", "fp_get_device_status",
+           "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
+           "fp_destroy")
+
+
+class fp_layout(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("sizes", ctypes.c_int64 * FP_MAX_DIMS), ("strides", ctypes.c_int64 * FP_MAX_DIMS),
+                ("channel_dim", ctypes.c_int32), ("n_batch_dims", ctypes.c_int32)]
+
+
+class FpError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"fp status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libfp.so; raises if it is missing (build it with ``_build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfp.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.fp_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, ctypes.c_float]
+    lib.fp_create.restype = I
+    lib.fp_forward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
+    lib.fp_forward.restype = I
+    lib.fp_reserve.argtypes = [P, I64]
+    lib.fp_reserve.restype = I
+    lib.fp_get_device_status.argtypes = [P, P]
+    lib.fp_get_device_status.restype = I
+    lib.fp_last_launch_count.argtypes = [P]
+    lib.fp_last_launch_count.restype = I
+    lib.fp_status_string.argtypes = [I]
+    lib.fp_status_string.restype = ctypes.c_char_p
+    lib.fp_last_error.argtypes = []
+    lib.fp_last_error.restype = ctypes.c_char_p
+    lib.fp_set_option.argtypes = [P, I, I64]
+    lib.fp_set_option.restype = I
+    lib.fp_destroy.argtypes = [P]
+    lib.fp_destroy.restype = None
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------- C-ABI mirrors
+
+def fp_status_string(status: int) -> str:
+    return load().fp_status_string(status).decode()
+
+
+def fp_last_error() -> str:
+    return load().fp_last_error().decode()
+
+
+def fp_create(C: int, ff_hidden: int, heads: int, head_dim: int, act: int,
+              rope_base: float) -> Tuple[int, Optional[int]]:
+    """Returns (status, plan handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().fp_create(ctypes.byref(h), C, ff_hidden, heads, head_dim, act, rope_base)
+    return st, (h.value if st == FP_OK else None)
+
+
+def fp_forward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int], pos: Optional[int],
+               out_ff: Optional[int], out_q: Optional[int], out_k: Optional[int],
+               out_v: Optional[int], stream: Optional[int]) -> int:
+    return load().fp_forward(plan, x, ctypes.byref(layout), W, b, pos, out_ff, out_q, out_k, out_v,
+                             stream)
+
+
+def fp_reserve(plan: int, max_tokens_per_batch: int) -> int:
+    return load().fp_reserve(plan, max_tokens_per_batch)
+
+
+def fp_get_device_status(plan: int, stream: Optional[int]) -> int:
+    return load().fp_get_device_status(plan, stream)
+
+
+def fp_last_launch_count(plan: int) -> int:
+    return load().fp_last_launch_count(plan)
+
+
+def fp_set_option(plan: int, opt: int, value: int) -> int:
+    return load().fp_set_option(plan, opt, value)
+
+
+def fp_destroy(plan: Optional[int]) -> None:
+    if plan:
+        load().fp_destroy(plan)
+
+
+def make_layout(sizes: Sequence[int], strides: Sequence[int], channel_dim: int, n_batch_dims: int,
+                dtype: int) -> fp_layout:
+    L = fp_layout()
+    L.dtype = dtype
+    L.ndim = len(sizes)
+    for i, (s, st) in enumerate(zip(sizes, strides)):
+        L.sizes[i] = int(s)
+        L.strides[i] = int(st)
+    L.channel_dim = channel_dim
+    L.n_batch_dims = n_batch_dims
+    return L
+
+
+def check(status: int) -> None:
+    if status != FP_OK:
+        raise FpError(status, f"{fp_status_string(status)}: {fp_last_error()}")
+
+
+# ----------------------------------------------------------------- torch wrapper
+
+class FusedProjection:
+    """A plan plus torch-tensor marshalling.
+
+    ``forward(x, W, b, pos)`` returns ``(ff, q, k, v)`` (None for empty
+    blocks), allocated on x's device with x's dtype; the work is enqueued on
+    torch's current stream of that device.
+    """
+
+    def __init__(self, C: int, ff_hidden: int, heads: int, head_dim: int, act="none",
+                 rope_base: float = 0.0):
+        a = ACTS[act] if isinstance(act, str) else int(act)
+        st, h = fp_create(C, ff_hidden, heads, head_dim, a, float(rope_base))
+        check(st)
+        self.plan = h
+        self.C, self.F, self.heads, self.head_dim = C, ff_hidden, heads, head_dim
+
+    def close(self):
+        if getattr(self, "plan", None):
+            fp_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, opt: int, value: int) -> None:
+        check(fp_set_option(self.plan, opt, value))
+
+    def reserve(self, max_tokens_per_batch: int) -> None:
+        check(fp_reserve(self.plan, max_tokens_per_batch))
+
+    def device_status(self, stream=None) -> int:
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        return fp_get_device_status(self.plan, s)
+
+    @property
+    def last_launch_count(self) -> int:
+        return fp_last_launch_count(self.plan)
+
+    def out_shapes(self, x_shape: Sequence[int], channel_dim: int, n_batch_dims: int):
+        tok = [s for a, s in enumerate(x_shape) if a != channel_dim]
+        Bb = 1
+        for s in tok[:n_batch_dims]:
+            Bb *= s
+        T = 1
+        for s in tok[n_batch_dims:]:
+            T *= s
+        return Bb, T
+
+    def forward(self, x, W, b=None, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
+                out=None, stream=None):
+        import torch
+        dt = {torch.bfloat16: FP_BF16, torch.float32: FP_F32}[x.dtype]
+        Bb, T = self.out_shapes(x.shape, channel_dim, n_batch_dims)
+        M = Bb * T
+        if out is None:
+            ff = torch.empty((M, self.F), device=x.device, dtype=x.dtype) if self.F else None
+            qkv = [torch.empty((Bb * self.heads, T, self.head_dim), device=x.device, dtype=x.dtype)
+                   for _ in range(3)] if self.heads else [None, None, None]
+            out = (ff, *qkv)
+        L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, dt)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        st = fp_forward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
+                        ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
+        check(st)
+        return out

@@ -1,0 +1,544 @@
+// C ABI of libfp: argument checks, layout analysis, tensor maps, launches.
+//
+// fp_forward never synchronises (the Walrus PR #12 "Make fused_ff_qkv
+// contiguous" profile counts five implicit device syncs per forward; this path
+// adds none). Checks run on the host before any CUDA call, so a rejected call
+// has launched nothing.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/fp.h"
+#include "fp_internal.h"
+
+struct fp_plan {
+  int C, F, heads, hd, groups, rope_n_elem;
+  int act;
+  float rope_base;
+  int device;
+  int* d_status;     // [2]: sticky device error, tag of an aborted launch
+  float2* d_table;   // rotary (cos, sin) table
+  int64_t table_cap; // entries
+  int64_t table_T;   // T of the default-position table held in d_table (-1: none)
+  cudaStream_t table_stream;  // stream that last wrote the table
+  cudaEvent_t table_ready;    // recorded after that write
+  int last_launches;
+  uint64_t wait_limit_ns;
+  int inject_stall;
+  int group_m;
+  int max_ctas;
+  uint32_t launch_seq;
+};
+
+namespace {
+
+thread_local char g_err[512];
+
+fp_status fail(fp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fp_status ok() {
+  g_err[0] = '\0';
+  return FP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(const Range& a, const Range& b) {
+  return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count(int dev) {
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Token axes after dropping unit axes and merging contiguous neighbours.
+struct TokAxes {
+  int64_t S_in = 1, s_stride = 1;
+  std::vector<int64_t> outer_size, outer_stride;  // innermost first
+  int64_t Bb = 1, T = 1, M = 1;
+};
+
+TokAxes analyse_tokens(const fp_layout& L) {
+  TokAxes ta;
+  int seen = 0;
+  for (int a = 0; a < L.ndim; ++a) {
+    if (a == L.channel_dim) continue;
+    if (seen < L.n_batch_dims) ta.Bb *= L.sizes[a];
+    else ta.T *= L.sizes[a];
+    ++seen;
+  }
+  ta.M = ta.Bb * ta.T;
+  // innermost-first list of (size, stride) groups
+  std::vector<std::pair<int64_t, int64_t>> g;
+  for (int a = L.ndim - 1; a >= 0; --a) {
+    if (a == L.channel_dim || L.sizes[a] == 1) continue;
+    if (!g.empty() && L.strides[a] == g.back().second * g.back().first)
+      g.back().first *= L.sizes[a];
+    else
+      g.push_back({L.sizes[a], L.strides[a]});
+  }
+  if (g.empty()) g.push_back({1, 1});
+  ta.S_in = g[0].first;
+  ta.s_stride = g[0].second;
+  for (size_t i = 1; i < g.size(); ++i) {
+    ta.outer_size.push_back(g[i].first);
+    ta.outer_stride.push_back(g[i].second);
+  }
+  return ta;
+}
+
+fp_status ensure_device_state(fp_plan* p, int64_t table_entries) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  if (p->d_status && p->device != dev)
+    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
+                p->device, dev);
+  if (!p->d_status) {
+    int* s = nullptr;
+    if (cudaMalloc(&s, 2 * sizeof(int)) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "status word allocation failed");
+    if (cudaMemset(s, 0, 2 * sizeof(int)) != cudaSuccess) {
+      cudaFree(s);
+      return fail(FP_ERR_CUDA, "status word initialisation failed");
+    }
+    p->d_status = s;
+    p->device = dev;
+  }
+  if (table_entries > p->table_cap) {
+    float2* t = nullptr;
+    if (cudaMalloc(&t, static_cast<size_t>(table_entries) * sizeof(float2)) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "rotary table allocation (%lld entries) failed",
+                  static_cast<long long>(table_entries));
+    if (p->d_table) {
+      // the old table may still be read by work queued on any stream
+      cudaDeviceSynchronize();
+      cudaFree(p->d_table);
+    }
+    p->d_table = t;
+    p->table_cap = table_entries;
+    p->table_T = -1;
+  }
+  return FP_OK;
+}
+
+int rope_half_of(const fp_plan* p) {
+  if (p->rope_base <= 0.0f || p->heads == 0) return 0;
+  return (p->rope_n_elem > 0 ? p->rope_n_elem : p->hd) / 2;
+}
+
+int n_total(const fp_plan* p) {
+  if (p->groups > 0) return p->F + (p->heads + 2 * p->groups) * p->hd;
+  return p->F + 3 * p->heads * p->hd;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp_status_string(fp_status s) {
+  switch (s) {
+    case FP_OK: return "ok";
+    case FP_ERR_INVALID_ARG: return "invalid argument";
+    case FP_ERR_UNSUPPORTED_LAYOUT: return "unsupported activation layout";
+    case FP_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case FP_ERR_CUDA: return "CUDA call failed";
+    case FP_ERR_OUT_OF_MEMORY: return "device allocation failed";
+    case FP_ERR_TIMEOUT: return "device-side wait ran out";
+    case FP_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
+  }
+  return "unknown status";
+}
+
+const char* fp_last_error(void) { return g_err; }
+
+fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_dim, fp_act act,
+                    float rope_base) {
+  if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  *plan = nullptr;
+  if (C <= 0) return fail(FP_ERR_INVALID_ARG, "C must be > 0 (got %d)", C);
+  if (ff_hidden < 0) return fail(FP_ERR_INVALID_ARG, "ff_hidden must be >= 0");
+  if (heads < 0) return fail(FP_ERR_INVALID_ARG, "heads must be >= 0");
+  if (heads > 0) {
+    if (head_dim <= 0 || head_dim % 2)
+      return fail(FP_ERR_INVALID_ARG, "head_dim must be even and > 0 (got %d)", head_dim);
+    if (static_cast<int64_t>(heads) * head_dim != C)
+      return fail(FP_ERR_INVALID_ARG, "heads * head_dim (%d * %d) must equal C (%d)", heads,
+                  head_dim, C);
+    if (ff_hidden % head_dim)
+      return fail(FP_ERR_INVALID_ARG, "ff_hidden (%d) must be a multiple of head_dim (%d)",
+                  ff_hidden, head_dim);
+  }
+  if (ff_hidden == 0 && heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
+  if (act < FP_ACT_NONE || act > FP_ACT_SILU) return fail(FP_ERR_INVALID_ARG, "unknown act");
+  if (rope_base > 0.0f && heads > 0) {
+    if (head_dim > 128)
+      return fail(FP_ERR_INVALID_ARG, "rotary embedding needs head_dim <= 128 (got %d)",
+                  head_dim);
+  }
+  fp_plan* p = new (std::nothrow) fp_plan();
+  if (!p) return fail(FP_ERR_OUT_OF_MEMORY, "host allocation failed");
+  p->C = C;
+  p->F = ff_hidden;
+  p->heads = heads;
+  p->hd = heads > 0 ? head_dim : 0;
+  p->groups = 0;
+  p->rope_n_elem = 0;
+  p->act = act;
+  p->rope_base = rope_base;
+  p->device = -1;
+  p->d_status = nullptr;
+  p->d_table = nullptr;
+  p->table_cap = 0;
+  p->table_T = -1;
+  p->table_stream = nullptr;
+  p->table_ready = nullptr;
+  p->last_launches = 0;
+  p->wait_limit_ns = 2000000000ull;
+  p->inject_stall = 0;
+  p->group_m = 8;
+  p->max_ctas = 0;
+  p->launch_seq = 0;
+  *plan = p;
+  return ok();
+}
+
+void fp_destroy(fp_plan* plan) {
+  if (!plan) return;
+  if (plan->d_status || plan->d_table) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (plan->device >= 0) cudaSetDevice(plan->device);
+    if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->d_table) cudaFree(plan->d_table);
+    if (plan->table_ready) cudaEventDestroy(plan->table_ready);
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+  delete plan;
+}
+
+int fp_last_launch_count(const fp_plan* plan) { return plan ? plan->last_launches : 0; }
+
+fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value) {
+  if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  switch (opt) {
+    case FP_OPT_WAIT_LIMIT_NS:
+      if (value <= 0) return fail(FP_ERR_INVALID_ARG, "wait limit must be > 0");
+      plan->wait_limit_ns = static_cast<uint64_t>(value);
+      return ok();
+    case FP_OPT_INJECT_STALL:
+      plan->inject_stall = value ? 1 : 0;
+      return ok();
+    case FP_OPT_GROUP_M:
+      if (value < 1 || value > 4096) return fail(FP_ERR_INVALID_ARG, "group_m out of range");
+      plan->group_m = static_cast<int>(value);
+      return ok();
+    case FP_OPT_MAX_CTAS:
+      if (value < 0) return fail(FP_ERR_INVALID_ARG, "max_ctas must be >= 0");
+      plan->max_ctas = static_cast<int>(value);
+      return ok();
+  }
+  return fail(FP_ERR_INVALID_ARG, "unknown option %d", static_cast<int>(opt));
+}
+
+fp_status fp_reserve(fp_plan* plan, int64_t max_tokens_per_batch) {
+  if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (max_tokens_per_batch < 0) return fail(FP_ERR_INVALID_ARG, "negative size");
+  fp_status st = ensure_device_state(plan, max_tokens_per_batch * rope_half_of(plan));
+  return st == FP_OK ? ok() : st;
+}
+
+fp_status fp_get_device_status(fp_plan* plan, void* stream) {
+  if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->d_status) return ok();
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "stream synchronisation failed: %s",
+                cudaGetErrorString(cudaGetLastError()));
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, plan->d_status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "status read failed");
+  if (h[0] != 0) {
+    int zero[2] = {0, 0};
+    cudaMemcpy(plan->d_status, zero, sizeof zero, cudaMemcpyHostToDevice);
+    return fail(static_cast<fp_status>(h[0]), "device reported: %s",
+                fp_status_string(static_cast<fp_status>(h[0])));
+  }
+  return ok();
+}
+
+fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
+                     const int32_t* pos, void* out_ff, void* out_q, void* out_k, void* out_v,
+                     void* stream_v) {
+  // ---------------------------------------------------------------- host checks
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (!xl) return fail(FP_ERR_INVALID_ARG, "x_layout is NULL");
+  const fp_layout L = *xl;
+  if (L.dtype != FP_BF16 && L.dtype != FP_F32) return fail(FP_ERR_INVALID_ARG, "unknown dtype");
+  if (L.ndim < 1 || L.ndim > FP_MAX_DIMS) return fail(FP_ERR_INVALID_ARG, "ndim out of range");
+  if (L.channel_dim < 0 || L.channel_dim >= L.ndim)
+    return fail(FP_ERR_INVALID_ARG, "channel_dim out of range");
+  if (L.n_batch_dims < 0 || L.n_batch_dims > L.ndim - 1)
+    return fail(FP_ERR_INVALID_ARG, "n_batch_dims out of range");
+  for (int a = 0; a < L.ndim; ++a)
+    if (L.sizes[a] < 0 || L.strides[a] < 0)
+      return fail(FP_ERR_INVALID_ARG, "negative size or stride on axis %d", a);
+  if (L.sizes[L.channel_dim] != p->C)
+    return fail(FP_ERR_INVALID_ARG, "x has %lld channels, plan has C = %d",
+                static_cast<long long>(L.sizes[L.channel_dim]), p->C);
+  const int esz = L.dtype == FP_BF16 ? 2 : 4;
+  const int N = n_total(p);
+  const int nkv = p->groups > 0 ? p->groups : p->heads;
+  TokAxes ta = analyse_tokens(L);
+  if (ta.M == 0) {
+    p->last_launches = 0;
+    return ok();  // no tokens: nothing to do
+  }
+  if (!x || !W) return fail(FP_ERR_INVALID_ARG, "x and W must be non-NULL");
+  if ((p->F > 0) != (out_ff != nullptr))
+    return fail(FP_ERR_INVALID_ARG, "out_ff must be non-NULL exactly when ff_hidden > 0");
+  const bool want_qkv = p->heads > 0;
+  if (want_qkv != (out_q != nullptr) || want_qkv != (out_k != nullptr) ||
+      want_qkv != (out_v != nullptr))
+    return fail(FP_ERR_INVALID_ARG, "out_q/out_k/out_v must be non-NULL exactly when heads > 0");
+  const void* ptrs[] = {x, W, b, pos, out_ff, out_q, out_k, out_v};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
+  // aliasing: outputs against each other and against every input
+  int64_t x_span = 1;
+  for (int a = 0; a < L.ndim; ++a) x_span += (L.sizes[a] - 1) * L.strides[a];
+  auto rng = [](const void* q, int64_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(q);
+    return Range{lo, q ? lo + static_cast<uintptr_t>(bytes) : lo};
+  };
+  const Range ins[] = {rng(x, x_span * esz), rng(W, static_cast<int64_t>(p->C) * N * esz),
+                       rng(b, static_cast<int64_t>(N) * esz),
+                       rng(pos, static_cast<int64_t>(ta.T) * 4)};
+  const Range outs[] = {rng(out_ff, ta.M * p->F * esz),
+                        rng(out_q, ta.M * p->heads * p->hd * esz),
+                        rng(out_k, ta.M * nkv * p->hd * esz), rng(out_v, ta.M * nkv * p->hd * esz)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], outs[j])) return fail(FP_ERR_INVALID_ARG, "output buffers overlap");
+    for (const Range& in : ins)
+      if (overlaps(outs[i], in)) return fail(FP_ERR_INVALID_ARG, "an output overlaps an input");
+  }
+  const int rh = rope_half_of(p);
+  const int64_t c_stride = L.strides[L.channel_dim];
+  const bool rope = rh > 0;
+  int bn_eff;
+  fp::TokenMap tk{};
+  tk.S_in = ta.S_in;
+  tk.s_stride = ta.s_stride;
+  tk.c_stride = p->C == 1 ? 1 : c_stride;
+  tk.n_outer = 1;
+  tk.n_outer_dims = static_cast<int>(ta.outer_size.size());
+  for (size_t i = 0; i < ta.outer_size.size() && i < fp::kMaxOuter; ++i) {
+    tk.outer_size[i] = ta.outer_size[i];
+    tk.outer_stride[i] = ta.outer_stride[i];
+    tk.n_outer *= ta.outer_size[i];
+  }
+
+  const bool tc_path = L.dtype == FP_BF16;
+  bool a_mn = false;
+  if (tc_path) {
+    if (p->F % 16 || (p->heads > 0 && p->hd % 16))
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                  "bf16 path needs ff_hidden and head_dim multiples of 16 (F=%d, head_dim=%d)",
+                  p->F, p->hd);
+    if (rope && rh % 16)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                  "bf16 path needs rotated lanes / 2 to be a multiple of 16 (got %d)", rh);
+    if (tk.n_outer_dims > 3)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "bf16 path addresses at most 3 outer token axes");
+    if (tk.c_stride == 1) a_mn = false;
+    else if (tk.s_stride == 1 || tk.S_in == 1) a_mn = true;
+    else
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                  "bf16 path needs unit stride on the channel axis or the innermost token axis");
+    const int64_t other = a_mn ? tk.c_stride : tk.s_stride;
+    if ((other * esz) % 16 && !(a_mn ? p->C == 1 : tk.S_in == 1))
+      return fail(FP_ERR_MISALIGNED, "non-unit x strides must be multiples of 16 bytes");
+    for (int i = 0; i < tk.n_outer_dims; ++i)
+      if ((tk.outer_stride[i] * esz) % 16)
+        return fail(FP_ERR_MISALIGNED, "non-unit x strides must be multiples of 16 bytes");
+    bn_eff = rope ? (fp::kTcBN / p->hd) * p->hd : fp::kTcBN;
+  } else {
+    if (tk.n_outer_dims > fp::kMaxOuter)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "too many non-mergeable token axes");
+    bn_eff = rope ? (fp::kSimtBN / p->hd) * p->hd : fp::kSimtBN;
+  }
+
+  // ---------------------------------------------------------------- device work
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  fp_status st = ensure_device_state(p, rope ? ta.T * rh : 0);
+  if (st != FP_OK) return st;
+  int launches = 0;
+  // The table depends only on (positions, base, head_dim). With the default
+  // positions 0..T-1 it is a constant of the plan and of T, so it is built
+  // once and reused; caller-given positions rebuild it on every call.
+  if (rope && (pos != nullptr || p->table_T != ta.T)) {
+    cudaError_t err = fp::launch_rope_table(p->d_table, pos, ta.T, rh, 2 * rh,
+                                            static_cast<double>(p->rope_base), stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "rotary table launch: %s", cudaGetErrorString(err));
+    if (!p->table_ready &&
+        cudaEventCreateWithFlags(&p->table_ready, cudaEventDisableTiming) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event creation failed");
+    if (cudaEventRecord(p->table_ready, stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event record failed");
+    p->table_stream = stream;
+    p->table_T = pos ? -1 : ta.T;
+    ++launches;
+  } else if (rope && stream != p->table_stream) {
+    // cached table written on another stream: order this call after that write
+    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
+  }
+  fp::Epilogue e{};
+  e.M = ta.M;
+  e.T = ta.T;
+  e.N = N;
+  e.F = p->F;
+  e.C = p->C;
+  e.heads = p->heads;
+  e.hd = p->hd;
+  e.groups = p->groups;
+  e.act = p->act;
+  e.rope_half = rh;
+  e.rope_cs = rope ? p->d_table : nullptr;
+  e.bias = b;
+  e.out_ff = out_ff;
+  e.out_q = out_q;
+  e.out_k = out_k;
+  e.out_v = out_v;
+  e.status = p->d_status;
+  e.bn_eff = bn_eff;
+  const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
+
+  if (tc_path) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+    if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    fp::TcParams tp;
+    memset(&tp, 0, sizeof tp);
+    // A: 5-D map [inner, second, outer0, outer1, outer2]
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
+    if (a_mn) {
+      gdim[0] = ta.S_in;
+      gdim[1] = p->C;
+      gstride[0] = static_cast<cuuint64_t>(tk.c_stride) * esz;
+      box[0] = 64;
+      box[1] = fp::kTcBK;
+    } else {
+      gdim[0] = p->C;
+      gdim[1] = ta.S_in;
+      gstride[0] = static_cast<cuuint64_t>(tk.s_stride) * esz;
+      box[0] = fp::kTcBK;
+      box[1] = fp::kTcBM;
+    }
+    if (gstride[0] == 0 || gstride[0] % 16) gstride[0] = 16 * ((gdim[0] * esz + 15) / 16);
+    cuuint64_t last = gstride[0];
+    for (int d = 0; d < 3; ++d) {
+      if (d < tk.n_outer_dims) {
+        gdim[2 + d] = tk.outer_size[d];
+        gstride[1 + d] = static_cast<cuuint64_t>(tk.outer_stride[d]) * esz;
+        last = gstride[1 + d];
+      } else {
+        gdim[2 + d] = 1;
+        gstride[1 + d] = last;
+      }
+      box[2 + d] = 1;
+    }
+    CUresult r = encode(&tp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), gdim,
+                        gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for x rejected (CUresult %d)",
+                  static_cast<int>(r));
+    cuuint64_t bdim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(p->C)};
+    cuuint64_t bstride[1] = {static_cast<cuuint64_t>(N) * esz};
+    cuuint32_t bbox[2] = {64, fp::kTcBK};
+    r = encode(&tp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), bdim, bstride,
+               bbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
+                  static_cast<int>(r));
+    tp.tok = tk;
+    tp.epi = e;
+    tp.C = p->C;
+    tp.num_k_blocks = (p->C + fp::kTcBK - 1) / fp::kTcBK;
+    tp.m_tiles_per_slab = (ta.S_in + fp::kTcBM - 1) / fp::kTcBM;
+    tp.num_m_tiles = tk.n_outer * tp.m_tiles_per_slab;
+    tp.num_n_tiles = num_n_tiles;
+    tp.num_tiles = tp.num_m_tiles * num_n_tiles;
+    tp.group_m = p->group_m;
+    tp.wait_limit_ns = p->wait_limit_ns;
+    tp.inject_stall = p->inject_stall;
+    p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
+    tp.launch_tag = static_cast<int>(p->launch_seq);
+    int ctas = sm_count(p->device);
+    if (p->max_ctas > 0) ctas = std::min(ctas, p->max_ctas);
+    if (static_cast<int64_t>(ctas) > tp.num_tiles) ctas = static_cast<int>(tp.num_tiles);
+    cudaError_t err = fp::launch_tc_gemm(tp, a_mn, ctas, stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(err));
+    p->inject_stall = 0;
+    ++launches;
+  } else {
+    fp::SimtParams sp;
+    memset(&sp, 0, sizeof sp);
+    sp.x = static_cast<const float*>(x);
+    sp.W = static_cast<const float*>(W);
+    sp.tok = tk;
+    sp.epi = e;
+    sp.C = p->C;
+    sp.m_tiles_per_slab = (ta.S_in + fp::kSimtBM - 1) / fp::kSimtBM;
+    sp.num_m_tiles = tk.n_outer * sp.m_tiles_per_slab;
+    sp.num_n_tiles = num_n_tiles;
+    cudaError_t err = fp::launch_simt_gemm(sp, stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "FFMA GEMM launch: %s", cudaGetErrorString(err));
+    ++launches;
+  }
+  p->last_launches = launches;
+  return ok();
+}
+
+}  // extern "C"

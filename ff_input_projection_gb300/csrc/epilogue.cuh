@@ -1,0 +1,92 @@
+// Epilogue arithmetic shared by the tensor-core and FFMA kernels: column
+// decoding into (ff | q | k | v, head, lane), activations and output addressing.
+#pragma once
+
+#include <cuda_bf16.h>
+#include "fp_internal.h"
+
+namespace fp {
+
+struct ColInfo {
+  int seg;   // 0 ff, 1 q, 2 k, 3 v
+  int head;  // q head, or k/v head (group) index
+  int j;     // lane inside the head (ff: the column)
+};
+
+// Fused column n -> block, head and lane. Blocked order [ff | q | k | v]
+// (fused_ff_qkv of Walrus PR #12); with groups > 0 the q|k|v part follows the
+// split_qkv listing of nvFuser issue #1597: per group, q_per_kv query heads,
+// then its key head, then its value head.
+__device__ __forceinline__ ColInfo decode_col(const Epilogue& e, int n) {
+  ColInfo ci;
+  if (n < e.F) {
+    ci.seg = 0;
+    ci.head = 0;
+    ci.j = n;
+    return ci;
+  }
+  int w = n - e.F;
+  if (e.groups > 0) {
+    int qpk = e.heads / e.groups;
+    int per = (qpk + 2) * e.hd;
+    int g = w / per, r = w - g * per;
+    int slot = r / e.hd;
+    ci.j = r - slot * e.hd;
+    if (slot < qpk) {
+      ci.seg = 1;
+      ci.head = g * qpk + slot;
+    } else {
+      ci.seg = slot == qpk ? 2 : 3;
+      ci.head = g;
+    }
+    return ci;
+  }
+  int seg = w / e.C, r = w - seg * e.C;
+  ci.seg = 1 + seg;
+  ci.head = r / e.hd;
+  ci.j = r - ci.head * e.hd;
+  return ci;
+}
+
+// Element offset of (token m = b*T + t, column info) in its output buffer.
+__device__ __forceinline__ int64_t out_offset(const Epilogue& e, const ColInfo& ci, int64_t m,
+                                              int64_t b, int64_t t) {
+  if (ci.seg == 0) return m * e.F + ci.j;
+  int nh = (ci.seg == 1 || e.groups == 0) ? e.heads : e.groups;
+  return ((b * nh + ci.head) * e.T + t) * e.hd + ci.j;
+}
+
+__device__ __forceinline__ void* out_base(const Epilogue& e, int seg) {
+  return seg == 0 ? e.out_ff : seg == 1 ? e.out_q : seg == 2 ? e.out_k : e.out_v;
+}
+
+// Activations of the ff block, in fp32 (the caller's dtype is only the storage).
+__device__ __forceinline__ float activate(int act, float y) {
+  switch (act) {
+    case ACT_GELU_ERF:
+      return 0.5f * y * (1.0f + erff(y * 0.70710678118654752f));
+    case ACT_GELU_TANH: {
+      float u = 0.79788456080286536f * (y + 0.044715f * y * y * y);
+      return 0.5f * y * (1.0f + tanhf(u));
+    }
+    case ACT_SILU:
+      return y / (1.0f + expf(-y));
+    default:
+      return y;
+  }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace fp

@@ -1,0 +1,84 @@
+// Internal kernel parameter blocks and launchers of libfp (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp {
+
+constexpr int kMaxOuter = 6;
+
+enum : int { ACT_NONE = 0, ACT_GELU_ERF = 1, ACT_GELU_TANH = 2, ACT_SILU = 3 };
+enum : int { ST_OK = 0, ST_TIMEOUT = 6, ST_BOUNDS = 7 };
+
+// Token addressing shared by both GEMM kernels. The non-channel axes of x are
+// merged where contiguous; the innermost merged group is `S_in` tokens at
+// stride `s_stride`, the others are `n_outer_dims` outer axes. Token
+// m = o*S_in + s, o = row-major index over the outer axes. M-tiles never cross
+// an outer index, so rows in one tile are `s`-consecutive.
+struct TokenMap {
+  int64_t S_in;
+  int64_t s_stride;
+  int64_t c_stride;
+  int64_t n_outer;  // product of outer sizes
+  int n_outer_dims;
+  int64_t outer_size[kMaxOuter];    // innermost first
+  int64_t outer_stride[kMaxOuter];  // innermost first
+};
+
+// Epilogue description shared by both GEMM kernels.
+struct Epilogue {
+  int64_t M;  // tokens
+  int64_t T;  // tokens per batch element
+  int N, F, C, heads, hd, groups;  // groups > 0: grouped-query column order
+  int act;
+  int rope_half;      // 0: no rotation, else rotated lanes / 2
+  const float2* rope_cs;  // [T][rope_half] (cos, sin)
+  const void* bias;   // [N] or null, dtype of x
+  void* out_ff;
+  void* out_q;
+  void* out_k;
+  void* out_v;
+  int* status;
+  int bn_eff;         // columns of an N-tile that this tile owns
+};
+
+struct TcParams {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b;
+  TokenMap tok;
+  Epilogue epi;
+  int C;
+  int num_k_blocks;
+  int64_t m_tiles_per_slab;
+  int64_t num_m_tiles;
+  int num_n_tiles;
+  int64_t num_tiles;
+  int group_m;
+  uint64_t wait_limit_ns;
+  int inject_stall;  // 1: CTA 0 withholds its first operand stage (error-path test)
+  int launch_tag;    // >= 1, unique per launch: marks this launch as aborted in status[1]
+};
+
+struct SimtParams {
+  const float* x;
+  const float* W;
+  TokenMap tok;
+  Epilogue epi;
+  int C;
+  int64_t m_tiles_per_slab;
+  int64_t num_m_tiles;
+  int num_n_tiles;
+};
+
+// Launchers (defined in the .cu files). Return cudaSuccess or the launch error.
+cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
+                              double rope_base, cudaStream_t stream);
+cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream);
+cudaError_t launch_simt_gemm(const SimtParams& p, cudaStream_t stream);
+
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+constexpr int kSimtBM = 128, kSimtBN = 128;
+
+}  // namespace fp

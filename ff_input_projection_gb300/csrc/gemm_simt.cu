@@ -1,0 +1,200 @@
+// fp32 fused projection on the FFMA pipes (TF32 off).
+//
+// The fp32 leg of the projection: activations and weight stay fp32 and every
+// product is an fp32 FFMA, so results do not depend on whether TF32 matmul is
+// enabled (the fp32-vs-TF32 ambiguity raised in xformers PR #283 "[perf] Fused
+// linear", last comments). x is read in place through its strides, as in
+// Walrus PR #12 "Make fused_ff_qkv contiguous" (no permuted copy).
+//
+// Tile: 128 tokens x 128 fused columns, k-steps of 16, 256 threads with an
+// 8x8 register block each (rows ty*4+{0..3} and 64+ty*4+{0..3}, columns
+// likewise), operands double-buffered in shared memory with a register
+// prefetch of the next k-step. The epilogue stages the fp32 tile in shared
+// memory so a rotary pair (lane i, lane i + half) can be read by whichever
+// thread owns either lane, then adds bias, applies the activation or the
+// rotation, and writes ff token-major and q/k/v head-major with consecutive
+// threads on consecutive lanes.
+#include "epilogue.cuh"
+#include "fp_internal.h"
+
+namespace fp {
+
+namespace {
+
+constexpr int BM = kSimtBM, BN = kSimtBN, BK = 16, NT = 256;
+constexpr int CS_LD = BN + 4;
+constexpr int kSmemBytes = BM * CS_LD * 4;  // epilogue tile; covers the 2x(A+B) operand buffers
+static_assert(2 * BK * (BM + BN) * 4 <= kSmemBytes, "operand buffers must fit in the epilogue tile");
+
+__device__ __forceinline__ int64_t outer_offset(const TokenMap& tk, int64_t o) {
+  int64_t off = 0;
+  for (int d = 0; d < tk.n_outer_dims; ++d) {
+    int64_t sz = tk.outer_size[d];
+    int64_t i = o % sz;
+    o /= sz;
+    off += i * tk.outer_stride[d];
+  }
+  return off;
+}
+
+// K_MAJOR: unit channel stride, so a thread walks channels (16 consecutive
+// channels of one token per k-step); otherwise a thread keeps one token and
+// walks channels at their stride (coalesced when tokens are unit-stride).
+template <bool K_MAJOR>
+__global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
+  extern __shared__ __align__(16) float smem[];
+  float* As = smem;                // [2][BK][BM]
+  float* Bs = smem + 2 * BK * BM;  // [2][BK][BN]
+
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int64_t tile = blockIdx.x;
+  const int n_tile = static_cast<int>(tile % p.num_n_tiles);
+  const int64_t m_tile = tile / p.num_n_tiles;
+  const int64_t o = m_tile / p.m_tiles_per_slab;
+  const int64_t s0 = (m_tile - o * p.m_tiles_per_slab) * BM;
+  const int n0 = n_tile * p.epi.bn_eff;
+  const TokenMap& tk = p.tok;
+  const int64_t S_in = tk.S_in;
+  const int C = p.C, N = p.epi.N;
+
+  // A element (row m, channel k) of this tile: x[a_base + m*s_stride + k*c_stride]
+  //   K_MAJOR:  k = tid % 16 fixed, rows m = tid/16 + 16 i
+  //   else:     row m = tid % 128 fixed, channels k = tid/128 + 2 i
+  const int a_m0 = K_MAJOR ? tid / BK : tid % BM;
+  const int a_k0 = K_MAJOR ? tid % BK : tid / BM;
+  const int64_t a_base = outer_offset(tk, o) + (s0 + a_m0) * tk.s_stride;
+  const int64_t rows_left = S_in - s0 - a_m0;  // rows with m - a_m0 < rows_left exist
+
+  float a_reg[8], b_reg[8];
+  auto load_regs = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int dm = K_MAJOR ? 16 * i : 0;
+      const int k = k0 + a_k0 + (K_MAJOR ? 0 : 2 * i);
+      const bool okr = dm < rows_left && k < C;
+      a_reg[i] = okr ? __ldg(p.x + a_base + dm * tk.s_stride + static_cast<int64_t>(k) * tk.c_stride)
+                     : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int idx = tid + i * NT;
+      int n = idx % BN, k = k0 + idx / BN;
+      int col = n0 + n;
+      b_reg[i] = (k < C && col < N) ? __ldg(p.W + static_cast<int64_t>(k) * N + col) : 0.0f;
+    }
+  };
+  auto store_regs = [&](int buf) {
+    float* a = As + buf * BK * BM;
+    float* b = Bs + buf * BK * BN;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int m = a_m0 + (K_MAJOR ? 16 * i : 0);
+      const int k = a_k0 + (K_MAJOR ? 0 : 2 * i);
+      a[k * BM + m] = a_reg[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int idx = tid + i * NT;
+      b[(idx / BN) * BN + idx % BN] = b_reg[i];
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+  const int num_k = (C + BK - 1) / BK;
+  load_regs(0);
+  store_regs(0);
+  __syncthreads();
+  for (int kb = 0; kb < num_k; ++kb) {
+    const int buf = kb & 1;
+    if (kb + 1 < num_k) load_regs((kb + 1) * BK);
+    const float* a = As + buf * BK * BM;
+    const float* b = Bs + buf * BK * BN;
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float4 a0 = *reinterpret_cast<const float4*>(a + kk * BM + ty * 4);
+      float4 a1 = *reinterpret_cast<const float4*>(a + kk * BM + 64 + ty * 4);
+      float4 b0 = *reinterpret_cast<const float4*>(b + kk * BN + tx * 4);
+      float4 b1 = *reinterpret_cast<const float4*>(b + kk * BN + 64 + tx * 4);
+      float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kb + 1 < num_k) store_regs(buf ^ 1);
+    __syncthreads();
+  }
+
+  // ---- epilogue: stage the fp32 tile, then bias / activation / rotation / scatter
+  float* Cs = smem;  // [BM][CS_LD]
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + tx * 4) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + 64 + tx * 4) =
+        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+  __syncthreads();
+
+  const Epilogue& e = p.epi;
+  const float* bias = static_cast<const float*>(e.bias);
+  const int half = e.rope_half;
+  for (int idx = tid; idx < BM * BN; idx += NT) {
+    const int r = idx / BN, c = idx % BN;
+    const int n = n0 + c;
+    const int64_t s = s0 + r;
+    if (c >= e.bn_eff || n >= N || s >= S_in) continue;
+    const int64_t m = o * S_in + s;
+    const int64_t bb = m / e.T, t = m - bb * e.T;
+    float v = Cs[r * CS_LD + c] + (bias ? bias[n] : 0.0f);
+    ColInfo ci = decode_col(e, n);
+    if (ci.seg == 0) {
+      v = activate(e.act, v);
+    } else if (half > 0 && ci.seg <= 2 && ci.j < 2 * half) {
+      const bool lo = ci.j < half;
+      const int f = lo ? ci.j : ci.j - half;
+      const int pc = lo ? c + half : c - half;
+      const int pn = lo ? n + half : n - half;
+      float pv = Cs[r * CS_LD + pc] + (bias ? bias[pn] : 0.0f);
+      float2 cs = e.rope_cs[t * half + f];
+      // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
+      v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+    }
+    static_cast<float*>(out_base(e, ci.seg))[out_offset(e, ci, m, bb, t)] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_simt_gemm(const SimtParams& p, cudaStream_t stream) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_done[dev]) {
+    err = cudaFuncSetAttribute(simt_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(simt_gemm_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_done[dev] = 1;
+  }
+  int64_t tiles = p.num_m_tiles * p.num_n_tiles;
+  if (tiles == 0) return cudaSuccess;
+  if (p.tok.c_stride == 1)
+    simt_gemm_kernel<true><<<static_cast<unsigned>(tiles), NT, kSmemBytes, stream>>>(p);
+  else
+    simt_gemm_kernel<false><<<static_cast<unsigned>(tiles), NT, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp

@@ -1,0 +1,545 @@
+// bf16 fused projection on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes: Y = x W + b for a strided activation x read in place
+// (Walrus PR #12 "Make fused_ff_qkv contiguous": one GEMM over all tokens
+// instead of per-token GEMVs, and no permuted copy), then in the epilogue the
+// activation on the ff block (xformers PR #283 "[perf] Fused linear": w x + b
+// then the activation, fused), the rotate-half rotary embedding on q and k
+// (nvFuser issue #1597 "Improve performance on RoPE", rope_one_entry, with no
+// slice/cat/neg kernels), and the split into ff [M, F] and head-major
+// q/k/v [B*heads, T, head_dim] (memory-efficient-attention issue #7, the
+// [batch*heads, tokens, head_dim] layout).
+//
+// Structure (one persistent CTA per SM, 10 warps):
+//   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring
+//   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
+//              (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits
+//              completion to mbarriers
+//   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (one token row
+//              per thread), bias, activation / rotation in registers, bf16
+//              round-to-nearest-even, 16-byte stores
+// The accumulator is double-buffered in TMEM (2 x 256 columns), so the
+// epilogue of tile i overlaps the main loop of tile i+1.
+//
+// Operand layouts (128-byte swizzle, as written by TMA and read by the MMA):
+//   A, row-major x (unit channel stride): K-major, [128 rows][64 ch] per stage.
+//   A, channels-first x (unit token stride): MN-major, two [64 ch][64 tok] chunks.
+//   B, W [C, N] row-major: MN-major (N contiguous), four [64 ch][64 col] chunks.
+//
+// Every mbarrier wait is bounded (%globaltimer); a wait that runs out records
+// a timeout in the plan's status word, tags the launch as aborted so the other
+// roles and CTAs stop too, drains its own in-flight copies and MMAs, frees
+// TMEM and returns.
+#include "epilogue.cuh"
+#include "fp_internal.h"
+
+namespace fp {
+namespace {
+
+constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = BN * BK * 2;             // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int CHUNK_BYTES = 64 * BK * 2;         // one [64 ch][64 elems] MN-major chunk, 8 KB
+constexpr int ACC_COLS = BN;                     // fp32 accumulator: one TMEM column per output column
+constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: two accumulators
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct WaitCtl {
+  int* status;        // [0] sticky error code, [1] tag of an aborted launch
+  uint64_t limit_ns;
+  int launch_tag;
+};
+
+__device__ __forceinline__ bool launch_aborted(const WaitCtl& w) {
+  return *reinterpret_cast<volatile int*>(w.status + 1) == w.launch_tag;
+}
+
+__device__ __forceinline__ void abort_launch(const WaitCtl& w) {
+  atomicCAS(w.status, 0, ST_TIMEOUT);
+  atomicExch(w.status + 1, w.launch_tag);
+}
+
+// Wait for phase `parity` of an mbarrier, for at most limit_ns. Returns false
+// when the limit ran out (recorded as a timeout) or, if honor_abort, when
+// another role or CTA has aborted this launch.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                          bool honor_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 0) {
+      if (honor_abort && launch_aborted(w)) return false;
+      if (global_timer_ns() - t0 > w.limit_ns) {
+        abort_launch(w);
+        return false;
+      }
+    }
+  }
+}
+
+// 5-D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-47  descriptor version (1 for tcgen05)
+//   bits 61-63  swizzle mode (2 = 128-byte)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and
+// B, operand majorness, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tile helpers
+
+struct TileCoord {
+  int64_t o;    // outer slab
+  int64_t s0;   // first token of the tile inside the slab
+  int n0;       // first fused column
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t tile) {
+  // group_m consecutive M-tiles sweep all N-tiles, M fastest inside a group,
+  // so concurrently running CTAs share W tiles and x tiles in L2.
+  const int64_t per_group = static_cast<int64_t>(p.group_m) * p.num_n_tiles;
+  const int64_t g = tile / per_group;
+  const int64_t first_m = g * p.group_m;
+  const int64_t left = p.num_m_tiles - first_m;
+  const int64_t gm = left < p.group_m ? left : p.group_m;
+  const int64_t r = tile - g * per_group;
+  const int64_t m_tile = first_m + r % gm;
+  const int n_tile = static_cast<int>(r / gm);
+  TileCoord tc;
+  tc.o = m_tile / p.m_tiles_per_slab;
+  tc.s0 = (m_tile - tc.o * p.m_tiles_per_slab) * BM;
+  tc.n0 = n_tile * p.epi.bn_eff;
+  return tc;
+}
+
+__device__ __forceinline__ void outer_coords(const TokenMap& tk, int64_t o, int (&oc)[3]) {
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    if (d < tk.n_outer_dims) {
+      int64_t sz = tk.outer_size[d];
+      int64_t i = o % sz;
+      o /= sz;
+      oc[d] = static_cast<int>(i);
+    } else {
+      oc[d] = 0;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_bias16(const uint16_t* bias, int n, float (&b)[16]) {
+  if (bias == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = 0.0f;
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(bias + n);
+  uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+  uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    b[2 * i] = __uint_as_float(w[i] << 16);
+    b[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void store16_bf16(void* dst, const float (&v)[16]) {
+  uint4 a, b;
+  a.x = pack_bf16x2(v[0], v[1]);
+  a.y = pack_bf16x2(v[2], v[3]);
+  a.z = pack_bf16x2(v[4], v[5]);
+  a.w = pack_bf16x2(v[6], v[7]);
+  b.x = pack_bf16x2(v[8], v[9]);
+  b.y = pack_bf16x2(v[10], v[11]);
+  b.z = pack_bf16x2(v[12], v[13]);
+  b.w = pack_bf16x2(v[14], v[15]);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = a;
+  d[1] = b;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <bool A_MN_MAJOR>
+__global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KB alignment
+  uint8_t* sptr = smem_raw + (sbase - raw_addr);
+  const uint32_t bar0 = sbase + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + NUM_BARS * 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl wc{p.epi.status, p.wait_limit_ns, p.launch_tag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = p.num_k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool inject = (p.inject_stall & 1) && blockIdx.x == 0;
+      uint32_t armed_mask = 0, armed_parity = 0;  // per stage: armed, parity of its last arming
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = tile_coord(p, tile);
+        int oc[3];
+        outer_coords(p.tok, tc.o, oc);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
+            ok = false;
+            break;
+          }
+          if (inject) {
+            inject = false;  // withhold this stage: its consumer's wait runs out
+          } else {
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t a_dst = sbase + stage * STAGE_BYTES;
+            const uint32_t b_dst = a_dst + A_BYTES;
+            const int k0 = kb * BK;
+            if (A_MN_MAJOR) {
+              tma_load_5d(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1], oc[2]);
+              tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64, k0,
+                          oc[0], oc[1], oc[2]);
+            } else {
+              tma_load_5d(a_dst, &p.tmap_a, fb, k0, static_cast<int>(tc.s0), oc[0], oc[1], oc[2]);
+            }
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0);
+            armed_mask |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // drain: every armed stage's copies must land before the CTA exits
+      for (int s = 0; s < STAGES; ++s)
+        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, wc, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(A_MN_MAJOR, true);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued = false;
+      int it = 0;
+      for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!wait_bounded(tempty_bar(buf), acc_phase ^ 1u, wc, true)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * ACC_COLS;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wc, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + stage * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // A: MN-major -> 16 channel rows of 128 B per K step, chunks of 64 tokens 8 KB apart;
+            //    K-major  -> 32 B per K step inside the 128-B swizzled row, 8-row groups 1 KB apart.
+            const uint64_t a_desc = A_MN_MAJOR ? sw128_desc(a_addr + k * 2048, CHUNK_BYTES, 1024)
+                                               : sw128_desc(a_addr + k * 32, 16, 1024);
+            const uint64_t b_desc = sw128_desc(b_addr + k * 2048, CHUNK_BYTES, 1024);
+            umma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(buf));  // accumulator ready for the epilogue
+      }
+      if (issued) {
+        umma_commit(drain_bar);  // all MMAs of this CTA retired before TMEM is freed
+        wait_bounded(drain_bar, 0, wc, false);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const Epilogue& e = p.epi;
+    const int quarter = warp & 3;                  // TMEM lanes this warp may read
+    const int half_id = (warp - 2) >> 2;           // which alternate work units it takes
+    const int row = quarter * 32 + lane;
+    const int rh = e.rope_half;
+    const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const int ok = wait_bounded(tfull_bar(buf), acc_phase, wc, true) ? 1 : 0;
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const TileCoord tc = tile_coord(p, tile);
+      const int64_t s = tc.s0 + row;
+      const bool valid = s < p.tok.S_in;
+      const int64_t m = tc.o * p.tok.S_in + s;
+      const int64_t bidx = m / e.T;
+      const int64_t t = m - bidx * e.T;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
+      int unit = 0;
+      for (int c = 0; c < BN; c += 16) {
+        const int n = tc.n0 + c;
+        if (c >= e.bn_eff || n >= e.N) break;
+        const ColInfo ci = decode_col(e, n);
+        const bool rope = rh > 0 && (ci.seg == 1 || ci.seg == 2) && ci.j < 2 * rh;
+        if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
+        if ((unit++ & 1) != half_id) continue;
+        float bl[16];
+        load_bias16(bias, n, bl);
+        if (rope) {
+          uint32_t lo_u[16], hi_u[16];
+          tmem_ld16(t_row + c, lo_u);
+          tmem_ld16(t_row + c + rh, hi_u);
+          tmem_wait_ld();
+          float bh[16];
+          load_bias16(bias, n + rh, bh);
+          float lo[16], hi[16];
+          if (valid) {
+            const float4* cs4 = reinterpret_cast<const float4*>(e.rope_cs + t * rh + ci.j);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
+              const float x0 = __uint_as_float(lo_u[2 * i]) + bl[2 * i];
+              const float y0 = __uint_as_float(hi_u[2 * i]) + bh[2 * i];
+              const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bl[2 * i + 1];
+              const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bh[2 * i + 1];
+              lo[2 * i] = x0 * cs.x - y0 * cs.y;
+              hi[2 * i] = y0 * cs.x + x0 * cs.y;
+              lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
+              hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
+            }
+            char* base = static_cast<char*>(out_base(e, ci.seg));
+            store16_bf16(base + 2 * out_offset(e, ci, m, bidx, t), lo);
+            ColInfo ch = ci;
+            ch.j += rh;
+            store16_bf16(base + 2 * out_offset(e, ch, m, bidx, t), hi);
+          }
+        } else {
+          uint32_t v_u[16];
+          tmem_ld16(t_row + c, v_u);
+          tmem_wait_ld();
+          if (valid) {
+            float v[16];
+            if (ci.seg == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = activate(e.act, __uint_as_float(v_u[i]) + bl[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bl[i];
+            }
+            char* base = static_cast<char*>(out_base(e, ci.seg));
+            store16_bf16(base + 2 * out_offset(e, ci, m, bidx, t), v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    attr_done[dev] = 1;
+  }
+  if (p.num_tiles == 0) return cudaSuccess;
+  if (a_mn_major)
+    tc_gemm_kernel<true><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
+  else
+    tc_gemm_kernel<false><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp

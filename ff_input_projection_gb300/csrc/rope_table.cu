@@ -1,0 +1,46 @@
+// Rotary table kernel: cs[t, i] = (cos, sin)(pos[t] * base^(-2 i / n_elem)).
+//
+// The rotate-half embedding of nvFuser issue #1597 "Improve performance on
+// RoPE" (rope_one_entry listing) takes cos/sin tables [T, rope_n_elem] as
+// inputs. Both halves of a head use the same angle theta_i, so one (cos, sin)
+// pair per (position, frequency) is stored: T * n_elem/2 float2.
+//
+// Accuracy: the angle is formed and reduced to [-pi, pi] in fp64 (Cody-Waite
+// reduction with 2*pi split into a head and a tail), then cos/sin are taken in
+// fp32 on the small reduced angle, so large positions lose no bits to the
+// fp32 product pos * inv_freq.
+#include "fp_internal.h"
+
+namespace fp {
+
+__global__ void rope_table_kernel(float2* __restrict__ cs, const int32_t* __restrict__ pos,
+                                  int64_t T, int half, int n_elem, double log2_base) {
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= T * half) return;
+  int64_t t = i / half;
+  int f = static_cast<int>(i - t * half);
+  double p = pos ? static_cast<double>(pos[t]) : static_cast<double>(t);
+  double inv_freq = exp2(-(2.0 * f / n_elem) * log2_base);
+  double a = p * inv_freq;
+  const double two_pi_hi = 6.283185307179586232;      // nearest double to 2*pi
+  const double two_pi_lo = 2.4492935982947064e-16;    // 2*pi - two_pi_hi
+  double k = rint(a * 0.15915494309189533577);        // a / (2*pi), nearest integer
+  double r = fma(-k, two_pi_hi, a);
+  r = fma(-k, two_pi_lo, r);
+  float s, c;
+  sincosf(static_cast<float>(r), &s, &c);
+  cs[i] = make_float2(c, s);
+}
+
+cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
+                              double rope_base, cudaStream_t stream) {
+  int64_t n = T * half;
+  if (n == 0) return cudaSuccess;
+  int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  rope_table_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(cs, pos, T, half, n_elem,
+                                                                            log2(rope_base));
+  return cudaGetLastError();
+}
+
+}  // namespace fp

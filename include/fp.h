@@ -1,0 +1,181 @@
+/*
+ * fp.h — fused input projection on one GB300 (sm_103a): the C ABI of libfp.so.
+ *
+ * One call computes, for an activation x read in place through its strides,
+ *
+ *     Y = x W + b                         (one dense GEMM, fp32 accumulation)
+ *     ff = act(Y[:, :F])                  (GELU-erf / GELU-tanh / SiLU / none)
+ *     q, k = rotate_half_rope(Y[:, F:F+C]), rotate_half_rope(Y[:, F+C:F+2C])
+ *     v = Y[:, F+2C:F+3C]
+ *
+ * and writes ff token-major and q, k, v head-major [B*heads, T, head_dim].
+ *
+ * What each piece follows:
+ *  - reading a channels-first activation (b c h w d, optionally with a time
+ *    axis) as [tokens, C] with no permuted copy, and one fused ff+q+k+v weight
+ *    instead of per-token GEMVs: Walrus PR #12 "Make fused_ff_qkv contiguous"
+ *    (opening comment and the profiler comparison that follows it);
+ *  - bias and activation fused into the GEMM epilogue (w x + b, then the
+ *    activation), and a projection that writes straight into three buffers:
+ *    xformers PR #283 "[perf] Fused linear" (PR description; the comment on a
+ *    dedicated attention-projection kernel);
+ *  - rotate-half rotary embedding on q and k with no slice/cat/neg kernels:
+ *    nvFuser issue #1597 "Improve performance on RoPE" (rope_one_entry and
+ *    split_qkv listings);
+ *  - the [batch*heads, tokens, head_dim] output layout: memory-efficient-
+ *    attention issue #7 "Improve performance via batched-matmul and fused
+ *    multiplies" (the layout conversion in the opening comment).
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers on the current CUDA device, owned
+ *    by the caller; the library keeps no reference after a call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). fp_forward only enqueues work: it never synchronises.
+ *  - Argument checks run on the host before any launch; a rejected call
+ *    launches nothing and returns a non-zero fp_status. fp_last_error()
+ *    then gives a one-line reason (thread-local).
+ *  - Errors raised on the device (a bounded wait that ran out) are recorded
+ *    in a per-plan status word and reported by fp_get_device_status.
+ */
+#ifndef FP_H
+#define FP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP_OK = 0,
+  FP_ERR_INVALID_ARG = 1,        /* null/inconsistent argument, aliasing outputs */
+  FP_ERR_UNSUPPORTED_LAYOUT = 2, /* strides the selected kernel cannot address */
+  FP_ERR_MISALIGNED = 3,         /* pointer or stride not 16-byte aligned */
+  FP_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+  FP_ERR_OUT_OF_MEMORY = 5,      /* plan scratch could not be allocated */
+  FP_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out */
+  FP_ERR_DEVICE_BOUNDS = 7       /* a device-side bounds check failed */
+} fp_status;
+
+typedef enum {
+  FP_ACT_NONE = 0,
+  FP_ACT_GELU_ERF = 1,  /* 0.5 y (1 + erf(y / sqrt 2)) */
+  FP_ACT_GELU_TANH = 2, /* 0.5 y (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3))) */
+  FP_ACT_SILU = 3       /* y / (1 + exp(-y)) */
+} fp_act;
+
+typedef enum { FP_BF16 = 0, FP_F32 = 1 } fp_dtype;
+
+#define FP_MAX_DIMS 8
+
+/*
+ * Logical shape and element strides of x. Axis `channel_dim` holds C. The
+ * other axes, in order, index the tokens row-major: the first `n_batch_dims`
+ * of them form the batch index b, the rest the in-sequence index t, so token
+ * m = b*T + t. Rotary positions restart at every b.
+ * Examples: channels-first [B, T6, C, H, W, D] -> channel_dim 2, n_batch_dims 1;
+ *           row-major [B, S, C] -> channel_dim 2, n_batch_dims 1;
+ *           NCHW [B, C, H, W] -> channel_dim 1, n_batch_dims 1.
+ */
+typedef struct {
+  int32_t dtype; /* fp_dtype: the dtype of x, W, b and of every output */
+  int32_t ndim;  /* 1 .. FP_MAX_DIMS */
+  int64_t sizes[FP_MAX_DIMS];
+  int64_t strides[FP_MAX_DIMS]; /* in elements, >= 0 */
+  int32_t channel_dim;
+  int32_t n_batch_dims;
+} fp_layout;
+
+typedef struct fp_plan fp_plan;
+
+/*
+ * fp_create — a projection plan for fixed sizes. Host only: touches no GPU.
+ *   C          channels (> 0)
+ *   ff_hidden  F, width of the ff block (>= 0)
+ *   heads      attention heads (>= 0); heads * head_dim must equal C
+ *   head_dim   even, and ff_hidden a multiple of it; <= 128 with rotary embedding
+ *   act        activation of the ff block
+ *   rope_base  > 0: rotate q and k with theta_i = pos * rope_base^(-2i/head_dim);
+ *              <= 0: no rotary embedding
+ * The fused weight W is [C, N] row-major with N = F + 3*heads*head_dim and
+ * column blocks [ff | q | k | v]; inside a block, column = head*head_dim + j.
+ * Returns FP_ERR_INVALID_ARG for inconsistent sizes; *plan is set to NULL then.
+ */
+fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_dim, fp_act act,
+                    float rope_base);
+
+/*
+ * fp_forward — enqueue one fused projection on `stream`.
+ *   x        device pointer to element (0, ..., 0) of the activation; layout `x_layout`
+ *   W        [C, N] row-major, dtype of x
+ *   b        [N] or NULL (no bias), dtype of x
+ *   pos      int32 [T] rotary positions, or NULL for 0 .. T-1 (ignored without rope)
+ *   out_ff   [B*T, F] row-major, or NULL when F == 0
+ *   out_q, out_k, out_v   [B*heads, T, head_dim] each, or NULL when heads == 0
+ * All pointers must be 16-byte aligned. Outputs may not overlap each other or
+ * any input. bf16 activations run on the tcgen05 tensor-core kernel, which
+ * needs unit stride on the channel axis or on the innermost token axis and
+ * 16-byte-multiple other strides; f32 activations run on the FFMA kernel
+ * (TF32 off), which takes any strides.
+ * Rotary table: with pos == NULL the (cos, sin) table is a constant of the
+ * plan and T; it is built by the first such call and reused by later ones
+ * (calls on another stream are ordered after that build with an event).
+ * Caller-given positions rebuild the table on every call, so such calls on
+ * different streams must be ordered by the caller. The first call that needs
+ * more table room than the plan holds allocates it (see fp_reserve); every
+ * other call allocates nothing.
+ * Returns FP_OK once the work is enqueued.
+ */
+fp_status fp_forward(fp_plan* plan, const void* x, const fp_layout* x_layout, const void* W,
+                     const void* b, const int32_t* pos, void* out_ff, void* out_q, void* out_k,
+                     void* out_v, void* stream);
+
+/*
+ * fp_reserve — allocate, on the current device, the plan's device scratch
+ * (status word and a rotary table for up to max_tokens_per_batch positions) so
+ * that later fp_forward calls with T <= max_tokens_per_batch allocate nothing.
+ */
+fp_status fp_reserve(fp_plan* plan, int64_t max_tokens_per_batch);
+
+/*
+ * fp_get_device_status — synchronise `stream`, then report and clear the
+ * device-side status word: FP_OK, FP_ERR_TIMEOUT or FP_ERR_DEVICE_BOUNDS.
+ * Returns FP_ERR_CUDA if the synchronisation itself failed.
+ */
+fp_status fp_get_device_status(fp_plan* plan, void* stream);
+
+/* Number of kernels the plan's last successful fp_forward launched. */
+int fp_last_launch_count(const fp_plan* plan);
+
+/* Static description of the status code (never NULL). */
+const char* fp_status_string(fp_status s);
+
+/* Reason for the calling thread's most recent non-OK status ("" if none). */
+const char* fp_last_error(void);
+
+/*
+ * fp_set_option — tuning and test hooks (not needed for normal use).
+ *   FP_OPT_WAIT_LIMIT_NS   device-side bound on every wait (default 2e9 ns)
+ *   FP_OPT_INJECT_STALL    1: the next bf16 launch's first CTA withholds one
+ *                          operand load, so its consumers' bounded waits run
+ *                          out and the launch reports FP_ERR_TIMEOUT (tests the
+ *                          error path; the GPU stays usable). Cleared after use.
+ *   FP_OPT_GROUP_M         tile rasterisation: M-tiles per group (>= 1)
+ *   FP_OPT_MAX_CTAS        cap on the persistent grid (0 = one CTA per SM)
+ */
+typedef enum {
+  FP_OPT_WAIT_LIMIT_NS = 1,
+  FP_OPT_INJECT_STALL = 2,
+  FP_OPT_GROUP_M = 3,
+  FP_OPT_MAX_CTAS = 4
+} fp_option;
+fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value);
+
+/* Release the plan and its device scratch. NULL is a no-op. */
+void fp_destroy(fp_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP_H */

@@ -1,0 +1,142 @@
+"""The C ABI without a GPU: the library loads, exports what include/fp.h declares,
+and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ff_input_projection_gb300 as fpx
+from ff_input_projection_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fpx.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(fpx.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = fpx.fp_status_string(code)
+        assert s and s != "unknown status"
+    assert fpx.fp_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("args", [
+    (0, 64, 2, 16, 0, 0.0),      # C = 0
+    (32, 64, 2, 15, 0, 0.0),     # odd head_dim
+    (32, 64, 3, 16, 0, 0.0),     # heads * head_dim != C
+    (32, 40, 2, 16, 0, 0.0),     # ff_hidden not a multiple of head_dim
+    (32, 0, 0, 0, 0, 0.0),       # nothing to compute
+    (32, 64, 2, 16, 9, 0.0),     # unknown activation
+    (512, 0, 2, 256, 0, 10000.0),  # rotary with head_dim > 128
+    (32, -1, 2, 16, 0, 0.0),     # negative ff_hidden
+])
+def test_create_rejects(lib, args):
+    st, h = fpx.fp_create(*args)
+    assert st == fpx.FP_ERR_INVALID_ARG and h is None
+    assert fpx.fp_last_error()
+
+
+def _plan(C=64, F=64, heads=4, hd=16, act=1, rope=0.0):
+    st, h = fpx.fp_create(C, F, heads, hd, act, rope)
+    assert st == fpx.FP_OK, fpx.fp_last_error()
+    return h
+
+
+# fake, 16-byte-aligned device addresses: the checks below must reject the call
+# before anything dereferences them
+X, WP, BP, O1, O2, O3, O4 = (0x10000000 + i * 0x1000000 for i in range(7))
+
+
+def _cf_layout(dtype=fpx.FP_BF16, B=2, C=64, H=8, W=8):
+    return fpx.make_layout([B, C, H, W], [C * H * W, H * W, W, 1], 1, 1, dtype)
+
+
+def test_forward_rejects_on_host(lib):
+    h = _plan()
+    L = _cf_layout()
+    fwd = lambda **kw: fpx.fp_forward(h, kw.get("x", X), kw.get("L", L), kw.get("W", WP),
+                                      kw.get("b", BP), None, kw.get("ff", O1), kw.get("q", O2),
+                                      kw.get("k", O3), kw.get("v", O4), None)
+    assert fwd(x=None) == fpx.FP_ERR_INVALID_ARG
+    assert fwd(W=None) == fpx.FP_ERR_INVALID_ARG
+    assert fwd(ff=None) == fpx.FP_ERR_INVALID_ARG  # F > 0 needs out_ff
+    assert fwd(k=None) == fpx.FP_ERR_INVALID_ARG
+    assert fwd(x=X + 2) == fpx.FP_ERR_MISALIGNED
+    assert fwd(b=BP + 8) == fpx.FP_ERR_MISALIGNED
+    assert fwd(q=O1) == fpx.FP_ERR_INVALID_ARG       # outputs alias
+    assert fwd(v=X) == fpx.FP_ERR_INVALID_ARG        # output aliases input
+    bad = _cf_layout(C=32)
+    assert fwd(L=bad) == fpx.FP_ERR_INVALID_ARG      # channel count
+    L2 = _cf_layout()
+    L2.channel_dim = 7
+    assert fwd(L=L2) == fpx.FP_ERR_INVALID_ARG
+    L3 = _cf_layout()
+    L3.dtype = 5
+    assert fwd(L=L3) == fpx.FP_ERR_INVALID_ARG
+    # bf16 tensor-core path: no unit stride on channels or innermost tokens
+    L4 = fpx.make_layout([2, 64, 8, 8], [64 * 8 * 8 * 2, 2, 64 * 8 * 2, 64 * 2], 1, 1, fpx.FP_BF16)
+    assert fwd(L=L4) == fpx.FP_ERR_UNSUPPORTED_LAYOUT
+    # bf16 channels-first with a channel stride that is not a 16-byte multiple
+    L5 = fpx.make_layout([2, 64, 5, 7], [64 * 35, 35, 7, 1], 1, 1, fpx.FP_BF16)
+    assert fwd(L=L5) == fpx.FP_ERR_MISALIGNED
+    fpx.fp_destroy(h)
+
+
+def test_forward_bf16_granularity(lib):
+    # F not a multiple of 16 is fine for f32 but not for the bf16 tensor-core path
+    h = _plan(C=8, F=8, heads=1, hd=8, act=0)
+    L = fpx.make_layout([1, 16, 8], [128, 8, 1], 2, 1, fpx.FP_BF16)
+    assert fpx.fp_forward(h, X, L, WP, None, None, O1, O2, O3, O4, None) == \
+        fpx.FP_ERR_UNSUPPORTED_LAYOUT
+    fpx.fp_destroy(h)
+
+
+def test_empty_input_is_a_no_op(lib):
+    h = _plan()
+    L = fpx.make_layout([0, 64, 8, 8], [4096, 64, 8, 1], 1, 1, fpx.FP_BF16)
+    assert fpx.fp_forward(h, X, L, WP, BP, None, O1, O2, O3, O4, None) == fpx.FP_OK
+    assert fpx.fp_last_launch_count(h) == 0
+    fpx.fp_destroy(h)
+
+
+def test_options_and_status_without_device(lib):
+    h = _plan()
+    assert fpx.fp_set_option(h, fpx.FP_OPT_GROUP_M, 0) == fpx.FP_ERR_INVALID_ARG
+    assert fpx.fp_set_option(h, fpx.FP_OPT_GROUP_M, 16) == fpx.FP_OK
+    assert fpx.fp_set_option(h, fpx.FP_OPT_WAIT_LIMIT_NS, -5) == fpx.FP_ERR_INVALID_ARG
+    assert fpx.fp_set_option(h, 77, 1) == fpx.FP_ERR_INVALID_ARG
+    # no device state yet: nothing to report, no CUDA call made
+    assert fpx.fp_get_device_status(h, None) == fpx.FP_OK
+    fpx.fp_destroy(h)
+    fpx.fp_destroy(None)
+
+
+def test_wrapper_raises(lib):
+    with pytest.raises(fpx.FpError):
+        fpx.FusedProjection(30, 0, 4, 8)
+
+
+def test_binding_has_no_fallback(monkeypatch, tmp_path):
+    # a missing library is an error, never a silent substitute
+    monkeypatch.setattr(fpx, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        fpx.load()
