@@ -35,7 +35,7 @@ FP_OPT_GROUP_M = 3
 FP_OPT_MAX_CTAS = 4
 
 # the C ABI's entry points, as declared in include/fp.h
-EXPORTS = ("fp_create", "fp_forward", "fp_reserve", "fp_get_device_status",
+EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
 
@@ -44,6 +44,13 @@ class fp_layout(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("sizes", ctypes.c_int64 * FP_MAX_DIMS), ("strides", ctypes.c_int64 * FP_MAX_DIMS),
                 ("channel_dim", ctypes.c_int32), ("n_batch_dims", ctypes.c_int32)]
+
+
+class fp_config(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_int32), ("ff_hidden", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_query_groups", ctypes.c_int32),
+                ("rope_n_elem", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("rope_base", ctypes.c_float)]
 
 
 class FpError(RuntimeError):
@@ -71,6 +78,8 @@ def load():
     P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     lib.fp_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, ctypes.c_float]
     lib.fp_create.restype = I
+    lib.fp_create_ex.argtypes = [ctypes.POINTER(P), ctypes.POINTER(fp_config)]
+    lib.fp_create_ex.restype = I
     lib.fp_forward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
     lib.fp_forward.restype = I
     lib.fp_reserve.argtypes = [P, I64]
@@ -106,6 +115,13 @@ def fp_create(C: int, ff_hidden: int, heads: int, head_dim: int, act: int,
     """Returns (status, plan handle or None)."""
     h = ctypes.c_void_p()
     st = load().fp_create(ctypes.byref(h), C, ff_hidden, heads, head_dim, act, rope_base)
+    return st, (h.value if st == FP_OK else None)
+
+
+def fp_create_ex(config: fp_config) -> Tuple[int, Optional[int]]:
+    """Returns (status, plan handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().fp_create_ex(ctypes.byref(h), ctypes.byref(config))
     return st, (h.value if st == FP_OK else None)
 
 
@@ -166,12 +182,15 @@ class FusedProjection:
     """
 
     def __init__(self, C: int, ff_hidden: int, heads: int, head_dim: int, act="none",
-                 rope_base: float = 0.0):
+                 rope_base: float = 0.0, n_query_groups: int = 0, rope_n_elem: int = 0):
         a = ACTS[act] if isinstance(act, str) else int(act)
-        st, h = fp_create(C, ff_hidden, heads, head_dim, a, float(rope_base))
+        cfg = fp_config(C, ff_hidden, heads, head_dim, n_query_groups, rope_n_elem, a,
+                        float(rope_base))
+        st, h = fp_create_ex(cfg)
         check(st)
         self.plan = h
         self.C, self.F, self.heads, self.head_dim = C, ff_hidden, heads, head_dim
+        self.kv_heads = n_query_groups if n_query_groups else heads
 
     def close(self):
         if getattr(self, "plan", None):
@@ -217,8 +236,9 @@ class FusedProjection:
         M = Bb * T
         if out is None:
             ff = torch.empty((M, self.F), device=x.device, dtype=x.dtype) if self.F else None
-            qkv = [torch.empty((Bb * self.heads, T, self.head_dim), device=x.device, dtype=x.dtype)
-                   for _ in range(3)] if self.heads else [None, None, None]
+            qkv = [torch.empty((Bb * nh, T, self.head_dim), device=x.device, dtype=x.dtype)
+                   for nh in (self.heads, self.kv_heads, self.kv_heads)] \
+                if self.heads else [None, None, None]
             out = (ff, *qkv)
         L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, dt)
         ptr = lambda t: None if t is None else t.data_ptr()

@@ -187,40 +187,48 @@ const char* fp_status_string(fp_status s) {
 
 const char* fp_last_error(void) { return g_err; }
 
-fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_dim, fp_act act,
-                    float rope_base) {
+fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   *plan = nullptr;
+  if (!cfg) return fail(FP_ERR_INVALID_ARG, "config is NULL");
+  const int C = cfg->C, F = cfg->ff_hidden, heads = cfg->heads, hd = cfg->head_dim;
+  const int G = cfg->n_query_groups, ne = cfg->rope_n_elem;
   if (C <= 0) return fail(FP_ERR_INVALID_ARG, "C must be > 0 (got %d)", C);
-  if (ff_hidden < 0) return fail(FP_ERR_INVALID_ARG, "ff_hidden must be >= 0");
+  if (F < 0) return fail(FP_ERR_INVALID_ARG, "ff_hidden must be >= 0");
   if (heads < 0) return fail(FP_ERR_INVALID_ARG, "heads must be >= 0");
+  if (G < 0) return fail(FP_ERR_INVALID_ARG, "n_query_groups must be >= 0");
   if (heads > 0) {
-    if (head_dim <= 0 || head_dim % 2)
-      return fail(FP_ERR_INVALID_ARG, "head_dim must be even and > 0 (got %d)", head_dim);
-    if (static_cast<int64_t>(heads) * head_dim != C)
+    if (hd <= 0 || hd % 2)
+      return fail(FP_ERR_INVALID_ARG, "head_dim must be even and > 0 (got %d)", hd);
+    if (static_cast<int64_t>(heads) * hd != C)
       return fail(FP_ERR_INVALID_ARG, "heads * head_dim (%d * %d) must equal C (%d)", heads,
-                  head_dim, C);
-    if (ff_hidden % head_dim)
-      return fail(FP_ERR_INVALID_ARG, "ff_hidden (%d) must be a multiple of head_dim (%d)",
-                  ff_hidden, head_dim);
+                  hd, C);
+    if (F % hd)
+      return fail(FP_ERR_INVALID_ARG, "ff_hidden (%d) must be a multiple of head_dim (%d)", F,
+                  hd);
+    if (G > 0 && heads % G)
+      return fail(FP_ERR_INVALID_ARG, "heads (%d) must be a multiple of n_query_groups (%d)",
+                  heads, G);
+    if (ne < 0 || ne % 2 || ne > hd)
+      return fail(FP_ERR_INVALID_ARG, "rope_n_elem must be even and <= head_dim (got %d)", ne);
+  } else if (G > 0) {
+    return fail(FP_ERR_INVALID_ARG, "n_query_groups needs heads > 0");
   }
-  if (ff_hidden == 0 && heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
-  if (act < FP_ACT_NONE || act > FP_ACT_SILU) return fail(FP_ERR_INVALID_ARG, "unknown act");
-  if (rope_base > 0.0f && heads > 0) {
-    if (head_dim > 128)
-      return fail(FP_ERR_INVALID_ARG, "rotary embedding needs head_dim <= 128 (got %d)",
-                  head_dim);
-  }
+  if (F == 0 && heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
+  if (cfg->act < FP_ACT_NONE || cfg->act > FP_ACT_SILU)
+    return fail(FP_ERR_INVALID_ARG, "unknown act");
+  if (cfg->rope_base > 0.0f && heads > 0 && hd > 128)
+    return fail(FP_ERR_INVALID_ARG, "rotary embedding needs head_dim <= 128 (got %d)", hd);
   fp_plan* p = new (std::nothrow) fp_plan();
   if (!p) return fail(FP_ERR_OUT_OF_MEMORY, "host allocation failed");
   p->C = C;
-  p->F = ff_hidden;
+  p->F = F;
   p->heads = heads;
-  p->hd = heads > 0 ? head_dim : 0;
-  p->groups = 0;
-  p->rope_n_elem = 0;
-  p->act = act;
-  p->rope_base = rope_base;
+  p->hd = heads > 0 ? hd : 0;
+  p->groups = heads > 0 ? G : 0;
+  p->rope_n_elem = heads > 0 ? ne : 0;
+  p->act = cfg->act;
+  p->rope_base = cfg->rope_base;
   p->device = -1;
   p->d_status = nullptr;
   p->d_table = nullptr;
@@ -236,6 +244,12 @@ fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_di
   p->launch_seq = 0;
   *plan = p;
   return ok();
+}
+
+fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_dim, fp_act act,
+                    float rope_base) {
+  fp_config cfg{C, ff_hidden, heads, head_dim, 0, 0, static_cast<int32_t>(act), rope_base};
+  return fp_create_ex(plan, &cfg);
 }
 
 void fp_destroy(fp_plan* plan) {
@@ -360,7 +374,6 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   const int rh = rope_half_of(p);
   const int64_t c_stride = L.strides[L.channel_dim];
   const bool rope = rh > 0;
-  int bn_eff;
   fp::TokenMap tk{};
   tk.S_in = ta.S_in;
   tk.s_stride = ta.s_stride;
@@ -373,33 +386,31 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
     tk.n_outer *= ta.outer_size[i];
   }
 
-  const bool tc_path = L.dtype == FP_BF16;
+  // bf16 runs on the tensor-core kernel when its TMA maps and 16-column
+  // epilogue granules can describe the problem; otherwise (and for f32) on the
+  // FFMA kernel, which addresses any strides.
   bool a_mn = false;
+  bool tc_path = L.dtype == FP_BF16;
   if (tc_path) {
-    if (p->F % 16 || (p->heads > 0 && p->hd % 16))
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
-                  "bf16 path needs ff_hidden and head_dim multiples of 16 (F=%d, head_dim=%d)",
-                  p->F, p->hd);
-    if (rope && rh % 16)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
-                  "bf16 path needs rotated lanes / 2 to be a multiple of 16 (got %d)", rh);
-    if (tk.n_outer_dims > 3)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "bf16 path addresses at most 3 outer token axes");
+    if (p->F % 16 || (p->heads > 0 && p->hd % 16)) tc_path = false;
+    if (rope && rh % 16 && rh > 8) tc_path = false;
+    if (tk.n_outer_dims > 3) tc_path = false;
     if (tk.c_stride == 1) a_mn = false;
     else if (tk.s_stride == 1 || tk.S_in == 1) a_mn = true;
-    else
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
-                  "bf16 path needs unit stride on the channel axis or the innermost token axis");
+    else tc_path = false;
     const int64_t other = a_mn ? tk.c_stride : tk.s_stride;
-    if ((other * esz) % 16 && !(a_mn ? p->C == 1 : tk.S_in == 1))
-      return fail(FP_ERR_MISALIGNED, "non-unit x strides must be multiples of 16 bytes");
+    const bool other_unused = a_mn ? p->C == 1 : tk.S_in == 1;
+    if (!other_unused && (other * esz) % 16) tc_path = false;
     for (int i = 0; i < tk.n_outer_dims; ++i)
-      if ((tk.outer_stride[i] * esz) % 16)
-        return fail(FP_ERR_MISALIGNED, "non-unit x strides must be multiples of 16 bytes");
+      if ((tk.outer_stride[i] * esz) % 16) tc_path = false;
+  }
+  int bn_eff;
+  if (tc_path) {
     bn_eff = rope ? (fp::kTcBN / p->hd) * p->hd : fp::kTcBN;
   } else {
     if (tk.n_outer_dims > fp::kMaxOuter)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "too many non-mergeable token axes");
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "x has more than %d non-mergeable token axes",
+                  fp::kMaxOuter);
     bn_eff = rope ? (fp::kSimtBN / p->hd) * p->hd : fp::kSimtBN;
   }
 
@@ -524,15 +535,15 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   } else {
     fp::SimtParams sp;
     memset(&sp, 0, sizeof sp);
-    sp.x = static_cast<const float*>(x);
-    sp.W = static_cast<const float*>(W);
+    sp.x = x;
+    sp.W = W;
     sp.tok = tk;
     sp.epi = e;
     sp.C = p->C;
     sp.m_tiles_per_slab = (ta.S_in + fp::kSimtBM - 1) / fp::kSimtBM;
     sp.num_m_tiles = tk.n_outer * sp.m_tiles_per_slab;
     sp.num_n_tiles = num_n_tiles;
-    cudaError_t err = fp::launch_simt_gemm(sp, stream);
+    cudaError_t err = fp::launch_simt_gemm(sp, L.dtype == FP_BF16, stream);
     if (err != cudaSuccess)
       return fail(FP_ERR_CUDA, "FFMA GEMM launch: %s", cudaGetErrorString(err));
     ++launches;

@@ -62,8 +62,8 @@ struct TcParams {
 };
 
 struct SimtParams {
-  const float* x;
-  const float* W;
+  const void* x;  // float, or bf16 bits
+  const void* W;
   TokenMap tok;
   Epilogue epi;
   int C;
@@ -76,7 +76,7 @@ struct SimtParams {
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
                               double rope_base, cudaStream_t stream);
 cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream);
-cudaError_t launch_simt_gemm(const SimtParams& p, cudaStream_t stream);
+cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream);
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kSimtBM = 128, kSimtBN = 128;

@@ -1,10 +1,14 @@
-// fp32 fused projection on the FFMA pipes (TF32 off).
+// Fused projection on the FFMA pipes (TF32 off).
 //
 // The fp32 leg of the projection: activations and weight stay fp32 and every
 // product is an fp32 FFMA, so results do not depend on whether TF32 matmul is
 // enabled (the fp32-vs-TF32 ambiguity raised in xformers PR #283 "[perf] Fused
 // linear", last comments). x is read in place through its strides, as in
-// Walrus PR #12 "Make fused_ff_qkv contiguous" (no permuted copy).
+// Walrus PR #12 "Make fused_ff_qkv contiguous" (no permuted copy). The same
+// kernel, instantiated for bf16 storage (widened to fp32 on load, rounded once
+// at the store), serves bf16 activations whose strides a TMA map cannot
+// describe (e.g. an odd spatial extent) or whose block widths are not
+// multiples of 16.
 //
 // Tile: 128 tokens x 128 fused columns, k-steps of 16, 256 threads with an
 // 8x8 register block each (rows ty*4+{0..3} and 64+ty*4+{0..3}, columns
@@ -40,8 +44,27 @@ __device__ __forceinline__ int64_t outer_offset(const TokenMap& tk, int64_t o) {
 // K_MAJOR: unit channel stride, so a thread walks channels (16 consecutive
 // channels of one token per k-step); otherwise a thread keeps one token and
 // walks channels at their stride (coalesced when tokens are unit-stride).
-template <bool K_MAJOR>
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p, int64_t i) {
+  return __ldg(p + i);
+}
+template <>
+__device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t* p, int64_t i) {
+  return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
+}
+__device__ __forceinline__ void st_elem(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elem(uint16_t* p, int64_t i, float v) {
+  __nv_bfloat16 h = __float2bfloat16_rn(v);
+  p[i] = *reinterpret_cast<uint16_t*>(&h);
+}
+
+// T: storage type of x, W, b and the outputs (float, or uint16_t bf16 bits).
+template <typename T, bool K_MAJOR>
 __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
+  const T* X = static_cast<const T*>(p.x);
+  const T* Wt = static_cast<const T*>(p.W);
   extern __shared__ __align__(16) float smem[];
   float* As = smem;                // [2][BK][BM]
   float* Bs = smem + 2 * BK * BM;  // [2][BK][BN]
@@ -73,7 +96,7 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
       const int dm = K_MAJOR ? 16 * i : 0;
       const int k = k0 + a_k0 + (K_MAJOR ? 0 : 2 * i);
       const bool okr = dm < rows_left && k < C;
-      a_reg[i] = okr ? __ldg(p.x + a_base + dm * tk.s_stride + static_cast<int64_t>(k) * tk.c_stride)
+      a_reg[i] = okr ? ld_elem(X, a_base + dm * tk.s_stride + static_cast<int64_t>(k) * tk.c_stride)
                      : 0.0f;
     }
 #pragma unroll
@@ -81,7 +104,7 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
       int idx = tid + i * NT;
       int n = idx % BN, k = k0 + idx / BN;
       int col = n0 + n;
-      b_reg[i] = (k < C && col < N) ? __ldg(p.W + static_cast<int64_t>(k) * N + col) : 0.0f;
+      b_reg[i] = (k < C && col < N) ? ld_elem(Wt, static_cast<int64_t>(k) * N + col) : 0.0f;
     }
   };
   auto store_regs = [&](int buf) {
@@ -145,7 +168,7 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
   __syncthreads();
 
   const Epilogue& e = p.epi;
-  const float* bias = static_cast<const float*>(e.bias);
+  const T* bias = static_cast<const T*>(e.bias);
   const int half = e.rope_half;
   for (int idx = tid; idx < BM * BN; idx += NT) {
     const int r = idx / BN, c = idx % BN;
@@ -154,7 +177,7 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
     if (c >= e.bn_eff || n >= N || s >= S_in) continue;
     const int64_t m = o * S_in + s;
     const int64_t bb = m / e.T, t = m - bb * e.T;
-    float v = Cs[r * CS_LD + c] + (bias ? bias[n] : 0.0f);
+    float v = Cs[r * CS_LD + c] + (bias ? ld_elem(bias, n) : 0.0f);
     ColInfo ci = decode_col(e, n);
     if (ci.seg == 0) {
       v = activate(e.act, v);
@@ -163,38 +186,42 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
       const int f = lo ? ci.j : ci.j - half;
       const int pc = lo ? c + half : c - half;
       const int pn = lo ? n + half : n - half;
-      float pv = Cs[r * CS_LD + pc] + (bias ? bias[pn] : 0.0f);
+      float pv = Cs[r * CS_LD + pc] + (bias ? ld_elem(bias, pn) : 0.0f);
       float2 cs = e.rope_cs[t * half + f];
       // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
       v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
     }
-    static_cast<float*>(out_base(e, ci.seg))[out_offset(e, ci, m, bb, t)] = v;
+    st_elem(static_cast<T*>(out_base(e, ci.seg)), out_offset(e, ci, m, bb, t), v);
   }
 }
 
-}  // namespace
-
-cudaError_t launch_simt_gemm(const SimtParams& p, cudaStream_t stream) {
+template <typename T, bool K_MAJOR>
+cudaError_t launch_one(const SimtParams& p, int64_t tiles, cudaStream_t stream) {
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
-    err = cudaFuncSetAttribute(simt_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(simt_gemm_kernel<false>,
+    err = cudaFuncSetAttribute(simt_gemm_kernel<T, K_MAJOR>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
+  simt_gemm_kernel<T, K_MAJOR><<<static_cast<unsigned>(tiles), NT, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream) {
   int64_t tiles = p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
-  if (p.tok.c_stride == 1)
-    simt_gemm_kernel<true><<<static_cast<unsigned>(tiles), NT, kSmemBytes, stream>>>(p);
-  else
-    simt_gemm_kernel<false><<<static_cast<unsigned>(tiles), NT, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  const bool k_major = p.tok.c_stride == 1;
+  if (bf16)
+    return k_major ? launch_one<uint16_t, true>(p, tiles, stream)
+                   : launch_one<uint16_t, false>(p, tiles, stream);
+  return k_major ? launch_one<float, true>(p, tiles, stream)
+                 : launch_one<float, false>(p, tiles, stream);
 }
 
 }  // namespace fp

@@ -279,6 +279,34 @@ __device__ __forceinline__ void store16_bf16(void* dst, const float (&v)[16]) {
   d[1] = b;
 }
 
+// Rotation of lanes [0, 2*RH) of a head held in one 16-column granule (partial
+// rotary, rope_n_elem = 2*RH <= 16): pair (i, i + RH) with (cos, sin) of
+// frequency i.
+template <int RH>
+__device__ __forceinline__ void rotate_in_granule(float (&v)[16], const float2* __restrict__ cs) {
+#pragma unroll
+  for (int i = 0; i < RH; ++i) {
+    const float2 c = __ldg(cs + i);
+    const float x = v[i], y = v[i + RH];
+    v[i] = x * c.x - y * c.y;
+    v[i + RH] = y * c.x + x * c.y;
+  }
+}
+
+__device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, int rh) {
+  switch (rh) {
+    case 1: rotate_in_granule<1>(v, cs); break;
+    case 2: rotate_in_granule<2>(v, cs); break;
+    case 3: rotate_in_granule<3>(v, cs); break;
+    case 4: rotate_in_granule<4>(v, cs); break;
+    case 5: rotate_in_granule<5>(v, cs); break;
+    case 6: rotate_in_granule<6>(v, cs); break;
+    case 7: rotate_in_granule<7>(v, cs); break;
+    case 8: rotate_in_granule<8>(v, cs); break;
+    default: break;
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <bool A_MN_MAJOR>
@@ -450,7 +478,11 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         const int n = tc.n0 + c;
         if (c >= e.bn_eff || n >= e.N) break;
         const ColInfo ci = decode_col(e, n);
-        const bool rope = rh > 0 && (ci.seg == 1 || ci.seg == 2) && ci.j < 2 * rh;
+        const bool qk = ci.seg == 1 || ci.seg == 2;
+        // rh >= 16: lanes i and i+rh sit in different granules, handled as a pair;
+        // rh <= 8: every rotated lane sits in the head's first granule.
+        const bool rope = rh >= 16 && qk && ci.j < 2 * rh;
+        const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
         if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
         if ((unit++ & 1) != half_id) continue;
         float bl[16];
@@ -495,6 +527,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             } else {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bl[i];
+              if (rope_small) rotate_small(v, e.rope_cs + t * rh, rh);
             }
             char* base = static_cast<char*>(out_base(e, ci.seg));
             store16_bf16(base + 2 * out_offset(e, ci, m, bidx, t), v);

@@ -151,6 +151,11 @@ WORKLOADS: Dict[str, Workload] = {
                               ACT_NONE, 0.0, False, "bf16", 4),
     "unet_qkv_fp32": Workload("unet_qkv_fp32", (2, 320, 64, 64), 1, 1, 320, 0, 5, 64,
                               ACT_NONE, 0.0, False, "f32", 4),
+    # grouped-query QKV split + partial rotary of the RoPE fusion issue's toy
+    # config: x [2, 1024, 512], 16 heads x 32, 4 query groups, 8 rotated lanes
+    "gqa_rope_toy_bf16": Workload("gqa_rope_toy_bf16", (2, 1024, 512), 2, 1, 512, 0, 16, 32,
+                                  ACT_NONE, 10000.0, False, "bf16", 5, rope_n_elem=8,
+                                  n_query_groups=4),
 }
 
 

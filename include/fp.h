@@ -105,18 +105,47 @@ fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_di
                     float rope_base);
 
 /*
+ * fp_create_ex — fp_create with the grouped-query column order and partial
+ * rotary of the split_qkv / rope_one_entry listings (nvFuser issue #1597).
+ *   n_query_groups  0: as fp_create. > 0: the q|k|v part of W's columns is
+ *                   [group][q_per_kv query heads | 1 key head | 1 value head]
+ *                   x head_dim, q_per_kv = heads / n_query_groups;
+ *                   N = F + (heads + 2*n_query_groups) * head_dim, and out_k /
+ *                   out_v are [B*n_query_groups, T, head_dim] (one head per group;
+ *                   the listing's expand over q_per_kv is a broadcast, not data).
+ *   rope_n_elem     0: rotate the whole head. Else an even count <= head_dim:
+ *                   lanes [0, rope_n_elem) rotate with theta_i = pos *
+ *                   base^(-2i/rope_n_elem), pairs (i, i + rope_n_elem/2); the
+ *                   other lanes pass through.
+ */
+typedef struct {
+  int32_t C;
+  int32_t ff_hidden;
+  int32_t heads;
+  int32_t head_dim;
+  int32_t n_query_groups;
+  int32_t rope_n_elem;
+  int32_t act; /* fp_act */
+  float rope_base;
+} fp_config;
+
+fp_status fp_create_ex(fp_plan** plan, const fp_config* config);
+
+/*
  * fp_forward — enqueue one fused projection on `stream`.
  *   x        device pointer to element (0, ..., 0) of the activation; layout `x_layout`
  *   W        [C, N] row-major, dtype of x
  *   b        [N] or NULL (no bias), dtype of x
  *   pos      int32 [T] rotary positions, or NULL for 0 .. T-1 (ignored without rope)
  *   out_ff   [B*T, F] row-major, or NULL when F == 0
- *   out_q, out_k, out_v   [B*heads, T, head_dim] each, or NULL when heads == 0
+ *   out_q, out_k, out_v   [B*heads, T, head_dim] each (k, v: [B*n_query_groups, T,
+ *            head_dim] with grouped-query columns), or NULL when heads == 0
  * All pointers must be 16-byte aligned. Outputs may not overlap each other or
- * any input. bf16 activations run on the tcgen05 tensor-core kernel, which
- * needs unit stride on the channel axis or on the innermost token axis and
- * 16-byte-multiple other strides; f32 activations run on the FFMA kernel
- * (TF32 off), which takes any strides.
+ * any input. bf16 activations run on the tcgen05 tensor-core kernel when x has
+ * unit stride on the channel axis or on its innermost token axis, its other
+ * strides are 16-byte multiples, ff_hidden and head_dim are multiples of 16 and
+ * the rotated half-width is a multiple of 16 (or 1, 2, 4, 8); otherwise, and
+ * for f32, the FFMA kernel runs (TF32 off; any strides).
  * Rotary table: with pos == NULL the (cos, sin) table is a constant of the
  * plan and T; it is built by the first such call and reused by later ones
  * (calls on another stream are ordered after that build with an event).

@@ -28,7 +28,8 @@ def run(w: fpsynth.Workload, inp: Dict[str, np.ndarray], x_dev: Optional[torch.T
         proj: Optional[fpx.FusedProjection] = None, pos: Optional[np.ndarray] = None):
     """Run the library on workload ``w``. ``x_dev`` may be a strided view to read in place."""
     if proj is None:
-        proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+        proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                                   w.n_query_groups, w.rope_n_elem)
     x = to_device(inp["x"], w.dtype) if x_dev is None else x_dev
     W = to_device(inp["W"], w.dtype)
     b = to_device(inp["b"], w.dtype)

@@ -91,21 +91,34 @@ def test_forward_rejects_on_host(lib):
     L3 = _cf_layout()
     L3.dtype = 5
     assert fwd(L=L3) == fpx.FP_ERR_INVALID_ARG
-    # bf16 tensor-core path: no unit stride on channels or innermost tokens
-    L4 = fpx.make_layout([2, 64, 8, 8], [64 * 8 * 8 * 2, 2, 64 * 8 * 2, 64 * 2], 1, 1, fpx.FP_BF16)
-    assert fwd(L=L4) == fpx.FP_ERR_UNSUPPORTED_LAYOUT
-    # bf16 channels-first with a channel stride that is not a 16-byte multiple
-    L5 = fpx.make_layout([2, 64, 5, 7], [64 * 35, 35, 7, 1], 1, 1, fpx.FP_BF16)
-    assert fwd(L=L5) == fpx.FP_ERR_MISALIGNED
+    L4 = _cf_layout()
+    L4.sizes[2] = -1
+    assert fwd(L=L4) == fpx.FP_ERR_INVALID_ARG
+    L5 = _cf_layout()
+    L5.n_batch_dims = 4
+    assert fwd(L=L5) == fpx.FP_ERR_INVALID_ARG
     fpx.fp_destroy(h)
 
 
-def test_forward_bf16_granularity(lib):
-    # F not a multiple of 16 is fine for f32 but not for the bf16 tensor-core path
-    h = _plan(C=8, F=8, heads=1, hd=8, act=0)
-    L = fpx.make_layout([1, 16, 8], [128, 8, 1], 2, 1, fpx.FP_BF16)
-    assert fpx.fp_forward(h, X, L, WP, None, None, O1, O2, O3, O4, None) == \
-        fpx.FP_ERR_UNSUPPORTED_LAYOUT
+@pytest.mark.parametrize("kw", [
+    dict(n_query_groups=3),                 # heads % groups
+    dict(rope_n_elem=5),                    # odd
+    dict(rope_n_elem=20),                   # > head_dim
+    dict(n_query_groups=-1),
+])
+def test_create_ex_rejects(lib, kw):
+    base = dict(C=64, ff_hidden=0, heads=4, head_dim=16, n_query_groups=2, rope_n_elem=0,
+                act=0, rope_base=10000.0)
+    base.update(kw)
+    st, h = fpx.fp_create_ex(fpx.fp_config(**base))
+    assert st == fpx.FP_ERR_INVALID_ARG and h is None
+
+
+def test_create_ex_grouped_query(lib):
+    cfg = fpx.fp_config(C=512, ff_hidden=0, heads=16, head_dim=32, n_query_groups=4,
+                        rope_n_elem=8, act=0, rope_base=10000.0)
+    st, h = fpx.fp_create_ex(cfg)
+    assert st == fpx.FP_OK
     fpx.fp_destroy(h)
 
 

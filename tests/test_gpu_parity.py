@@ -40,6 +40,17 @@ SMALL = [
     W_("fp32_rowmajor", (3, 50, 48), 2, 1, 48, 96, 3, 16, A.ACT_GELU_ERF, 10000.0, True, "f32", 32),
     W_("one_token", (1, 1, 64), 2, 1, 64, 64, 1, 64, A.ACT_GELU_ERF, 10000.0, True, "bf16", 33),
     W_("k_tail_c48", (2, 70, 48), 2, 1, 48, 0, 1, 48, A.ACT_NONE, 0.0, True, "bf16", 34),
+    # bf16 shapes the TMA path cannot describe run on the FFMA kernel
+    W_("bf16_odd_spatial", (2, 64, 5, 7), 1, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 10000.0, True,
+       "bf16", 40),
+    W_("bf16_hd16_rope", (2, 3, 32, 8, 8, 1), 2, 1, 32, 64, 2, 16, A.ACT_GELU_TANH, 10000.0, True,
+       "bf16", 41),
+    # grouped-query columns + partial rotary
+    A.WORKLOADS["gqa_rope_toy_bf16"],
+    W_("gqa_fp32", (2, 40, 48), 2, 1, 48, 0, 4, 12, A.ACT_NONE, 10000.0, True, "f32", 43,
+       rope_n_elem=8, n_query_groups=2),
+    W_("gqa_bf16_full_rope", (2, 200, 256), 2, 1, 256, 0, 4, 64, A.ACT_NONE, 10000.0, True, "bf16",
+       44, n_query_groups=2),
 ]
 
 
