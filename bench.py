@@ -222,6 +222,7 @@ def main():
     import torch
     import ff_input_projection_gb300 as fpx
     from ff_input_projection_gb300 import _build
+    from ff_input_projection_gb300.shard import max_over_ranks
     _build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -284,10 +285,7 @@ def main():
         dist.barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
     fpx.check(proj.device_status(stream.cuda_stream))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     total_flops = flops * world
     value = total_flops / (ms * 1e-3) / 1e12
     tokens_per_s = w.M * world / (ms * 1e-3)
@@ -321,10 +319,7 @@ def main():
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     pk, pk_src = peaks()
     tensor_time = flops / (pk["bf16_tflops"] * 1e12)

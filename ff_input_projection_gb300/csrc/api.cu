@@ -10,7 +10,6 @@
 #include <cstring>
 #include <mutex>
 #include <new>
-#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -90,7 +89,8 @@ int sm_count(int dev) {
 // Token axes after dropping unit axes and merging contiguous neighbours.
 struct TokAxes {
   int64_t S_in = 1, s_stride = 1;
-  std::vector<int64_t> outer_size, outer_stride;  // innermost first
+  int n_outer = 0;
+  int64_t outer_size[FP_MAX_DIMS], outer_stride[FP_MAX_DIMS];  // innermost first
   int64_t Bb = 1, T = 1, M = 1;
 };
 
@@ -105,20 +105,29 @@ TokAxes analyse_tokens(const fp_layout& L) {
   }
   ta.M = ta.Bb * ta.T;
   // innermost-first list of (size, stride) groups
-  std::vector<std::pair<int64_t, int64_t>> g;
+  int64_t gs[FP_MAX_DIMS], gt[FP_MAX_DIMS];
+  int ng = 0;
   for (int a = L.ndim - 1; a >= 0; --a) {
     if (a == L.channel_dim || L.sizes[a] == 1) continue;
-    if (!g.empty() && L.strides[a] == g.back().second * g.back().first)
-      g.back().first *= L.sizes[a];
-    else
-      g.push_back({L.sizes[a], L.strides[a]});
+    if (ng > 0 && L.strides[a] == gt[ng - 1] * gs[ng - 1]) {
+      gs[ng - 1] *= L.sizes[a];
+    } else {
+      gs[ng] = L.sizes[a];
+      gt[ng] = L.strides[a];
+      ++ng;
+    }
   }
-  if (g.empty()) g.push_back({1, 1});
-  ta.S_in = g[0].first;
-  ta.s_stride = g[0].second;
-  for (size_t i = 1; i < g.size(); ++i) {
-    ta.outer_size.push_back(g[i].first);
-    ta.outer_stride.push_back(g[i].second);
+  if (ng == 0) {
+    gs[0] = 1;
+    gt[0] = 1;
+    ng = 1;
+  }
+  ta.S_in = gs[0];
+  ta.s_stride = gt[0];
+  ta.n_outer = ng - 1;
+  for (int i = 1; i < ng; ++i) {
+    ta.outer_size[i - 1] = gs[i];
+    ta.outer_stride[i - 1] = gt[i];
   }
   return ta;
 }
@@ -165,6 +174,271 @@ int rope_half_of(const fp_plan* p) {
 int n_total(const fp_plan* p) {
   if (p->groups > 0) return p->F + (p->heads + 2 * p->groups) * p->hd;
   return p->F + 3 * p->heads * p->hd;
+}
+
+}  // namespace
+
+namespace {
+
+// Caller arguments of one forward call.
+struct Args {
+  const void* x;
+  const fp_layout* xl;
+  const void* W;
+  const void* b;
+  const int32_t* pos;
+  void* out_ff;
+  void* out_q;
+  void* out_k;
+  void* out_v;
+};
+
+// Result of the host-side checks: the token map and the kernel to run.
+struct Prepared {
+  fp_layout L;
+  TokAxes ta;
+  fp::TokenMap tk;
+  int esz = 2, N = 0, rh = 0, bn_eff = 0;
+  bool rope = false, tc_path = false, a_mn = false;
+};
+
+// Device scratch and launch knobs a launch uses.
+struct Scratch {
+  int* status;     // [2]
+  float2* table;   // >= T * rh entries when rope
+  int device;
+  int launch_tag;  // >= 1
+  uint64_t wait_limit_ns;
+  int inject_stall;
+  int group_m;
+  int max_ctas;
+};
+
+// Every check of a forward call; touches no GPU.
+fp_status prepare(const fp_plan& P, const Args& a, Prepared& pr) {
+  const fp_plan* p = &P;
+  if (!a.xl) return fail(FP_ERR_INVALID_ARG, "x_layout is NULL");
+  const fp_layout L = *a.xl;
+  pr.L = L;
+  if (L.dtype != FP_BF16 && L.dtype != FP_F32) return fail(FP_ERR_INVALID_ARG, "unknown dtype");
+  if (L.ndim < 1 || L.ndim > FP_MAX_DIMS) return fail(FP_ERR_INVALID_ARG, "ndim out of range");
+  if (L.channel_dim < 0 || L.channel_dim >= L.ndim)
+    return fail(FP_ERR_INVALID_ARG, "channel_dim out of range");
+  if (L.n_batch_dims < 0 || L.n_batch_dims > L.ndim - 1)
+    return fail(FP_ERR_INVALID_ARG, "n_batch_dims out of range");
+  for (int d = 0; d < L.ndim; ++d)
+    if (L.sizes[d] < 0 || L.strides[d] < 0)
+      return fail(FP_ERR_INVALID_ARG, "negative size or stride on axis %d", d);
+  if (L.sizes[L.channel_dim] != p->C)
+    return fail(FP_ERR_INVALID_ARG, "x has %lld channels, plan has C = %d",
+                static_cast<long long>(L.sizes[L.channel_dim]), p->C);
+  const int esz = L.dtype == FP_BF16 ? 2 : 4;
+  const int N = n_total(p);
+  const int nkv = p->groups > 0 ? p->groups : p->heads;
+  pr.esz = esz;
+  pr.N = N;
+  pr.ta = analyse_tokens(L);
+  const TokAxes& ta = pr.ta;
+  if (ta.M == 0) return FP_OK;
+  if (!a.x || !a.W) return fail(FP_ERR_INVALID_ARG, "x and W must be non-NULL");
+  if ((p->F > 0) != (a.out_ff != nullptr))
+    return fail(FP_ERR_INVALID_ARG, "out_ff must be non-NULL exactly when ff_hidden > 0");
+  const bool want_qkv = p->heads > 0;
+  if (want_qkv != (a.out_q != nullptr) || want_qkv != (a.out_k != nullptr) ||
+      want_qkv != (a.out_v != nullptr))
+    return fail(FP_ERR_INVALID_ARG, "out_q/out_k/out_v must be non-NULL exactly when heads > 0");
+  const void* ptrs[] = {a.x, a.W, a.b, a.pos, a.out_ff, a.out_q, a.out_k, a.out_v};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
+  // aliasing: outputs against each other and against every input
+  int64_t x_span = 1;
+  for (int d = 0; d < L.ndim; ++d) x_span += (L.sizes[d] - 1) * L.strides[d];
+  auto rng = [](const void* q, int64_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(q);
+    return Range{lo, q ? lo + static_cast<uintptr_t>(bytes) : lo};
+  };
+  const Range ins[] = {rng(a.x, x_span * esz), rng(a.W, static_cast<int64_t>(p->C) * N * esz),
+                       rng(a.b, static_cast<int64_t>(N) * esz),
+                       rng(a.pos, static_cast<int64_t>(ta.T) * 4)};
+  const Range outs[] = {rng(a.out_ff, ta.M * p->F * esz),
+                        rng(a.out_q, ta.M * p->heads * p->hd * esz),
+                        rng(a.out_k, ta.M * nkv * p->hd * esz),
+                        rng(a.out_v, ta.M * nkv * p->hd * esz)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], outs[j])) return fail(FP_ERR_INVALID_ARG, "output buffers overlap");
+    for (const Range& in : ins)
+      if (overlaps(outs[i], in)) return fail(FP_ERR_INVALID_ARG, "an output overlaps an input");
+  }
+  const int rh = rope_half_of(p);
+  const bool rope = rh > 0;
+  pr.rh = rh;
+  pr.rope = rope;
+  fp::TokenMap& tk = pr.tk;
+  tk = fp::TokenMap{};
+  tk.S_in = ta.S_in;
+  tk.s_stride = ta.s_stride;
+  tk.c_stride = p->C == 1 ? 1 : L.strides[L.channel_dim];
+  tk.n_outer = 1;
+  tk.n_outer_dims = ta.n_outer;
+  if (tk.n_outer_dims > fp::kMaxOuter)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "x has more than %d non-mergeable token axes",
+                fp::kMaxOuter);
+  for (int i = 0; i < tk.n_outer_dims; ++i) {
+    tk.outer_size[i] = ta.outer_size[i];
+    tk.outer_stride[i] = ta.outer_stride[i];
+    tk.n_outer *= ta.outer_size[i];
+  }
+  // bf16 runs on the tensor-core kernel when its TMA maps and 16-column
+  // epilogue granules can describe the problem; otherwise (and for f32) on the
+  // FFMA kernel, which addresses any strides.
+  bool a_mn = false;
+  bool tc_path = L.dtype == FP_BF16;
+  if (tc_path) {
+    if (p->F % 16 || (p->heads > 0 && p->hd % 16)) tc_path = false;
+    if (rope && rh % 16 && rh > 8) tc_path = false;
+    if (tk.n_outer_dims > 3) tc_path = false;
+    if (tk.c_stride == 1) a_mn = false;
+    else if (tk.s_stride == 1 || tk.S_in == 1) a_mn = true;
+    else tc_path = false;
+    const int64_t other = a_mn ? tk.c_stride : tk.s_stride;
+    const bool other_unused = a_mn ? p->C == 1 : tk.S_in == 1;
+    if (!other_unused && (other * esz) % 16) tc_path = false;
+    for (int i = 0; i < tk.n_outer_dims; ++i)
+      if ((tk.outer_stride[i] * esz) % 16) tc_path = false;
+  }
+  pr.tc_path = tc_path;
+  pr.a_mn = a_mn;
+  if (tc_path)
+    pr.bn_eff = rope ? (fp::kTcBN / p->hd) * p->hd : fp::kTcBN;
+  else
+    pr.bn_eff = rope ? (fp::kSimtBN / p->hd) * p->hd : fp::kSimtBN;
+  return FP_OK;
+}
+
+// Enqueue the rotary table (when build_table) and the GEMM kernel on `stream`.
+// Uses only the scratch it is given; allocates nothing.
+fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scratch& sc,
+                 bool build_table, cudaStream_t stream, int* launches) {
+  const fp_plan* p = &P;
+  const TokAxes& ta = pr.ta;
+  const fp::TokenMap& tk = pr.tk;
+  const int N = pr.N, esz = pr.esz, rh = pr.rh, bn_eff = pr.bn_eff;
+  *launches = 0;
+  if (build_table) {
+    cudaError_t err = fp::launch_rope_table(sc.table, a.pos, ta.T, rh, 2 * rh,
+                                            static_cast<double>(p->rope_base), stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "rotary table launch: %s", cudaGetErrorString(err));
+    ++*launches;
+  }
+  fp::Epilogue e{};
+  e.M = ta.M;
+  e.T = ta.T;
+  e.N = N;
+  e.F = p->F;
+  e.C = p->C;
+  e.heads = p->heads;
+  e.hd = p->hd;
+  e.groups = p->groups;
+  e.act = p->act;
+  e.rope_half = rh;
+  e.rope_cs = pr.rope ? sc.table : nullptr;
+  e.bias = a.b;
+  e.out_ff = a.out_ff;
+  e.out_q = a.out_q;
+  e.out_k = a.out_k;
+  e.out_v = a.out_v;
+  e.status = sc.status;
+  e.bn_eff = bn_eff;
+  const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
+
+  if (pr.tc_path) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+    if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    fp::TcParams tp;
+    memset(&tp, 0, sizeof tp);
+    // A: 5-D map [inner, second, outer0, outer1, outer2]
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
+    if (pr.a_mn) {
+      gdim[0] = ta.S_in;
+      gdim[1] = p->C;
+      gstride[0] = static_cast<cuuint64_t>(tk.c_stride) * esz;
+      box[0] = 64;
+      box[1] = fp::kTcBK;
+    } else {
+      gdim[0] = p->C;
+      gdim[1] = ta.S_in;
+      gstride[0] = static_cast<cuuint64_t>(tk.s_stride) * esz;
+      box[0] = fp::kTcBK;
+      box[1] = fp::kTcBM;
+    }
+    // a unit-extent second axis may carry any stride: give TMA a valid one
+    if (gstride[0] == 0 || gstride[0] % 16) gstride[0] = 16 * ((gdim[0] * esz + 15) / 16);
+    cuuint64_t last = gstride[0];
+    for (int d = 0; d < 3; ++d) {
+      if (d < tk.n_outer_dims) {
+        gdim[2 + d] = tk.outer_size[d];
+        gstride[1 + d] = static_cast<cuuint64_t>(tk.outer_stride[d]) * esz;
+        last = gstride[1 + d];
+      } else {
+        gdim[2 + d] = 1;
+        gstride[1 + d] = last;
+      }
+      box[2 + d] = 1;
+    }
+    CUresult r = encode(&tp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a.x),
+                        gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for x rejected (CUresult %d)",
+                  static_cast<int>(r));
+    cuuint64_t bdim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(p->C)};
+    cuuint64_t bstride[1] = {static_cast<cuuint64_t>(N) * esz};
+    cuuint32_t bbox[2] = {64, fp::kTcBK};
+    r = encode(&tp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), bdim,
+               bstride, bbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
+                  static_cast<int>(r));
+    tp.tok = tk;
+    tp.epi = e;
+    tp.C = p->C;
+    tp.num_k_blocks = (p->C + fp::kTcBK - 1) / fp::kTcBK;
+    tp.m_tiles_per_slab = (ta.S_in + fp::kTcBM - 1) / fp::kTcBM;
+    tp.num_m_tiles = tk.n_outer * tp.m_tiles_per_slab;
+    tp.num_n_tiles = num_n_tiles;
+    tp.num_tiles = tp.num_m_tiles * num_n_tiles;
+    tp.group_m = sc.group_m;
+    tp.wait_limit_ns = sc.wait_limit_ns;
+    tp.inject_stall = sc.inject_stall;
+    tp.launch_tag = sc.launch_tag;
+    int ctas = sm_count(sc.device);
+    if (sc.max_ctas > 0) ctas = std::min(ctas, sc.max_ctas);
+    if (static_cast<int64_t>(ctas) > tp.num_tiles) ctas = static_cast<int>(tp.num_tiles);
+    cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, ctas, stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(err));
+  } else {
+    fp::SimtParams sp;
+    memset(&sp, 0, sizeof sp);
+    sp.x = a.x;
+    sp.W = a.W;
+    sp.tok = tk;
+    sp.epi = e;
+    sp.C = p->C;
+    sp.m_tiles_per_slab = (ta.S_in + fp::kSimtBM - 1) / fp::kSimtBM;
+    sp.num_m_tiles = tk.n_outer * sp.m_tiles_per_slab;
+    sp.num_n_tiles = num_n_tiles;
+    cudaError_t err = fp::launch_simt_gemm(sp, pr.L.dtype == FP_BF16, stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "FFMA GEMM launch: %s", cudaGetErrorString(err));
+  }
+  ++*launches;
+  return FP_OK;
 }
 
 }  // namespace
@@ -318,235 +592,42 @@ fp_status fp_get_device_status(fp_plan* plan, void* stream) {
 fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
                      const int32_t* pos, void* out_ff, void* out_q, void* out_k, void* out_v,
                      void* stream_v) {
-  // ---------------------------------------------------------------- host checks
   if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
-  if (!xl) return fail(FP_ERR_INVALID_ARG, "x_layout is NULL");
-  const fp_layout L = *xl;
-  if (L.dtype != FP_BF16 && L.dtype != FP_F32) return fail(FP_ERR_INVALID_ARG, "unknown dtype");
-  if (L.ndim < 1 || L.ndim > FP_MAX_DIMS) return fail(FP_ERR_INVALID_ARG, "ndim out of range");
-  if (L.channel_dim < 0 || L.channel_dim >= L.ndim)
-    return fail(FP_ERR_INVALID_ARG, "channel_dim out of range");
-  if (L.n_batch_dims < 0 || L.n_batch_dims > L.ndim - 1)
-    return fail(FP_ERR_INVALID_ARG, "n_batch_dims out of range");
-  for (int a = 0; a < L.ndim; ++a)
-    if (L.sizes[a] < 0 || L.strides[a] < 0)
-      return fail(FP_ERR_INVALID_ARG, "negative size or stride on axis %d", a);
-  if (L.sizes[L.channel_dim] != p->C)
-    return fail(FP_ERR_INVALID_ARG, "x has %lld channels, plan has C = %d",
-                static_cast<long long>(L.sizes[L.channel_dim]), p->C);
-  const int esz = L.dtype == FP_BF16 ? 2 : 4;
-  const int N = n_total(p);
-  const int nkv = p->groups > 0 ? p->groups : p->heads;
-  TokAxes ta = analyse_tokens(L);
-  if (ta.M == 0) {
+  const Args a{x, xl, W, b, pos, out_ff, out_q, out_k, out_v};
+  Prepared pr;
+  fp_status st = prepare(*p, a, pr);
+  if (st != FP_OK) return st;
+  if (pr.ta.M == 0) {
     p->last_launches = 0;
     return ok();  // no tokens: nothing to do
   }
-  if (!x || !W) return fail(FP_ERR_INVALID_ARG, "x and W must be non-NULL");
-  if ((p->F > 0) != (out_ff != nullptr))
-    return fail(FP_ERR_INVALID_ARG, "out_ff must be non-NULL exactly when ff_hidden > 0");
-  const bool want_qkv = p->heads > 0;
-  if (want_qkv != (out_q != nullptr) || want_qkv != (out_k != nullptr) ||
-      want_qkv != (out_v != nullptr))
-    return fail(FP_ERR_INVALID_ARG, "out_q/out_k/out_v must be non-NULL exactly when heads > 0");
-  const void* ptrs[] = {x, W, b, pos, out_ff, out_q, out_k, out_v};
-  for (const void* q : ptrs)
-    if (q && !aligned16(q)) return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
-  // aliasing: outputs against each other and against every input
-  int64_t x_span = 1;
-  for (int a = 0; a < L.ndim; ++a) x_span += (L.sizes[a] - 1) * L.strides[a];
-  auto rng = [](const void* q, int64_t bytes) {
-    uintptr_t lo = reinterpret_cast<uintptr_t>(q);
-    return Range{lo, q ? lo + static_cast<uintptr_t>(bytes) : lo};
-  };
-  const Range ins[] = {rng(x, x_span * esz), rng(W, static_cast<int64_t>(p->C) * N * esz),
-                       rng(b, static_cast<int64_t>(N) * esz),
-                       rng(pos, static_cast<int64_t>(ta.T) * 4)};
-  const Range outs[] = {rng(out_ff, ta.M * p->F * esz),
-                        rng(out_q, ta.M * p->heads * p->hd * esz),
-                        rng(out_k, ta.M * nkv * p->hd * esz), rng(out_v, ta.M * nkv * p->hd * esz)};
-  for (int i = 0; i < 4; ++i) {
-    for (int j = i + 1; j < 4; ++j)
-      if (overlaps(outs[i], outs[j])) return fail(FP_ERR_INVALID_ARG, "output buffers overlap");
-    for (const Range& in : ins)
-      if (overlaps(outs[i], in)) return fail(FP_ERR_INVALID_ARG, "an output overlaps an input");
-  }
-  const int rh = rope_half_of(p);
-  const int64_t c_stride = L.strides[L.channel_dim];
-  const bool rope = rh > 0;
-  fp::TokenMap tk{};
-  tk.S_in = ta.S_in;
-  tk.s_stride = ta.s_stride;
-  tk.c_stride = p->C == 1 ? 1 : c_stride;
-  tk.n_outer = 1;
-  tk.n_outer_dims = static_cast<int>(ta.outer_size.size());
-  for (size_t i = 0; i < ta.outer_size.size() && i < fp::kMaxOuter; ++i) {
-    tk.outer_size[i] = ta.outer_size[i];
-    tk.outer_stride[i] = ta.outer_stride[i];
-    tk.n_outer *= ta.outer_size[i];
-  }
-
-  // bf16 runs on the tensor-core kernel when its TMA maps and 16-column
-  // epilogue granules can describe the problem; otherwise (and for f32) on the
-  // FFMA kernel, which addresses any strides.
-  bool a_mn = false;
-  bool tc_path = L.dtype == FP_BF16;
-  if (tc_path) {
-    if (p->F % 16 || (p->heads > 0 && p->hd % 16)) tc_path = false;
-    if (rope && rh % 16 && rh > 8) tc_path = false;
-    if (tk.n_outer_dims > 3) tc_path = false;
-    if (tk.c_stride == 1) a_mn = false;
-    else if (tk.s_stride == 1 || tk.S_in == 1) a_mn = true;
-    else tc_path = false;
-    const int64_t other = a_mn ? tk.c_stride : tk.s_stride;
-    const bool other_unused = a_mn ? p->C == 1 : tk.S_in == 1;
-    if (!other_unused && (other * esz) % 16) tc_path = false;
-    for (int i = 0; i < tk.n_outer_dims; ++i)
-      if ((tk.outer_stride[i] * esz) % 16) tc_path = false;
-  }
-  int bn_eff;
-  if (tc_path) {
-    bn_eff = rope ? (fp::kTcBN / p->hd) * p->hd : fp::kTcBN;
-  } else {
-    if (tk.n_outer_dims > fp::kMaxOuter)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "x has more than %d non-mergeable token axes",
-                  fp::kMaxOuter);
-    bn_eff = rope ? (fp::kSimtBN / p->hd) * p->hd : fp::kSimtBN;
-  }
-
-  // ---------------------------------------------------------------- device work
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  fp_status st = ensure_device_state(p, rope ? ta.T * rh : 0);
+  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0);
   if (st != FP_OK) return st;
+  // The table depends only on (positions, base, rotated width). With the
+  // default positions 0..T-1 it is a constant of the plan and of T, so it is
+  // built once and reused; caller-given positions rebuild it on every call.
+  const bool build_table = pr.rope && (pos != nullptr || p->table_T != pr.ta.T);
+  if (pr.rope && !build_table && stream != p->table_stream) {
+    // cached table written on another stream: order this call after that write
+    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
+  }
+  p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
+  const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
+                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas};
   int launches = 0;
-  // The table depends only on (positions, base, head_dim). With the default
-  // positions 0..T-1 it is a constant of the plan and of T, so it is built
-  // once and reused; caller-given positions rebuild it on every call.
-  if (rope && (pos != nullptr || p->table_T != ta.T)) {
-    cudaError_t err = fp::launch_rope_table(p->d_table, pos, ta.T, rh, 2 * rh,
-                                            static_cast<double>(p->rope_base), stream);
-    if (err != cudaSuccess)
-      return fail(FP_ERR_CUDA, "rotary table launch: %s", cudaGetErrorString(err));
+  st = launch(*p, pr, a, sc, build_table, stream, &launches);
+  if (st != FP_OK) return st;
+  p->inject_stall = 0;
+  if (build_table) {
     if (!p->table_ready &&
         cudaEventCreateWithFlags(&p->table_ready, cudaEventDisableTiming) != cudaSuccess)
       return fail(FP_ERR_CUDA, "event creation failed");
     if (cudaEventRecord(p->table_ready, stream) != cudaSuccess)
       return fail(FP_ERR_CUDA, "event record failed");
     p->table_stream = stream;
-    p->table_T = pos ? -1 : ta.T;
-    ++launches;
-  } else if (rope && stream != p->table_stream) {
-    // cached table written on another stream: order this call after that write
-    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
-      return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
-  }
-  fp::Epilogue e{};
-  e.M = ta.M;
-  e.T = ta.T;
-  e.N = N;
-  e.F = p->F;
-  e.C = p->C;
-  e.heads = p->heads;
-  e.hd = p->hd;
-  e.groups = p->groups;
-  e.act = p->act;
-  e.rope_half = rh;
-  e.rope_cs = rope ? p->d_table : nullptr;
-  e.bias = b;
-  e.out_ff = out_ff;
-  e.out_q = out_q;
-  e.out_k = out_k;
-  e.out_v = out_v;
-  e.status = p->d_status;
-  e.bn_eff = bn_eff;
-  const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
-
-  if (tc_path) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-    if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-    fp::TcParams tp;
-    memset(&tp, 0, sizeof tp);
-    // A: 5-D map [inner, second, outer0, outer1, outer2]
-    cuuint64_t gdim[5], gstride[4];
-    cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
-    if (a_mn) {
-      gdim[0] = ta.S_in;
-      gdim[1] = p->C;
-      gstride[0] = static_cast<cuuint64_t>(tk.c_stride) * esz;
-      box[0] = 64;
-      box[1] = fp::kTcBK;
-    } else {
-      gdim[0] = p->C;
-      gdim[1] = ta.S_in;
-      gstride[0] = static_cast<cuuint64_t>(tk.s_stride) * esz;
-      box[0] = fp::kTcBK;
-      box[1] = fp::kTcBM;
-    }
-    if (gstride[0] == 0 || gstride[0] % 16) gstride[0] = 16 * ((gdim[0] * esz + 15) / 16);
-    cuuint64_t last = gstride[0];
-    for (int d = 0; d < 3; ++d) {
-      if (d < tk.n_outer_dims) {
-        gdim[2 + d] = tk.outer_size[d];
-        gstride[1 + d] = static_cast<cuuint64_t>(tk.outer_stride[d]) * esz;
-        last = gstride[1 + d];
-      } else {
-        gdim[2 + d] = 1;
-        gstride[1 + d] = last;
-      }
-      box[2 + d] = 1;
-    }
-    CUresult r = encode(&tp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), gdim,
-                        gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for x rejected (CUresult %d)",
-                  static_cast<int>(r));
-    cuuint64_t bdim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(p->C)};
-    cuuint64_t bstride[1] = {static_cast<cuuint64_t>(N) * esz};
-    cuuint32_t bbox[2] = {64, fp::kTcBK};
-    r = encode(&tp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), bdim, bstride,
-               bbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
-                  static_cast<int>(r));
-    tp.tok = tk;
-    tp.epi = e;
-    tp.C = p->C;
-    tp.num_k_blocks = (p->C + fp::kTcBK - 1) / fp::kTcBK;
-    tp.m_tiles_per_slab = (ta.S_in + fp::kTcBM - 1) / fp::kTcBM;
-    tp.num_m_tiles = tk.n_outer * tp.m_tiles_per_slab;
-    tp.num_n_tiles = num_n_tiles;
-    tp.num_tiles = tp.num_m_tiles * num_n_tiles;
-    tp.group_m = p->group_m;
-    tp.wait_limit_ns = p->wait_limit_ns;
-    tp.inject_stall = p->inject_stall;
-    p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
-    tp.launch_tag = static_cast<int>(p->launch_seq);
-    int ctas = sm_count(p->device);
-    if (p->max_ctas > 0) ctas = std::min(ctas, p->max_ctas);
-    if (static_cast<int64_t>(ctas) > tp.num_tiles) ctas = static_cast<int>(tp.num_tiles);
-    cudaError_t err = fp::launch_tc_gemm(tp, a_mn, ctas, stream);
-    if (err != cudaSuccess)
-      return fail(FP_ERR_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(err));
-    p->inject_stall = 0;
-    ++launches;
-  } else {
-    fp::SimtParams sp;
-    memset(&sp, 0, sizeof sp);
-    sp.x = x;
-    sp.W = W;
-    sp.tok = tk;
-    sp.epi = e;
-    sp.C = p->C;
-    sp.m_tiles_per_slab = (ta.S_in + fp::kSimtBM - 1) / fp::kSimtBM;
-    sp.num_m_tiles = tk.n_outer * sp.m_tiles_per_slab;
-    sp.num_n_tiles = num_n_tiles;
-    cudaError_t err = fp::launch_simt_gemm(sp, L.dtype == FP_BF16, stream);
-    if (err != cudaSuccess)
-      return fail(FP_ERR_CUDA, "FFMA GEMM launch: %s", cudaGetErrorString(err));
-    ++launches;
+    p->table_T = pos ? -1 : pr.ta.T;
   }
   p->last_launches = launches;
   return ok();
