@@ -35,7 +35,7 @@ FP_OPT_GROUP_M = 3
 FP_OPT_MAX_CTAS = 4
 
 # the C ABI's entry points, as declared in include/fp.h
-EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_reserve", "fp_get_device_status",
+EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_noalloc", "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
 
@@ -82,6 +82,9 @@ def load():
     lib.fp_create_ex.restype = I
     lib.fp_forward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
     lib.fp_forward.restype = I
+    lib.fp_forward_noalloc.argtypes = [ctypes.POINTER(fp_config), P, ctypes.POINTER(fp_layout), P,
+                                       P, P, P, P, P, P, P]
+    lib.fp_forward_noalloc.restype = I
     lib.fp_reserve.argtypes = [P, I64]
     lib.fp_reserve.restype = I
     lib.fp_get_device_status.argtypes = [P, P]
@@ -130,6 +133,14 @@ def fp_forward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int], p
                out_v: Optional[int], stream: Optional[int]) -> int:
     return load().fp_forward(plan, x, ctypes.byref(layout), W, b, pos, out_ff, out_q, out_k, out_v,
                              stream)
+
+
+def fp_forward_noalloc(config: fp_config, x: int, layout: fp_layout, W: int, b: Optional[int],
+                       pos: Optional[int], out_ff: Optional[int], out_q: Optional[int],
+                       out_k: Optional[int], out_v: Optional[int], stream: Optional[int]) -> int:
+    """fp_forward without a plan and without any device allocation (static scratch)."""
+    return load().fp_forward_noalloc(ctypes.byref(config), x, ctypes.byref(layout), W, b, pos,
+                                     out_ff, out_q, out_k, out_v, stream)
 
 
 def fp_reserve(plan: int, max_tokens_per_batch: int) -> int:

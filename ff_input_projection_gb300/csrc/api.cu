@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -633,4 +634,126 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   return ok();
 }
 
+// ---------------------------------------------------------------- no-allocation entry point
+//
+// fp_forward_noalloc serves callers that must not allocate device memory
+// themselves or through this library once they are running: plug-ins of a
+// host framework that owns every device byte through its own pool, and
+// fixed-budget serving processes that size memory once at start-up and treat
+// a later cudaMalloc (which can also stall the device) as a failure. It runs
+// the same kernels as fp_forward; their device scratch (status words and the
+// rotary table) lives in the static array below instead of in a plan.
+
 }  // extern "C"
+
+namespace {
+
+constexpr int64_t kNoAllocTableEntries = int64_t{1} << 19;  // (cos, sin) pairs: 4 MiB
+constexpr int64_t kNoAllocHeaderBytes = 256;                // status words live here
+
+}  // namespace
+
+// [status words (256 B) | rotary table (4 MiB)]. Every GPU that loads this
+// library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocHeaderBytes +
+                                                                 8 * kNoAllocTableEntries];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// symbol's name is only a host-side stand-in, so the address is asked of the
+// runtime once per device (with that device current) and cached.
+fp_status noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= 64) return fail(FP_ERR_INVALID_ARG, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (err != cudaSuccess || !ptr)
+      return fail(FP_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
+                  cudaGetErrorString(err));
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
+  return FP_OK;
+}
+
+// The rules fp_create_ex applies, for a configuration that gets no plan.
+fp_status check_config(const fp_config& c) {
+  if (c.C <= 0) return fail(FP_ERR_INVALID_ARG, "C must be > 0 (got %d)", c.C);
+  if (c.ff_hidden < 0 || c.heads < 0 || c.n_query_groups < 0)
+    return fail(FP_ERR_INVALID_ARG, "ff_hidden, heads and n_query_groups must be >= 0");
+  if (c.heads > 0) {
+    if (c.head_dim <= 0 || c.head_dim % 2)
+      return fail(FP_ERR_INVALID_ARG, "head_dim must be even and > 0 (got %d)", c.head_dim);
+    if (static_cast<int64_t>(c.heads) * c.head_dim != c.C)
+      return fail(FP_ERR_INVALID_ARG, "heads * head_dim must equal C");
+    if (c.ff_hidden % c.head_dim)
+      return fail(FP_ERR_INVALID_ARG, "ff_hidden must be a multiple of head_dim");
+    if (c.n_query_groups > 0 && c.heads % c.n_query_groups)
+      return fail(FP_ERR_INVALID_ARG, "heads must be a multiple of n_query_groups");
+    if (c.rope_n_elem < 0 || c.rope_n_elem % 2 || c.rope_n_elem > c.head_dim)
+      return fail(FP_ERR_INVALID_ARG, "rope_n_elem must be even and <= head_dim");
+    if (c.rope_base > 0.0f && c.head_dim > 128)
+      return fail(FP_ERR_INVALID_ARG, "rotary embedding needs head_dim <= 128");
+  } else if (c.n_query_groups > 0) {
+    return fail(FP_ERR_INVALID_ARG, "n_query_groups needs heads > 0");
+  }
+  if (c.ff_hidden == 0 && c.heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
+  if (c.act < FP_ACT_NONE || c.act > FP_ACT_SILU) return fail(FP_ERR_INVALID_ARG, "unknown act");
+  return FP_OK;
+}
+
+std::atomic<uint32_t> g_noalloc_seq{0};
+
+}  // namespace
+
+extern "C" fp_status fp_forward_noalloc(const fp_config* config, const void* x,
+                                        const fp_layout* x_layout, const void* W, const void* b,
+                                        const int32_t* pos, void* out_ff, void* out_q,
+                                        void* out_k, void* out_v, void* stream_v) {
+  if (!config) return fail(FP_ERR_INVALID_ARG, "config is NULL");
+  fp_status st = check_config(*config);
+  if (st != FP_OK) return st;
+  fp_plan pl{};  // on the stack: no plan object, no device state of its own
+  pl.C = config->C;
+  pl.F = config->ff_hidden;
+  pl.heads = config->heads;
+  pl.hd = config->heads > 0 ? config->head_dim : 0;
+  pl.groups = config->heads > 0 ? config->n_query_groups : 0;
+  pl.rope_n_elem = config->heads > 0 ? config->rope_n_elem : 0;
+  pl.act = config->act;
+  pl.rope_base = config->rope_base;
+  const Args a{x, x_layout, W, b, pos, out_ff, out_q, out_k, out_v};
+  Prepared pr;
+  st = prepare(pl, a, pr);
+  if (st != FP_OK) return st;
+  if (pr.ta.M == 0) return ok();
+  const int64_t need = pr.rope ? pr.ta.T * pr.rh : 0;
+  if (need > kNoAllocTableEntries)
+    return fail(FP_ERR_INVALID_ARG,
+                "rotary table needs %lld entries (T = %lld positions x %d frequencies); "
+                "fp_forward_noalloc holds at most %lld",
+                static_cast<long long>(need), static_cast<long long>(pr.ta.T), pr.rh,
+                static_cast<long long>(kNoAllocTableEntries));
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  unsigned char* base = nullptr;
+  st = noalloc_scratch(dev, &base);
+  if (st != FP_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int* status = reinterpret_cast<int*>(base);
+  // the array keeps the previous call's contents: the status words must start at zero
+  if (cudaMemsetAsync(status, 0, 2 * sizeof(int), stream) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "clearing the static status words failed");
+  const uint32_t tag = g_noalloc_seq.fetch_add(1) % 0x7FFFFFFEu + 1u;
+  const Scratch sc{status, reinterpret_cast<float2*>(base + kNoAllocHeaderBytes), dev,
+                   static_cast<int>(tag), 2000000000ull, 0, 8, 0};
+  int launches = 0;
+  // the shared table may hold another call's positions: always rebuild it
+  st = launch(pl, pr, a, sc, pr.rope, stream, &launches);
+  return st == FP_OK ? ok() : st;
+}

@@ -160,6 +160,35 @@ fp_status fp_forward(fp_plan* plan, const void* x, const fp_layout* x_layout, co
                      void* out_v, void* stream);
 
 /*
+ * fp_forward_noalloc — fp_forward for callers that may not allocate device
+ * memory. The pages have no counterpart: it exists for callers such as a
+ * plug-in running inside a host framework that owns every device byte through
+ * its own pool, or a fixed-budget serving process that sizes memory once at
+ * start-up, where a cudaMalloc during a call (which can also stall the device)
+ * is not allowed. It takes the configuration directly (no plan) and runs the
+ * same kernels as fp_forward, with their device scratch (two status words and
+ * the rotary (cos, sin) table) in a static device array of 4 MiB + 256 bytes
+ * that the library holds on every GPU that loads it, until process exit.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   Sizes: the rotary table may need at most 524288 (cos, sin) entries, i.e.
+ *   T * rope_n_elem/2 <= 524288 (T = tokens per batch element; rope_n_elem =
+ *   head_dim when 0); larger problems are rejected with FP_ERR_INVALID_ARG and
+ *   a message from fp_last_error(). Other arguments as fp_forward.
+ *   Set-up: the first call on each device asks the runtime for the array's
+ *   device address with that device current; make that first call before any
+ *   stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous call's
+ *   contents; each call clears the status words and rebuilds the table on its
+ *   stream. Calls whose work overlaps on the GPU (other streams, other host
+ *   threads) race on the array and must be serialised by the caller.
+ *   Device-side timeouts still stop the kernels cleanly but are not reported
+ *   here (there is no plan to hold the status); use fp_forward for that.
+ */
+fp_status fp_forward_noalloc(const fp_config* config, const void* x, const fp_layout* x_layout,
+                             const void* W, const void* b, const int32_t* pos, void* out_ff,
+                             void* out_q, void* out_k, void* out_v, void* stream);
+
+/*
  * fp_reserve — allocate, on the current device, the plan's device scratch
  * (status word and a rotary table for up to max_tokens_per_batch positions) so
  * that later fp_forward calls with T <= max_tokens_per_batch allocate nothing.
