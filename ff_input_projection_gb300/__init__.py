@@ -202,6 +202,7 @@ class FusedProjection:
         self.plan = h
         self.C, self.F, self.heads, self.head_dim = C, ff_hidden, heads, head_dim
         self.kv_heads = n_query_groups if n_query_groups else heads
+        self.N = ff_hidden + (heads + 2 * self.kv_heads) * head_dim
 
     def close(self):
         if getattr(self, "plan", None):
@@ -242,15 +243,38 @@ class FusedProjection:
     def forward(self, x, W, b=None, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
                 out=None, stream=None):
         import torch
-        dt = {torch.bfloat16: FP_BF16, torch.float32: FP_F32}[x.dtype]
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
+        dt = FP_BF16 if x.dtype == torch.bfloat16 else FP_F32
         Bb, T = self.out_shapes(x.shape, channel_dim, n_batch_dims)
         M = Bb * T
+        # the C ABI sees raw pointers: check the buffer sizes here
+        if tuple(W.shape) != (self.C, self.N) or not W.is_contiguous() or W.dtype != x.dtype:
+            raise ValueError(f"W must be a contiguous [{self.C}, {self.N}] {x.dtype} tensor, "
+                             f"got {tuple(W.shape)} {W.dtype}")
+        if b is not None and (tuple(b.shape) != (self.N,) or not b.is_contiguous()
+                              or b.dtype != x.dtype):
+            raise ValueError(f"b must be a contiguous [{self.N}] {x.dtype} tensor")
+        if pos is not None and (tuple(pos.shape) != (T,) or pos.dtype != torch.int32
+                                or not pos.is_contiguous()):
+            raise ValueError(f"pos must be a contiguous int32 [{T}] tensor")
+        for t in (W, b, pos):
+            if t is not None and t.device != x.device:
+                raise ValueError("all tensors must be on x's device")
         if out is None:
             ff = torch.empty((M, self.F), device=x.device, dtype=x.dtype) if self.F else None
             qkv = [torch.empty((Bb * nh, T, self.head_dim), device=x.device, dtype=x.dtype)
                    for nh in (self.heads, self.kv_heads, self.kv_heads)] \
                 if self.heads else [None, None, None]
             out = (ff, *qkv)
+        else:
+            want = [(M, self.F) if self.F else None] + \
+                   [(Bb * nh, T, self.head_dim) if self.heads else None
+                    for nh in (self.heads, self.kv_heads, self.kv_heads)]
+            for o, shp in zip(out, want):
+                if (o is None) != (shp is None) or (o is not None and (
+                        tuple(o.shape) != shp or not o.is_contiguous() or o.dtype != x.dtype)):
+                    raise ValueError(f"output buffers must be contiguous {want}")
         L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, dt)
         ptr = lambda t: None if t is None else t.data_ptr()
         if stream is None:

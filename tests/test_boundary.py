@@ -153,3 +153,23 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         fpx.load()
+
+
+def test_wrapper_checks_buffer_sizes(lib):
+    """The C ABI gets raw pointers, so the torch wrapper checks sizes on the
+    host: a weight with the wrong column count (e.g. a grouped-query weight
+    given to a plan built without groups) is rejected before any launch."""
+    import torch
+    proj = fpx.FusedProjection(512, 0, 16, 32, "none", 10000.0)  # blocked q|k|v: N = 1536
+    x = torch.zeros((2, 8, 512), dtype=torch.bfloat16)
+    W_gqa = torch.zeros((512, 768), dtype=torch.bfloat16)       # grouped-query width
+    with pytest.raises(ValueError):
+        proj.forward(x, W_gqa, None, None, channel_dim=2)
+    W = torch.zeros((512, 1536), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        proj.forward(x, W, torch.zeros(10, dtype=torch.bfloat16), None, channel_dim=2)
+    with pytest.raises(ValueError):
+        proj.forward(x, W, None, torch.zeros(8, dtype=torch.int64), channel_dim=2)
+    with pytest.raises(ValueError):
+        proj.forward(x, W.float(), None, None, channel_dim=2)
+    proj.close()
