@@ -282,7 +282,8 @@ def main():
         with torch.cuda.graph(graph, stream=stream):
             for i in range(G):
                 step(i)
-        graph.replay()
+        with torch.cuda.stream(stream):
+            graph.replay()
         torch.cuda.synchronize(dev)
     except Exception as exc:  # capture unsupported here: time the eager loop instead
         graph = None
@@ -292,7 +293,8 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(uuid) as clk:
+    # graph.replay() launches on torch's current stream: make that the timed stream
+    with ClockSampler(uuid) as clk, torch.cuda.stream(stream):
         ev0.record(stream)
         if graph is not None:
             for _ in range(args.steps // G):

@@ -10,12 +10,12 @@
 // q/k/v [B*heads, T, head_dim] (memory-efficient-attention issue #7, the
 // [batch*heads, tokens, head_dim] layout).
 //
-// Structure (one persistent CTA per SM, 10 warps):
+// Structure (one persistent CTA per SM, 18 warps):
 //   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring
 //   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
 //              (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits
 //              completion to mbarriers
-//   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (one token row
+//   warps 2-17 epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //              per thread), bias, activation / rotation in registers, bf16
 //              round-to-nearest-even, 16-byte stores
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the
@@ -39,7 +39,7 @@ namespace {
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
 constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
-constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 16;  // 4 per SM sub-partition: latency hiding for the epilogue
 constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
@@ -309,7 +309,9 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 
 // ------------------------------------------------------------------ the kernel
 
-template <bool A_MN_MAJOR>
+// ACT: the ff-block activation, fixed at compile time so the per-value code
+// has no branch on it.
+template <bool A_MN_MAJOR, int ACT>
 __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     // ------------------------------------------------ epilogue warps
     const Epilogue& e = p.epi;
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    const int half_id = (warp - 2) >> 2;           // which alternate work units it takes
+    const int part = (warp - 2) >> 2;              // which of every 4 work units it takes
     const int row = quarter * 32 + lane;
     const int rh = e.rope_half;
     const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         const bool rope = rh >= 16 && qk && ci.j < 2 * rh;
         const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
         if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
-        if ((unit++ & 1) != half_id) continue;
+        if ((unit++ & 3) != part) continue;
         float bl[16];
         load_bias16(bias, n, bl);
         if (rope) {
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             float v[16];
             if (ci.seg == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = activate(e.act, __uint_as_float(v_u[i]) + bl[i]);
+              for (int i = 0; i < 16; ++i) v[i] = activate(ACT, __uint_as_float(v_u[i]) + bl[i]);
             } else {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bl[i];
@@ -551,28 +553,37 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   }
 }
 
-}  // namespace
-
-cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream) {
+template <bool A_MN, int ACT>
+cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream) {
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
+  if (dev >= 64 || !attr_done[dev]) {
+    err = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, ACT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    attr_done[dev] = 1;
+    if (dev < 64) attr_done[dev] = 1;
   }
-  if (p.num_tiles == 0) return cudaSuccess;
-  if (a_mn_major)
-    tc_gemm_kernel<true><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
-  else
-    tc_gemm_kernel<false><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
+  tc_gemm_kernel<A_MN, ACT><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <bool A_MN>
+cudaError_t launch_act(const TcParams& p, int num_ctas, cudaStream_t stream) {
+  switch (p.epi.act) {
+    case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF>(p, num_ctas, stream);
+    case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH>(p, num_ctas, stream);
+    case ACT_SILU: return launch_variant<A_MN, ACT_SILU>(p, num_ctas, stream);
+    default: return launch_variant<A_MN, ACT_NONE>(p, num_ctas, stream);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream) {
+  if (p.num_tiles == 0) return cudaSuccess;
+  return a_mn_major ? launch_act<true>(p, num_ctas, stream) : launch_act<false>(p, num_ctas, stream);
 }
 
 }  // namespace fp
