@@ -48,6 +48,60 @@ __device__ __forceinline__ ColInfo decode_col(const Epilogue& e, int n) {
   return ci;
 }
 
+// Walks the fused columns 16 at a time (ff_hidden and head_dim are multiples
+// of 16 on the tensor-core path), so a tile decodes its first column once and
+// then only adds.
+struct ColCursor {
+  ColInfo ci;
+  int grp, slot;  // grouped-query position: group and slot inside [q.. | k | v]
+};
+
+__device__ __forceinline__ void cursor_init(const Epilogue& e, int n, ColCursor& c) {
+  c.ci = decode_col(e, n);
+  c.grp = 0;
+  c.slot = 0;
+  if (e.groups > 0 && c.ci.seg > 0) {
+    const int qpk = e.heads / e.groups;
+    if (c.ci.seg == 1) {
+      c.grp = c.ci.head / qpk;
+      c.slot = c.ci.head - c.grp * qpk;
+    } else {
+      c.grp = c.ci.head;
+      c.slot = c.ci.seg == 2 ? qpk : qpk + 1;
+    }
+  }
+}
+
+__device__ __forceinline__ void cursor_advance16(const Epilogue& e, ColCursor& c) {
+  c.ci.j += 16;
+  if (c.ci.seg == 0) {
+    if (c.ci.j >= e.F) {
+      c.ci.seg = 1;
+      c.ci.head = 0;
+      c.ci.j = 0;
+      c.grp = 0;
+      c.slot = 0;
+    }
+    return;
+  }
+  if (c.ci.j < e.hd) return;
+  c.ci.j = 0;
+  if (e.groups == 0) {
+    if (++c.ci.head == e.heads) {
+      c.ci.head = 0;
+      ++c.ci.seg;
+    }
+    return;
+  }
+  const int qpk = e.heads / e.groups;
+  if (++c.slot == qpk + 2) {
+    c.slot = 0;
+    ++c.grp;
+  }
+  c.ci.seg = c.slot < qpk ? 1 : (c.slot == qpk ? 2 : 3);
+  c.ci.head = c.slot < qpk ? c.grp * qpk + c.slot : c.grp;
+}
+
 // Element offset of (token m = b*T + t, column info) in its output buffer.
 __device__ __forceinline__ int64_t out_offset(const Epilogue& e, const ColInfo& ci, int64_t m,
                                               int64_t b, int64_t t) {

@@ -248,20 +248,21 @@ __device__ __forceinline__ void outer_coords(const TokenMap& tk, int64_t o, int 
   }
 }
 
-__device__ __forceinline__ void load_bias16(const uint16_t* bias, int n, float (&b)[16]) {
+// 16 bf16 bias values kept packed (two per word) until used.
+__device__ __forceinline__ void load_bias16(const uint16_t* bias, int n, uint32_t (&w)[8]) {
   if (bias == nullptr) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) b[i] = 0.0f;
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(bias + n);
-  uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-  uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    b[2 * i] = __uint_as_float(w[i] << 16);
-    b[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
+  const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+  w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+  w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+}
+
+__device__ __forceinline__ float bias_at(const uint32_t (&w)[8], int i) {
+  return (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u) : __uint_as_float(w[i >> 1] << 16);
 }
 
 __device__ __forceinline__ void store16_bf16(void* dst, const float (&v)[16]) {
@@ -475,11 +476,20 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       const int64_t bidx = m / e.T;
       const int64_t t = m - bidx * e.T;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
+      // per-row output bases, once per tile; a column group then adds head*T*hd + lane
+      const int nkv = e.groups > 0 ? e.groups : e.heads;
+      const int64_t head_stride = e.T * e.hd;
+      uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F;
+      uint16_t* const q_row = static_cast<uint16_t*>(e.out_q) + (bidx * e.heads * e.T + t) * e.hd;
+      uint16_t* const k_row = static_cast<uint16_t*>(e.out_k) + (bidx * nkv * e.T + t) * e.hd;
+      uint16_t* const v_row = static_cast<uint16_t*>(e.out_v) + (bidx * nkv * e.T + t) * e.hd;
+      const float2* const cs_row = e.rope_cs + t * rh;
+      const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
+      ColCursor cur;
+      cursor_init(e, tc.n0, cur);
       int unit = 0;
-      for (int c = 0; c < BN; c += 16) {
-        const int n = tc.n0 + c;
-        if (c >= e.bn_eff || n >= e.N) break;
-        const ColInfo ci = decode_col(e, n);
+      for (int c = 0; c < cols; c += 16, cursor_advance16(e, cur)) {
+        const ColInfo& ci = cur.ci;
         const bool qk = ci.seg == 1 || ci.seg == 2;
         // rh >= 16: lanes i and i+rh sit in different granules, handled as a pair;
         // rh <= 8: every rotated lane sits in the head's first granule.
@@ -487,35 +497,37 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
         if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
         if ((unit++ & 3) != part) continue;
-        float bl[16];
+        const int n = tc.n0 + c;
+        uint16_t* const dst =
+            ci.seg == 0 ? ff_row + ci.j
+                        : (ci.seg == 1 ? q_row : ci.seg == 2 ? k_row : v_row) +
+                              ci.head * head_stride + ci.j;
+        uint32_t bl[8];
         load_bias16(bias, n, bl);
         if (rope) {
           uint32_t lo_u[16], hi_u[16];
           tmem_ld16(t_row + c, lo_u);
           tmem_ld16(t_row + c + rh, hi_u);
           tmem_wait_ld();
-          float bh[16];
+          uint32_t bh[8];
           load_bias16(bias, n + rh, bh);
           float lo[16], hi[16];
           if (valid) {
-            const float4* cs4 = reinterpret_cast<const float4*>(e.rope_cs + t * rh + ci.j);
+            const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
-              const float x0 = __uint_as_float(lo_u[2 * i]) + bl[2 * i];
-              const float y0 = __uint_as_float(hi_u[2 * i]) + bh[2 * i];
-              const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bl[2 * i + 1];
-              const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bh[2 * i + 1];
+              const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
+              const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
+              const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
+              const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
               lo[2 * i] = x0 * cs.x - y0 * cs.y;
               hi[2 * i] = y0 * cs.x + x0 * cs.y;
               lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
               hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
             }
-            char* base = static_cast<char*>(out_base(e, ci.seg));
-            store16_bf16(base + 2 * out_offset(e, ci, m, bidx, t), lo);
-            ColInfo ch = ci;
-            ch.j += rh;
-            store16_bf16(base + 2 * out_offset(e, ch, m, bidx, t), hi);
+            store16_bf16(dst, lo);
+            store16_bf16(dst + rh, hi);
           }
         } else {
           uint32_t v_u[16];
@@ -525,14 +537,13 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             float v[16];
             if (ci.seg == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = activate(ACT, __uint_as_float(v_u[i]) + bl[i]);
+              for (int i = 0; i < 16; ++i) v[i] = activate(ACT, __uint_as_float(v_u[i]) + bias_at(bl, i));
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bl[i];
-              if (rope_small) rotate_small(v, e.rope_cs + t * rh, rh);
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
+              if (rope_small) rotate_small(v, cs_row, rh);
             }
-            char* base = static_cast<char*>(out_base(e, ci.seg));
-            store16_bf16(base + 2 * out_offset(e, ci, m, bidx, t), v);
+            store16_bf16(dst, v);
           }
         }
       }
