@@ -33,6 +33,7 @@ FP_OPT_WAIT_LIMIT_NS = 1
 FP_OPT_INJECT_STALL = 2
 FP_OPT_GROUP_M = 3
 FP_OPT_MAX_CTAS = 4
+FP_OPT_CLUSTER = 5
 
 # the C ABI's entry points, as declared in include/fp.h
 EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_noalloc", "fp_reserve", "fp_get_device_status",

@@ -33,6 +33,7 @@ struct fp_plan {
   int inject_stall;
   int group_m;
   int max_ctas;
+  int cluster;  // CTAs per cluster on the tensor-core path (1 or 2)
   uint32_t launch_seq;
 };
 
@@ -213,6 +214,7 @@ struct Scratch {
   int inject_stall;
   int group_m;
   int max_ctas;
+  int cluster;
 };
 
 // Every check of a forward call; touches no GPU.
@@ -413,13 +415,17 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     tp.num_m_tiles = tk.n_outer * tp.m_tiles_per_slab;
     tp.num_n_tiles = num_n_tiles;
     tp.num_tiles = tp.num_m_tiles * num_n_tiles;
+    // two CTAs share each W tile when there are M-tiles to pair
+    tp.cluster = (sc.cluster == 2 && tp.num_m_tiles >= 2) ? 2 : 1;
+    tp.num_units = (tp.num_m_tiles + tp.cluster - 1) / tp.cluster * num_n_tiles;
     tp.group_m = sc.group_m;
     tp.wait_limit_ns = sc.wait_limit_ns;
     tp.inject_stall = sc.inject_stall;
     tp.launch_tag = sc.launch_tag;
     int ctas = sm_count(sc.device);
     if (sc.max_ctas > 0) ctas = std::min(ctas, sc.max_ctas);
-    if (static_cast<int64_t>(ctas) > tp.num_tiles) ctas = static_cast<int>(tp.num_tiles);
+    if (static_cast<int64_t>(ctas) > tp.num_units * tp.cluster)
+      ctas = static_cast<int>(tp.num_units * tp.cluster);
     cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, ctas, stream);
     if (err != cudaSuccess)
       return fail(FP_ERR_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(err));
@@ -516,6 +522,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->inject_stall = 0;
   p->group_m = 8;
   p->max_ctas = 0;
+  p->cluster = 2;
   p->launch_seq = 0;
   *plan = p;
   return ok();
@@ -560,6 +567,10 @@ fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value) {
     case FP_OPT_MAX_CTAS:
       if (value < 0) return fail(FP_ERR_INVALID_ARG, "max_ctas must be >= 0");
       plan->max_ctas = static_cast<int>(value);
+      return ok();
+    case FP_OPT_CLUSTER:
+      if (value != 1 && value != 2) return fail(FP_ERR_INVALID_ARG, "cluster must be 1 or 2");
+      plan->cluster = static_cast<int>(value);
       return ok();
   }
   return fail(FP_ERR_INVALID_ARG, "unknown option %d", static_cast<int>(opt));
@@ -616,7 +627,7 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   }
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
-                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas};
+                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster};
   int launches = 0;
   st = launch(*p, pr, a, sc, build_table, stream, &launches);
   if (st != FP_OK) return st;
@@ -751,7 +762,7 @@ extern "C" fp_status fp_forward_noalloc(const fp_config* config, const void* x,
     return fail(FP_ERR_CUDA, "clearing the static status words failed");
   const uint32_t tag = g_noalloc_seq.fetch_add(1) % 0x7FFFFFFEu + 1u;
   const Scratch sc{status, reinterpret_cast<float2*>(base + kNoAllocHeaderBytes), dev,
-                   static_cast<int>(tag), 2000000000ull, 0, 8, 0};
+                   static_cast<int>(tag), 2000000000ull, 0, 8, 0, 2};
   int launches = 0;
   // the shared table may hold another call's positions: always rebuild it
   st = launch(pl, pr, a, sc, pr.rope, stream, &launches);

@@ -55,6 +55,8 @@ struct TcParams {
   int64_t num_m_tiles;
   int num_n_tiles;
   int64_t num_tiles;
+  int cluster;        // CTAs per cluster sharing one W tile (1 or 2)
+  int64_t num_units;  // work items: (M-tile group of `cluster`, N-tile) pairs
   int group_m;
   uint64_t wait_limit_ns;
   int inject_stall;  // 1: CTA 0 withholds its first operand stage (error-path test)

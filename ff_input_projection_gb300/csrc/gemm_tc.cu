@@ -142,6 +142,30 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Same, written to the same shared-memory offset of every CTA in `mask` of the
+// cluster, each destination's mbarrier (same offset) receiving its bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar, int c0, int c1,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA in the cluster; orders shared-memory writes
+// (barrier init) before the peers' use of them.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -186,6 +210,16 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Arrive on the mbarrier at the same offset in every CTA of `mask` once this
+// thread's earlier MMAs have completed.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -211,25 +245,33 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // ------------------------------------------------------------------ tile helpers
 
 struct TileCoord {
-  int64_t o;    // outer slab
-  int64_t s0;   // first token of the tile inside the slab
-  int n0;       // first fused column
+  int64_t o;     // outer slab
+  int64_t s0;    // first token of the tile inside the slab
+  int n0;        // first fused column
+  bool phantom;  // M-tile past the end (odd M-tile count in a CTA pair): compute, store nothing
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t tile) {
-  // group_m consecutive M-tiles sweep all N-tiles, M fastest inside a group,
-  // so concurrently running CTAs share W tiles and x tiles in L2.
-  const int64_t per_group = static_cast<int64_t>(p.group_m) * p.num_n_tiles;
-  const int64_t g = tile / per_group;
-  const int64_t first_m = g * p.group_m;
-  const int64_t left = p.num_m_tiles - first_m;
-  const int64_t gm = left < p.group_m ? left : p.group_m;
-  const int64_t r = tile - g * per_group;
-  const int64_t m_tile = first_m + r % gm;
+// Work item `unit` -> this CTA's tile. A cluster of CL CTAs takes CL
+// consecutive M-tiles with the same N-tile (they share its W tile). Groups of
+// group_m M-tiles sweep all N-tiles, M fastest inside a group, so concurrently
+// running clusters share W and x tiles in L2.
+template <int CL>
+__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t unit, int rank) {
+  const int64_t m_units = (p.num_m_tiles + CL - 1) / CL;
+  const int64_t gsz = p.group_m >= CL ? p.group_m / CL : 1;
+  const int64_t per_group = gsz * p.num_n_tiles;
+  const int64_t g = unit / per_group;
+  const int64_t first = g * gsz;
+  const int64_t left = m_units - first;
+  const int64_t gm = left < gsz ? left : gsz;
+  const int64_t r = unit - g * per_group;
+  const int64_t m_tile = (first + r % gm) * CL + rank;
   const int n_tile = static_cast<int>(r / gm);
   TileCoord tc;
-  tc.o = m_tile / p.m_tiles_per_slab;
-  tc.s0 = (m_tile - tc.o * p.m_tiles_per_slab) * BM;
+  tc.phantom = m_tile >= p.num_m_tiles;
+  const int64_t mt = tc.phantom ? p.num_m_tiles - 1 : m_tile;
+  tc.o = mt / p.m_tiles_per_slab;
+  tc.s0 = (mt - tc.o * p.m_tiles_per_slab) * BM;
   tc.n0 = n_tile * p.epi.bn_eff;
   return tc;
 }
@@ -312,7 +354,10 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 
 // ACT: the ff-block activation, fixed at compile time so the per-value code
 // has no branch on it.
-template <bool A_MN_MAJOR, int ACT>
+// CL: CTAs per cluster. With CL == 2 the two CTAs take neighbouring M-tiles of
+// one N-tile and each multicasts half of the W tile into both, so each CTA
+// reads 32 KB instead of 48 KB from L2 per k-step.
+template <bool A_MN_MAJOR, int ACT, int CL>
 __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -329,11 +374,15 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl wc{p.epi.status, p.wait_limit_ns, p.launch_tag};
+  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t first_unit = blockIdx.x / CL;
+  const int64_t unit_step = gridDim.x / CL;
+  constexpr uint16_t kPairMask = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // the MMA of every CTA that reads this stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -354,6 +403,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // peers signal our barriers only after they exist
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = p.num_k_blocks;
@@ -365,8 +415,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       uint32_t armed_mask = 0, armed_parity = 0;  // per stage: armed, parity of its last arming
       int stage = 0;
       uint32_t phase = 0;
-      for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(p, tile);
+      for (int64_t u = first_unit; u < p.num_units; u += unit_step) {
+        const TileCoord tc = tile_coord<CL>(p, u, rank);
         int oc[3];
         outer_coords(p.tok, tc.o, oc);
         bool ok = true;
@@ -390,9 +440,20 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             } else {
               tma_load_5d(a_dst, &p.tmap_a, fb, k0, static_cast<int>(tc.s0), oc[0], oc[1], oc[2]);
             }
+            if (CL == 1) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0);
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0);
+            } else {
+              // this CTA's share of the W tile, written into every CTA of the pair
+              constexpr int per = BN / 64 / CL;
+#pragma unroll
+              for (int jj = 0; jj < per; ++jj) {
+                const int j = rank * per + jj;
+                tma_load_2d_multicast(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0,
+                                      kPairMask);
+              }
+            }
             armed_mask |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -415,7 +476,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       uint32_t phase = 0;
       bool issued = false;
       int it = 0;
-      for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
         const int buf = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!wait_bounded(tempty_bar(buf), acc_phase ^ 1u, wc, true)) break;
@@ -440,7 +501,11 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             umma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          umma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          // frees the stage (in every CTA whose producer writes into ours) once read
+          if (CL == 1)
+            umma_commit(empty_bar(stage));
+          else
+            umma_commit_multicast(empty_bar(stage), kPairMask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -463,15 +528,15 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     const int rh = e.rope_half;
     const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
     int it = 0;
-    for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       const int ok = wait_bounded(tfull_bar(buf), acc_phase, wc, true) ? 1 : 0;
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const TileCoord tc = tile_coord(p, tile);
+      const TileCoord tc = tile_coord<CL>(p, u, rank);
       const int64_t s = tc.s0 + row;
-      const bool valid = s < p.tok.S_in;
+      const bool valid = !tc.phantom && s < p.tok.S_in;
       const int64_t m = tc.o * p.tok.S_in + s;
       const int64_t bidx = m / e.T;
       const int64_t t = m - bidx * e.T;
@@ -555,6 +620,9 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer may still write into its shared memory or
+  // arrive on its barriers
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -564,37 +632,72 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   }
 }
 
-template <bool A_MN, int ACT>
+template <bool A_MN, int ACT, int CL>
 cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream) {
+  auto kernel = tc_gemm_kernel<A_MN, ACT, CL>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
-    err = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, ACT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
-  tc_gemm_kernel<A_MN, ACT><<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  if (CL == 1) {
+    kernel<<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many clusters as can be resident at once (one CTA per SM)
+  static int max_clusters[64] = {0};
+  if (dev >= 64 || !max_clusters[dev]) {
+    cfg.gridDim = dim3(num_ctas, 1, 1);
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) max_clusters[dev] = n;
+    else return cudaErrorInvalidDevice;
+  }
+  int64_t clusters = num_ctas / CL;
+  if (clusters > max_clusters[dev]) clusters = max_clusters[dev];
+  if (clusters > p.num_units) clusters = p.num_units;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kernel, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-template <bool A_MN>
+template <bool A_MN, int CL>
 cudaError_t launch_act(const TcParams& p, int num_ctas, cudaStream_t stream) {
   switch (p.epi.act) {
-    case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF>(p, num_ctas, stream);
-    case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH>(p, num_ctas, stream);
-    case ACT_SILU: return launch_variant<A_MN, ACT_SILU>(p, num_ctas, stream);
-    default: return launch_variant<A_MN, ACT_NONE>(p, num_ctas, stream);
+    case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF, CL>(p, num_ctas, stream);
+    case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH, CL>(p, num_ctas, stream);
+    case ACT_SILU: return launch_variant<A_MN, ACT_SILU, CL>(p, num_ctas, stream);
+    default: return launch_variant<A_MN, ACT_NONE, CL>(p, num_ctas, stream);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream) {
-  if (p.num_tiles == 0) return cudaSuccess;
-  return a_mn_major ? launch_act<true>(p, num_ctas, stream) : launch_act<false>(p, num_ctas, stream);
+  if (p.num_units == 0) return cudaSuccess;
+  if (p.cluster == 2)
+    return a_mn_major ? launch_act<true, 2>(p, num_ctas, stream)
+                      : launch_act<false, 2>(p, num_ctas, stream);
+  return a_mn_major ? launch_act<true, 1>(p, num_ctas, stream)
+                    : launch_act<false, 1>(p, num_ctas, stream);
 }
 
 }  // namespace fp

@@ -220,12 +220,15 @@ const char* fp_last_error(void);
  *                          error path; the GPU stays usable). Cleared after use.
  *   FP_OPT_GROUP_M         tile rasterisation: M-tiles per group (>= 1)
  *   FP_OPT_MAX_CTAS        cap on the persistent grid (0 = one CTA per SM)
+ *   FP_OPT_CLUSTER         2 (default): CTA pairs share each weight tile by
+ *                          multicast; 1: every CTA loads its own
  */
 typedef enum {
   FP_OPT_WAIT_LIMIT_NS = 1,
   FP_OPT_INJECT_STALL = 2,
   FP_OPT_GROUP_M = 3,
-  FP_OPT_MAX_CTAS = 4
+  FP_OPT_MAX_CTAS = 4,
+  FP_OPT_CLUSTER = 5
 } fp_option;
 fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value);
 

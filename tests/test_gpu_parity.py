@@ -192,3 +192,23 @@ def test_empty_tokens_on_device(cuda_ok):
     ff, q, k, v = proj.forward(x, W, None, None, channel_dim=2)
     assert ff.shape == (0, 64) and q.shape == (0, 10, 64)
     assert proj.last_launch_count == 0
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[3], SMALL[5], SMALL[8]], ids=lambda w: w.name)
+def test_cluster_pairs_match_single_ctas(w, cuda_ok):
+    """CTA pairs that multicast the shared weight tile (default) and single
+    CTAs give identical bits; odd M-tile counts leave one CTA of the last pair
+    with nothing to store."""
+    inp = fpsynth.make_inputs(w)
+    outs = []
+    for cl in (1, 2):
+        proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+        proj.set_option(fpx.FP_OPT_CLUSTER, cl)
+        outs.append(run(w, inp, proj=proj))
+    for k in ("ff", "q", "k", "v"):
+        if outs[0][k] is not None:
+            assert torch.equal(outs[0][k], outs[1][k]), k
+    ref = oracle.forward_workload(w, inp)
+    for k in ("ff", "q", "k", "v"):
+        if outs[1][k] is not None:
+            assert_close(host(outs[1][k]), ref[k], w.dtype, f"{w.name}:{k}")
