@@ -27,7 +27,8 @@ namespace {
 
 constexpr int BM = kSimtBM, BN = kSimtBN, BK = 16, NT = 256;
 constexpr int CS_LD = BN + 4;
-constexpr int kSmemBytes = BM * CS_LD * 4;  // epilogue tile; covers the 2x(A+B) operand buffers
+// epilogue tile + per-row output bases; covers the 2x(A+B) operand buffers
+constexpr int kSmemBytes = BM * CS_LD * 4 + 4 * BM * 8;
 static_assert(2 * BK * (BM + BN) * 4 <= kSmemBytes, "operand buffers must fit in the epilogue tile");
 
 __device__ __forceinline__ int64_t outer_offset(const TokenMap& tk, int64_t o) {
@@ -58,6 +59,64 @@ __device__ __forceinline__ void st_elem(float* p, int64_t i, float v) { p[i] = v
 __device__ __forceinline__ void st_elem(uint16_t* p, int64_t i, float v) {
   __nv_bfloat16 h = __float2bfloat16_rn(v);
   p[i] = *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Epilogue of one tile, kept out of line so the main loop's register
+// allocation does not carry it. Cs holds the fp32 accumulator tile [BM][CS_LD]
+// followed by room for four [BM] int64 arrays.
+template <typename T>
+__device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64_t o, int64_t s0,
+                                           int n0) {
+  const int tid = threadIdx.x;
+  const int64_t S_in = p.tok.S_in;
+  const int N = p.epi.N;
+  const Epilogue& e = p.epi;
+  const T* bias = static_cast<const T*>(e.bias);
+  const int half = e.rope_half;
+  // Per-row output bases, once per tile (rows of a tile are consecutive tokens
+  // of one slab): token index into ff, q and k/v buffers, and the position.
+  int64_t* row_ff = reinterpret_cast<int64_t*>(Cs + BM * CS_LD);  // [BM]
+  int64_t* row_q = row_ff + BM;
+  int64_t* row_kv = row_q + BM;
+  int64_t* row_t = row_kv + BM;
+  const int nkv = e.groups > 0 ? e.groups : e.heads;
+  if (tid < BM) {
+    const int64_t m = o * S_in + s0 + tid;
+    const int64_t bb = m / e.T, t = m - bb * e.T;
+    row_ff[tid] = m * e.F;
+    row_q[tid] = (bb * e.heads * e.T + t) * e.hd;
+    row_kv[tid] = (bb * nkv * e.T + t) * e.hd;
+    row_t[tid] = t;
+  }
+  __syncthreads();
+  // each thread owns one column of the tile and every other row
+  const int c = tid % BN;
+  const int n = n0 + c;
+  if (c >= e.bn_eff || n >= N) return;
+  const ColInfo ci = decode_col(e, n);
+  const float bv = bias ? ld_elem(bias, n) : 0.0f;
+  const bool rot = half > 0 && (ci.seg == 1 || ci.seg == 2) && ci.j < 2 * half;
+  const bool lo = ci.j < half;
+  const int f = lo ? ci.j : ci.j - half;
+  const int pc = lo ? c + half : c - half;
+  const float pbv = (rot && bias) ? ld_elem(bias, lo ? n + half : n - half) : 0.0f;
+  T* const base = static_cast<T*>(out_base(e, ci.seg));
+  const int64_t col_off = ci.seg == 0 ? ci.j : static_cast<int64_t>(ci.head) * e.T * e.hd + ci.j;
+  const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : row_kv;
+  const int64_t tile_rows = S_in - s0;
+  for (int r = tid / BN; r < BM; r += NT / BN) {
+    if (r >= tile_rows) break;
+    float v = Cs[r * CS_LD + c] + bv;
+    if (ci.seg == 0) {
+      v = activate(e.act, v);
+    } else if (rot) {
+      const float pv = Cs[r * CS_LD + pc] + pbv;
+      const float2 cs = e.rope_cs[row_t[r] * half + f];
+      // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
+      v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+    }
+    st_elem(base, rb[r] + col_off, v);
+  }
 }
 
 // T: storage type of x, W, b and the outputs (float, or uint16_t bf16 bits).
@@ -167,32 +226,7 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
   }
   __syncthreads();
 
-  const Epilogue& e = p.epi;
-  const T* bias = static_cast<const T*>(e.bias);
-  const int half = e.rope_half;
-  for (int idx = tid; idx < BM * BN; idx += NT) {
-    const int r = idx / BN, c = idx % BN;
-    const int n = n0 + c;
-    const int64_t s = s0 + r;
-    if (c >= e.bn_eff || n >= N || s >= S_in) continue;
-    const int64_t m = o * S_in + s;
-    const int64_t bb = m / e.T, t = m - bb * e.T;
-    float v = Cs[r * CS_LD + c] + (bias ? ld_elem(bias, n) : 0.0f);
-    ColInfo ci = decode_col(e, n);
-    if (ci.seg == 0) {
-      v = activate(e.act, v);
-    } else if (half > 0 && ci.seg <= 2 && ci.j < 2 * half) {
-      const bool lo = ci.j < half;
-      const int f = lo ? ci.j : ci.j - half;
-      const int pc = lo ? c + half : c - half;
-      const int pn = lo ? n + half : n - half;
-      float pv = Cs[r * CS_LD + pc] + (bias ? ld_elem(bias, pn) : 0.0f);
-      float2 cs = e.rope_cs[t * half + f];
-      // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
-      v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
-    }
-    st_elem(static_cast<T*>(out_base(e, ci.seg)), out_offset(e, ci, m, bb, t), v);
-  }
+  simt_epilogue<T>(p, Cs, o, s0, n0);
 }
 
 template <typename T, bool K_MAJOR>
