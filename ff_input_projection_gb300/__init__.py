@@ -24,8 +24,8 @@ FP_ERR_OUT_OF_MEMORY = 5
 FP_ERR_TIMEOUT = 6
 FP_ERR_DEVICE_BOUNDS = 7
 
-FP_ACT_NONE, FP_ACT_GELU_ERF, FP_ACT_GELU_TANH, FP_ACT_SILU = 0, 1, 2, 3
-ACTS = {"none": 0, "gelu": 1, "gelu_erf": 1, "gelu_tanh": 2, "silu": 3}
+FP_ACT_NONE, FP_ACT_GELU_ERF, FP_ACT_GELU_TANH, FP_ACT_SILU, FP_ACT_RELU2 = 0, 1, 2, 3, 4
+ACTS = {"none": 0, "gelu": 1, "gelu_erf": 1, "gelu_tanh": 2, "silu": 3, "relu2": 4}
 FP_BF16, FP_F32 = 0, 1
 FP_MAX_DIMS = 8
 

@@ -496,7 +496,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
     return fail(FP_ERR_INVALID_ARG, "n_query_groups needs heads > 0");
   }
   if (F == 0 && heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
-  if (cfg->act < FP_ACT_NONE || cfg->act > FP_ACT_SILU)
+  if (cfg->act < FP_ACT_NONE || cfg->act > FP_ACT_RELU2)
     return fail(FP_ERR_INVALID_ARG, "unknown act");
   if (cfg->rope_base > 0.0f && heads > 0 && hd > 128)
     return fail(FP_ERR_INVALID_ARG, "rotary embedding needs head_dim <= 128 (got %d)", hd);
@@ -714,7 +714,7 @@ fp_status check_config(const fp_config& c) {
     return fail(FP_ERR_INVALID_ARG, "n_query_groups needs heads > 0");
   }
   if (c.ff_hidden == 0 && c.heads == 0) return fail(FP_ERR_INVALID_ARG, "nothing to compute");
-  if (c.act < FP_ACT_NONE || c.act > FP_ACT_SILU) return fail(FP_ERR_INVALID_ARG, "unknown act");
+  if (c.act < FP_ACT_NONE || c.act > FP_ACT_RELU2) return fail(FP_ERR_INVALID_ARG, "unknown act");
   return FP_OK;
 }
 

@@ -125,6 +125,10 @@ __device__ __forceinline__ float activate(int act, float y) {
     }
     case ACT_SILU:
       return y / (1.0f + expf(-y));
+    case ACT_RELU2: {
+      const float r = fmaxf(y, 0.0f);
+      return r * r;
+    }
     default:
       return y;
   }

@@ -9,7 +9,7 @@ namespace fp {
 
 constexpr int kMaxOuter = 6;
 
-enum : int { ACT_NONE = 0, ACT_GELU_ERF = 1, ACT_GELU_TANH = 2, ACT_SILU = 3 };
+enum : int { ACT_NONE = 0, ACT_GELU_ERF = 1, ACT_GELU_TANH = 2, ACT_SILU = 3, ACT_RELU2 = 4 };
 enum : int { ST_OK = 0, ST_TIMEOUT = 6, ST_BOUNDS = 7 };
 
 // Token addressing shared by both GEMM kernels. The non-channel axes of x are

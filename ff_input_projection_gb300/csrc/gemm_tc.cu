@@ -685,6 +685,7 @@ cudaError_t launch_act(const TcParams& p, int num_ctas, cudaStream_t stream) {
     case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF, CL>(p, num_ctas, stream);
     case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH, CL>(p, num_ctas, stream);
     case ACT_SILU: return launch_variant<A_MN, ACT_SILU, CL>(p, num_ctas, stream);
+    case ACT_RELU2: return launch_variant<A_MN, ACT_RELU2, CL>(p, num_ctas, stream);
     default: return launch_variant<A_MN, ACT_NONE, CL>(p, num_ctas, stream);
   }
 }

@@ -27,8 +27,9 @@ _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
-ACT_NAMES = {ACT_NONE: "none", ACT_GELU_ERF: "gelu", ACT_GELU_TANH: "gelu_tanh", ACT_SILU: "silu"}
+ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH, ACT_SILU, ACT_RELU2 = 0, 1, 2, 3, 4
+ACT_NAMES = {ACT_NONE: "none", ACT_GELU_ERF: "gelu", ACT_GELU_TANH: "gelu_tanh", ACT_SILU: "silu",
+             ACT_RELU2: "relu2"}
 
 # stream ids of the tensors one workload draws
 STREAM_X, STREAM_W, STREAM_B = 1, 2, 3

@@ -61,7 +61,8 @@ typedef enum {
   FP_ACT_NONE = 0,
   FP_ACT_GELU_ERF = 1,  /* 0.5 y (1 + erf(y / sqrt 2)) */
   FP_ACT_GELU_TANH = 2, /* 0.5 y (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3))) */
-  FP_ACT_SILU = 3       /* y / (1 + exp(-y)) */
+  FP_ACT_SILU = 3,      /* y / (1 + exp(-y)) */
+  FP_ACT_RELU2 = 4      /* max(y, 0)^2, squared ReLU */
 } fp_act;
 
 typedef enum { FP_BF16 = 0, FP_F32 = 1 } fp_dtype;

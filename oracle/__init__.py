@@ -23,12 +23,13 @@ _SRC = os.path.join(_HERE, "fp_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH, ACT_SILU = 0, 1, 2, 3
+ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH, ACT_SILU, ACT_RELU2 = 0, 1, 2, 3, 4
 
 MUTATIONS = {
     "drop_bias": 1, "rope_sign": 2, "w_transposed": 3, "tanh_const": 4, "scatter_order": 5,
     "rope_interleaved": 6, "rope_freq": 7, "view_not_permute": 8, "act_on_q": 9,
     "pos_global": 10, "rope_on_v": 11, "qk_swapped": 12, "gelu_scale": 13,
+    "relu2_unsquared": 14,
 }
 
 

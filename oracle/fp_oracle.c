@@ -19,8 +19,9 @@
  *     column = head*head_dim + j.
  *  3. Bias, then activation ("[perf] Fused linear", xformers PR #283, PR
  *     description: the op is w x + b followed by the activation). Bias applies
- *     to every column; the activation (exact erf GELU, tanh GELU or SiLU) only
- *     to the ff block.
+ *     to every column; the activation (exact erf GELU, tanh GELU, SiLU, or the
+ *     squared ReLU the same PR's thread names among activations that are slow
+ *     in eager PyTorch) only to the ff block.
  *  4. Rotary embedding of q and k ("Improve performance on RoPE", nvFuser
  *     issue #1597, the rope_one_entry listing): over the first rope_n_elem
  *     lanes of a head, x1/x2 are the two halves, rotated = cat(-x2, x1), and
@@ -50,7 +51,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ACT_NONE = 0, ACT_GELU_ERF = 1, ACT_GELU_TANH = 2, ACT_SILU = 3 };
+enum { ACT_NONE = 0, ACT_GELU_ERF = 1, ACT_GELU_TANH = 2, ACT_SILU = 3, ACT_RELU2 = 4 };
 
 enum {
   MUT_NONE = 0,
@@ -67,6 +68,7 @@ enum {
   MUT_ROPE_ON_V = 11,        /* v rotated too */
   MUT_QK_SWAPPED = 12,       /* q and k column blocks exchanged */
   MUT_GELU_SCALE = 13,       /* erf(y/2) instead of erf(y/sqrt 2) */
+  MUT_RELU2_UNSQUARED = 14,  /* squared ReLU returned as plain ReLU */
 };
 
 typedef struct {
@@ -134,6 +136,9 @@ static double activation(int act, double y, int mutate) {
     }
     case ACT_SILU:
       return y / (1.0 + exp(-y));
+    case ACT_RELU2:
+      if (mutate == MUT_RELU2_UNSQUARED) return y > 0.0 ? y : 0.0;
+      return y > 0.0 ? y * y : 0.0;
     default:
       return y;
   }

@@ -47,6 +47,8 @@ def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, ch
         ff = Fn.gelu(ff, approximate="tanh")
     elif act == 3:
         ff = Fn.silu(ff)
+    elif act == 4:
+        ff = torch.square(Fn.relu(ff))
     hd = head_dim
     rest = Y[:, F:]
     if groups:

@@ -45,6 +45,7 @@ def test_status_strings(lib):
     (32, 40, 2, 16, 0, 0.0),     # ff_hidden not a multiple of head_dim
     (32, 0, 0, 0, 0, 0.0),       # nothing to compute
     (32, 64, 2, 16, 9, 0.0),     # unknown activation
+    (32, 64, 2, 16, 5, 0.0),     # unknown activation
     (512, 0, 2, 256, 0, 10000.0),  # rotary with head_dim > 128
     (32, -1, 2, 16, 0, 0.0),     # negative ff_hidden
 ])

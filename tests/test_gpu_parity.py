@@ -51,6 +51,8 @@ SMALL = [
        rope_n_elem=8, n_query_groups=2),
     W_("gqa_bf16_full_rope", (2, 200, 256), 2, 1, 256, 0, 4, 64, A.ACT_NONE, 10000.0, True, "bf16",
        44, n_query_groups=2),
+    W_("relu2_bf16", (2, 3, 64, 8, 16, 1), 2, 1, 64, 192, 2, 32, A.ACT_RELU2, 0.0, True, "bf16", 45),
+    W_("relu2_fp32", (2, 40, 48), 2, 1, 48, 96, 3, 16, A.ACT_RELU2, 10000.0, True, "f32", 46),
 ]
 
 

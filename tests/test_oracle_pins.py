@@ -55,6 +55,8 @@ SMALL = {
     "gqa_partial_rope": fpsynth.Workload("gqa_partial_rope", (2, 6, 32), 2, 1, 32, 0, 4, 8,
                                          fpsynth.ACT_NONE, 10000.0, False, "bf16", 12,
                                          rope_n_elem=4, n_query_groups=2),
+    "relu2_f32": fpsynth.Workload("relu2_f32", (2, 7, 16), 2, 1, 16, 24, 2, 8,
+                                  fpsynth.ACT_RELU2, 0.0, True, "f32", 13),
 }
 
 
@@ -184,7 +186,9 @@ def pin_activation_closed_forms(mutate=0):
     tanh_ref = [float(y / 2 * (1 + mp.tanh(mp.sqrt(2 / mp.pi) * (y + mp.mpf("0.044715") * y ** 3))))
                 for y in ys]
     silu_ref = [float(y / (1 + mp.exp(-y))) for y in ys]
-    for act, ref, nm in ((1, erf_ref, "gelu"), (2, tanh_ref, "gelu_tanh"), (3, silu_ref, "silu")):
+    relu2_ref = [float(max(y, 0) ** 2) for y in ys]
+    for act, ref, nm in ((1, erf_ref, "gelu"), (2, tanh_ref, "gelu_tanh"), (3, silu_ref, "silu"),
+                         (4, relu2_ref, "relu2")):
         got = _single_column(PTS, act, mutate=mutate)
         # absolute floor: 1 + erf(y/sqrt 2) cancels for y << 0 (error ~ulp(1)*|y|)
         if not _close(got, ref, rtol=1e-14, atol=1e-15):
