@@ -51,7 +51,7 @@ class fp_config(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int32), ("ff_hidden", ctypes.c_int32), ("heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_query_groups", ctypes.c_int32),
                 ("rope_n_elem", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("rope_base", ctypes.c_float)]
+                ("rope_base", ctypes.c_float), ("k_transposed", ctypes.c_int32)]
 
 
 class FpError(RuntimeError):
@@ -194,10 +194,12 @@ class FusedProjection:
     """
 
     def __init__(self, C: int, ff_hidden: int, heads: int, head_dim: int, act="none",
-                 rope_base: float = 0.0, n_query_groups: int = 0, rope_n_elem: int = 0):
+                 rope_base: float = 0.0, n_query_groups: int = 0, rope_n_elem: int = 0,
+                 k_transposed: bool = False):
         a = ACTS[act] if isinstance(act, str) else int(act)
         cfg = fp_config(C, ff_hidden, heads, head_dim, n_query_groups, rope_n_elem, a,
-                        float(rope_base))
+                        float(rope_base), int(bool(k_transposed)))
+        self.k_transposed = bool(k_transposed) and heads > 0
         st, h = fp_create_ex(cfg)
         check(st)
         self.plan = h
@@ -230,6 +232,9 @@ class FusedProjection:
     @property
     def last_launch_count(self) -> int:
         return fp_last_launch_count(self.plan)
+
+    def _head_shape(self, Bb: int, nh: int, T: int, transposed: bool):
+        return (Bb * nh, self.head_dim, T) if transposed else (Bb * nh, T, self.head_dim)
 
     def out_shapes(self, x_shape: Sequence[int], channel_dim: int, n_batch_dims: int):
         tok = [s for a, s in enumerate(x_shape) if a != channel_dim]
@@ -264,14 +269,16 @@ class FusedProjection:
                 raise ValueError("all tensors must be on x's device")
         if out is None:
             ff = torch.empty((M, self.F), device=x.device, dtype=x.dtype) if self.F else None
-            qkv = [torch.empty((Bb * nh, T, self.head_dim), device=x.device, dtype=x.dtype)
-                   for nh in (self.heads, self.kv_heads, self.kv_heads)] \
+            qkv = [torch.empty(self._head_shape(Bb, nh, T, kt), device=x.device, dtype=x.dtype)
+                   for nh, kt in ((self.heads, False), (self.kv_heads, self.k_transposed),
+                                  (self.kv_heads, False))] \
                 if self.heads else [None, None, None]
             out = (ff, *qkv)
         else:
             want = [(M, self.F) if self.F else None] + \
-                   [(Bb * nh, T, self.head_dim) if self.heads else None
-                    for nh in (self.heads, self.kv_heads, self.kv_heads)]
+                   [self._head_shape(Bb, nh, T, kt) if self.heads else None
+                    for nh, kt in ((self.heads, False), (self.kv_heads, self.k_transposed),
+                                   (self.kv_heads, False))]
             for o, shp in zip(out, want):
                 if (o is None) != (shp is None) or (o is not None and (
                         tuple(o.shape) != shp or not o.is_contiguous() or o.dtype != x.dtype)):

@@ -19,6 +19,7 @@
 
 struct fp_plan {
   int C, F, heads, hd, groups, rope_n_elem;
+  int k_transposed;
   int act;
   float rope_base;
   int device;
@@ -354,6 +355,7 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
   e.out_v = a.out_v;
   e.status = sc.status;
   e.bn_eff = bn_eff;
+  e.k_transposed = p->k_transposed;
   const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
 
   if (pr.tc_path) {
@@ -508,6 +510,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->hd = heads > 0 ? hd : 0;
   p->groups = heads > 0 ? G : 0;
   p->rope_n_elem = heads > 0 ? ne : 0;
+  p->k_transposed = heads > 0 && cfg->k_transposed ? 1 : 0;
   p->act = cfg->act;
   p->rope_base = cfg->rope_base;
   p->device = -1;
@@ -530,7 +533,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
 
 fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_dim, fp_act act,
                     float rope_base) {
-  fp_config cfg{C, ff_hidden, heads, head_dim, 0, 0, static_cast<int32_t>(act), rope_base};
+  fp_config cfg{C, ff_hidden, heads, head_dim, 0, 0, static_cast<int32_t>(act), rope_base, 0};
   return fp_create_ex(plan, &cfg);
 }
 
@@ -736,6 +739,7 @@ extern "C" fp_status fp_forward_noalloc(const fp_config* config, const void* x,
   pl.hd = config->heads > 0 ? config->head_dim : 0;
   pl.groups = config->heads > 0 ? config->n_query_groups : 0;
   pl.rope_n_elem = config->heads > 0 ? config->rope_n_elem : 0;
+  pl.k_transposed = config->heads > 0 && config->k_transposed ? 1 : 0;
   pl.act = config->act;
   pl.rope_base = config->rope_base;
   const Args a{x, x_layout, W, b, pos, out_ff, out_q, out_k, out_v};

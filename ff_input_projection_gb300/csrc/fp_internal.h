@@ -42,6 +42,7 @@ struct Epilogue {
   void* out_v;
   int* status;
   int bn_eff;         // columns of an N-tile that this tile owns
+  int k_transposed;   // 1: k is written [B*kv, hd, T]
 };
 
 struct TcParams {

@@ -28,7 +28,7 @@ namespace {
 constexpr int BM = kSimtBM, BN = kSimtBN, BK = 16, NT = 256;
 constexpr int CS_LD = BN + 4;
 // epilogue tile + per-row output bases; covers the 2x(A+B) operand buffers
-constexpr int kSmemBytes = BM * CS_LD * 4 + 4 * BM * 8;
+constexpr int kSmemBytes = BM * CS_LD * 4 + 5 * BM * 8;
 static_assert(2 * BK * (BM + BN) * 4 <= kSmemBytes, "operand buffers must fit in the epilogue tile");
 
 __device__ __forceinline__ int64_t outer_offset(const TokenMap& tk, int64_t o) {
@@ -63,7 +63,7 @@ __device__ __forceinline__ void st_elem(uint16_t* p, int64_t i, float v) {
 
 // Epilogue of one tile, kept out of line so the main loop's register
 // allocation does not carry it. Cs holds the fp32 accumulator tile [BM][CS_LD]
-// followed by room for four [BM] int64 arrays.
+// followed by room for five [BM] int64 arrays.
 template <typename T>
 __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64_t o, int64_t s0,
                                            int n0) {
@@ -79,6 +79,7 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
   int64_t* row_q = row_ff + BM;
   int64_t* row_kv = row_q + BM;
   int64_t* row_t = row_kv + BM;
+  int64_t* row_kt = row_t + BM;
   const int nkv = e.groups > 0 ? e.groups : e.heads;
   if (tid < BM) {
     const int64_t m = o * S_in + s0 + tid;
@@ -87,6 +88,7 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
     row_q[tid] = (bb * e.heads * e.T + t) * e.hd;
     row_kv[tid] = (bb * nkv * e.T + t) * e.hd;
     row_t[tid] = t;
+    row_kt[tid] = bb * nkv * e.hd * e.T + t;
   }
   __syncthreads();
   // each thread owns one column of the tile and every other row
@@ -101,8 +103,12 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
   const int pc = lo ? c + half : c - half;
   const float pbv = (rot && bias) ? ld_elem(bias, lo ? n + half : n - half) : 0.0f;
   T* const base = static_cast<T*>(out_base(e, ci.seg));
-  const int64_t col_off = ci.seg == 0 ? ci.j : static_cast<int64_t>(ci.head) * e.T * e.hd + ci.j;
-  const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : row_kv;
+  // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
+  const bool kt = e.k_transposed && ci.seg == 2;
+  const int64_t col_off = ci.seg == 0 ? ci.j
+                          : kt        ? (static_cast<int64_t>(ci.head) * e.hd + ci.j) * e.T
+                                      : static_cast<int64_t>(ci.head) * e.T * e.hd + ci.j;
+  const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : kt ? row_kt : row_kv;
   const int64_t tile_rows = S_in - s0;
   for (int r = tid / BN; r < BM; r += NT / BN) {
     if (r >= tile_rows) break;

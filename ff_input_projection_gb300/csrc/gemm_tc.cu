@@ -307,6 +307,16 @@ __device__ __forceinline__ float bias_at(const uint32_t (&w)[8], int i) {
   return (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u) : __uint_as_float(w[i >> 1] << 16);
 }
 
+// 16 values at stride `stride` elements (a head lane-column of pre-transposed k).
+__device__ __forceinline__ void store16_bf16_strided(uint16_t* dst, int64_t stride,
+                                                     const float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
+    dst[i * stride] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+}
+
 __device__ __forceinline__ void store16_bf16(void* dst, const float (&v)[16]) {
   uint4 a, b;
   a.x = pack_bf16x2(v[0], v[1]);
@@ -548,6 +558,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       uint16_t* const q_row = static_cast<uint16_t*>(e.out_q) + (bidx * e.heads * e.T + t) * e.hd;
       uint16_t* const k_row = static_cast<uint16_t*>(e.out_k) + (bidx * nkv * e.T + t) * e.hd;
       uint16_t* const v_row = static_cast<uint16_t*>(e.out_v) + (bidx * nkv * e.T + t) * e.hd;
+      // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
+      uint16_t* const kt_row = static_cast<uint16_t*>(e.out_k) + bidx * nkv * head_stride + t;
       const float2* const cs_row = e.rope_cs + t * rh;
       const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
       ColCursor cur;
@@ -567,6 +579,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             ci.seg == 0 ? ff_row + ci.j
                         : (ci.seg == 1 ? q_row : ci.seg == 2 ? k_row : v_row) +
                               ci.head * head_stride + ci.j;
+        const bool kt = e.k_transposed && ci.seg == 2;
+        uint16_t* const dst_t = kt_row + (static_cast<int64_t>(ci.head) * e.hd + ci.j) * e.T;
         uint32_t bl[8];
         load_bias16(bias, n, bl);
         if (rope) {
@@ -591,8 +605,13 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
               hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
             }
-            store16_bf16(dst, lo);
-            store16_bf16(dst + rh, hi);
+            if (kt) {
+              store16_bf16_strided(dst_t, e.T, lo);
+              store16_bf16_strided(dst_t + rh * e.T, e.T, hi);
+            } else {
+              store16_bf16(dst, lo);
+              store16_bf16(dst + rh, hi);
+            }
           }
         } else {
           uint32_t v_u[16];
@@ -608,7 +627,10 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
               if (rope_small) rotate_small(v, cs_row, rh);
             }
-            store16_bf16(dst, v);
+            if (kt)
+              store16_bf16_strided(dst_t, e.T, v);
+            else
+              store16_bf16(dst, v);
           }
         }
       }

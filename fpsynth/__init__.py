@@ -99,6 +99,7 @@ class Workload:
     seed: int
     rope_n_elem: int = 0  # 0: the whole head is rotated
     n_query_groups: int = 0  # 0: one k/v head per q head, blocked [q|k|v] columns
+    k_transposed: bool = False  # k emitted [B*kv, head_dim, T]
 
     @property
     def N(self) -> int:

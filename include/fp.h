@@ -118,6 +118,10 @@ fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_di
  *                   lanes [0, rope_n_elem) rotate with theta_i = pos *
  *                   base^(-2i/rope_n_elem), pairs (i, i + rope_n_elem/2); the
  *                   other lanes pass through.
+ *   k_transposed    0: out_k is [B*kv, T, head_dim] like q and v. 1: out_k is
+ *                   written pre-transposed, [B*kv, head_dim, T], the layout a
+ *                   q k^T product wants (memory-efficient-attention issue #7,
+ *                   the comments on transposing the key once, up front).
  */
 typedef struct {
   int32_t C;
@@ -128,6 +132,7 @@ typedef struct {
   int32_t rope_n_elem;
   int32_t act; /* fp_act */
   float rope_base;
+  int32_t k_transposed;
 } fp_config;
 
 fp_status fp_create_ex(fp_plan** plan, const fp_config* config);

@@ -55,7 +55,7 @@ def _load():
         P = ctypes.c_void_p
         I = ctypes.c_int
         I64 = ctypes.c_int64
-        f.argtypes = [P, I, I, P, P, I, I, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+        f.argtypes = [P, I, I, P, P, I, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_double,
                       P, I64, P, P, P, P, I, I]
         _lib = lib
     return _lib
@@ -68,7 +68,8 @@ def _ptr(a: Optional[np.ndarray]):
 def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_dim: int,
             n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
             rope_base: float, dtype: str, pos: Optional[np.ndarray] = None,
-            groups: int = 0, rope_n_elem: int = 0, rows: Optional[Sequence[int]] = None,
+            groups: int = 0, rope_n_elem: int = 0, k_transposed: bool = False,
+            rows: Optional[Sequence[int]] = None,
             threads: Optional[int] = None, mutate: int = 0,
             x_strides: Optional[Sequence[int]] = None, x_base: Optional[np.ndarray] = None
             ) -> Dict[str, np.ndarray]:
@@ -80,7 +81,7 @@ def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_di
     element strides as ``x_strides``.
 
     Returns ``ff`` [M, F], ``q`` [B*heads, T, hd], ``k``/``v`` [B*kv, T, hd]
-    when ``rows`` is None, else per-row arrays ``ff`` [R, F], ``q`` [R, heads*hd],
+    (``k`` [B*kv, hd, T] with ``k_transposed``) when ``rows`` is None, else per-row arrays ``ff`` [R, F], ``q`` [R, heads*hd],
     ``k``/``v`` [R, kv*hd] for the requested token indices.
     """
     lib = _load()
@@ -106,8 +107,9 @@ def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_di
     T = int(np.prod(tok[n_batch_dims:], dtype=np.int64))
     M = Bb * T
     if rows is None:
+        kshape = (Bb * nkv, head_dim, T) if k_transposed else (Bb * nkv, T, head_dim)
         out = {"ff": np.zeros((M, F)), "q": np.zeros((Bb * heads, T, head_dim)),
-               "k": np.zeros((Bb * nkv, T, head_dim)), "v": np.zeros((Bb * nkv, T, head_dim))}
+               "k": np.zeros(kshape), "v": np.zeros((Bb * nkv, T, head_dim))}
         rr = None
         R = 0
     else:
@@ -119,7 +121,8 @@ def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_di
         threads = os.cpu_count() or 1
     rc = lib.oracle_forward(_ptr(xb), int(is_bf16), x.ndim, _ptr(sizes), _ptr(strides), channel_dim,
                             n_batch_dims, _ptr(Wc), _ptr(bc), _ptr(posc), C, F, heads, head_dim,
-                            groups, rope_n_elem, act, float(rope_base), _ptr(rr), R,
+                            groups, rope_n_elem, act, int(bool(k_transposed)), float(rope_base),
+                            _ptr(rr), R,
                             _ptr(out["ff"]), _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]),
                             int(threads), int(mutate))
     if rc != 0:
@@ -133,4 +136,4 @@ def forward_workload(w, inputs: Dict[str, np.ndarray], **kw) -> Dict[str, np.nda
                    n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
                    head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, dtype=w.dtype,
                    pos=inputs.get("pos"), groups=w.n_query_groups, rope_n_elem=w.rope_n_elem,
-                   **kw)
+                   k_transposed=w.k_transposed, **kw)

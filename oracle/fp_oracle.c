@@ -32,6 +32,8 @@
  *     and fused multiplies", memory-efficient-attention issue #7: the
  *     [batch*heads, tokens, head_dim] layout): ff -> [M, F] token-major,
  *     q/k/v element (b, t, head, j) -> ((b*heads + head)*T + t)*head_dim + j.
+ *     Optionally k is emitted pre-transposed, [batch*heads, head_dim, tokens]
+ *     (same issue, the comments on transposing the key once up front).
  *
  * Grouped-query layout (nvFuser issue #1597, split_qkv listing), selected by
  * n_query_groups > 0: the q|k|v part of a token row is [groups][q_per_kv + 2]
@@ -82,7 +84,7 @@ typedef struct {
   const void* W;
   const void* bias;
   const int32_t* pos;
-  int C, F, heads, hd, groups, rope_n_elem, act;
+  int C, F, heads, hd, groups, rope_n_elem, act, k_transposed;
   double rope_base;
   const int64_t* rows;
   int64_t n_rows;
@@ -263,7 +265,10 @@ static void* run_rows(void* arg) {
       }
       for (int g = 0; g < nkv; ++g) {
         int64_t row = (j->mutate == MUT_SCATTER_ORDER) ? ((int64_t)g * j->Bb + b) : (b * nkv + g);
-        memcpy(&j->out_k[(row * j->T + t) * hd], kh[g], sizeof(double) * (size_t)hd);
+        if (j->k_transposed) /* [B*kv, hd, T]: lane-major, tokens contiguous */
+          for (int i = 0; i < hd; ++i) j->out_k[(row * hd + i) * j->T + t] = kh[g][i];
+        else
+          memcpy(&j->out_k[(row * j->T + t) * hd], kh[g], sizeof(double) * (size_t)hd);
         memcpy(&j->out_v[(row * j->T + t) * hd], vh[g], sizeof(double) * (size_t)hd);
       }
     }
@@ -287,8 +292,9 @@ static void* run_rows(void* arg) {
 int oracle_forward(const void* x, int x_bf16, int ndim, const int64_t* sizes, const int64_t* strides,
                    int channel_dim, int n_batch_dims, const void* W, const void* bias, const int32_t* pos,
                    int C, int F, int heads, int head_dim, int groups, int rope_n_elem, int act,
-                   double rope_base, const int64_t* rows, int64_t n_rows, double* out_ff, double* out_q,
-                   double* out_k, double* out_v, int n_threads, int mutate) {
+                   int k_transposed, double rope_base, const int64_t* rows, int64_t n_rows,
+                   double* out_ff, double* out_q, double* out_k, double* out_v, int n_threads,
+                   int mutate) {
   if (ndim < 1 || ndim > 16 || channel_dim < 0 || channel_dim >= ndim) return -1;
   if (sizes[channel_dim] != C || C <= 0 || F < 0 || heads < 0) return -2;
   if (heads > 0 && (head_dim <= 0 || head_dim % 2 || head_dim > 1024 || heads > 1024)) return -3;
@@ -314,6 +320,7 @@ int oracle_forward(const void* x, int x_bf16, int ndim, const int64_t* sizes, co
   j.groups = groups;
   j.rope_n_elem = rope_n_elem;
   j.act = act;
+  j.k_transposed = k_transposed;
   j.rope_base = rope_base;
   j.rows = rows;
   j.out_ff = out_ff;

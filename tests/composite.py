@@ -27,7 +27,7 @@ import torch.nn.functional as Fn
 def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, channel_dim: int,
               n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
               rope_base: float, pos: Optional[np.ndarray] = None, groups: int = 0,
-              rope_n_elem: int = 0) -> Dict[str, np.ndarray]:
+              rope_n_elem: int = 0, k_transposed: bool = False) -> Dict[str, np.ndarray]:
     x = torch.from_numpy(np.asarray(x64, dtype=np.float64))
     nd = x.dim()
     perm = [a for a in range(nd) if a != channel_dim] + [channel_dim]
@@ -78,7 +78,7 @@ def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, ch
     out = {
         "ff": ff.contiguous().numpy(),
         "q": q.flatten(end_dim=1).contiguous().numpy(),
-        "k": k.flatten(end_dim=1).contiguous().numpy(),
+        "k": (k.transpose(-1, -2) if k_transposed else k).flatten(end_dim=1).contiguous().numpy(),
         "v": v.flatten(end_dim=1).contiguous().numpy(),
     }
     return out

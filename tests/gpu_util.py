@@ -29,7 +29,7 @@ def run(w: fpsynth.Workload, inp: Dict[str, np.ndarray], x_dev: Optional[torch.T
     """Run the library on workload ``w``. ``x_dev`` may be a strided view to read in place."""
     if proj is None:
         proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
-                                   w.n_query_groups, w.rope_n_elem)
+                                   w.n_query_groups, w.rope_n_elem, w.k_transposed)
     x = to_device(inp["x"], w.dtype) if x_dev is None else x_dev
     W = to_device(inp["W"], w.dtype)
     b = to_device(inp["b"], w.dtype)
@@ -77,6 +77,9 @@ def gather_rows(out: Dict[str, torch.Tensor], w: fpsynth.Workload, rows: Sequenc
         if nh == 0:
             res[k] = np.zeros((len(rows), 0))
             continue
-        v = out[k].view(w.Bb, nh, w.T, w.head_dim)[b, :, t, :]
+        if k == "k" and w.k_transposed:
+            v = out[k].view(w.Bb, nh, w.head_dim, w.T)[b, :, :, t]
+        else:
+            v = out[k].view(w.Bb, nh, w.T, w.head_dim)[b, :, t, :]
         res[k] = host(v.reshape(len(rows), nh * w.head_dim))
     return res

@@ -53,6 +53,13 @@ SMALL = [
        44, n_query_groups=2),
     W_("relu2_bf16", (2, 3, 64, 8, 16, 1), 2, 1, 64, 192, 2, 32, A.ACT_RELU2, 0.0, True, "bf16", 45),
     W_("relu2_fp32", (2, 40, 48), 2, 1, 48, 96, 3, 16, A.ACT_RELU2, 10000.0, True, "f32", 46),
+    # k emitted pre-transposed [B*kv, hd, T]: tensor-core (full and partial rotary) and FFMA paths
+    W_("kt_bf16", (2, 3, 64, 8, 16, 1), 2, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 10000.0, True, "bf16",
+       47, k_transposed=True),
+    W_("kt_gqa_bf16", (2, 130, 256), 2, 1, 256, 0, 8, 32, A.ACT_NONE, 10000.0, False, "bf16", 48,
+       rope_n_elem=8, n_query_groups=2, k_transposed=True),
+    W_("kt_fp32", (2, 24, 6, 10), 1, 1, 24, 36, 2, 12, A.ACT_SILU, 10000.0, True, "f32", 49,
+       k_transposed=True),
 ]
 
 

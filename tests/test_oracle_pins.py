@@ -57,6 +57,9 @@ SMALL = {
                                          rope_n_elem=4, n_query_groups=2),
     "relu2_f32": fpsynth.Workload("relu2_f32", (2, 7, 16), 2, 1, 16, 24, 2, 8,
                                   fpsynth.ACT_RELU2, 0.0, True, "f32", 13),
+    "k_transposed": fpsynth.Workload("k_transposed", (2, 5, 24), 2, 1, 24, 0, 3, 8,
+                                     fpsynth.ACT_NONE, 10000.0, True, "f32", 14,
+                                     k_transposed=True),
 }
 
 
@@ -69,7 +72,8 @@ def _composite(w, inp):
                      fpsynth.as_float64(inp["b"], w.dtype), channel_dim=w.channel_dim,
                      n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
                      head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, pos=inp.get("pos"),
-                     groups=w.n_query_groups, rope_n_elem=w.rope_n_elem)
+                     groups=w.n_query_groups, rope_n_elem=w.rope_n_elem,
+                     k_transposed=w.k_transposed)
 
 
 # ---------------------------------------------------------------- pins

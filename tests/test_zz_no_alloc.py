@@ -37,7 +37,7 @@ def _noalloc(w, inp, pos):
     qkv = [torch.empty((Bb * nh, T, w.head_dim), dtype=dt, device="cuda")
            for nh in (w.heads, kvh, kvh)] if w.heads else [None] * 3
     cfg = fpx.fp_config(w.C, w.F, w.heads, w.head_dim, w.n_query_groups, w.rope_n_elem, w.act,
-                        w.rope_base)
+                        w.rope_base, int(w.k_transposed))
     L = fpx.make_layout(x.shape, x.stride(), w.channel_dim, w.n_batch_dims,
                         fpx.FP_BF16 if w.dtype == "bf16" else fpx.FP_F32)
     p = lambda t: None if t is None else t.data_ptr()
