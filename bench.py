@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cluster", type=int, default=2, choices=[1, 2],
+                    help="tensor-core path: CTA pairs sharing weight tiles (2) or single CTAs (1)")
     return ap.parse_args()
 
 
@@ -249,7 +251,8 @@ def main():
     Ws = [to_dev(inp["W"]) for _ in range(n_sets)]
     bs = [to_dev(inp["b"]) for _ in range(n_sets)]
     proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
-                               w.n_query_groups, w.rope_n_elem)
+                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
+    proj.set_option(fpx.FP_OPT_CLUSTER, args.cluster)
     proj.reserve(w.T)
     stream = torch.cuda.Stream(device=dev)
     outs = None
@@ -372,6 +375,7 @@ def main():
                    "C": w.C, "F": w.F, "heads": w.heads, "head_dim": w.head_dim, "N": w.N,
                    "tokens": w.M, "act": fpsynth.ACT_NAMES[w.act], "rope_base": w.rope_base,
                    "bias": w.bias, "parallelism": f"replicas x{world}",
+                   "cta_cluster": args.cluster,
                    "l2": f"inputs rotate over {n_sets} copies ({n_sets * in_bytes / 1e6:.0f} MB) "
                          f"> L2 129 MB; each step also writes {w.M * w.N * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB",
                    "timing": timing_note},
