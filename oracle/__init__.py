@@ -55,8 +55,8 @@ def _load():
         P = ctypes.c_void_p
         I = ctypes.c_int
         I64 = ctypes.c_int64
-        f.argtypes = [P, I, I, P, P, I, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_double,
-                      P, I64, P, P, P, P, I, I]
+        f.argtypes = [P, I, I, P, P, I, I, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                      ctypes.c_double, P, I64, P, P, P, P, I, I]
         _lib = lib
     return _lib
 
@@ -68,6 +68,7 @@ def _ptr(a: Optional[np.ndarray]):
 def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_dim: int,
             n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
             rope_base: float, dtype: str, pos: Optional[np.ndarray] = None,
+            rope_cos: Optional[np.ndarray] = None, rope_sin: Optional[np.ndarray] = None,
             groups: int = 0, rope_n_elem: int = 0, k_transposed: bool = False,
             rows: Optional[Sequence[int]] = None,
             threads: Optional[int] = None, mutate: int = 0,
@@ -101,6 +102,11 @@ def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_di
     Wc = np.ascontiguousarray(W, dtype=want)
     bc = None if b is None else np.ascontiguousarray(b, dtype=want)
     posc = None if pos is None else np.ascontiguousarray(pos, dtype=np.int32)
+    # caller tables: [T, n_rot] values, widened exactly to float64
+    tcos = None if rope_cos is None else np.ascontiguousarray(rope_cos, dtype=np.float64)
+    tsin = None if rope_sin is None else np.ascontiguousarray(rope_sin, dtype=np.float64)
+    if (tcos is None) != (tsin is None):
+        raise ValueError("rope_cos and rope_sin go together")
     nkv = groups if groups else heads
     tok = [s for a, s in enumerate(x.shape) if a != channel_dim]
     Bb = int(np.prod(tok[:n_batch_dims], dtype=np.int64))
@@ -120,7 +126,8 @@ def forward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], *, channel_di
     if threads is None:
         threads = os.cpu_count() or 1
     rc = lib.oracle_forward(_ptr(xb), int(is_bf16), x.ndim, _ptr(sizes), _ptr(strides), channel_dim,
-                            n_batch_dims, _ptr(Wc), _ptr(bc), _ptr(posc), C, F, heads, head_dim,
+                            n_batch_dims, _ptr(Wc), _ptr(bc), _ptr(posc), _ptr(tcos), _ptr(tsin),
+                            C, F, heads, head_dim,
                             groups, rope_n_elem, act, int(bool(k_transposed)), float(rope_base),
                             _ptr(rr), R,
                             _ptr(out["ff"]), _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]),
@@ -135,5 +142,6 @@ def forward_workload(w, inputs: Dict[str, np.ndarray], **kw) -> Dict[str, np.nda
     return forward(inputs["x"], inputs["W"], inputs["b"], channel_dim=w.channel_dim,
                    n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
                    head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, dtype=w.dtype,
-                   pos=inputs.get("pos"), groups=w.n_query_groups, rope_n_elem=w.rope_n_elem,
-                   k_transposed=w.k_transposed, **kw)
+                   pos=inputs.get("pos"), rope_cos=inputs.get("rope_cos"),
+                   rope_sin=inputs.get("rope_sin"), groups=w.n_query_groups,
+                   rope_n_elem=w.rope_n_elem, k_transposed=w.k_transposed, **kw)

@@ -84,6 +84,8 @@ typedef struct {
   const void* W;
   const void* bias;
   const int32_t* pos;
+  const double* rope_cos;  /* [T, n_elem] or NULL */
+  const double* rope_sin;
   int C, F, heads, hd, groups, rope_n_elem, act, k_transposed;
   double rope_base;
   const int64_t* rows;
@@ -146,16 +148,27 @@ static double activation(int act, double y, int mutate) {
   }
 }
 
-/* rope_one_entry on one head vector u[hd] at position p (in place). */
-static void rotate_half(double* u, int hd, int n_elem, double p, double base, int mutate) {
+/* rope_one_entry on one head vector u[hd] at position p (in place). With
+ * tab_cos/tab_sin (the n_elem values of the token's row of caller-given
+ * [T, n_elem] tables) those are the per-lane cos/sin; otherwise both halves
+ * of pair i use cos/sin of theta_i = p * base^(-2i/n_elem). */
+static void rotate_half(double* u, int hd, int n_elem, double p, double base, int mutate,
+                        const double* tab_cos, const double* tab_sin) {
   double xr[1024], rotated[1024], cosv[1024], sinv[1024];
   int half = n_elem / 2;
   for (int i = 0; i < n_elem; ++i) xr[i] = u[i];
-  for (int i = 0; i < half; ++i) {
-    double e = (mutate == MUT_ROPE_FREQ) ? (double)i / n_elem : 2.0 * i / n_elem;
-    double theta = p * pow(base, -e);
-    cosv[i] = cosv[i + half] = cos(theta);
-    sinv[i] = sinv[i + half] = sin(theta);
+  if (tab_cos) {
+    for (int i = 0; i < n_elem; ++i) {
+      cosv[i] = tab_cos[i];
+      sinv[i] = tab_sin[i];
+    }
+  } else {
+    for (int i = 0; i < half; ++i) {
+      double e = (mutate == MUT_ROPE_FREQ) ? (double)i / n_elem : 2.0 * i / n_elem;
+      double theta = p * pow(base, -e);
+      cosv[i] = cosv[i + half] = cos(theta);
+      sinv[i] = sinv[i + half] = sin(theta);
+    }
   }
   if (mutate == MUT_ROPE_INTERLEAVED) {
     /* a plausible mix-up with the interleaved (GPT-J) convention */
@@ -242,10 +255,12 @@ static void* run_rows(void* arg) {
       int64_t tp = (j->mutate == MUT_POS_GLOBAL) ? m : t;
       double p = j->pos ? (double)j->pos[tp % j->T] : (double)tp;
       int ne = j->rope_n_elem > 0 ? j->rope_n_elem : hd;
-      for (int h = 0; h < nq; ++h) rotate_half(qh[h], hd, ne, p, j->rope_base, j->mutate);
-      for (int g = 0; g < nkv; ++g) rotate_half(kh[g], hd, ne, p, j->rope_base, j->mutate);
+      const double* tc = j->rope_cos ? j->rope_cos + (tp % j->T) * ne : NULL;
+      const double* ts = j->rope_sin ? j->rope_sin + (tp % j->T) * ne : NULL;
+      for (int h = 0; h < nq; ++h) rotate_half(qh[h], hd, ne, p, j->rope_base, j->mutate, tc, ts);
+      for (int g = 0; g < nkv; ++g) rotate_half(kh[g], hd, ne, p, j->rope_base, j->mutate, tc, ts);
       if (j->mutate == MUT_ROPE_ON_V)
-        for (int g = 0; g < nkv; ++g) rotate_half(vh[g], hd, ne, p, j->rope_base, 0);
+        for (int g = 0; g < nkv; ++g) rotate_half(vh[g], hd, ne, p, j->rope_base, 0, tc, ts);
     }
 
     /* 5. split / scatter */
@@ -285,12 +300,15 @@ static void* run_rows(void* arg) {
  *    x is addressed through sizes/strides (elements). W is [C, N] row-major,
  *    N = F + 3*heads*hd (or F + (heads + 2*groups)*hd when groups > 0).
  *    bias is [N] or NULL. pos is [T] int32 or NULL (positions 0..T-1).
+ *  rope_cos/rope_sin: NULL, or caller-given [T, n_rot] tables (row t is the
+ *    token's cos/sin per rotated lane; pos is then unused).
  *  rows/n_rows: NULL for every token (outputs scattered to the head-major
  *    layout), else the token indices to evaluate (outputs per sampled row).
  *  n_threads: worker threads (>= 1).
  */
 int oracle_forward(const void* x, int x_bf16, int ndim, const int64_t* sizes, const int64_t* strides,
                    int channel_dim, int n_batch_dims, const void* W, const void* bias, const int32_t* pos,
+                   const double* rope_cos, const double* rope_sin,
                    int C, int F, int heads, int head_dim, int groups, int rope_n_elem, int act,
                    int k_transposed, double rope_base, const int64_t* rows, int64_t n_rows,
                    double* out_ff, double* out_q, double* out_k, double* out_v, int n_threads,
@@ -313,6 +331,8 @@ int oracle_forward(const void* x, int x_bf16, int ndim, const int64_t* sizes, co
   j.W = W;
   j.bias = bias;
   j.pos = pos;
+  j.rope_cos = rope_cos;
+  j.rope_sin = rope_sin;
   j.C = C;
   j.F = F;
   j.heads = heads;

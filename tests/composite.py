@@ -27,7 +27,9 @@ import torch.nn.functional as Fn
 def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, channel_dim: int,
               n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
               rope_base: float, pos: Optional[np.ndarray] = None, groups: int = 0,
-              rope_n_elem: int = 0, k_transposed: bool = False) -> Dict[str, np.ndarray]:
+              rope_n_elem: int = 0, k_transposed: bool = False,
+              rope_cos: Optional[np.ndarray] = None,
+              rope_sin: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     x = torch.from_numpy(np.asarray(x64, dtype=np.float64))
     nd = x.dim()
     perm = [a for a in range(nd) if a != channel_dim] + [channel_dim]
@@ -73,6 +75,17 @@ def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, ch
         def rope(u):
             z = torch.complex(u[..., :half], u[..., half:n]) * rot
             return torch.cat([z.real, z.imag, u[..., n:]], dim=-1)
+
+        if rope_cos is not None:
+            # caller tables, one cos/sin per rotated lane: the elementwise form
+            # x*cos + cat(-x2, x1)*sin
+            tc = torch.from_numpy(np.asarray(rope_cos, dtype=np.float64))
+            ts = torch.from_numpy(np.asarray(rope_sin, dtype=np.float64))
+
+            def rope(u):  # noqa: F811
+                xr = u[..., :n]
+                rotated = torch.cat([-xr[..., half:], xr[..., :half]], dim=-1)
+                return torch.cat([xr * tc + rotated * ts, u[..., n:]], dim=-1)
 
         q, k = rope(q), rope(k)
     out = {

@@ -73,7 +73,8 @@ def _composite(w, inp):
                      n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
                      head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, pos=inp.get("pos"),
                      groups=w.n_query_groups, rope_n_elem=w.rope_n_elem,
-                     k_transposed=w.k_transposed)
+                     k_transposed=w.k_transposed, rope_cos=inp.get("rope_cos"),
+                     rope_sin=inp.get("rope_sin"))
 
 
 # ---------------------------------------------------------------- pins
@@ -319,9 +320,69 @@ def pin_strided_view(mutate=0):
     return [] if all(_close(a[k], b[k], rtol=0, atol=0) for k in "qkv") else ["strided"]
 
 
+def _table_case(seed=3):
+    w = SMALL["gqa_partial_rope"].scaled(name="table_case", rope_n_elem=6)
+    inp = fpsynth.make_inputs(w)
+    rng = np.random.default_rng(seed)
+    n = w.rope_n_elem
+    inp["rope_cos"] = rng.standard_normal((w.T, n))
+    inp["rope_sin"] = rng.standard_normal((w.T, n))
+    return w, inp
+
+
+def pin_rope_table_forms(mutate=0):
+    """Caller cos/sin tables (the rope_one_entry listing's inputs, random as in
+    its test): the torch elementwise form, two exact special tables, linearity
+    in (cos, sin), and agreement with the computed angles when the table holds
+    them."""
+    bad = []
+    w, inp = _table_case()
+    got = _oracle(w, inp, mutate)
+    ref = _composite(w, inp)
+    for k in ("q", "k", "v"):
+        if not _close(got[k], ref[k], rtol=1e-12, atol=1e-12):
+            bad.append(f"table-composite:{k}")
+    n, h = w.rope_n_elem, w.rope_n_elem // 2
+    plain = _oracle(w.scaled(rope_base=0.0), {**inp, "rope_cos": None, "rope_sin": None}, mutate)
+    # cos = 1, sin = 0: identity; cos = 0, sin = 1: the rotated vector cat(-x2, x1), exactly
+    ident = _oracle(w, {**inp, "rope_cos": np.ones((w.T, n)), "rope_sin": np.zeros((w.T, n))},
+                    mutate)
+    quarter = _oracle(w, {**inp, "rope_cos": np.zeros((w.T, n)), "rope_sin": np.ones((w.T, n))},
+                      mutate)
+    for k in ("q", "k"):
+        if not _close(ident[k], plain[k], rtol=0, atol=0):
+            bad.append(f"table-identity:{k}")
+        want = plain[k].copy()
+        want[..., :h] = -plain[k][..., h:n]
+        want[..., h:n] = plain[k][..., :h]
+        if not _close(quarter[k], want, rtol=0, atol=0):
+            bad.append(f"table-quarter:{k}")
+    # linearity: the rotated lanes are linear in (cos, sin) jointly
+    rng = np.random.default_rng(9)
+    c2, s2 = rng.standard_normal((w.T, n)), rng.standard_normal((w.T, n))
+    o2 = _oracle(w, {**inp, "rope_cos": c2, "rope_sin": s2}, mutate)
+    o12 = _oracle(w, {**inp, "rope_cos": inp["rope_cos"] + c2, "rope_sin": inp["rope_sin"] + s2},
+                  mutate)
+    for k in ("q", "k"):
+        if not _close(o12[k][..., :n], got[k][..., :n] + o2[k][..., :n], rtol=1e-12, atol=1e-12):
+            bad.append(f"table-linear:{k}")
+    # a table holding cos/sin of the default angles reproduces the computed path
+    wf = w.scaled(rope_n_elem=0)
+    nf = wf.head_dim
+    ang = np.arange(wf.T)[:, None] * wf.rope_base ** (-2.0 * np.arange(nf // 2) / nf)[None, :]
+    ang = np.concatenate([ang, ang], axis=1)
+    tab = _oracle(wf, {**inp, "rope_cos": np.cos(ang), "rope_sin": np.sin(ang)}, mutate)
+    comp = _oracle(wf, {**inp, "rope_cos": None, "rope_sin": None}, mutate)
+    for k in ("q", "k"):
+        if not _close(tab[k], comp[k], rtol=1e-12, atol=1e-12):
+            bad.append(f"table-vs-angles:{k}")
+    return bad
+
+
 PINS = [pin_composite, pin_hand_linear, pin_hand_scatter, pin_quarter_turn,
         pin_activation_closed_forms, pin_linear_is_unsplit_gemm, pin_rope_position_zero_identity,
-        pin_rope_pair_norm, pin_rope_relative_position, pin_rows_match_full, pin_strided_view]
+        pin_rope_pair_norm, pin_rope_relative_position, pin_rows_match_full, pin_strided_view,
+        pin_rope_table_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
