@@ -36,7 +36,8 @@ FP_OPT_MAX_CTAS = 4
 FP_OPT_CLUSTER = 5
 
 # the C ABI's entry points, as declared in include/fp.h
-EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_noalloc", "fp_reserve", "fp_get_device_status",
+EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_rope_table",
+           "fp_forward_noalloc", "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
 
@@ -52,6 +53,11 @@ class fp_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("n_query_groups", ctypes.c_int32),
                 ("rope_n_elem", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("rope_base", ctypes.c_float), ("k_transposed", ctypes.c_int32)]
+
+
+class fp_rope_table(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("stride_t", ctypes.c_int64),
+                ("stride_i", ctypes.c_int64)]
 
 
 class FpError(RuntimeError):
@@ -83,6 +89,9 @@ def load():
     lib.fp_create_ex.restype = I
     lib.fp_forward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
     lib.fp_forward.restype = I
+    lib.fp_forward_rope_table.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P,
+                                          ctypes.POINTER(fp_rope_table), P, P, P, P, P]
+    lib.fp_forward_rope_table.restype = I
     lib.fp_forward_noalloc.argtypes = [ctypes.POINTER(fp_config), P, ctypes.POINTER(fp_layout), P,
                                        P, P, P, P, P, P, P]
     lib.fp_forward_noalloc.restype = I
@@ -134,6 +143,14 @@ def fp_forward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int], p
                out_v: Optional[int], stream: Optional[int]) -> int:
     return load().fp_forward(plan, x, ctypes.byref(layout), W, b, pos, out_ff, out_q, out_k, out_v,
                              stream)
+
+
+def fp_forward_rope_table(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
+                          rope_cos: int, rope_sin: int, table: fp_rope_table,
+                          out_ff: Optional[int], out_q: Optional[int], out_k: Optional[int],
+                          out_v: Optional[int], stream: Optional[int]) -> int:
+    return load().fp_forward_rope_table(plan, x, ctypes.byref(layout), W, b, rope_cos, rope_sin,
+                                        ctypes.byref(table), out_ff, out_q, out_k, out_v, stream)
 
 
 def fp_forward_noalloc(config: fp_config, x: int, layout: fp_layout, W: int, b: Optional[int],
@@ -247,7 +264,9 @@ class FusedProjection:
         return Bb, T
 
     def forward(self, x, W, b=None, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
-                out=None, stream=None):
+                out=None, stream=None, rope_cos=None, rope_sin=None):
+        """rope_cos/rope_sin: optional [T, n_rot] tables (any strides) used per lane
+        instead of positions."""
         import torch
         if x.dtype not in (torch.bfloat16, torch.float32):
             raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
@@ -287,7 +306,20 @@ class FusedProjection:
         ptr = lambda t: None if t is None else t.data_ptr()
         if stream is None:
             stream = torch.cuda.current_stream(x.device).cuda_stream
-        st = fp_forward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
-                        ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
+        if rope_cos is not None or rope_sin is not None:
+            if rope_cos is None or rope_sin is None or pos is not None:
+                raise ValueError("give rope_cos and rope_sin together, without pos")
+            if rope_cos.shape != rope_sin.shape or rope_cos.stride() != rope_sin.stride() or \
+                    rope_cos.dim() != 2 or rope_cos.shape[0] != T or rope_cos.dtype != rope_sin.dtype \
+                    or rope_cos.dtype not in (torch.bfloat16, torch.float32):
+                raise ValueError("rope_cos/rope_sin must be matching [T, n_rot] bf16/f32 tensors")
+            tl = fp_rope_table(FP_BF16 if rope_cos.dtype == torch.bfloat16 else FP_F32,
+                               rope_cos.stride(0), rope_cos.stride(1))
+            st = fp_forward_rope_table(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b),
+                                       rope_cos.data_ptr(), rope_sin.data_ptr(), tl, ptr(out[0]),
+                                       ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
+        else:
+            st = fp_forward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
+                            ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
         check(st)
         return out

@@ -320,16 +320,33 @@ fp_status prepare(const fp_plan& P, const Args& a, Prepared& pr) {
   return FP_OK;
 }
 
-// Enqueue the rotary table (when build_table) and the GEMM kernel on `stream`.
-// Uses only the scratch it is given; allocates nothing.
+// Caller-given rotary tables [T, n_rot] (cos and sin, any strides).
+struct ExtTable {
+  const void* cosv;
+  const void* sinv;
+  bool bf16;
+  int64_t stride_t, stride_i;
+};
+
+// Enqueue the rotary table (when build_table, or the import of caller tables
+// when ext is given) and the GEMM kernel on `stream`. Uses only the scratch it
+// is given; allocates nothing.
 fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scratch& sc,
-                 bool build_table, cudaStream_t stream, int* launches) {
+                 bool build_table, cudaStream_t stream, int* launches,
+                 const ExtTable* ext = nullptr) {
   const fp_plan* p = &P;
   const TokAxes& ta = pr.ta;
   const fp::TokenMap& tk = pr.tk;
   const int N = pr.N, esz = pr.esz, rh = pr.rh, bn_eff = pr.bn_eff;
   *launches = 0;
-  if (build_table) {
+  if (ext) {
+    cudaError_t err = fp::launch_rope_import(reinterpret_cast<float4*>(sc.table), ext->cosv,
+                                             ext->sinv, ext->bf16, ta.T, rh, ext->stride_t,
+                                             ext->stride_i, stream);
+    if (err != cudaSuccess)
+      return fail(FP_ERR_CUDA, "rotary table import launch: %s", cudaGetErrorString(err));
+    ++*launches;
+  } else if (build_table) {
     cudaError_t err = fp::launch_rope_table(sc.table, a.pos, ta.T, rh, 2 * rh,
                                             static_cast<double>(p->rope_base), stream);
     if (err != cudaSuccess)
@@ -347,7 +364,9 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
   e.groups = p->groups;
   e.act = p->act;
   e.rope_half = rh;
-  e.rope_cs = pr.rope ? sc.table : nullptr;
+  e.rope_cs = pr.rope && !ext ? sc.table : nullptr;
+  e.rope_cs4 = ext ? reinterpret_cast<const float4*>(sc.table) : nullptr;
+  e.rope_per_lane = ext ? 1 : 0;
   e.bias = a.b;
   e.out_ff = a.out_ff;
   e.out_q = a.out_q;
@@ -644,6 +663,62 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
     p->table_stream = stream;
     p->table_T = pos ? -1 : pr.ta.T;
   }
+  p->last_launches = launches;
+  return ok();
+}
+
+fp_status fp_forward_rope_table(fp_plan* p, const void* x, const fp_layout* x_layout,
+                                const void* W, const void* b, const void* rope_cos,
+                                const void* rope_sin, const fp_rope_table* tl, void* out_ff,
+                                void* out_q, void* out_k, void* out_v, void* stream_v) {
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (rope_half_of(p) == 0) return fail(FP_ERR_INVALID_ARG, "the plan has no rotary embedding");
+  if (!rope_cos || !rope_sin || !tl)
+    return fail(FP_ERR_INVALID_ARG, "rope_cos, rope_sin and their layout must be non-NULL");
+  if (tl->dtype != FP_BF16 && tl->dtype != FP_F32)
+    return fail(FP_ERR_INVALID_ARG, "unknown table dtype");
+  if (tl->stride_t < 0 || tl->stride_i < 0)
+    return fail(FP_ERR_INVALID_ARG, "negative table stride");
+  const int tsz = tl->dtype == FP_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(rope_cos) % tsz || reinterpret_cast<uintptr_t>(rope_sin) % tsz)
+    return fail(FP_ERR_MISALIGNED, "tables must be aligned to their element size");
+  const Args a{x, x_layout, W, b, nullptr, out_ff, out_q, out_k, out_v};
+  Prepared pr;
+  fp_status st = prepare(*p, a, pr);
+  if (st != FP_OK) return st;
+  if (pr.ta.M == 0) {
+    p->last_launches = 0;
+    return ok();
+  }
+  // outputs may not overlap the tables either
+  const int n_rot = 2 * pr.rh;
+  const int64_t span = (pr.ta.T - 1) * tl->stride_t + (n_rot - 1) * tl->stride_i + 1;
+  auto rng = [](const void* q, int64_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(q);
+    return Range{lo, q ? lo + static_cast<uintptr_t>(bytes) : lo};
+  };
+  const int nkv = p->groups > 0 ? p->groups : p->heads;
+  const Range tabs[] = {rng(rope_cos, span * tsz), rng(rope_sin, span * tsz)};
+  const Range outs[] = {rng(out_ff, pr.ta.M * p->F * pr.esz),
+                        rng(out_q, pr.ta.M * p->heads * p->hd * pr.esz),
+                        rng(out_k, pr.ta.M * nkv * p->hd * pr.esz),
+                        rng(out_v, pr.ta.M * nkv * p->hd * pr.esz)};
+  for (const Range& o : outs)
+    for (const Range& t : tabs)
+      if (overlaps(o, t)) return fail(FP_ERR_INVALID_ARG, "an output overlaps a rotary table");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  // the imported table is one float4 per (position, pair): two float2 entries
+  st = ensure_device_state(p, 2 * pr.ta.T * pr.rh);
+  if (st != FP_OK) return st;
+  p->table_T = -1;  // the default-position table (if any) is overwritten
+  p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
+  const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
+                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster};
+  const ExtTable ext{rope_cos, rope_sin, tl->dtype == FP_BF16, tl->stride_t, tl->stride_i};
+  int launches = 0;
+  st = launch(*p, pr, a, sc, false, stream, &launches, &ext);
+  if (st != FP_OK) return st;
+  p->inject_stall = 0;
   p->last_launches = launches;
   return ok();
 }

@@ -34,7 +34,9 @@ struct Epilogue {
   int N, F, C, heads, hd, groups;  // groups > 0: grouped-query column order
   int act;
   int rope_half;      // 0: no rotation, else rotated lanes / 2
-  const float2* rope_cs;  // [T][rope_half] (cos, sin)
+  const float2* rope_cs;  // [T][rope_half] (cos, sin) of theta_i, shared by lanes i and i+half
+  const float4* rope_cs4; // per-lane tables: [T][rope_half] (cos_i, sin_i, cos_i+h, sin_i+h)
+  int rope_per_lane;      // 1: use rope_cs4
   const void* bias;   // [N] or null, dtype of x
   void* out_ff;
   void* out_q;
@@ -78,6 +80,9 @@ struct SimtParams {
 // Launchers (defined in the .cu files). Return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
                               double rope_base, cudaStream_t stream);
+cudaError_t launch_rope_import(float4* dst, const void* cosv, const void* sinv, bool bf16,
+                               int64_t T, int half, int64_t stride_t, int64_t stride_i,
+                               cudaStream_t stream);
 cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream);
 cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream);
 

@@ -117,9 +117,14 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
       v = activate(e.act, v);
     } else if (rot) {
       const float pv = Cs[r * CS_LD + pc] + pbv;
-      const float2 cs = e.rope_cs[row_t[r] * half + f];
       // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
-      v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+      if (e.rope_per_lane) {
+        const float4 c4 = e.rope_cs4[row_t[r] * half + f];
+        v = lo ? v * c4.x - pv * c4.y : v * c4.z + pv * c4.w;
+      } else {
+        const float2 cs = e.rope_cs[row_t[r] * half + f];
+        v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+      }
     }
     st_elem(base, rb[r] + col_off, v);
   }

@@ -346,6 +346,32 @@ __device__ __forceinline__ void rotate_in_granule(float (&v)[16], const float2* 
   }
 }
 
+// Per-lane tables: lane i uses (cos_i, sin_i), lane i+RH uses (cos_i+RH, sin_i+RH).
+template <int RH>
+__device__ __forceinline__ void rotate_in_granule4(float (&v)[16], const float4* __restrict__ cs) {
+#pragma unroll
+  for (int i = 0; i < RH; ++i) {
+    const float4 c = __ldg(cs + i);
+    const float x = v[i], y = v[i + RH];
+    v[i] = x * c.x - y * c.y;
+    v[i + RH] = y * c.z + x * c.w;
+  }
+}
+
+__device__ __forceinline__ void rotate_small4(float (&v)[16], const float4* cs, int rh) {
+  switch (rh) {
+    case 1: rotate_in_granule4<1>(v, cs); break;
+    case 2: rotate_in_granule4<2>(v, cs); break;
+    case 3: rotate_in_granule4<3>(v, cs); break;
+    case 4: rotate_in_granule4<4>(v, cs); break;
+    case 5: rotate_in_granule4<5>(v, cs); break;
+    case 6: rotate_in_granule4<6>(v, cs); break;
+    case 7: rotate_in_granule4<7>(v, cs); break;
+    case 8: rotate_in_granule4<8>(v, cs); break;
+    default: break;
+  }
+}
+
 __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, int rh) {
   switch (rh) {
     case 1: rotate_in_granule<1>(v, cs); break;
@@ -591,7 +617,17 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           uint32_t bh[8];
           load_bias16(bias, n + rh, bh);
           float lo[16], hi[16];
-          if (valid) {
+          if (valid && e.rope_per_lane) {
+            const float4* t4 = e.rope_cs4 + t * rh + ci.j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 c = __ldg(t4 + i);  // (cos, sin) of lane i and of lane i + rh
+              const float x = __uint_as_float(lo_u[i]) + bias_at(bl, i);
+              const float y = __uint_as_float(hi_u[i]) + bias_at(bh, i);
+              lo[i] = x * c.x - y * c.y;
+              hi[i] = y * c.z + x * c.w;
+            }
+          } else if (valid) {
             const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -625,7 +661,12 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             } else {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
-              if (rope_small) rotate_small(v, cs_row, rh);
+              if (rope_small) {
+                if (e.rope_per_lane)
+                  rotate_small4(v, e.rope_cs4 + t * rh, rh);
+                else
+                  rotate_small(v, cs_row, rh);
+              }
             }
             if (kt)
               store16_bf16_strided(dst_t, e.T, v);

@@ -32,6 +32,37 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, const int32_t* __rest
   cs[i] = make_float2(c, s);
 }
 
+// Caller-given tables (the rope_one_entry listing's cos/sin inputs, [T, n_rot],
+// any strides, bf16 or f32): repacked per rotated pair as (cos_i, sin_i,
+// cos_{i+half}, sin_{i+half}) in fp32, so the epilogue reads one float4 per pair.
+__device__ __forceinline__ float load_any(const void* p, bool bf16, int64_t i) {
+  if (bf16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16);
+  return static_cast<const float*>(p)[i];
+}
+
+__global__ void rope_import_kernel(float4* __restrict__ dst, const void* cosv, const void* sinv,
+                                   bool bf16, int64_t T, int half, int64_t st_t, int64_t st_i) {
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= T * half) return;
+  int64_t t = i / half;
+  int64_t f = i - t * half;
+  const int64_t lo = t * st_t + f * st_i, hi = t * st_t + (f + half) * st_i;
+  dst[i] = make_float4(load_any(cosv, bf16, lo), load_any(sinv, bf16, lo), load_any(cosv, bf16, hi),
+                       load_any(sinv, bf16, hi));
+}
+
+cudaError_t launch_rope_import(float4* dst, const void* cosv, const void* sinv, bool bf16,
+                               int64_t T, int half, int64_t stride_t, int64_t stride_i,
+                               cudaStream_t stream) {
+  int64_t n = T * half;
+  if (n == 0) return cudaSuccess;
+  int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  rope_import_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      dst, cosv, sinv, bf16, T, half, stride_t, stride_i);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
                               double rope_base, cudaStream_t stream) {
   int64_t n = T * half;

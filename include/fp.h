@@ -166,6 +166,30 @@ fp_status fp_forward(fp_plan* plan, const void* x, const fp_layout* x_layout, co
                      void* out_v, void* stream);
 
 /*
+ * fp_forward_rope_table — fp_forward with caller-given rotary tables instead
+ * of positions: the cos and sin inputs of the rope_one_entry listing (nvFuser
+ * issue #1597 "Improve performance on RoPE"), [T, n_rot] with n_rot =
+ * rope_n_elem (or head_dim), addressed through `layout` (the listing notes the
+ * inner dimension need not be contiguous). Lane i < n_rot/2 of a rotated head
+ * becomes x_i cos[t,i] - x_{i+n_rot/2} sin[t,i], lane i + n_rot/2 becomes
+ * x_{i+n_rot/2} cos[t,i+n_rot/2] + x_i sin[t,i+n_rot/2]; t is the token's index
+ * inside its batch element. The plan must have been created with rotary
+ * embedding (its base is then unused). The tables are repacked on `stream` into
+ * the plan's scratch (allocated on first use, 16 bytes per position and pair);
+ * they must stay valid until the work completes. Other arguments as fp_forward.
+ */
+typedef struct {
+  int32_t dtype;    /* fp_dtype of cos and sin */
+  int64_t stride_t; /* elements between consecutive positions */
+  int64_t stride_i; /* elements between consecutive lanes */
+} fp_rope_table;
+
+fp_status fp_forward_rope_table(fp_plan* plan, const void* x, const fp_layout* x_layout,
+                                const void* W, const void* b, const void* rope_cos,
+                                const void* rope_sin, const fp_rope_table* layout, void* out_ff,
+                                void* out_q, void* out_k, void* out_v, void* stream);
+
+/*
  * fp_forward_noalloc — fp_forward for callers that may not allocate device
  * memory. The pages have no counterpart: it exists for callers such as a
  * plug-in running inside a host framework that owns every device byte through

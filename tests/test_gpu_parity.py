@@ -221,3 +221,48 @@ def test_cluster_pairs_match_single_ctas(w, cuda_ok):
     for k in ("ff", "q", "k", "v"):
         if outs[1][k] is not None:
             assert_close(host(outs[1][k]), ref[k], w.dtype, f"{w.name}:{k}")
+
+
+TABLE_CASES = [
+    W_("table_bf16_full", (2, 3, 64, 8, 16, 1), 2, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 10000.0, True,
+       "bf16", 71),
+    W_("table_bf16_partial", (2, 130, 256), 2, 1, 256, 0, 8, 32, A.ACT_NONE, 10000.0, False, "bf16",
+       72, rope_n_elem=8, n_query_groups=2),
+    W_("table_fp32", (2, 24, 6, 10), 1, 1, 24, 36, 2, 12, A.ACT_SILU, 10000.0, True, "f32", 73,
+       k_transposed=True),
+]
+
+
+@pytest.mark.parametrize("w", TABLE_CASES, ids=lambda w: w.name)
+def test_caller_rope_tables(w, cuda_ok):
+    """cos/sin given per lane as [T, n_rot] tables with a non-contiguous inner
+    dimension (every other column of a wider buffer), filled at random like the
+    rope_one_entry test."""
+    inp = fpsynth.make_inputs(w)
+    n = w.rope_n_elem or w.head_dim
+    rng = np.random.default_rng(w.seed)
+    store = (lambda a: fpsynth.f32_to_bf16_bits(a.astype(np.float32))) if w.dtype == "bf16" \
+        else (lambda a: a.astype(np.float32))
+    wide_c = store(rng.standard_normal((w.T, 2 * n)))
+    wide_s = store(rng.standard_normal((w.T, 2 * n)))
+    cos_d = to_device(wide_c, w.dtype)[:, ::2]
+    sin_d = to_device(wide_s, w.dtype)[:, ::2]
+    assert cos_d.stride(1) == 2
+    inp["rope_cos"] = fpsynth.as_float64(np.ascontiguousarray(wide_c[:, ::2]), w.dtype)
+    inp["rope_sin"] = fpsynth.as_float64(np.ascontiguousarray(wide_s[:, ::2]), w.dtype)
+    ref = oracle.forward_workload(w, inp)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
+    x, W, b = (to_device(inp[k], w.dtype) for k in ("x", "W", "b"))
+    out = proj.forward(x, W, b, None, channel_dim=w.channel_dim, rope_cos=cos_d, rope_sin=sin_d)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK
+    assert proj.last_launch_count == 2  # table import + GEMM
+    for k, o in zip(("ff", "q", "k", "v"), out):
+        if o is not None:
+            assert_close(host(o), ref[k], w.dtype, f"{w.name}:{k}")
+    # a later default-position call rebuilds its own table
+    ref2 = oracle.forward_workload(w, {**inp, "rope_cos": None, "rope_sin": None})
+    out2 = run(w, {**inp, "rope_cos": None, "rope_sin": None}, proj=proj)
+    for k in ("q", "k"):
+        assert_close(host(out2[k]), ref2[k], w.dtype, f"{w.name}:default:{k}")
