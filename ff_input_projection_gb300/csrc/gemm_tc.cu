@@ -617,29 +617,31 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           uint32_t bh[8];
           load_bias16(bias, n + rh, bh);
           float lo[16], hi[16];
-          if (valid && e.rope_per_lane) {
-            const float4* t4 = e.rope_cs4 + t * rh + ci.j;
+          if (valid) {
+            if (e.rope_per_lane) {
+              const float4* t4 = e.rope_cs4 + t * rh + ci.j;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float4 c = __ldg(t4 + i);  // (cos, sin) of lane i and of lane i + rh
-              const float x = __uint_as_float(lo_u[i]) + bias_at(bl, i);
-              const float y = __uint_as_float(hi_u[i]) + bias_at(bh, i);
-              lo[i] = x * c.x - y * c.y;
-              hi[i] = y * c.z + x * c.w;
-            }
-          } else if (valid) {
-            const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
+              for (int i = 0; i < 16; ++i) {
+                const float4 c = __ldg(t4 + i);  // (cos, sin) of lane i and of lane i + rh
+                const float x = __uint_as_float(lo_u[i]) + bias_at(bl, i);
+                const float y = __uint_as_float(hi_u[i]) + bias_at(bh, i);
+                lo[i] = x * c.x - y * c.y;
+                hi[i] = y * c.z + x * c.w;
+              }
+            } else {
+              const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
-              const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
-              const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
-              const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
-              const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
-              lo[2 * i] = x0 * cs.x - y0 * cs.y;
-              hi[2 * i] = y0 * cs.x + x0 * cs.y;
-              lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
-              hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
+              for (int i = 0; i < 8; ++i) {
+                const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
+                const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
+                const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
+                const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
+                const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
+                lo[2 * i] = x0 * cs.x - y0 * cs.y;
+                hi[2 * i] = y0 * cs.x + x0 * cs.y;
+                lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
+                hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
+              }
             }
             if (kt) {
               store16_bf16_strided(dst_t, e.T, lo);
