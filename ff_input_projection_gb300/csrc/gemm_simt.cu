@@ -110,23 +110,44 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
                                       : static_cast<int64_t>(ci.head) * e.T * e.hd + ci.j;
   const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : kt ? row_kt : row_kv;
   const int64_t tile_rows = S_in - s0;
-  for (int r = tid / BN; r < BM; r += NT / BN) {
-    if (r >= tile_rows) break;
-    float v = Cs[r * CS_LD + c] + bv;
-    if (ci.seg == 0) {
-      v = activate(e.act, v);
-    } else if (rot) {
-      const float pv = Cs[r * CS_LD + pc] + pbv;
-      // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
-      if (e.rope_per_lane) {
-        const float4 c4 = e.rope_cs4[row_t[r] * half + f];
-        v = lo ? v * c4.x - pv * c4.y : v * c4.z + pv * c4.w;
-      } else {
-        const float2 cs = e.rope_cs[row_t[r] * half + f];
-        v = lo ? v * cs.x - pv * cs.y : v * cs.x + pv * cs.y;
+  // rows in batches of 8: every load of a batch (accumulator, rotation partner,
+  // cos/sin) is issued before its stores, so table latency is paid once per batch
+  constexpr int kStep = NT / BN, kBatch = 8;
+  for (int r0 = tid / BN; r0 < BM; r0 += kStep * kBatch) {
+    float v[kBatch], pv[kBatch], cc[kBatch], ss[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int r = r0 + q * kStep;
+      const bool in = r < BM && r < tile_rows;
+      v[q] = in ? Cs[r * CS_LD + c] + bv : 0.0f;
+      pv[q] = 0.0f;
+      cc[q] = 1.0f;
+      ss[q] = 0.0f;
+      if (in && rot) {
+        pv[q] = Cs[r * CS_LD + pc] + pbv;
+        if (e.rope_per_lane) {
+          const float4 c4 = e.rope_cs4[row_t[r] * half + f];
+          cc[q] = lo ? c4.x : c4.z;
+          ss[q] = lo ? c4.y : c4.w;
+        } else {
+          const float2 cs = e.rope_cs[row_t[r] * half + f];
+          cc[q] = cs.x;
+          ss[q] = cs.y;
+        }
       }
     }
-    st_elem(base, rb[r] + col_off, v);
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int r = r0 + q * kStep;
+      if (r >= BM || r >= tile_rows) break;
+      float out = v[q];
+      if (ci.seg == 0)
+        out = activate(e.act, out);
+      else if (rot)
+        // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
+        out = lo ? out * cc[q] - pv[q] * ss[q] : out * cc[q] + pv[q] * ss[q];
+      st_elem(base, rb[r] + col_off, out);
+    }
   }
 }
 
@@ -160,22 +181,26 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
   const int64_t rows_left = S_in - s0 - a_m0;  // rows with m - a_m0 < rows_left exist
 
   float a_reg[8], b_reg[8];
+  // per-thread operand pointers, advanced by one k-step per call
+  const int64_t a_step_i = K_MAJOR ? 16 * tk.s_stride : 2 * tk.c_stride;  // between a thread's 8 loads
+  const T* a_ptr = X + a_base + static_cast<int64_t>(a_k0) * tk.c_stride;
+  const int b_col = n0 + tid % BN;
+  const bool b_col_ok = b_col < N;
+  const T* b_ptr = Wt + static_cast<int64_t>(tid / BN) * N + b_col;
   auto load_regs = [&](int k0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int dm = K_MAJOR ? 16 * i : 0;
       const int k = k0 + a_k0 + (K_MAJOR ? 0 : 2 * i);
-      const bool okr = dm < rows_left && k < C;
-      a_reg[i] = okr ? ld_elem(X, a_base + dm * tk.s_stride + static_cast<int64_t>(k) * tk.c_stride)
-                     : 0.0f;
+      a_reg[i] = (dm < rows_left && k < C) ? ld_elem(a_ptr, i * a_step_i) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      int idx = tid + i * NT;
-      int n = idx % BN, k = k0 + idx / BN;
-      int col = n0 + n;
-      b_reg[i] = (k < C && col < N) ? ld_elem(Wt, static_cast<int64_t>(k) * N + col) : 0.0f;
+      const int k = k0 + tid / BN + 2 * i;
+      b_reg[i] = (b_col_ok && k < C) ? ld_elem(b_ptr, static_cast<int64_t>(2 * i) * N) : 0.0f;
     }
+    a_ptr += static_cast<int64_t>(BK) * tk.c_stride;
+    b_ptr += static_cast<int64_t>(BK) * N;
   };
   auto store_regs = [&](int buf) {
     float* a = As + buf * BK * BM;
