@@ -134,6 +134,56 @@ __device__ __forceinline__ float activate(int act, float y) {
   }
 }
 
+// Hardware approximations (PTX rcp.approx / ex2.approx): about 1 ulp and
+// 2^-22 relative error respectively.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Activations for bf16 outputs, branch-free and short:
+//  - exact-erf GELU with erf from Abramowitz & Stegun, "Handbook of
+//    Mathematical Functions" (1964), eq. 7.1.26: for z >= 0,
+//    erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+//    t = 1 / (1 + p z), absolute error <= 1.5e-7;
+//    GELU(y) = y/2 (1 + sign(y) erf(|y|/sqrt 2)) = (y + |y| erf(|y|/sqrt 2)) / 2;
+//  - tanh-GELU with tanh(u) = 1 - 2 / (1 + exp(2u));
+//  - SiLU y / (1 + exp(-y)).
+// Absolute errors stay near 1e-7 of the input scale, far below bf16 rounding.
+template <int ACT>
+__device__ __forceinline__ float activate_bf16out(float y) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  if (ACT == ACT_GELU_ERF) {
+    const float a = fabsf(y);
+    const float z = a * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    poly *= t;
+    const float ez = ex2_approx(-(z * z) * kLog2e);
+    const float erf_z = fmaf(-poly, ez, 1.0f);
+    return 0.5f * fmaf(a, erf_z, y);
+  } else if (ACT == ACT_GELU_TANH) {
+    const float u = 0.79788456080286536f * fmaf(0.044715f * y, y * y, y);
+    const float th = fmaf(-2.0f, rcp_approx(1.0f + ex2_approx(2.0f * kLog2e * u)), 1.0f);
+    return 0.5f * y * (1.0f + th);
+  } else if (ACT == ACT_SILU) {
+    return y * rcp_approx(1.0f + ex2_approx(-kLog2e * y));
+  } else if (ACT == ACT_RELU2) {
+    const float r = fmaxf(y, 0.0f);
+    return r * r;
+  }
+  return y;
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }

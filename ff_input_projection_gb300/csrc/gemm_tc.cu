@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             float v[16];
             if (ci.seg == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = activate(ACT, __uint_as_float(v_u[i]) + bias_at(bl, i));
+              for (int i = 0; i < 16; ++i) v[i] = activate_bf16out<ACT>(__uint_as_float(v_u[i]) + bias_at(bl, i));
             } else {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
