@@ -428,6 +428,37 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     if (r != CUDA_SUCCESS)
       return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
                   static_cast<int>(r));
+    // output maps: when they encode, the epilogue writes whole 32-row blocks by TMA
+    {
+      const cuuint32_t ostr[3] = {1, 1, 1};
+      bool okm = true;
+      if (a.out_ff) {
+        cuuint64_t d[2] = {static_cast<cuuint64_t>(p->F), static_cast<cuuint64_t>(ta.M)};
+        cuuint64_t st[1] = {static_cast<cuuint64_t>(p->F) * esz};
+        cuuint32_t bx[2] = {16, 32};
+        okm = okm && encode(&tp.tmap_ff, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_ff, d, st, bx,
+                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      }
+      const int nkv = p->groups > 0 ? p->groups : p->heads;
+      void* const outs3[3] = {a.out_q, a.out_k, a.out_v};
+      CUtensorMap* const maps3[3] = {&tp.tmap_q, &tp.tmap_k, &tp.tmap_v};
+      for (int i = 0; i < 3 && p->heads > 0; ++i) {
+        if (i == 1 && p->k_transposed) continue;  // pre-transposed k is stored directly
+        const int nh = i == 0 ? p->heads : nkv;
+        cuuint64_t d[3] = {static_cast<cuuint64_t>(p->hd), static_cast<cuuint64_t>(ta.T),
+                           static_cast<cuuint64_t>(ta.Bb * nh)};
+        cuuint64_t st[2] = {static_cast<cuuint64_t>(p->hd) * esz,
+                            static_cast<cuuint64_t>(ta.T * p->hd) * esz};
+        cuuint32_t bx[3] = {16, 32, 1};
+        okm = okm && encode(maps3[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, outs3[i], d, st, bx,
+                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      }
+      tp.tma_store = okm ? 1 : 0;
+    }
     tp.tok = tk;
     tp.epi = e;
     tp.C = p->C;

@@ -50,6 +50,9 @@ struct Epilogue {
 struct TcParams {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b;
+  // output maps for TMA stores: ff [M, F] (2-D), q/k/v [B*heads, T, hd] (3-D)
+  CUtensorMap tmap_ff, tmap_q, tmap_k, tmap_v;
+  int tma_store;  // 1: the output maps are valid
   TokenMap tok;
   Epilogue epi;
   int C;

@@ -41,6 +41,7 @@ constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int NUM_EPI_WARPS = 16;  // 4 per SM sub-partition: latency hiding for the epilogue
 constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
+static_assert(NT * 112 <= 65536, "the 112-register cap must fit the block in one SM");
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
@@ -48,7 +49,10 @@ constexpr int CHUNK_BYTES = 64 * BK * 2;         // one [64 ch][64 elems] MN-maj
 constexpr int ACC_COLS = BN;                     // fp32 accumulator: one TMEM column per output column
 constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: two accumulators
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+// per epilogue warp, two 1 KB buffers staging [32 rows][16 bf16] blocks for TMA stores
+constexpr int STAGING_BYTES_PER_WARP = 2 * 1024;
+constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
 
@@ -164,6 +168,49 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // (barrier init) before the peers' use of them.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Tiled TMA stores from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// at most one bulk group may still be reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// generic-proxy shared-memory writes become visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -307,29 +354,15 @@ __device__ __forceinline__ float bias_at(const uint32_t (&w)[8], int i) {
   return (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u) : __uint_as_float(w[i >> 1] << 16);
 }
 
-// 16 values at stride `stride` elements (a head lane-column of pre-transposed k).
-__device__ __forceinline__ void store16_bf16_strided(uint16_t* dst, int64_t stride,
-                                                     const float (&v)[16]) {
+// 16 bf16 values (two per word) at stride `stride` elements: a head's lane
+// column of pre-transposed k.
+__device__ __forceinline__ void store16_packed_strided(uint16_t* dst, int64_t stride,
+                                                       const uint32_t (&w)[8]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
-    dst[i * stride] = *reinterpret_cast<const uint16_t*>(&h);
+  for (int i = 0; i < 8; ++i) {
+    dst[(2 * i) * stride] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+    dst[(2 * i + 1) * stride] = static_cast<uint16_t>(w[i] >> 16);
   }
-}
-
-__device__ __forceinline__ void store16_bf16(void* dst, const float (&v)[16]) {
-  uint4 a, b;
-  a.x = pack_bf16x2(v[0], v[1]);
-  a.y = pack_bf16x2(v[2], v[3]);
-  a.z = pack_bf16x2(v[4], v[5]);
-  a.w = pack_bf16x2(v[6], v[7]);
-  b.x = pack_bf16x2(v[8], v[9]);
-  b.y = pack_bf16x2(v[10], v[11]);
-  b.z = pack_bf16x2(v[12], v[13]);
-  b.w = pack_bf16x2(v[14], v[15]);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = a;
-  d[1] = b;
 }
 
 // Rotation of lanes [0, 2*RH) of a head held in one 16-column granule (partial
@@ -393,19 +426,23 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 // CL: CTAs per cluster. With CL == 2 the two CTAs take neighbouring M-tiles of
 // one N-tile and each multicasts half of the W tile into both, so each CTA
 // reads 32 KB instead of 48 KB from L2 per k-step.
+// 112 registers a thread: 18 warps x 32 x 112 = 64 512 of the SM's 65 536, one
+// CTA per SM (the shared-memory footprint allows no second one anyway).
 template <bool A_MN_MAJOR, int ACT, int CL>
-__global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __maxnreg__(112) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KB alignment
   uint8_t* sptr = smem_raw + (sbase - raw_addr);
-  const uint32_t bar0 = sbase + STAGES * STAGE_BYTES;
+  const uint32_t staging0 = sbase + STAGES * STAGE_BYTES;
+  const uint32_t bar0 = staging0 + STAGING_BYTES;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + NUM_BARS * 8);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -563,6 +600,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     const int row = quarter * 32 + lane;
     const int rh = e.rope_half;
     const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
+    const uint32_t staging_warp = staging0 + (warp - 2) * STAGING_BYTES_PER_WARP;
+    uint32_t stage_sel = 0;  // alternates this warp's two staging buffers
     int it = 0;
     for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
       const int buf = it & 1;
@@ -587,6 +626,39 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
       uint16_t* const kt_row = static_cast<uint16_t*>(e.out_k) + bidx * nkv * head_stride + t;
       const float2* const cs_row = e.rope_cs + t * rh;
+      // A TMA store writes the warp's 32 rows as one block: they must all be
+      // valid and, for the head-major buffers, lie in one batch element
+      // (tokens t .. t+31). Lane 0 issues the stores with its own coordinates.
+      const bool tma_ff = p.tma_store && __all_sync(0xFFFFFFFFu, valid);
+      const bool tma_heads =
+          tma_ff && __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 31) -
+                            __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 0) == 31;
+      auto put16 = [&](int seg, int head, int j, uint16_t* dst, const uint32_t (&w)[8]) {
+        if (!(seg == 0 ? tma_ff : tma_heads)) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          return;
+        }
+        const uint32_t stg = staging_warp + (stage_sel & 1) * 1024;
+        ++stage_sel;
+        if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it
+        __syncwarp();
+        st_shared_v4(stg + lane * 32, w[0], w[1], w[2], w[3]);
+        st_shared_v4(stg + lane * 32 + 16, w[4], w[5], w[6], w[7]);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if (seg == 0) {
+            tma_store_2d(&p.tmap_ff, stg, j, static_cast<int>(m));
+          } else {
+            const int nh = seg == 1 ? e.heads : nkv;
+            const CUtensorMap* map = seg == 1 ? &p.tmap_q : seg == 2 ? &p.tmap_k : &p.tmap_v;
+            tma_store_3d(map, stg, j, static_cast<int>(t), static_cast<int>(bidx * nh + head));
+          }
+          bulk_commit();
+        }
+      };
       const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
       ColCursor cur;
       cursor_init(e, tc.n0, cur);
@@ -616,17 +688,19 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           tmem_wait_ld();
           uint32_t bh[8];
           load_bias16(bias, n + rh, bh);
-          float lo[16], hi[16];
+          uint32_t lo_w[8], hi_w[8];  // results, two bf16 per word
           if (valid) {
             if (e.rope_per_lane) {
               const float4* t4 = e.rope_cs4 + t * rh + ci.j;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float4 c = __ldg(t4 + i);  // (cos, sin) of lane i and of lane i + rh
-                const float x = __uint_as_float(lo_u[i]) + bias_at(bl, i);
-                const float y = __uint_as_float(hi_u[i]) + bias_at(bh, i);
-                lo[i] = x * c.x - y * c.y;
-                hi[i] = y * c.z + x * c.w;
+              for (int i = 0; i < 8; ++i) {
+                const float4 c0 = __ldg(t4 + 2 * i), c1 = __ldg(t4 + 2 * i + 1);
+                const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
+                const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
+                const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
+                const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
+                lo_w[i] = pack_bf16x2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
+                hi_w[i] = pack_bf16x2(y0 * c0.z + x0 * c0.w, y1 * c1.z + x1 * c1.w);
               }
             } else {
               const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
@@ -637,18 +711,16 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                 const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
                 const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
                 const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
-                lo[2 * i] = x0 * cs.x - y0 * cs.y;
-                hi[2 * i] = y0 * cs.x + x0 * cs.y;
-                lo[2 * i + 1] = x1 * cs.z - y1 * cs.w;
-                hi[2 * i + 1] = y1 * cs.z + x1 * cs.w;
+                lo_w[i] = pack_bf16x2(x0 * cs.x - y0 * cs.y, x1 * cs.z - y1 * cs.w);
+                hi_w[i] = pack_bf16x2(y0 * cs.x + x0 * cs.y, y1 * cs.z + x1 * cs.w);
               }
             }
-            if (kt) {
-              store16_bf16_strided(dst_t, e.T, lo);
-              store16_bf16_strided(dst_t + rh * e.T, e.T, hi);
+            if (kt) {  // pre-transposed k is stored directly, one lane column at a time
+              store16_packed_strided(dst_t, e.T, lo_w);
+              store16_packed_strided(dst_t + rh * e.T, e.T, hi_w);
             } else {
-              store16_bf16(dst, lo);
-              store16_bf16(dst + rh, hi);
+              put16(ci.seg, ci.head, ci.j, dst, lo_w);
+              put16(ci.seg, ci.head, ci.j + rh, dst + rh, hi_w);
             }
           }
         } else {
@@ -656,24 +728,33 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           tmem_ld16(t_row + c, v_u);
           tmem_wait_ld();
           if (valid) {
-            float v[16];
+            uint32_t w[8];
             if (ci.seg == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = activate_bf16out<ACT>(__uint_as_float(v_u[i]) + bias_at(bl, i));
-            } else {
+              for (int i = 0; i < 8; ++i)
+                w[i] = pack_bf16x2(
+                    activate_bf16out<ACT>(__uint_as_float(v_u[2 * i]) + bias_at(bl, 2 * i)),
+                    activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1]) + bias_at(bl, 2 * i + 1)));
+            } else if (rope_small) {
+              float v[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
-              if (rope_small) {
-                if (e.rope_per_lane)
-                  rotate_small4(v, e.rope_cs4 + t * rh, rh);
-                else
-                  rotate_small(v, cs_row, rh);
-              }
+              if (e.rope_per_lane)
+                rotate_small4(v, e.rope_cs4 + t * rh, rh);
+              else
+                rotate_small(v, cs_row, rh);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                w[i] = pack_bf16x2(__uint_as_float(v_u[2 * i]) + bias_at(bl, 2 * i),
+                                   __uint_as_float(v_u[2 * i + 1]) + bias_at(bl, 2 * i + 1));
             }
             if (kt)
-              store16_bf16_strided(dst_t, e.T, v);
+              store16_packed_strided(dst_t, e.T, w);
             else
-              store16_bf16(dst, v);
+              put16(ci.seg, ci.head, ci.j, dst, w);
           }
         }
       }
@@ -681,6 +762,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(buf));
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+    __syncwarp();
   }
 
   tc_fence_before();
