@@ -10,12 +10,12 @@
 // q/k/v [B*heads, T, head_dim] (memory-efficient-attention issue #7, the
 // [batch*heads, tokens, head_dim] layout).
 //
-// Structure (one persistent CTA per SM, 18 warps):
+// Structure (one persistent CTA per SM, 14 warps):
 //   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring
 //   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
 //              (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits
 //              completion to mbarriers
-//   warps 2-17 epilogue: tcgen05.ld of the fp32 accumulator (one token row
+//   warps 2-13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //              per thread), bias, activation / rotation in registers, bf16
 //              round-to-nearest-even, 16-byte stores
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the
@@ -39,9 +39,10 @@ namespace {
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
 constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
-constexpr int NUM_EPI_WARPS = 16;  // 4 per SM sub-partition: latency hiding for the epilogue
+constexpr int NUM_EPI_WARPS = 12;  // 3 per SM sub-partition (one per TMEM lane quarter each)
 constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
-static_assert(NT * 112 <= 65536, "the 112-register cap must fit the block in one SM");
+// registers are granted per 4 warps: 14 warps count as 16, so 128 a thread fit
+static_assert(((NT / 32 + 3) / 4 * 4) * 32 * 128 <= 65536, "register budget");
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
@@ -426,10 +427,9 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 // CL: CTAs per cluster. With CL == 2 the two CTAs take neighbouring M-tiles of
 // one N-tile and each multicasts half of the W tile into both, so each CTA
 // reads 32 KB instead of 48 KB from L2 per k-step.
-// 112 registers a thread: 18 warps x 32 x 112 = 64 512 of the SM's 65 536, one
-// CTA per SM (the shared-memory footprint allows no second one anyway).
+// One CTA per SM (its shared-memory footprint allows no second one).
 template <bool A_MN_MAJOR, int ACT, int CL>
-__global__ void __maxnreg__(112) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KB alignment
@@ -596,7 +596,7 @@ __global__ void __maxnreg__(112) tc_gemm_kernel(const __grid_constant__ TcParams
     // ------------------------------------------------ epilogue warps
     const Epilogue& e = p.epi;
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    const int part = (warp - 2) >> 2;              // which of every 4 work units it takes
+    const int part = (warp - 2) >> 2;              // which of every 3 work units it takes
     const int row = quarter * 32 + lane;
     const int rh = e.rope_half;
     const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
@@ -671,7 +671,7 @@ __global__ void __maxnreg__(112) tc_gemm_kernel(const __grid_constant__ TcParams
         const bool rope = rh >= 16 && qk && ci.j < 2 * rh;
         const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
         if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
-        if ((unit++ & 3) != part) continue;
+        if (unit++ % 3 != part) continue;
         const int n = tc.n0 + c;
         uint16_t* const dst =
             ci.seg == 0 ? ff_row + ci.j
