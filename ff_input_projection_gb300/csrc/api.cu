@@ -428,7 +428,9 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     if (r != CUDA_SUCCESS)
       return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
                   static_cast<int>(r));
-    // output maps: when they encode, the epilogue writes whole 32-row blocks by TMA
+    // output maps: when they encode, the epilogue writes whole 32-row blocks by
+    // TMA from 32-byte-swizzled staging rows (the 16-byte halves of rows 4-7 of
+    // every 8 swapped, so the staging stores are free of bank conflicts)
     {
       const cuuint32_t ostr[3] = {1, 1, 1};
       bool okm = true;
@@ -437,7 +439,7 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
         cuuint64_t st[1] = {static_cast<cuuint64_t>(p->F) * esz};
         cuuint32_t bx[2] = {16, 32};
         okm = okm && encode(&tp.tmap_ff, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_ff, d, st, bx,
-                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                             CU_TENSOR_MAP_L2_PROMOTION_NONE,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
       }
@@ -453,7 +455,7 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
                             static_cast<cuuint64_t>(ta.T * p->hd) * esz};
         cuuint32_t bx[3] = {16, 32, 1};
         okm = okm && encode(maps3[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, outs3[i], d, st, bx,
-                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                             CU_TENSOR_MAP_L2_PROMOTION_NONE,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
       }
@@ -470,6 +472,8 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     // two CTAs share each W tile when there are M-tiles to pair
     tp.cluster = (sc.cluster == 2 && tp.num_m_tiles >= 2) ? 2 : 1;
     tp.num_units = (tp.num_m_tiles + tp.cluster - 1) / tp.cluster * num_n_tiles;
+    if (tp.num_units * tp.cluster > INT32_MAX)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "more than 2^31 output tiles");
     tp.group_m = sc.group_m;
     tp.wait_limit_ns = sc.wait_limit_ns;
     tp.inject_stall = sc.inject_stall;

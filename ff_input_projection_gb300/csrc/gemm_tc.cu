@@ -11,15 +11,23 @@
 // [batch*heads, tokens, head_dim] layout).
 //
 // Structure (one persistent CTA per SM, 14 warps):
-//   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring
+//   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring,
+//              and each tile's bias row into a bias operand
 //   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
 //              (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits
 //              completion to mbarriers
 //   warps 2-13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
-//              per thread), bias, activation / rotation in registers, bf16
-//              round-to-nearest-even, 16-byte stores
+//              per thread), activation / rotation in registers, bf16
+//              round-to-nearest-even, TMA tensor stores of 32 x 16 blocks
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the
 // epilogue of tile i overlaps the main loop of tile i+1.
+//
+// The bias enters through the tensor core: each tile starts with one K=16 MMA
+// (accumulate off) whose A operand is a constant atom with 0.5 in k-row 0 and
+// zeros elsewhere, and whose B operand holds the tile's bias in k-row 0. Both
+// descriptors give the second 8-row k group a stride of 0, so it reads the
+// same atom again: every accumulator starts at 0.5 b + 0.5 b = b exactly, and
+// the epilogue has no bias loads or adds.
 //
 // Operand layouts (128-byte swizzle, as written by TMA and read by the MMA):
 //   A, row-major x (unit channel stride): K-major, [128 rows][64 ch] per stage.
@@ -49,11 +57,16 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int CHUNK_BYTES = 64 * BK * 2;         // one [64 ch][64 elems] MN-major chunk, 8 KB
 constexpr int ACC_COLS = BN;                     // fp32 accumulator: one TMEM column per output column
 constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: two accumulators
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1 + 2;  // ring, accumulators, drain, bias
+// bias operands: A, two [8 k][64 m] MN-major atoms (k-row 0 = 0.5); B, four
+// [8 k][64 n] atoms whose k-row 0 is the tile's bias
+constexpr int BIAS_A_BYTES = 2 * 1024;
+constexpr int BIAS_B_BYTES = 4 * 1024;
 // per epilogue warp, two 1 KB buffers staging [32 rows][16 bf16] blocks for TMA stores
 constexpr int STAGING_BYTES_PER_WARP = 2 * 1024;
 constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
+constexpr int SMEM_BYTES =
+    1024 + STAGES * STAGE_BYTES + BIAS_A_BYTES + BIAS_B_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
 
@@ -156,6 +169,17 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of
+// 16), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -304,24 +328,35 @@ struct TileCoord {
 // group_m M-tiles sweep all N-tiles, M fastest inside a group, so concurrently
 // running clusters share W and x tiles in L2.
 template <int CL>
-__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t unit, int rank) {
-  const int64_t m_units = (p.num_m_tiles + CL - 1) / CL;
-  const int64_t gsz = p.group_m >= CL ? p.group_m / CL : 1;
-  const int64_t per_group = gsz * p.num_n_tiles;
-  const int64_t g = unit / per_group;
-  const int64_t first = g * gsz;
-  const int64_t left = m_units - first;
-  const int64_t gm = left < gsz ? left : gsz;
-  const int64_t r = unit - g * per_group;
-  const int64_t m_tile = (first + r % gm) * CL + rank;
-  const int n_tile = static_cast<int>(r / gm);
+__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t unit64, int rank) {
+  // tile counts fit in 31 bits (the host checks), so the index arithmetic is 32-bit
+  const uint32_t unit = static_cast<uint32_t>(unit64);
+  const uint32_t m_units = (static_cast<uint32_t>(p.num_m_tiles) + CL - 1) / CL;
+  const uint32_t gsz = p.group_m >= CL ? static_cast<uint32_t>(p.group_m) / CL : 1u;
+  const uint32_t per_group = gsz * static_cast<uint32_t>(p.num_n_tiles);
+  const uint32_t g = unit / per_group;
+  const uint32_t first = g * gsz;
+  const uint32_t left = m_units - first;
+  const uint32_t gm = left < gsz ? left : gsz;
+  const uint32_t r = unit - g * per_group;
+  const uint32_t rn = r / gm;
+  const uint32_t m_tile = (first + (r - rn * gm)) * CL + rank;
   TileCoord tc;
-  tc.phantom = m_tile >= p.num_m_tiles;
-  const int64_t mt = tc.phantom ? p.num_m_tiles - 1 : m_tile;
-  tc.o = mt / p.m_tiles_per_slab;
-  tc.s0 = (mt - tc.o * p.m_tiles_per_slab) * BM;
-  tc.n0 = n_tile * p.epi.bn_eff;
+  tc.phantom = m_tile >= static_cast<uint32_t>(p.num_m_tiles);
+  const uint32_t mt = tc.phantom ? static_cast<uint32_t>(p.num_m_tiles) - 1 : m_tile;
+  const uint32_t per_slab = static_cast<uint32_t>(p.m_tiles_per_slab);
+  const uint32_t o = mt / per_slab;
+  tc.o = o;
+  tc.s0 = static_cast<int64_t>(mt - o * per_slab) * BM;
+  tc.n0 = static_cast<int>(rn) * p.epi.bn_eff;
   return tc;
+}
+
+// a / b for non-negative operands, in 32 bits when both fit
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
 }
 
 __device__ __forceinline__ void outer_coords(const TokenMap& tk, int64_t o, int (&oc)[3]) {
@@ -336,23 +371,6 @@ __device__ __forceinline__ void outer_coords(const TokenMap& tk, int64_t o, int 
       oc[d] = 0;
     }
   }
-}
-
-// 16 bf16 bias values kept packed (two per word) until used.
-__device__ __forceinline__ void load_bias16(const uint16_t* bias, int n, uint32_t (&w)[8]) {
-  if (bias == nullptr) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0u;
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(bias + n);
-  const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-  w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
-  w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
-}
-
-__device__ __forceinline__ float bias_at(const uint32_t (&w)[8], int i) {
-  return (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u) : __uint_as_float(w[i >> 1] << 16);
 }
 
 // 16 bf16 values (two per word) at stride `stride` elements: a head's lane
@@ -434,15 +452,20 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KB alignment
   uint8_t* sptr = smem_raw + (sbase - raw_addr);
-  const uint32_t staging0 = sbase + STAGES * STAGE_BYTES;
+  const uint32_t bias_a = sbase + STAGES * STAGE_BYTES;
+  const uint32_t bias_b = bias_a + BIAS_A_BYTES;
+  const uint32_t staging0 = bias_b + BIAS_B_BYTES;
   const uint32_t bar0 = staging0 + STAGING_BYTES;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8);
+  const uint32_t bias_full = bar0 + 8u * (2 * STAGES + 5);   // bias row landed
+  const uint32_t bias_empty = bar0 + 8u * (2 * STAGES + 6);  // bias MMA has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
+      sptr + STAGES * STAGE_BYTES + BIAS_A_BYTES + BIAS_B_BYTES + STAGING_BYTES + NUM_BARS * 8);
+  const bool has_bias = p.epi.bias != nullptr;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -462,10 +485,22 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       mbar_init(tempty_bar(b), NUM_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(bias_full, 1);
+    mbar_init(bias_empty, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     prefetch_tmap(&p.tmap_a);
     prefetch_tmap(&p.tmap_b);
+  }
+  if (has_bias) {
+    // bias operands: A atoms hold 0.5 (bf16 0x3F00) in k-row 0, B atoms start
+    // at zero (their k-row 0 is overwritten per tile; rows 1-7 stay zero)
+    for (int i = threadIdx.x; i < (BIAS_A_BYTES + BIAS_B_BYTES) / 16; i += NT) {
+      const uint32_t off = static_cast<uint32_t>(i) * 16u;
+      const uint32_t v = (off < BIAS_A_BYTES && (off & 1023u) < 128u) ? 0x3F003F00u : 0u;
+      st_shared_v4(bias_a + off, v, v, v, v);
+    }
+    fence_async_shared();  // visible to the tensor core (async proxy)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -488,10 +523,29 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       uint32_t armed_mask = 0, armed_parity = 0;  // per stage: armed, parity of its last arming
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t bias_phase = 0;
+      bool bias_armed = false;
+      const uint16_t* const bias = static_cast<const uint16_t*>(p.epi.bias);
       for (int64_t u = first_unit; u < p.num_units; u += unit_step) {
         const TileCoord tc = tile_coord<CL>(p, u, rank);
         int oc[3];
         outer_coords(p.tok, tc.o, oc);
+        if (has_bias) {
+          // the tile's bias row into k-row 0 of the four B atoms, once the
+          // previous tile's bias MMA has read them
+          if (!wait_bounded(bias_empty, bias_phase ^ 1u, wc, true)) break;
+          const int cols = min(p.epi.bn_eff, p.epi.N - tc.n0);
+          mbar_arrive_expect_tx(bias_full, static_cast<uint32_t>(cols) * 2u);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) {
+            const int len = min(64, cols - 64 * j);
+            if (len > 0)
+              bulk_load(bias_b + j * 1024, bias + tc.n0 + 64 * j, static_cast<uint32_t>(len) * 2u,
+                        bias_full);
+          }
+          bias_armed = true;
+          bias_phase ^= 1u;
+        }
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
@@ -540,13 +594,20 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       // drain: every armed stage's copies must land before the CTA exits
       for (int s = 0; s < STAGES; ++s)
         if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, wc, false);
+      if (bias_armed) wait_bounded(bias_full, bias_phase ^ 1u, wc, false);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
       const uint32_t idesc = make_idesc(A_MN_MAJOR, true);
+      // bias MMA: both operands MN-major; m (n) chunks 1 KB apart, and a k-group
+      // stride of 0 so k-rows 8-15 read the same atom as k-rows 0-7
+      const uint32_t idesc_bias = make_idesc(true, true);
+      const uint64_t bias_a_desc = sw128_desc(bias_a, 1024, 0);
+      const uint64_t bias_b_desc = sw128_desc(bias_b, 1024, 0);
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t bias_phase = 0;
       bool issued = false;
       int it = 0;
       for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
@@ -555,6 +616,15 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         if (!wait_bounded(tempty_bar(buf), acc_phase ^ 1u, wc, true)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * ACC_COLS;
+        if (has_bias) {
+          if (!wait_bounded(bias_full, bias_phase, wc, true)) break;
+          tc_fence_after();
+          umma_bf16(d_tmem, bias_a_desc, bias_b_desc, idesc_bias, 0u);  // D = bias
+          umma_commit(bias_empty);
+          bias_phase ^= 1u;
+          issued = true;
+        }
+        const uint32_t acc0 = has_bias ? 1u : 0u;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, wc, true)) {
@@ -571,7 +641,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             const uint64_t a_desc = A_MN_MAJOR ? sw128_desc(a_addr + k * 2048, CHUNK_BYTES, 1024)
                                                : sw128_desc(a_addr + k * 32, 16, 1024);
             const uint64_t b_desc = sw128_desc(b_addr + k * 2048, CHUNK_BYTES, 1024);
-            umma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : acc0);
           }
           issued = true;
           // frees the stage (in every CTA whose producer writes into ours) once read
@@ -599,9 +669,18 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     const int part = (warp - 2) >> 2;              // which of every 3 work units it takes
     const int row = quarter * 32 + lane;
     const int rh = e.rope_half;
-    const uint16_t* bias = static_cast<const uint16_t*>(e.bias);
+    const int nkv = e.groups > 0 ? e.groups : e.heads;
+    const int64_t head_stride = e.T * e.hd;
     const uint32_t staging_warp = staging0 + (warp - 2) * STAGING_BYTES_PER_WARP;
+    // the staging rows are 32 B; the output maps use the 32-byte swizzle, which
+    // swaps the two 16-byte halves of rows 4-7 of every 8, so the eight rows a
+    // quarter-warp stores at once fall in distinct banks
+    const uint32_t swz = ((lane >> 2) & 1u) * 16u;
     uint32_t stage_sel = 0;  // alternates this warp's two staging buffers
+    // a quarter's three warps take its work units round-robin; the count runs
+    // on across tiles, so a tile whose unit count is not a multiple of 3 does
+    // not always load the same warp
+    int turn = 0;
     int it = 0;
     for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
       const int buf = it & 1;
@@ -610,135 +689,178 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
       const TileCoord tc = tile_coord<CL>(p, u, rank);
-      const int64_t s = tc.s0 + row;
-      const bool valid = !tc.phantom && s < p.tok.S_in;
-      const int64_t m = tc.o * p.tok.S_in + s;
-      const int64_t bidx = m / e.T;
-      const int64_t t = m - bidx * e.T;
+      const bool valid = !tc.phantom && tc.s0 + row < p.tok.S_in;
+      const int64_t m0 = tc.o * p.tok.S_in + tc.s0;  // the tile's first token
+      const int64_t m = m0 + row;
+      // batch element and position: one division per tile, a step per row
+      int64_t bidx, t;
+      if (e.T >= BM) {
+        bidx = div_nonneg(m0, e.T);
+        t = m0 - bidx * e.T + row;
+        if (t >= e.T) {
+          t -= e.T;
+          ++bidx;
+        }
+      } else {
+        bidx = div_nonneg(m, e.T);
+        t = m - bidx * e.T;
+      }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
-      // per-row output bases, once per tile; a column group then adds head*T*hd + lane
-      const int nkv = e.groups > 0 ? e.groups : e.heads;
-      const int64_t head_stride = e.T * e.hd;
-      uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F;
-      uint16_t* const q_row = static_cast<uint16_t*>(e.out_q) + (bidx * e.heads * e.T + t) * e.hd;
-      uint16_t* const k_row = static_cast<uint16_t*>(e.out_k) + (bidx * nkv * e.T + t) * e.hd;
-      uint16_t* const v_row = static_cast<uint16_t*>(e.out_v) + (bidx * nkv * e.T + t) * e.hd;
-      // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
-      uint16_t* const kt_row = static_cast<uint16_t*>(e.out_k) + bidx * nkv * head_stride + t;
-      const float2* const cs_row = e.rope_cs + t * rh;
+      const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
       // A TMA store writes the warp's 32 rows as one block: they must all be
       // valid and, for the head-major buffers, lie in one batch element
       // (tokens t .. t+31). Lane 0 issues the stores with its own coordinates.
       const bool tma_ff = p.tma_store && __all_sync(0xFFFFFFFFu, valid);
-      const bool tma_heads =
-          tma_ff && __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 31) -
-                            __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 0) == 31;
-      auto put16 = [&](int seg, int head, int j, uint16_t* dst, const uint32_t (&w)[8]) {
-        if (!(seg == 0 ? tma_ff : tma_heads)) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          return;
-        }
+      auto stage_store = [&](const CUtensorMap* map, int c0, int c1, int c2, bool three_d,
+                             const uint32_t (&w)[8]) {
         const uint32_t stg = staging_warp + (stage_sel & 1) * 1024;
         ++stage_sel;
         if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it
         __syncwarp();
-        st_shared_v4(stg + lane * 32, w[0], w[1], w[2], w[3]);
-        st_shared_v4(stg + lane * 32 + 16, w[4], w[5], w[6], w[7]);
+        st_shared_v4(stg + lane * 32 + swz, w[0], w[1], w[2], w[3]);
+        st_shared_v4(stg + lane * 32 + (swz ^ 16u), w[4], w[5], w[6], w[7]);
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
-          if (seg == 0) {
-            tma_store_2d(&p.tmap_ff, stg, j, static_cast<int>(m));
-          } else {
-            const int nh = seg == 1 ? e.heads : nkv;
-            const CUtensorMap* map = seg == 1 ? &p.tmap_q : seg == 2 ? &p.tmap_k : &p.tmap_v;
-            tma_store_3d(map, stg, j, static_cast<int>(t), static_cast<int>(bidx * nh + head));
-          }
+          if (three_d)
+            tma_store_3d(map, stg, c0, c1, c2);
+          else
+            tma_store_2d(map, stg, c0, c1);
           bulk_commit();
         }
       };
-      const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
-      ColCursor cur;
-      cursor_init(e, tc.n0, cur);
-      int unit = 0;
-      for (int c = 0; c < cols; c += 16, cursor_advance16(e, cur)) {
-        const ColInfo& ci = cur.ci;
-        const bool qk = ci.seg == 1 || ci.seg == 2;
-        // rh >= 16: lanes i and i+rh sit in different granules, handled as a pair;
-        // rh <= 8: every rotated lane sits in the head's first granule.
-        const bool rope = rh >= 16 && qk && ci.j < 2 * rh;
-        const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
-        if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
-        if (unit++ % 3 != part) continue;
-        const int n = tc.n0 + c;
-        uint16_t* const dst =
-            ci.seg == 0 ? ff_row + ci.j
-                        : (ci.seg == 1 ? q_row : ci.seg == 2 ? k_row : v_row) +
-                              ci.head * head_stride + ci.j;
-        const bool kt = e.k_transposed && ci.seg == 2;
-        uint16_t* const dst_t = kt_row + (static_cast<int64_t>(ci.head) * e.hd + ci.j) * e.T;
-        uint32_t bl[8];
-        load_bias16(bias, n, bl);
-        if (rope) {
-          uint32_t lo_u[16], hi_u[16];
-          tmem_ld16(t_row + c, lo_u);
-          tmem_ld16(t_row + c + rh, hi_u);
+      if (tc.n0 + cols <= e.F) {
+        // ---- a tile inside the ff block: activation, then [M, F] row-major
+        uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F + tc.n0;
+        for (int c = 0; c < cols; c += 16) {
+          const bool mine = turn == part;
+          turn = turn == 2 ? 0 : turn + 1;
+          if (!mine) continue;
+          uint32_t v_u[16];
+          tmem_ld16(t_row + c, v_u);
           tmem_wait_ld();
-          uint32_t bh[8];
-          load_bias16(bias, n + rh, bh);
-          uint32_t lo_w[8], hi_w[8];  // results, two bf16 per word
-          if (valid) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = pack_bf16x2(activate_bf16out<ACT>(__uint_as_float(v_u[2 * i])),
+                               activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1])));
+          if (tma_ff) {
+            stage_store(&p.tmap_ff, tc.n0 + c, static_cast<int>(m), 0, false, w);
+          } else if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(ff_row + c);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+      } else {
+        // ---- a tile that reaches the head-major blocks
+        const bool tma_heads =
+            tma_ff && __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 31) -
+                              __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 0) == 31;
+        uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F;
+        uint16_t* const q_row = static_cast<uint16_t*>(e.out_q) + (bidx * e.heads * e.T + t) * e.hd;
+        uint16_t* const k_row = static_cast<uint16_t*>(e.out_k) + (bidx * nkv * e.T + t) * e.hd;
+        uint16_t* const v_row = static_cast<uint16_t*>(e.out_v) + (bidx * nkv * e.T + t) * e.hd;
+        // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
+        uint16_t* const kt_row = static_cast<uint16_t*>(e.out_k) + bidx * nkv * head_stride + t;
+        const float2* const cs_row = e.rope_cs + t * rh;
+        auto put16 = [&](int seg, int head, int j, uint16_t* dst, const uint32_t (&w)[8]) {
+          if (!(seg == 0 ? tma_ff : tma_heads)) {
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            return;
+          }
+          if (seg == 0) {
+            stage_store(&p.tmap_ff, j, static_cast<int>(m), 0, false, w);
+          } else {
+            const int nh = seg == 1 ? e.heads : nkv;
+            const CUtensorMap* map = seg == 1 ? &p.tmap_q : seg == 2 ? &p.tmap_k : &p.tmap_v;
+            stage_store(map, j, static_cast<int>(t), static_cast<int>(bidx * nh + head), true, w);
+          }
+        };
+        ColCursor cur;
+        cursor_init(e, tc.n0, cur);
+        for (int c = 0; c < cols; c += 16, cursor_advance16(e, cur)) {
+          const ColInfo& ci = cur.ci;
+          const bool qk = ci.seg == 1 || ci.seg == 2;
+          // rh >= 16: lanes i and i+rh sit in different granules, handled as a pair;
+          // rh <= 8: every rotated lane sits in the head's first granule.
+          const bool rope = rh >= 16 && qk && ci.j < 2 * rh;
+          const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
+          if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
+          const bool mine = turn == part;
+          turn = turn == 2 ? 0 : turn + 1;
+          if (!mine) continue;
+          uint16_t* const dst =
+              ci.seg == 0 ? ff_row + ci.j
+                          : (ci.seg == 1 ? q_row : ci.seg == 2 ? k_row : v_row) +
+                                ci.head * head_stride + ci.j;
+          const bool kt = e.k_transposed && ci.seg == 2;
+          uint16_t* const dst_t = kt_row + (static_cast<int64_t>(ci.head) * e.hd + ci.j) * e.T;
+          if (rope) {
+            uint32_t lo_u[16], hi_u[16];
+            tmem_ld16(t_row + c, lo_u);
+            tmem_ld16(t_row + c + rh, hi_u);
+            tmem_wait_ld();
+            uint32_t lo_w[8], hi_w[8];  // results, two bf16 per word
             if (e.rope_per_lane) {
               const float4* t4 = e.rope_cs4 + t * rh + ci.j;
+              // two halves, so that at most eight table entries are in flight
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 c0 = __ldg(t4 + 2 * i), c1 = __ldg(t4 + 2 * i + 1);
-                const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
-                const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
-                const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
-                const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
-                lo_w[i] = pack_bf16x2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
-                hi_w[i] = pack_bf16x2(y0 * c0.z + x0 * c0.w, y1 * c1.z + x1 * c1.w);
+              for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int i = 4 * h; i < 4 * h + 4; ++i) {
+                  const float4 c0 = valid ? __ldg(t4 + 2 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  const float4 c1 =
+                      valid ? __ldg(t4 + 2 * i + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  const float x0 = __uint_as_float(lo_u[2 * i]);
+                  const float y0 = __uint_as_float(hi_u[2 * i]);
+                  const float x1 = __uint_as_float(lo_u[2 * i + 1]);
+                  const float y1 = __uint_as_float(hi_u[2 * i + 1]);
+                  lo_w[i] = pack_bf16x2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
+                  hi_w[i] = pack_bf16x2(y0 * c0.z + x0 * c0.w, y1 * c1.z + x1 * c1.w);
+                }
+                asm volatile("" ::: "memory");
               }
             } else {
               const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
-                const float x0 = __uint_as_float(lo_u[2 * i]) + bias_at(bl, 2 * i);
-                const float y0 = __uint_as_float(hi_u[2 * i]) + bias_at(bh, 2 * i);
-                const float x1 = __uint_as_float(lo_u[2 * i + 1]) + bias_at(bl, 2 * i + 1);
-                const float y1 = __uint_as_float(hi_u[2 * i + 1]) + bias_at(bh, 2 * i + 1);
+                // (cos, sin) of frequencies 2i and 2i+1
+                const float4 cs = valid ? __ldg(cs4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float x0 = __uint_as_float(lo_u[2 * i]), y0 = __uint_as_float(hi_u[2 * i]);
+                const float x1 = __uint_as_float(lo_u[2 * i + 1]);
+                const float y1 = __uint_as_float(hi_u[2 * i + 1]);
                 lo_w[i] = pack_bf16x2(x0 * cs.x - y0 * cs.y, x1 * cs.z - y1 * cs.w);
                 hi_w[i] = pack_bf16x2(y0 * cs.x + x0 * cs.y, y1 * cs.z + x1 * cs.w);
               }
             }
             if (kt) {  // pre-transposed k is stored directly, one lane column at a time
-              store16_packed_strided(dst_t, e.T, lo_w);
-              store16_packed_strided(dst_t + rh * e.T, e.T, hi_w);
+              if (valid) {
+                store16_packed_strided(dst_t, e.T, lo_w);
+                store16_packed_strided(dst_t + rh * e.T, e.T, hi_w);
+              }
             } else {
               put16(ci.seg, ci.head, ci.j, dst, lo_w);
               put16(ci.seg, ci.head, ci.j + rh, dst + rh, hi_w);
             }
-          }
-        } else {
-          uint32_t v_u[16];
-          tmem_ld16(t_row + c, v_u);
-          tmem_wait_ld();
-          if (valid) {
+          } else {
+            uint32_t v_u[16];
+            tmem_ld16(t_row + c, v_u);
+            tmem_wait_ld();
             uint32_t w[8];
             if (ci.seg == 0) {
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                w[i] = pack_bf16x2(
-                    activate_bf16out<ACT>(__uint_as_float(v_u[2 * i]) + bias_at(bl, 2 * i)),
-                    activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1]) + bias_at(bl, 2 * i + 1)));
-            } else if (rope_small) {
+                w[i] = pack_bf16x2(activate_bf16out<ACT>(__uint_as_float(v_u[2 * i])),
+                                   activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1])));
+            } else if (rope_small && valid) {
               float v[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]) + bias_at(bl, i);
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]);
               if (e.rope_per_lane)
                 rotate_small4(v, e.rope_cs4 + t * rh, rh);
               else
@@ -748,13 +870,13 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             } else {
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                w[i] = pack_bf16x2(__uint_as_float(v_u[2 * i]) + bias_at(bl, 2 * i),
-                                   __uint_as_float(v_u[2 * i + 1]) + bias_at(bl, 2 * i + 1));
+                w[i] = pack_bf16x2(__uint_as_float(v_u[2 * i]), __uint_as_float(v_u[2 * i + 1]));
             }
-            if (kt)
-              store16_packed_strided(dst_t, e.T, w);
-            else
+            if (kt) {
+              if (valid) store16_packed_strided(dst_t, e.T, w);
+            } else {
               put16(ci.seg, ci.head, ci.j, dst, w);
+            }
           }
         }
       }
