@@ -711,6 +711,11 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       // valid and, for the head-major buffers, lie in one batch element
       // (tokens t .. t+31). Lane 0 issues the stores with its own coordinates.
       const bool tma_ff = p.tma_store && __all_sync(0xFFFFFFFFu, valid);
+      // whole heads of the blocked q|k|v order, rotation absent or in 16-lane
+      // groups, k not pre-transposed
+      const bool fast_heads = tc.n0 >= e.F && e.groups == 0 && !e.k_transposed &&
+                              (rh == 0 || rh >= 16) && (tc.n0 - e.F) % e.hd == 0 &&
+                              cols % e.hd == 0;
       auto stage_store = [&](const CUtensorMap* map, int c0, int c1, int c2, bool three_d,
                              const uint32_t (&w)[8]) {
         const uint32_t stg = staging_warp + (stage_sel & 1) * 1024;
@@ -752,8 +757,86 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
         }
+      } else if (fast_heads && tma_ff &&
+                 __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 31) -
+                         __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 0) == 31) {
+        // ---- whole heads of the blocked q|k|v part, every row valid and in one
+        // batch element: each 32 x 16 block leaves by TMA at (lane j, token t,
+        // b*heads + head); heads are decoded once per head, not per column
+        const int w0 = tc.n0 - e.F;
+        int seg = w0 / e.C;                       // 0 q, 1 k, 2 v
+        int head = (w0 - seg * e.C) / e.hd;
+        const int nh_tile = cols / e.hd;
+        const int z_b = static_cast<int>(bidx) * e.heads;
+        for (int hl = 0; hl < nh_tile; ++hl) {
+          const uint32_t t_head = t_row + hl * e.hd;
+          const CUtensorMap* map = seg == 0 ? &p.tmap_q : seg == 1 ? &p.tmap_k : &p.tmap_v;
+          const int z = z_b + head;
+          int j0 = 0;
+          if (rh > 0 && seg < 2) {
+            // rotated pairs (j, j + rh), 16 lanes at a time
+            for (int j = 0; j < rh; j += 16) {
+              const bool mine = turn == part;
+              turn = turn == 2 ? 0 : turn + 1;
+              if (!mine) continue;
+              uint32_t lo_u[16], hi_u[16];
+              tmem_ld16(t_head + j, lo_u);
+              tmem_ld16(t_head + j + rh, hi_u);
+              tmem_wait_ld();
+              uint32_t lo_w[8], hi_w[8];
+              if (e.rope_per_lane) {
+                const float4* t4 = e.rope_cs4 + t * rh + j;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                  for (int i = 4 * h; i < 4 * h + 4; ++i) {
+                    const float4 c0 = __ldg(t4 + 2 * i), c1 = __ldg(t4 + 2 * i + 1);
+                    const float x0 = __uint_as_float(lo_u[2 * i]);
+                    const float y0 = __uint_as_float(hi_u[2 * i]);
+                    const float x1 = __uint_as_float(lo_u[2 * i + 1]);
+                    const float y1 = __uint_as_float(hi_u[2 * i + 1]);
+                    lo_w[i] = pack_bf16x2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
+                    hi_w[i] = pack_bf16x2(y0 * c0.z + x0 * c0.w, y1 * c1.z + x1 * c1.w);
+                  }
+                  asm volatile("" ::: "memory");
+                }
+              } else {
+                const float4* cs4 = reinterpret_cast<const float4*>(e.rope_cs + t * rh + j);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
+                  const float x0 = __uint_as_float(lo_u[2 * i]), y0 = __uint_as_float(hi_u[2 * i]);
+                  const float x1 = __uint_as_float(lo_u[2 * i + 1]);
+                  const float y1 = __uint_as_float(hi_u[2 * i + 1]);
+                  lo_w[i] = pack_bf16x2(x0 * cs.x - y0 * cs.y, x1 * cs.z - y1 * cs.w);
+                  hi_w[i] = pack_bf16x2(y0 * cs.x + x0 * cs.y, y1 * cs.z + x1 * cs.w);
+                }
+              }
+              stage_store(map, j, static_cast<int>(t), z, true, lo_w);
+              stage_store(map, j + rh, static_cast<int>(t), z, true, hi_w);
+            }
+            j0 = 2 * rh;  // lanes past the rotated ones pass through
+          }
+          for (int j = j0; j < e.hd; j += 16) {
+            const bool mine = turn == part;
+            turn = turn == 2 ? 0 : turn + 1;
+            if (!mine) continue;
+            uint32_t v_u[16];
+            tmem_ld16(t_head + j, v_u);
+            tmem_wait_ld();
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(v_u[2 * i]), __uint_as_float(v_u[2 * i + 1]));
+            stage_store(map, j, static_cast<int>(t), z, true, w);
+          }
+          if (++head == e.heads) {
+            head = 0;
+            ++seg;
+          }
+        }
       } else {
-        // ---- a tile that reaches the head-major blocks
+        // ---- any other tile that reaches the head-major blocks
         const bool tma_heads =
             tma_ff && __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 31) -
                               __shfl_sync(0xFFFFFFFFu, static_cast<int>(t), 0) == 31;
