@@ -428,6 +428,18 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     if (r != CUDA_SUCCESS)
       return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for W rejected (CUresult %d)",
                   static_cast<int>(r));
+    if (a.b) {
+      // bias: one row of N, loaded 64 columns at a time into the bias operand
+      cuuint64_t d[2] = {static_cast<cuuint64_t>(N), 1};
+      cuuint64_t st[1] = {static_cast<cuuint64_t>(N) * esz};
+      cuuint32_t bx[2] = {64, 1};
+      r = encode(&tp.tmap_bias, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.b), d, st,
+                 bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS)
+        return fail(FP_ERR_UNSUPPORTED_LAYOUT, "tensor map for the bias rejected (CUresult %d)",
+                    static_cast<int>(r));
+    }
     // output maps: when they encode, the epilogue writes whole 32-row blocks by
     // TMA from 32-byte-swizzled staging rows (the 16-byte halves of rows 4-7 of
     // every 8 swapped, so the staging stores are free of bank conflicts)

@@ -52,6 +52,8 @@ struct TcParams {
   CUtensorMap tmap_b;
   // output maps for TMA stores: ff [M, F] (2-D), q/k/v [B*heads, T, hd] (3-D)
   CUtensorMap tmap_ff, tmap_q, tmap_k, tmap_v;
+  // bias [N] as a 1-row 2-D map (64-column boxes), when there is a bias
+  CUtensorMap tmap_bias;
   int tma_store;  // 1: the output maps are valid
   TokenMap tok;
   Epilogue epi;

@@ -10,12 +10,13 @@
 // q/k/v [B*heads, T, head_dim] (memory-efficient-attention issue #7, the
 // [batch*heads, tokens, head_dim] layout).
 //
-// Structure (one persistent CTA per SM, 14 warps):
-//   warp 0     TMA producer: loads x and W tiles into a 4-stage shared ring,
-//              and each tile's bias row into a bias operand
-//   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
-//              (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits
-//              completion to mbarriers
+// Structure (one persistent CTA per SM, 14 warps; CTA pairs by default):
+//   warp 0     TMA producer: loads x and W tiles into a shared ring (6 stages
+//              of 32 KB in a pair, 4 of 48 KB alone), and each tile's bias
+//              row into a bias operand
+//   warp 1     allocates 512 TMEM columns; in the even CTA one thread issues
+//              tcgen05.mma (2-SM M=256 or 1-SM M=128; N=256, K=16, bf16 in,
+//              fp32 accumulate) and commits completion to mbarriers
 //   warps 2-13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //              per thread), activation / rotation in registers, bf16
 //              round-to-nearest-even, TMA tensor stores of 32 x 16 blocks
@@ -45,30 +46,39 @@ namespace fp {
 namespace {
 
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
-constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int NUM_EPI_WARPS = 12;  // 3 per SM sub-partition (one per TMEM lane quarter each)
 constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
 // registers are granted per 4 warps: 14 warps count as 16, so 128 a thread fit
 static_assert(((NT / 32 + 3) / 4 * 4) * 32 * 128 <= 65536, "register budget");
-constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's 128 token rows
 constexpr int CHUNK_BYTES = 64 * BK * 2;         // one [64 ch][64 elems] MN-major chunk, 8 KB
 constexpr int ACC_COLS = BN;                     // fp32 accumulator: one TMEM column per output column
 constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: two accumulators
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1 + 2;  // ring, accumulators, drain, bias
-// bias operands: A, two [8 k][64 m] MN-major atoms (k-row 0 = 0.5); B, four
-// [8 k][64 n] atoms whose k-row 0 is the tile's bias
+// bias operands: A, two [8 k][64 m] MN-major atoms (k-row 0 = 0.5); B, one
+// [8 k][64 n] atom per 64 W columns held, k-row 0 = the tile's bias
 constexpr int BIAS_A_BYTES = 2 * 1024;
-constexpr int BIAS_B_BYTES = 4 * 1024;
 // per epilogue warp, two 1 KB buffers staging [32 rows][16 bf16] blocks for TMA stores
 constexpr int STAGING_BYTES_PER_WARP = 2 * 1024;
 constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
-constexpr int SMEM_BYTES =
-    1024 + STAGES * STAGE_BYTES + BIAS_A_BYTES + BIAS_B_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
+
+// Per cluster size: a single CTA holds all 256 W columns of its tile; a CTA
+// pair runs 2-SM MMAs (M = 256), each CTA holding its own 128 token rows and
+// its own 128 of the 256 W columns, so a stage is 32 KB instead of 48 KB.
+template <int CL>
+struct Cfg {
+  static constexpr int B_COLS = BN / CL;
+  static constexpr int B_BYTES = B_COLS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = CL == 2 ? 6 : 4;
+  static constexpr int BIAS_B_BYTES = (B_COLS / 64) * 1024;
+  // full and empty per stage; two accumulators full/empty; drain; bias full, empty
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BIAS_A_BYTES + BIAS_B_BYTES +
+                                    STAGING_BYTES + NUM_BARS * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -99,6 +109,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -160,26 +183,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Same, written to the same shared-memory offset of every CTA in `mask` of the
-// cluster, each destination's mbarrier (same offset) receiving its bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      uint32_t bar, int c0, int c1,
-                                                      uint16_t mask) {
+// The odd CTA of a pair: tiled loads into its own shared memory whose bytes
+// complete on an mbarrier of the even CTA (`bar`, a cluster address).
+__device__ __forceinline__ void tma_load_5d_peer(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2, int c3,
+                                                 int c4) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
 
-// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of
-// 16), completing on an mbarrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d_peer(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -259,37 +280,62 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and
-// B, operand majorness, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_major) {
+// B, operand majorness, N >> 3 at bit 17, M >> 4 at bit 24 (M = 256 for a
+// 2-SM MMA).
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_major, int m) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// One MMA. CL == 1: M = 128 on this SM. CL == 2: a 2-SM MMA issued by the even
+// CTA of the pair: A rows come from both CTAs' shared memory (same offsets),
+// B columns half from each, and each CTA's TMEM receives its 128 rows.
+template <int CL>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (CL == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
+// Arrive on this CTA's mbarrier once the thread's earlier MMAs have completed.
+template <int CL>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+  if constexpr (CL == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
 }
 
-// Arrive on the mbarrier at the same offset in every CTA of `mask` once this
-// thread's earlier MMAs have completed.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
+// Same, on the mbarrier at the same offset in every CTA of the cluster.
+template <int CL>
+__device__ __forceinline__ void umma_commit_all(uint32_t bar) {
+  if constexpr (CL == 1) {
+    umma_commit<1>(bar);
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+  }
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -442,29 +488,42 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 
 // ACT: the ff-block activation, fixed at compile time so the per-value code
 // has no branch on it.
-// CL: CTAs per cluster. With CL == 2 the two CTAs take neighbouring M-tiles of
-// one N-tile and each multicasts half of the W tile into both, so each CTA
-// reads 32 KB instead of 48 KB from L2 per k-step.
+// CL: CTAs per cluster. With CL == 2 the two CTAs (neighbouring M-tiles of one
+// N-tile) run as a pair: the even CTA issues 2-SM MMAs (M = 256, N = 256) that
+// read each CTA's own 128 token rows and each CTA's own half of the W tile, so
+// a CTA streams 32 KB per k-step into shared memory and the tensor core reads
+// 32 KB back, against 48 KB each way for a single CTA. The odd CTA's loads
+// complete directly on the even CTA's full barriers (the cta_group::2 form of
+// the tensor copy), which the even CTA's producer arms for both halves. (A
+// relay of the odd CTA's completions through a second thread, or a second
+// barrier per stage, each measured 20-100 % slower.)
 // One CTA per SM (its shared-memory footprint allows no second one).
 template <bool A_MN_MAJOR, int ACT, int CL>
 __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using G = Cfg<CL>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KB alignment
   uint8_t* sptr = smem_raw + (sbase - raw_addr);
   const uint32_t bias_a = sbase + STAGES * STAGE_BYTES;
   const uint32_t bias_b = bias_a + BIAS_A_BYTES;
-  const uint32_t staging0 = bias_b + BIAS_B_BYTES;
+  const uint32_t staging0 = bias_b + G::BIAS_B_BYTES;
   const uint32_t bar0 = staging0 + STAGING_BYTES;
+  // full: the stage landed (in a pair: both CTAs' halves, on the even CTA's
+  // barrier); empty: the MMAs read it
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  const uint32_t bias_full = bar0 + 8u * (2 * STAGES + 5);   // bias row landed
-  const uint32_t bias_empty = bar0 + 8u * (2 * STAGES + 6);  // bias MMA has read it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
-      sptr + STAGES * STAGE_BYTES + BIAS_A_BYTES + BIAS_B_BYTES + STAGING_BYTES + NUM_BARS * 8);
+  const uint32_t bar1 = bar0 + 8u * (2 * STAGES);
+  auto tfull_bar = [&](int b) { return bar1 + 8u * b; };
+  auto tempty_bar = [&](int b) { return bar1 + 8u * (2 + b); };
+  const uint32_t drain_bar = bar1 + 8u * 4;
+  const uint32_t bias_full = bar1 + 8u * 5;    // the bias row landed (both halves)
+  const uint32_t bias_empty = bar1 + 8u * 6;   // the bias MMA has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + BIAS_A_BYTES +
+                                                    G::BIAS_B_BYTES + STAGING_BYTES +
+                                                    G::NUM_BARS * 8);
   const bool has_bias = p.epi.bias != nullptr;
 
   const int warp = threadIdx.x >> 5;
@@ -473,16 +532,15 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int64_t first_unit = blockIdx.x / CL;
   const int64_t unit_step = gridDim.x / CL;
-  constexpr uint16_t kPairMask = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // the MMA of every CTA that reads this stage
+      mbar_init(empty_bar(s), 1);  // one commit from the MMA thread of the pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+      mbar_init(tempty_bar(b), CL * NUM_EPI_WARPS);  // every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     mbar_init(bias_full, 1);
@@ -495,7 +553,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   if (has_bias) {
     // bias operands: A atoms hold 0.5 (bf16 0x3F00) in k-row 0, B atoms start
     // at zero (their k-row 0 is overwritten per tile; rows 1-7 stay zero)
-    for (int i = threadIdx.x; i < (BIAS_A_BYTES + BIAS_B_BYTES) / 16; i += NT) {
+    for (int i = threadIdx.x; i < (BIAS_A_BYTES + G::BIAS_B_BYTES) / 16; i += NT) {
       const uint32_t off = static_cast<uint32_t>(i) * 16u;
       const uint32_t v = (off < BIAS_A_BYTES && (off & 1023u) < 128u) ? 0x3F003F00u : 0u;
       st_shared_v4(bias_a + off, v, v, v, v);
@@ -503,11 +561,20 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     fence_async_shared();  // visible to the tensor core (async proxy)
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // a pair allocates collectively: one warp of each CTA, 512 columns in each
+    if constexpr (CL == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -517,92 +584,117 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   const int num_kb = p.num_k_blocks;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer (every CTA)
     if (lane == 0) {
       bool inject = (p.inject_stall & 1) && blockIdx.x == 0;
       uint32_t armed_mask = 0, armed_parity = 0;  // per stage: armed, parity of its last arming
       int stage = 0;
       uint32_t phase = 0;
       uint32_t bias_phase = 0;
-      bool bias_armed = false;
-      const uint16_t* const bias = static_cast<const uint16_t*>(p.epi.bias);
-      for (int64_t u = first_unit; u < p.num_units; u += unit_step) {
+      bool bias_armed = false, aborted = false;
+      const bool peer = CL > 1 && rank != 0;
+      const int col0 = rank * G::B_COLS;  // first tile column this CTA holds
+      for (int64_t u = first_unit; u < p.num_units && !aborted; u += unit_step) {
         const TileCoord tc = tile_coord<CL>(p, u, rank);
         int oc[3];
         outer_coords(p.tok, tc.o, oc);
         if (has_bias) {
-          // the tile's bias row into k-row 0 of the four B atoms, once the
-          // previous tile's bias MMA has read them
-          if (!wait_bounded(bias_empty, bias_phase ^ 1u, wc, true)) break;
-          const int cols = min(p.epi.bn_eff, p.epi.N - tc.n0);
-          mbar_arrive_expect_tx(bias_full, static_cast<uint32_t>(cols) * 2u);
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) {
-            const int len = min(64, cols - 64 * j);
-            if (len > 0)
-              bulk_load(bias_b + j * 1024, bias + tc.n0 + 64 * j, static_cast<uint32_t>(len) * 2u,
-                        bias_full);
-          }
-          bias_armed = true;
-          bias_phase ^= 1u;
-        }
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
-            ok = false;
+          // this CTA's part of the tile's bias row into k-row 0 of its B atoms,
+          // once the previous tile's bias MMA has read them (columns past N
+          // read as zeros)
+          if (!wait_bounded(bias_empty, bias_phase ^ 1u, wc, true)) {
+            aborted = true;
             break;
           }
-          if (inject) {
-            inject = false;  // withhold this stage: its consumer's wait runs out
+          if (!peer) {
+            mbar_arrive_expect_tx(bias_full, CL * G::B_COLS * 2);  // both CTAs' parts
+#pragma unroll
+            for (int j = 0; j < G::B_COLS / 64; ++j)
+              tma_load_2d(bias_b + j * 1024, &p.tmap_bias, bias_full, tc.n0 + 64 * j, 0);
+            bias_armed = true;
           } else {
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            const uint32_t a_dst = sbase + stage * STAGE_BYTES;
-            const uint32_t b_dst = a_dst + A_BYTES;
-            const int k0 = kb * BK;
+            const uint32_t pb = mapa_shared(bias_full, 0);
+#pragma unroll
+            for (int j = 0; j < G::B_COLS / 64; ++j)
+              tma_load_2d_peer(bias_b + j * 1024, &p.tmap_bias, pb, tc.n0 + col0 + 64 * j, 0);
+          }
+          bias_phase ^= 1u;
+        }
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t a_dst = sbase + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const int k0 = kb * BK;
+          if (peer) {
+            // the even CTA armed its full barrier for these bytes too
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
             if (A_MN_MAJOR) {
-              tma_load_5d(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1], oc[2]);
-              tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64, k0,
-                          oc[0], oc[1], oc[2]);
+              tma_load_5d_peer(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1],
+                               oc[2]);
+              tma_load_5d_peer(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64,
+                               k0, oc[0], oc[1], oc[2]);
             } else {
-              tma_load_5d(a_dst, &p.tmap_a, fb, k0, static_cast<int>(tc.s0), oc[0], oc[1], oc[2]);
+              tma_load_5d_peer(a_dst, &p.tmap_a, fb, k0, static_cast<int>(tc.s0), oc[0], oc[1],
+                               oc[2]);
             }
-            if (CL == 1) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0);
+            for (int j = 0; j < G::B_COLS / 64; ++j)
+              tma_load_2d_peer(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + col0 + 64 * j, k0);
+          } else {
+            if (inject) {
+              inject = false;  // withhold this stage: its consumer's wait runs out
             } else {
-              // this CTA's share of the W tile, written into every CTA of the pair
-              constexpr int per = BN / 64 / CL;
-#pragma unroll
-              for (int jj = 0; jj < per; ++jj) {
-                const int j = rank * per + jj;
-                tma_load_2d_multicast(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0,
-                                      kPairMask);
+              const uint32_t fb = full_bar(stage);
+              mbar_arrive_expect_tx(fb, CL * STAGE_BYTES);  // both CTAs' halves
+              if (A_MN_MAJOR) {
+                tma_load_5d(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1],
+                            oc[2]);
+                tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64, k0,
+                            oc[0], oc[1], oc[2]);
+              } else {
+                tma_load_5d(a_dst, &p.tmap_a, fb, k0, static_cast<int>(tc.s0), oc[0], oc[1],
+                            oc[2]);
               }
+#pragma unroll
+              for (int j = 0; j < G::B_COLS / 64; ++j)
+                tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, tc.n0 + 64 * j, k0);
+              armed_mask |= 1u << stage;
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             }
-            armed_mask |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (!ok) break;
       }
-      // drain: every armed stage's copies must land before the CTA exits
+      // drain: this CTA's copies must land before it exits. The even CTA waits
+      // on the barriers it armed (an armed phase whose peer half never came
+      // runs out after 10 ms: nothing is then in flight). The odd CTA's
+      // copies complete on the even CTA's barriers, all of which the even
+      // CTA's MMA thread waits for in a normal run; after an abort the odd CTA
+      // allows its last copies a bounded grace period instead.
+      const WaitCtl dc{wc.status, wc.limit_ns < 10000000ull ? wc.limit_ns : 10000000ull,
+                       wc.launch_tag};
       for (int s = 0; s < STAGES; ++s)
-        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, wc, false);
-      if (bias_armed) wait_bounded(bias_full, bias_phase ^ 1u, wc, false);
+        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, dc, false);
+      if (bias_armed) wait_bounded(bias_full, bias_phase ^ 1u, dc, false);
+      if (peer && aborted) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000ull) {
+        }
+      }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && rank == 0) {
     // ------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
-      const uint32_t idesc = make_idesc(A_MN_MAJOR, true);
+      const uint32_t idesc = make_idesc(A_MN_MAJOR, true, BM * CL);
       // bias MMA: both operands MN-major; m (n) chunks 1 KB apart, and a k-group
       // stride of 0 so k-rows 8-15 read the same atom as k-rows 0-7
-      const uint32_t idesc_bias = make_idesc(true, true);
+      const uint32_t idesc_bias = make_idesc(true, true, BM * CL);
       const uint64_t bias_a_desc = sw128_desc(bias_a, 1024, 0);
       const uint64_t bias_b_desc = sw128_desc(bias_b, 1024, 0);
       int stage = 0;
@@ -619,8 +711,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         if (has_bias) {
           if (!wait_bounded(bias_full, bias_phase, wc, true)) break;
           tc_fence_after();
-          umma_bf16(d_tmem, bias_a_desc, bias_b_desc, idesc_bias, 0u);  // D = bias
-          umma_commit(bias_empty);
+          umma_bf16<CL>(d_tmem, bias_a_desc, bias_b_desc, idesc_bias, 0u);  // D = bias
+          umma_commit_all<CL>(bias_empty);
           bias_phase ^= 1u;
           issued = true;
         }
@@ -641,28 +733,24 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             const uint64_t a_desc = A_MN_MAJOR ? sw128_desc(a_addr + k * 2048, CHUNK_BYTES, 1024)
                                                : sw128_desc(a_addr + k * 32, 16, 1024);
             const uint64_t b_desc = sw128_desc(b_addr + k * 2048, CHUNK_BYTES, 1024);
-            umma_bf16(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : acc0);
+            umma_bf16<CL>(d_tmem, a_desc, b_desc, idesc, (kb | k) != 0 ? 1u : acc0);
           }
           issued = true;
-          // frees the stage (in every CTA whose producer writes into ours) once read
-          if (CL == 1)
-            umma_commit(empty_bar(stage));
-          else
-            umma_commit_multicast(empty_bar(stage), kPairMask);
+          umma_commit_all<CL>(empty_bar(stage));  // frees the stage in every CTA of the pair
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(buf));  // accumulator ready for the epilogue
+        umma_commit_all<CL>(tfull_bar(buf));  // accumulators ready for the epilogues
       }
       if (issued) {
-        umma_commit(drain_bar);  // all MMAs of this CTA retired before TMEM is freed
+        umma_commit<CL>(drain_bar);  // all MMAs retired before TMEM is freed
         wait_bounded(drain_bar, 0, wc, false);
       }
     }
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------------ epilogue warps
     const Epilogue& e = p.epi;
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
@@ -965,7 +1053,14 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      // release the accumulator: the even CTA's MMA thread waits on every
+      // epilogue warp of the pair
+      if (lane == 0) {
+        if (CL == 1 || rank == 0)
+          mbar_arrive(tempty_bar(buf));
+        else
+          mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));
+      }
     }
     if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
     __syncwarp();
@@ -979,9 +1074,14 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    if constexpr (CL == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
   }
 }
 
@@ -993,17 +1093,18 @@ cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream)
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<CL>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
   if (CL == 1) {
-    kernel<<<num_ctas, NT, SMEM_BYTES, stream>>>(p);
+    kernel<<<num_ctas, NT, Cfg<CL>::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<CL>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
