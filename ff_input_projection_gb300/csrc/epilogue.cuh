@@ -147,41 +147,104 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return r;
 }
 
-// Activations for bf16 outputs, branch-free and short:
+// Packed fp32 pairs (sm_100 f32x2 arithmetic: two IEEE fp32 operations per
+// instruction, the same results as two scalar ones).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi);
+
+// Activation of two fp32 values, rounded to a bf16 pair (low = y0). Branch-free
+// and short, on packed fp32 pairs:
 //  - exact-erf GELU with erf from Abramowitz & Stegun, "Handbook of
 //    Mathematical Functions" (1964), eq. 7.1.26: for z >= 0,
-//    erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
-//    t = 1 / (1 + p z), absolute error <= 1.5e-7;
-//    GELU(y) = y/2 (1 + sign(y) erf(|y|/sqrt 2)) = (y + |y| erf(|y|/sqrt 2)) / 2;
-//  - tanh-GELU with tanh(u) = 1 - 2 / (1 + exp(2u));
-//  - SiLU y / (1 + exp(-y)).
+//    erf(z) = 1 - t P(t) exp(-z^2), t = 1 / (1 + p z),
+//    P(t) = a1 + a2 t + a3 t^2 + a4 t^3 + a5 t^4, absolute error <= 1.5e-7.
+//    With a = |y| and z = a / sqrt 2 both signs of y reduce to
+//    GELU(y) = relu(y) - (a/2) t P(t) exp(-a^2/2);
+//    the a in front is clamped at 1e30 so y = +-inf gives inf and 0, not NaN
+//    (a NaN still propagates through t);
+//  - tanh-GELU as y * sigmoid(2u), u = sqrt(2/pi) (y + 0.044715 y^3);
+//  - SiLU y * sigmoid(y).
 // Absolute errors stay near 1e-7 of the input scale, far below bf16 rounding.
 template <int ACT>
-__device__ __forceinline__ float activate_bf16out(float y) {
+__device__ __forceinline__ uint32_t activate2_bf16(uint32_t u0, uint32_t u1) {
   constexpr float kLog2e = 1.4426950408889634f;
+  const float y0 = __uint_as_float(u0), y1 = __uint_as_float(u1);
   if (ACT == ACT_GELU_ERF) {
-    const float a = fabsf(y);
-    const float z = a * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    poly *= t;
-    const float ez = ex2_approx(-(z * z) * kLog2e);
-    const float erf_z = fmaf(-poly, ez, 1.0f);
-    return 0.5f * fmaf(a, erf_z, y);
+    const float a0 = fabsf(y0), a1 = fabsf(y1);
+    const uint64_t A = f2_pack(a0, a1);
+    const uint64_t D = f2_fma(A, f2_splat(0.3275911f * 0.70710678118654752f), f2_splat(1.0f));
+    float d0, d1;
+    f2_unpack(D, d0, d1);
+    const uint64_t T = f2_pack(rcp_approx(d0), rcp_approx(d1));
+    // -(1/2) a_k: the sign and the 1/2 of the GELU form folded into P
+    uint64_t P = f2_fma(f2_splat(-0.5f * 1.061405429f), T, f2_splat(-0.5f * -1.453152027f));
+    P = f2_fma(P, T, f2_splat(-0.5f * 1.421413741f));
+    P = f2_fma(P, T, f2_splat(-0.5f * -0.284496736f));
+    P = f2_fma(P, T, f2_splat(-0.5f * 0.254829592f));
+    const uint64_t AC = f2_pack(fminf(a0, 1e30f), fminf(a1, 1e30f));
+    const uint64_t S = f2_mul(f2_mul(P, T), AC);  // -(a/2) t P(t)
+    const uint64_t Q = f2_mul(f2_mul(A, f2_splat(-0.5f * kLog2e)), A);  // log2 exp(-a^2/2)
+    float q0, q1;
+    f2_unpack(Q, q0, q1);
+    const uint64_t E = f2_pack(ex2_approx(q0), ex2_approx(q1));
+    const uint64_t R = f2_fma(S, E, f2_pack(fmaxf(y0, 0.0f), fmaxf(y1, 0.0f)));
+    float r0, r1;
+    f2_unpack(R, r0, r1);
+    return pack_bf16x2(r0, r1);
   } else if (ACT == ACT_GELU_TANH) {
-    const float u = 0.79788456080286536f * fmaf(0.044715f * y, y * y, y);
-    const float th = fmaf(-2.0f, rcp_approx(1.0f + ex2_approx(2.0f * kLog2e * u)), 1.0f);
-    return 0.5f * y * (1.0f + th);
+    // sigmoid(2u) = 1 / (1 + 2^(y (k1 + k3 y^2))), k1 = -2 log2(e) sqrt(2/pi)
+    constexpr float k1 = -2.0f * kLog2e * 0.79788456080286536f;
+    const uint64_t Y = f2_pack(y0, y1);
+    const uint64_t G = f2_mul(f2_fma(f2_mul(Y, Y), f2_splat(k1 * 0.044715f), f2_splat(k1)), Y);
+    float g0, g1;
+    f2_unpack(G, g0, g1);
+    const uint64_t E1 = f2_add(f2_pack(ex2_approx(g0), ex2_approx(g1)), f2_splat(1.0f));
+    float e0, e1;
+    f2_unpack(E1, e0, e1);
+    float r0, r1;
+    f2_unpack(f2_mul(Y, f2_pack(rcp_approx(e0), rcp_approx(e1))), r0, r1);
+    return pack_bf16x2(r0, r1);
   } else if (ACT == ACT_SILU) {
-    return y * rcp_approx(1.0f + ex2_approx(-kLog2e * y));
+    const uint64_t Y = f2_pack(y0, y1);
+    float g0, g1;
+    f2_unpack(f2_mul(Y, f2_splat(-kLog2e)), g0, g1);
+    const uint64_t E1 = f2_add(f2_pack(ex2_approx(g0), ex2_approx(g1)), f2_splat(1.0f));
+    float e0, e1;
+    f2_unpack(E1, e0, e1);
+    float r0, r1;
+    f2_unpack(f2_mul(Y, f2_pack(rcp_approx(e0), rcp_approx(e1))), r0, r1);
+    return pack_bf16x2(r0, r1);
   } else if (ACT == ACT_RELU2) {
-    const float r = fmaxf(y, 0.0f);
-    return r * r;
+    const uint64_t Rl = f2_pack(fmaxf(y0, 0.0f), fmaxf(y1, 0.0f));
+    float r0, r1;
+    f2_unpack(f2_mul(Rl, Rl), r0, r1);
+    return pack_bf16x2(r0, r1);
   }
-  return y;
+  return pack_bf16x2(y0, y1);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {

@@ -835,8 +835,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           uint32_t w[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            w[i] = pack_bf16x2(activate_bf16out<ACT>(__uint_as_float(v_u[2 * i])),
-                               activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1])));
+            w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
           if (tma_ff) {
             stage_store(&p.tmap_ff, tc.n0 + c, static_cast<int>(m), 0, false, w);
           } else if (valid) {
@@ -1026,8 +1025,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             if (ci.seg == 0) {
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                w[i] = pack_bf16x2(activate_bf16out<ACT>(__uint_as_float(v_u[2 * i])),
-                                   activate_bf16out<ACT>(__uint_as_float(v_u[2 * i + 1])));
+                w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
             } else if (rope_small && valid) {
               float v[16];
 #pragma unroll
