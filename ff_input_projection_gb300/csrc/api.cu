@@ -454,6 +454,11 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
                             ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                             CU_TENSOR_MAP_L2_PROMOTION_NONE,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        cuuint32_t bx32[2] = {32, 32};  // 64-byte rows, 64-byte swizzle
+        okm = okm && encode(&tp.tmap_ff32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_ff, d, st,
+                            bx32, ostr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
       }
       const int nkv = p->groups > 0 ? p->groups : p->heads;
       void* const outs3[3] = {a.out_q, a.out_k, a.out_v};

@@ -51,7 +51,8 @@ struct TcParams {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b;
   // output maps for TMA stores: ff [M, F] (2-D), q/k/v [B*heads, T, hd] (3-D)
-  CUtensorMap tmap_ff, tmap_q, tmap_k, tmap_v;
+  // (ff twice: 16-column boxes, and 32-column boxes for tiles inside the ff block)
+  CUtensorMap tmap_ff, tmap_ff32, tmap_q, tmap_k, tmap_v;
   // bias [N] as a 1-row 2-D map (64-column boxes), when there is a bias
   CUtensorMap tmap_bias;
   int tma_store;  // 1: the output maps are valid

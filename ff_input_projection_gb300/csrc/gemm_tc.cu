@@ -58,8 +58,9 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;          // 512: two accumulators
 // bias operands: A, two [8 k][64 m] MN-major atoms (k-row 0 = 0.5); B, one
 // [8 k][64 n] atom per 64 W columns held, k-row 0 = the tile's bias
 constexpr int BIAS_A_BYTES = 2 * 1024;
-// per epilogue warp, two 1 KB buffers staging [32 rows][16 bf16] blocks for TMA stores
-constexpr int STAGING_BYTES_PER_WARP = 2 * 1024;
+// per epilogue warp, two 2 KB buffers staging a [32 rows][32 bf16] block (ff)
+// or a [32 rows][16 bf16] block (q/k/v, mixed tiles) for a TMA store
+constexpr int STAGING_BYTES_PER_WARP = 2 * 2048;
 constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
 static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
 
@@ -71,7 +72,7 @@ struct Cfg {
   static constexpr int B_COLS = BN / CL;
   static constexpr int B_BYTES = B_COLS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = CL == 2 ? 6 : 4;
+  static constexpr int STAGES = CL == 2 ? 5 : 3;
   static constexpr int BIAS_B_BYTES = (B_COLS / 64) * 1024;
   // full and empty per stage; two accumulators full/empty; drain; bias full, empty
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2;
@@ -352,6 +353,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
 }
@@ -806,7 +821,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                               cols % e.hd == 0;
       auto stage_store = [&](const CUtensorMap* map, int c0, int c1, int c2, bool three_d,
                              const uint32_t (&w)[8]) {
-        const uint32_t stg = staging_warp + (stage_sel & 1) * 1024;
+        const uint32_t stg = staging_warp + (stage_sel & 1) * 2048;
         ++stage_sel;
         if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it
         __syncwarp();
@@ -822,26 +837,42 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           bulk_commit();
         }
       };
-      if (tc.n0 + cols <= e.F) {
-        // ---- a tile inside the ff block: activation, then [M, F] row-major
+      if (tc.n0 + cols <= e.F && (cols & 31) == 0) {
+        // ---- a tile inside the ff block: activation, then [M, F] row-major,
+        // 32 columns per work unit (the tile's width is a multiple of 32)
         uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F + tc.n0;
-        for (int c = 0; c < cols; c += 16) {
+        // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)
+        const uint32_t sw64 = (lane >> 1) & 3u;
+        for (int c = 0; c < cols; c += 32) {
           const bool mine = turn == part;
           turn = turn == 2 ? 0 : turn + 1;
           if (!mine) continue;
-          uint32_t v_u[16];
-          tmem_ld16(t_row + c, v_u);
+          uint32_t v_u[32];
+          tmem_ld32(t_row + c, v_u);
           tmem_wait_ld();
-          uint32_t w[8];
+          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
           if (tma_ff) {
-            stage_store(&p.tmap_ff, tc.n0 + c, static_cast<int>(m), 0, false, w);
+            const uint32_t stg = staging_warp + (stage_sel & 1) * 2048;
+            ++stage_sel;
+            if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(stg + lane * 64 + ((q ^ sw64) << 4), w[4 * q], w[4 * q + 1],
+                           w[4 * q + 2], w[4 * q + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.tmap_ff32, stg, tc.n0 + c, static_cast<int>(m));
+              bulk_commit();
+            }
           } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(ff_row + c);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
       } else if (fast_heads && tma_ff &&
