@@ -33,6 +33,7 @@ ACT_NAMES = {ACT_NONE: "none", ACT_GELU_ERF: "gelu", ACT_GELU_TANH: "gelu_tanh",
 
 # stream ids of the tensors one workload draws
 STREAM_X, STREAM_W, STREAM_B = 1, 2, 3
+STREAM_GFF, STREAM_GQ, STREAM_GK, STREAM_GV = 4, 5, 6, 7  # upstream gradients (backward)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -180,6 +181,29 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Dict[str, np.ndarray
     W = W.reshape(w.C, w.N)
     b = _to_dtype(normal(seed, STREAM_B, w.N) * np.sqrt(0.02), w.dtype) if w.bias else None
     return {"x": x, "W": W, "b": b, "pos": None}
+
+
+def make_grads(w: Workload, seed: Optional[int] = None) -> Dict[str, Optional[np.ndarray]]:
+    """Draw upstream gradients for the backward of workload ``w``: N(0, 1)
+    values in the forward's output layouts and dtype — ff [M, F], q
+    [B*heads, T, hd], k [B*kv, T, hd] (or [B*kv, hd, T] pre-transposed), v
+    [B*kv, T, hd]; None for an empty block."""
+    seed = w.seed if seed is None else seed
+    nkv = w.n_query_groups or w.heads
+    B, T, hd = w.Bb, w.T, w.head_dim
+
+    def draw(stream, shape):
+        n = int(np.prod(shape, dtype=np.int64))
+        return _to_dtype(normal(seed, stream, n), w.dtype).reshape(shape)
+
+    out: Dict[str, Optional[np.ndarray]] = {"ff": None, "q": None, "k": None, "v": None}
+    if w.F:
+        out["ff"] = draw(STREAM_GFF, (w.M, w.F))
+    if w.heads:
+        out["q"] = draw(STREAM_GQ, (B * w.heads, T, hd))
+        out["k"] = draw(STREAM_GK, (B * nkv, hd, T) if w.k_transposed else (B * nkv, T, hd))
+        out["v"] = draw(STREAM_GV, (B * nkv, T, hd))
+    return out
 
 
 def as_float64(a: Optional[np.ndarray], dtype: str) -> Optional[np.ndarray]:

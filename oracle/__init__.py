@@ -31,6 +31,11 @@ MUTATIONS = {
     "pos_global": 10, "rope_on_v": 11, "qk_swapped": 12, "gelu_scale": 13,
     "relu2_unsquared": 14,
 }
+# planted mistakes of the backward
+BWD_MUTATIONS = {
+    "bwd_rope_forward": 21, "bwd_act_value": 22, "bwd_no_recompute_bias": 23,
+    "bwd_dw_swap": 24, "bwd_dx_no_w": 25,
+}
 
 
 def build(force: bool = False) -> str:
@@ -57,6 +62,10 @@ def _load():
         I64 = ctypes.c_int64
         f.argtypes = [P, I, I, P, P, I, I, P, P, P, P, P, I, I, I, I, I, I, I, I,
                       ctypes.c_double, P, I64, P, P, P, P, I, I]
+        g = lib.oracle_backward
+        g.restype = ctypes.c_int
+        g.argtypes = [P, I, I, P, P, I, I, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                      ctypes.c_double, P, P, P, P, I, P, I64, P, I64, P, P, P, I, I]
         _lib = lib
     return _lib
 
@@ -145,3 +154,78 @@ def forward_workload(w, inputs: Dict[str, np.ndarray], **kw) -> Dict[str, np.nda
                    pos=inputs.get("pos"), rope_cos=inputs.get("rope_cos"),
                    rope_sin=inputs.get("rope_sin"), groups=w.n_query_groups,
                    rope_n_elem=w.rope_n_elem, k_transposed=w.k_transposed, **kw)
+
+
+def backward(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], grads: Dict[str, np.ndarray],
+             *, channel_dim: int, n_batch_dims: int, C: int, F: int, heads: int, head_dim: int,
+             act: int, rope_base: float, dtype: str, pos: Optional[np.ndarray] = None,
+             rope_cos: Optional[np.ndarray] = None, rope_sin: Optional[np.ndarray] = None,
+             groups: int = 0, rope_n_elem: int = 0, k_transposed: bool = False,
+             rows: Optional[Sequence[int]] = None, cols: Optional[Sequence[int]] = None,
+             threads: Optional[int] = None, mutate: int = 0) -> Dict[str, np.ndarray]:
+    """Gradients of the projection in fp64, given upstream gradients ``grads``
+    (keys ff, q, k, v; stored values in the forward's output layouts, dtype of x).
+
+    Default: ``dx`` [M, C] (token order m = b*T + t), ``dW`` [C, N], ``db`` [N].
+    With ``rows``: ``dx`` [R, C] of those tokens. With ``cols``: ``dW`` [C, K] and
+    ``db`` [K] of those fused columns (summed over every token).
+    """
+    lib = _load()
+    is_bf16 = dtype == "bf16"
+    want = np.uint16 if is_bf16 else np.float32
+    sizes = np.array(x.shape, dtype=np.int64)
+    xb = np.ascontiguousarray(x)
+    if xb.dtype != want:
+        raise TypeError(f"x must be {want}")
+    strides = np.array([s // xb.itemsize for s in xb.strides], dtype=np.int64)
+    Wc = np.ascontiguousarray(W, dtype=want)
+    bc = None if b is None else np.ascontiguousarray(b, dtype=want)
+    posc = None if pos is None else np.ascontiguousarray(pos, dtype=np.int32)
+    tcos = None if rope_cos is None else np.ascontiguousarray(rope_cos, dtype=np.float64)
+    tsin = None if rope_sin is None else np.ascontiguousarray(rope_sin, dtype=np.float64)
+    g = {k: (None if grads.get(k) is None else np.ascontiguousarray(grads[k], dtype=want))
+         for k in ("ff", "q", "k", "v")}
+    nkv = groups if groups else heads
+    N = F + ((heads + 2 * groups) * head_dim if groups else 3 * heads * head_dim)
+    tok = [s for a, s in enumerate(x.shape) if a != channel_dim]
+    M = int(np.prod(tok, dtype=np.int64))
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rr = cc = None
+    R = K = 0
+    if rows is not None:
+        mode = 1
+        rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        R = len(rr)
+        out = {"dx": np.zeros((R, C))}
+    elif cols is not None:
+        mode = 2
+        cc = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        K = len(cc)
+        out = {"dW": np.zeros((C, K)), "db": np.zeros(K)}
+    else:
+        mode = 0
+        out = {"dx": np.zeros((M, C)), "dW": np.zeros((C, N)), "db": np.zeros(N)}
+    del nkv
+    rc = lib.oracle_backward(_ptr(xb), int(is_bf16), x.ndim, _ptr(sizes), _ptr(strides),
+                             channel_dim, n_batch_dims, _ptr(Wc), _ptr(bc), _ptr(posc),
+                             _ptr(tcos), _ptr(tsin), C, F, heads, head_dim, groups, rope_n_elem,
+                             act, int(bool(k_transposed)), float(rope_base),
+                             _ptr(g["ff"]), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), mode,
+                             _ptr(rr), R, _ptr(cc), K,
+                             _ptr(out.get("dx")), _ptr(out.get("dW")), _ptr(out.get("db")),
+                             int(threads), int(mutate))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
+
+
+def backward_workload(w, inputs: Dict[str, np.ndarray], grads: Dict[str, np.ndarray], **kw
+                      ) -> Dict[str, np.ndarray]:
+    """``backward`` with the shape parameters of an ``fpsynth.Workload``."""
+    return backward(inputs["x"], inputs["W"], inputs["b"], grads, channel_dim=w.channel_dim,
+                    n_batch_dims=w.n_batch_dims, C=w.C, F=w.F, heads=w.heads,
+                    head_dim=w.head_dim, act=w.act, rope_base=w.rope_base, dtype=w.dtype,
+                    pos=inputs.get("pos"), rope_cos=inputs.get("rope_cos"),
+                    rope_sin=inputs.get("rope_sin"), groups=w.n_query_groups,
+                    rope_n_elem=w.rope_n_elem, k_transposed=w.k_transposed, **kw)

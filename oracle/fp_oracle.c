@@ -44,6 +44,21 @@
  * All arithmetic is float64 on the exactly-widened stored inputs (bf16 or
  * f32). cos/sin/erf/tanh/exp/pow come from the C library.
  *
+ * Backward (oracle_backward, below): the gradients of the same operation
+ * with respect to x, W and b, given upstream gradients in the output layouts.
+ * The pages name the backward pass of the fused linear only as the part that
+ * is left unfused and slow ("[perf] Fused linear", xformers PR #283); its
+ * content is the chain rule through steps 5..1 taken in reverse:
+ *  5'. gather the upstream gradient row of token m from the split buffers;
+ *  4'. rotary embedding: the transpose of the rotation, per pair (i, i+half):
+ *      du_i = g_i cos_i + g_{i+half} sin_{i+half},
+ *      du_{i+half} = g_{i+half} cos_{i+half} - g_i sin_i; other lanes copy;
+ *  3'. activation: times act'(y) at the pre-activation y = x W + b of the ff
+ *      block, recomputed from the inputs (nothing is saved by the forward);
+ *      bias: db = sum over tokens of G;
+ *  2'. fused linear: dx[m, c] = sum_n W[c, n] G[m, n], dW = X^T G;
+ *  1'. dx is returned per token, [M, C] in token order m = b*T + t.
+ *
  * `mutate` != 0 plants one deliberate mistake (see the MUT_* list). Only the
  * oracle's own pin tests use it, to show that each pin catches a real error.
  */
@@ -71,6 +86,12 @@ enum {
   MUT_QK_SWAPPED = 12,       /* q and k column blocks exchanged */
   MUT_GELU_SCALE = 13,       /* erf(y/2) instead of erf(y/sqrt 2) */
   MUT_RELU2_UNSQUARED = 14,  /* squared ReLU returned as plain ReLU */
+  /* backward */
+  MUT_BWD_ROPE_FORWARD = 21, /* gradient rotated by R instead of its transpose */
+  MUT_BWD_ACT_VALUE = 22,    /* act(y) used where act'(y) belongs */
+  MUT_BWD_NO_RECOMPUTE_BIAS = 23, /* pre-activation recomputed without the bias */
+  MUT_BWD_DW_SWAP = 24,      /* dW accumulated as G^T x (rows and columns crossed) */
+  MUT_BWD_DX_NO_W = 25,      /* dx from W's row sums (missing the gradient weights) */
 };
 
 typedef struct {
@@ -375,5 +396,284 @@ int oracle_forward(const void* x, int x_bf16, int ndim, const int64_t* sizes, co
   for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, run_rows, &jobs[i]);
   run_rows(&jobs[0]);
   for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+  return 0;
+}
+
+
+/* ------------------------------------------------------------------ backward */
+
+/* Derivative of the ff activation at pre-activation y, in fp64. */
+static double activation_deriv(int act, double y, int mutate) {
+  if (mutate == MUT_BWD_ACT_VALUE) return activation(act, y, 0);
+  const double pi = acos(-1.0);
+  switch (act) {
+    case ACT_GELU_ERF: /* d/dy [y Phi(y)] = Phi(y) + y phi(y) */
+      return 0.5 * (1.0 + erf(y / sqrt(2.0))) + y * exp(-0.5 * y * y) / sqrt(2.0 * pi);
+    case ACT_GELU_TANH: {
+      const double k0 = sqrt(2.0 / pi), k3 = 0.044715;
+      const double th = tanh(k0 * (y + k3 * y * y * y));
+      return 0.5 * (1.0 + th) + 0.5 * y * (1.0 - th * th) * k0 * (1.0 + 3.0 * k3 * y * y);
+    }
+    case ACT_SILU: {
+      const double sg = 1.0 / (1.0 + exp(-y));
+      return sg * (1.0 + y * (1.0 - sg));
+    }
+    case ACT_RELU2:
+      return y > 0.0 ? 2.0 * y : 0.0;
+    default:
+      return 1.0;
+  }
+}
+
+typedef struct {
+  job_t f;  /* the forward description (x, W, bias, pos, tables, shape) */
+  const void *g_ff, *g_q, *g_k, *g_v;
+  int mode; /* 0: dx of every token, dW, db; 1: dx of the sampled rows; 2: dW, db of sampled columns */
+  const int64_t* cols;
+  int64_t n_cols;
+  double *dx, *dW, *db; /* thread-private dW/db partials in modes 0 and 2 */
+} bjob_t;
+
+/* Column n of the fused output -> block (0 ff, 1 q, 2 k, 3 v), head, lane. */
+static void decode_column(const job_t* j, int64_t n, int* seg, int* head, int* lane) {
+  if (n < j->F) {
+    *seg = 0;
+    *head = 0;
+    *lane = (int)n;
+    return;
+  }
+  int64_t w = n - j->F;
+  if (j->groups) {
+    int qpk = j->heads / j->groups;
+    int64_t per = (int64_t)(qpk + 2) * j->hd;
+    int g = (int)(w / per);
+    int r = (int)(w % per), slot = r / j->hd;
+    *lane = r % j->hd;
+    if (slot < qpk) {
+      *seg = 1;
+      *head = g * qpk + slot;
+    } else {
+      *seg = slot == qpk ? 2 : 3;
+      *head = g;
+    }
+    return;
+  }
+  *seg = 1 + (int)(w / j->C);
+  int r = (int)(w % j->C);
+  *head = r / j->hd;
+  *lane = r % j->hd;
+}
+
+/* Upstream gradient of (block, head, lane) at token m = (b, t), widened. */
+static double upstream(const bjob_t* bj, int seg, int head, int lane, int64_t m, int64_t b,
+                       int64_t t) {
+  const job_t* j = &bj->f;
+  const int nkv = j->groups ? j->groups : j->heads;
+  switch (seg) {
+    case 0:
+      return widen(bj->g_ff, j->x_bf16, m * j->F + lane);
+    case 1:
+      return widen(bj->g_q, j->x_bf16, ((b * j->heads + head) * j->T + t) * j->hd + lane);
+    case 2:
+      if (j->k_transposed)
+        return widen(bj->g_k, j->x_bf16, ((b * nkv + head) * j->hd + lane) * j->T + t);
+      return widen(bj->g_k, j->x_bf16, ((b * nkv + head) * j->T + t) * j->hd + lane);
+    default:
+      return widen(bj->g_v, j->x_bf16, ((b * nkv + head) * j->T + t) * j->hd + lane);
+  }
+}
+
+/* cos and sin used by rotated lane `lane` at token t (forward's convention). */
+static void lane_angle(const job_t* j, int lane, int64_t t, double* c, double* s) {
+  int ne = j->rope_n_elem > 0 ? j->rope_n_elem : j->hd;
+  int half = ne / 2;
+  if (j->rope_cos) {
+    *c = j->rope_cos[(t % j->T) * ne + lane];
+    *s = j->rope_sin[(t % j->T) * ne + lane];
+    return;
+  }
+  double p = j->pos ? (double)j->pos[t % j->T] : (double)t;
+  double theta = p * pow(j->rope_base, -2.0 * (lane % half) / ne);
+  *c = cos(theta);
+  *s = sin(theta);
+}
+
+/* G[m, n]: gradient of the loss with respect to the pre-activation, pre-rotation
+ * value of fused column n at token m. X is the token's gathered channel row. */
+static double grad_at(const bjob_t* bj, int64_t m, int64_t b, int64_t t, int64_t n,
+                      const double* X) {
+  const job_t* j = &bj->f;
+  int seg, head, lane;
+  decode_column(j, n, &seg, &head, &lane);
+  if (seg == 0) {
+    double y = 0.0;
+    for (int c = 0; c < j->C; ++c) y += X[c] * widen(j->W, j->x_bf16, (int64_t)c * j->N + n);
+    if (j->bias && bj->f.mutate != MUT_BWD_NO_RECOMPUTE_BIAS) y += widen(j->bias, j->x_bf16, n);
+    return upstream(bj, 0, 0, lane, m, b, t) * activation_deriv(j->act, y, j->mutate);
+  }
+  const double g = upstream(bj, seg, head, lane, m, b, t);
+  const int ne = j->rope_n_elem > 0 ? j->rope_n_elem : j->hd;
+  if (seg == 3 || !(j->rope_base > 0.0) || lane >= ne) return g;
+  const int half = ne / 2;
+  const int partner = lane < half ? lane + half : lane - half;
+  const double gp = upstream(bj, seg, head, partner, m, b, t);
+  double c, s, cp, sp;
+  lane_angle(j, lane, t, &c, &s);
+  lane_angle(j, partner, t, &cp, &sp);
+  if (j->mutate == MUT_BWD_ROPE_FORWARD) /* forward rotation: x c + rotated s */
+    return lane < half ? g * c - gp * s : g * c + gp * s;
+  /* transpose: lane < half: g c + g' s'; lane >= half: g c - g' s' */
+  return lane < half ? g * c + gp * sp : g * c - gp * sp;
+}
+
+static void* run_backward(void* arg) {
+  bjob_t* bj = (bjob_t*)arg;
+  const job_t* j = &bj->f;
+  const int C = j->C;
+  const int64_t N = j->N;
+  double* X = (double*)malloc(sizeof(double) * (size_t)C);
+  double* G = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+  for (int64_t r = j->row_begin; r < j->row_end; ++r) {
+    int64_t m = (bj->mode == 1 && j->rows) ? j->rows[r] : r;
+    int64_t off, b, t;
+    locate_token(j, m, &off, &b, &t);
+    for (int c = 0; c < C; ++c)
+      X[c] = widen(j->x, j->x_bf16, off + (int64_t)c * j->strides[j->channel_dim]);
+    if (bj->mode == 2) {
+      for (int64_t k = 0; k < bj->n_cols; ++k) {
+        const double gv = grad_at(bj, m, b, t, bj->cols[k], X);
+        bj->db[k] += gv;
+        for (int c = 0; c < C; ++c) bj->dW[(int64_t)c * bj->n_cols + k] += X[c] * gv;
+      }
+      continue;
+    }
+    for (int64_t n = 0; n < N; ++n) G[n] = grad_at(bj, m, b, t, n, X);
+    double* dxr = bj->dx + (bj->mode == 1 ? r : m) * C;
+    for (int c = 0; c < C; ++c) {
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n)
+        acc += (j->mutate == MUT_BWD_DX_NO_W ? 1.0 : G[n]) * widen(j->W, j->x_bf16, (int64_t)c * N + n);
+      dxr[c] = acc;
+    }
+    if (bj->mode == 0) {
+      for (int64_t n = 0; n < N; ++n) {
+        bj->db[n] += G[n];
+        for (int c = 0; c < C; ++c) {
+          if (j->mutate == MUT_BWD_DW_SWAP) /* crossed indices, same buffer size */
+            bj->dW[(n * C + c) % (N * C)] += X[c] * G[n];
+          else
+            bj->dW[(int64_t)c * N + n] += X[c] * G[n];
+        }
+      }
+    }
+  }
+  free(X);
+  free(G);
+  return NULL;
+}
+
+/*
+ * Backward entry point. Same shape arguments as oracle_forward, plus:
+ *  g_ff, g_q, g_k, g_v: upstream gradients in the forward's output layouts
+ *    (dtype of x; g_k pre-transposed when k_transposed); NULL for an empty block.
+ *  mode 0: dx [M, C] (token order), dW [C, N], db [N] (db, dW zero-filled here);
+ *  mode 1: dx [n_rows, C] of the tokens in rows[];
+ *  mode 2: dW [C, n_cols] and db [n_cols] of the fused columns in cols[].
+ * Returns 0, or a negative number on a rejected argument.
+ */
+int oracle_backward(const void* x, int x_bf16, int ndim, const int64_t* sizes,
+                    const int64_t* strides, int channel_dim, int n_batch_dims, const void* W,
+                    const void* bias, const int32_t* pos, const double* rope_cos,
+                    const double* rope_sin, int C, int F, int heads, int head_dim, int groups,
+                    int rope_n_elem, int act, int k_transposed, double rope_base,
+                    const void* g_ff, const void* g_q, const void* g_k, const void* g_v, int mode,
+                    const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+                    double* dx, double* dW, double* db, int n_threads, int mutate) {
+  if (ndim < 1 || ndim > 16 || channel_dim < 0 || channel_dim >= ndim) return -1;
+  if (sizes[channel_dim] != C || C <= 0 || F < 0 || heads < 0) return -2;
+  if (heads > 0 && (head_dim <= 0 || head_dim % 2 || head_dim > 1024 || heads > 1024)) return -3;
+  if (groups > 0 && (heads % groups)) return -4;
+  if (!groups && heads > 0 && heads * head_dim != C) return -5;
+  if (rope_n_elem < 0 || rope_n_elem > head_dim || rope_n_elem % 2) return -6;
+  if (mode < 0 || mode > 2) return -8;
+  bjob_t bj;
+  memset(&bj, 0, sizeof bj);
+  job_t* j = &bj.f;
+  j->x = x;
+  j->x_bf16 = x_bf16;
+  j->ndim = ndim;
+  j->sizes = sizes;
+  j->strides = strides;
+  j->channel_dim = channel_dim;
+  j->n_batch_dims = n_batch_dims;
+  j->W = W;
+  j->bias = bias;
+  j->pos = pos;
+  j->rope_cos = rope_cos;
+  j->rope_sin = rope_sin;
+  j->C = C;
+  j->F = F;
+  j->heads = heads;
+  j->hd = head_dim;
+  j->groups = groups;
+  j->rope_n_elem = rope_n_elem;
+  j->act = act;
+  j->k_transposed = k_transposed;
+  j->rope_base = rope_base;
+  j->rows = rows;
+  j->mutate = mutate;
+  int64_t Bb = 1, T = 1;
+  int seen = 0;
+  for (int a = 0; a < ndim; ++a) {
+    if (a == channel_dim) continue;
+    if (seen < n_batch_dims) Bb *= sizes[a];
+    else T *= sizes[a];
+    ++seen;
+  }
+  if (n_batch_dims < 0 || n_batch_dims > seen) return -7;
+  j->Bb = Bb;
+  j->T = T;
+  j->M = Bb * T;
+  j->N = (int64_t)F + (groups ? (int64_t)(heads + 2 * groups) * head_dim : 3 * (int64_t)heads * head_dim);
+  bj.g_ff = g_ff;
+  bj.g_q = g_q;
+  bj.g_k = g_k;
+  bj.g_v = g_v;
+  bj.mode = mode;
+  bj.cols = cols;
+  bj.n_cols = n_cols;
+  const int64_t total = mode == 1 ? n_rows : j->M;
+  const int64_t wcols = mode == 2 ? n_cols : j->N;
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  if ((int64_t)n_threads > total) n_threads = total > 0 ? (int)total : 1;
+  pthread_t th[256];
+  bjob_t* jobs = (bjob_t*)calloc((size_t)n_threads, sizeof(bjob_t));
+  const int partials = mode != 1;
+  for (int i = 0; i < n_threads; ++i) {
+    jobs[i] = bj;
+    jobs[i].f.row_begin = total * i / n_threads;
+    jobs[i].f.row_end = total * (i + 1) / n_threads;
+    jobs[i].dx = dx;
+    if (partials) {
+      jobs[i].dW = (double*)calloc((size_t)(C * wcols), sizeof(double));
+      jobs[i].db = (double*)calloc((size_t)(wcols > 0 ? wcols : 1), sizeof(double));
+    }
+  }
+  for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, run_backward, &jobs[i]);
+  run_backward(&jobs[0]);
+  for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+  if (partials) {
+    /* fixed summation order: thread 0, 1, ... */
+    memset(dW, 0, sizeof(double) * (size_t)(C * wcols));
+    memset(db, 0, sizeof(double) * (size_t)wcols);
+    for (int i = 0; i < n_threads; ++i) {
+      for (int64_t e = 0; e < C * wcols; ++e) dW[e] += jobs[i].dW[e];
+      for (int64_t e = 0; e < wcols; ++e) db[e] += jobs[i].db[e];
+      free(jobs[i].dW);
+      free(jobs[i].db);
+    }
+  }
+  free(jobs);
   return 0;
 }

@@ -1,7 +1,8 @@
 """An independent float64 restatement of the projection with PyTorch CPU library ops.
 
 Used only to pin the oracle. Each step is a library routine or textbook
-identity rather than the oracle's own loops:
+identity rather than the oracle's own loops (and ``composite_backward``
+differentiates it with ``torch.autograd``, pinning the oracle's backward):
 
 * gather: ``torch.permute`` + ``reshape`` (the rearrange of "Make fused_ff_qkv
   contiguous", Walrus PR #12);
@@ -24,13 +25,39 @@ import torch
 import torch.nn.functional as Fn
 
 
-def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, channel_dim: int,
-              n_batch_dims: int, C: int, F: int, heads: int, head_dim: int, act: int,
-              rope_base: float, pos: Optional[np.ndarray] = None, groups: int = 0,
-              rope_n_elem: int = 0, k_transposed: bool = False,
-              rope_cos: Optional[np.ndarray] = None,
-              rope_sin: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], **kw
+              ) -> Dict[str, np.ndarray]:
     x = torch.from_numpy(np.asarray(x64, dtype=np.float64))
+    Wt = torch.from_numpy(np.asarray(W64, dtype=np.float64))
+    bt = None if b64 is None else torch.from_numpy(np.asarray(b64, dtype=np.float64))
+    return {k: v.detach().contiguous().numpy() for k, v in _composite_t(x, Wt, bt, **kw).items()}
+
+
+def composite_backward(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray],
+                       grads64: Dict[str, Optional[np.ndarray]], **kw) -> Dict[str, np.ndarray]:
+    """Gradients of sum(g * output) by ``torch.autograd`` through the composite:
+    dx [M, C] in token order, dW [C, N], db [N] (zeros when there is no bias)."""
+    x = torch.from_numpy(np.asarray(x64, dtype=np.float64)).requires_grad_(True)
+    Wt = torch.from_numpy(np.asarray(W64, dtype=np.float64)).requires_grad_(True)
+    bt = torch.zeros(Wt.shape[1], dtype=torch.float64, requires_grad=True) if b64 is None else \
+        torch.from_numpy(np.asarray(b64, dtype=np.float64)).requires_grad_(True)
+    out = _composite_t(x, Wt, bt, **kw)
+    loss = sum((out[k] * torch.from_numpy(np.asarray(g, dtype=np.float64))).sum()
+               for k, g in grads64.items() if g is not None)
+    dx, dW, db = torch.autograd.grad(loss, (x, Wt, bt))
+    channel_dim = kw["channel_dim"]
+    nd = x.dim()
+    perm = [a for a in range(nd) if a != channel_dim] + [channel_dim]
+    return {"dx": dx.permute(*perm).reshape(-1, x.shape[channel_dim]).numpy(),
+            "dW": dW.numpy(), "db": db.numpy()}
+
+
+def _composite_t(x: torch.Tensor, Wt: torch.Tensor, bt: Optional[torch.Tensor], *,
+                 channel_dim: int, n_batch_dims: int, C: int, F: int, heads: int, head_dim: int,
+                 act: int, rope_base: float, pos: Optional[np.ndarray] = None, groups: int = 0,
+                 rope_n_elem: int = 0, k_transposed: bool = False,
+                 rope_cos: Optional[np.ndarray] = None,
+                 rope_sin: Optional[np.ndarray] = None) -> Dict[str, torch.Tensor]:
     nd = x.dim()
     perm = [a for a in range(nd) if a != channel_dim] + [channel_dim]
     tok = [x.shape[a] for a in range(nd) if a != channel_dim]
@@ -38,9 +65,8 @@ def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, ch
     T = int(np.prod(tok[n_batch_dims:], dtype=np.int64))
     M = Bb * T
     X = x.permute(*perm).reshape(M, C)
-    Wt = torch.from_numpy(np.asarray(W64, dtype=np.float64))
-    bt = torch.zeros(Wt.shape[1], dtype=torch.float64) if b64 is None else torch.from_numpy(
-        np.asarray(b64, dtype=np.float64))
+    if bt is None:
+        bt = torch.zeros(Wt.shape[1], dtype=torch.float64)
     Y = torch.addmm(bt, X, Wt)
     ff = Y[:, :F]
     if act == 1:
@@ -88,10 +114,9 @@ def composite(x64: np.ndarray, W64: np.ndarray, b64: Optional[np.ndarray], *, ch
                 return torch.cat([xr * tc + rotated * ts, u[..., n:]], dim=-1)
 
         q, k = rope(q), rope(k)
-    out = {
-        "ff": ff.contiguous().numpy(),
-        "q": q.flatten(end_dim=1).contiguous().numpy(),
-        "k": (k.transpose(-1, -2) if k_transposed else k).flatten(end_dim=1).contiguous().numpy(),
-        "v": v.flatten(end_dim=1).contiguous().numpy(),
+    return {
+        "ff": ff,
+        "q": q.flatten(end_dim=1),
+        "k": (k.transpose(-1, -2) if k_transposed else k).flatten(end_dim=1),
+        "v": v.flatten(end_dim=1),
     }
-    return out
