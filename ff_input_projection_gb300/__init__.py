@@ -37,7 +37,8 @@ FP_OPT_CLUSTER = 5
 
 # the C ABI's entry points, as declared in include/fp.h
 EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_rope_table",
-           "fp_forward_noalloc", "fp_reserve", "fp_get_device_status",
+           "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward",
+           "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
 
@@ -95,6 +96,12 @@ def load():
     lib.fp_forward_noalloc.argtypes = [ctypes.POINTER(fp_config), P, ctypes.POINTER(fp_layout), P,
                                        P, P, P, P, P, P, P]
     lib.fp_forward_noalloc.restype = I
+    lib.fp_backward_workspace_size.argtypes = [P, ctypes.POINTER(fp_layout),
+                                               ctypes.POINTER(ctypes.c_size_t)]
+    lib.fp_backward_workspace_size.restype = I
+    lib.fp_backward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P, P, P, P,
+                                ctypes.c_size_t, P]
+    lib.fp_backward.restype = I
     lib.fp_reserve.argtypes = [P, I64]
     lib.fp_reserve.restype = I
     lib.fp_get_device_status.argtypes = [P, P]
@@ -159,6 +166,20 @@ def fp_forward_noalloc(config: fp_config, x: int, layout: fp_layout, W: int, b: 
     """fp_forward without a plan and without any device allocation (static scratch)."""
     return load().fp_forward_noalloc(ctypes.byref(config), x, ctypes.byref(layout), W, b, pos,
                                      out_ff, out_q, out_k, out_v, stream)
+
+
+def fp_backward_workspace_size(plan: int, layout: fp_layout) -> Tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    st = load().fp_backward_workspace_size(plan, ctypes.byref(layout), ctypes.byref(n))
+    return st, n.value
+
+
+def fp_backward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
+                pos: Optional[int], g_ff: Optional[int], g_q: Optional[int], g_k: Optional[int],
+                g_v: Optional[int], dx: int, dW: int, db: Optional[int], workspace: int,
+                workspace_bytes: int, stream: Optional[int]) -> int:
+    return load().fp_backward(plan, x, ctypes.byref(layout), W, b, pos, g_ff, g_q, g_k, g_v, dx,
+                              dW, db, workspace, workspace_bytes, stream)
 
 
 def fp_reserve(plan: int, max_tokens_per_batch: int) -> int:
@@ -323,3 +344,53 @@ class FusedProjection:
                             ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
         check(st)
         return out
+
+    def backward(self, x, W, b, grads, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
+                  dx=None, workspace=None, stream=None):
+        """Gradients of ``forward``'s outputs: ``grads`` = (g_ff, g_q, g_k, g_v) in the
+        output layouts (None where the output is None). Returns ``(dx, dW, db)``: dx
+        laid out like x (x's strides), dW float32 [C, N], db float32 [N] (None
+        without bias). The work is enqueued on torch's current stream."""
+        import torch
+        if x.dtype != torch.bfloat16:
+            raise TypeError("the backward takes bfloat16 activations")
+        Bb, T = self.out_shapes(x.shape, channel_dim, n_batch_dims)
+        M = Bb * T
+        if tuple(W.shape) != (self.C, self.N) or not W.is_contiguous() or W.dtype != x.dtype:
+            raise ValueError(f"W must be a contiguous [{self.C}, {self.N}] {x.dtype} tensor")
+        if b is not None and (tuple(b.shape) != (self.N,) or not b.is_contiguous()
+                              or b.dtype != x.dtype):
+            raise ValueError(f"b must be a contiguous [{self.N}] {x.dtype} tensor")
+        if pos is not None and (tuple(pos.shape) != (T,) or pos.dtype != torch.int32
+                                or not pos.is_contiguous()):
+            raise ValueError(f"pos must be a contiguous int32 [{T}] tensor")
+        want = [(M, self.F) if self.F else None] + \
+               [self._head_shape(Bb, nh, T, kt) if self.heads else None
+                for nh, kt in ((self.heads, False), (self.kv_heads, self.k_transposed),
+                               (self.kv_heads, False))]
+        grads = tuple(grads)
+        for g, shp in zip(grads, want):
+            if (g is None) != (shp is None) or (g is not None and (
+                    tuple(g.shape) != shp or not g.is_contiguous() or g.dtype != x.dtype
+                    or g.device != x.device)):
+                raise ValueError(f"gradients must be contiguous {want} on x's device")
+        if dx is None:
+            dx = torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+        elif tuple(dx.shape) != tuple(x.shape) or dx.stride() != x.stride() or dx.dtype != x.dtype:
+            raise ValueError("dx must have x's shape, strides and dtype")
+        dW = torch.empty((self.C, self.N), dtype=torch.float32, device=x.device)
+        db = torch.empty((self.N,), dtype=torch.float32, device=x.device) if b is not None else None
+        L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, FP_BF16)
+        st, need = fp_backward_workspace_size(self.plan, L)
+        check(st)
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        check(fp_backward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos), ptr(grads[0]),
+                          ptr(grads[1]), ptr(grads[2]), ptr(grads[3]), dx.data_ptr(), dW.data_ptr(),
+                          ptr(db), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), stream))
+        return dx, dW, db
+

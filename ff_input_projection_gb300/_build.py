@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfp.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "rope_table.cu"]
-HEADERS = ["fp_internal.h", "epilogue.cuh"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_bwd.cu", "gemm_simt.cu", "rope_table.cu"]
+HEADERS = ["fp_internal.h", "epilogue.cuh", "tc_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

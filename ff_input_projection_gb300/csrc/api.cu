@@ -775,6 +775,282 @@ fp_status fp_forward_rope_table(fp_plan* p, const void* x, const fp_layout* x_la
   return ok();
 }
 
+// ---------------------------------------------------------------- backward
+
+namespace {
+
+// 5-D map over x (or over dx, which has x's strides): tokens or channels
+// innermost, the non-mergeable token axes outermost, as in the forward.
+CUresult encode_x_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, const void* base,
+                      const Prepared& pr, int C, bool tokens_inner, cuuint32_t box0,
+                      cuuint32_t box1, CUtensorMapSwizzle sw) {
+  const fp::TokenMap& tk = pr.tk;
+  const int esz = pr.esz;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t box[5] = {box0, box1, 1, 1, 1}, estr[5] = {1, 1, 1, 1, 1};
+  if (tokens_inner) {
+    gdim[0] = tk.S_in;
+    gdim[1] = C;
+    gstride[0] = static_cast<cuuint64_t>(tk.c_stride) * esz;
+  } else {
+    gdim[0] = C;
+    gdim[1] = tk.S_in;
+    gstride[0] = static_cast<cuuint64_t>(tk.s_stride) * esz;
+  }
+  if (gstride[0] == 0 || gstride[0] % 16) gstride[0] = 16 * ((gdim[0] * esz + 15) / 16);
+  cuuint64_t last = gstride[0];
+  for (int d = 0; d < 3; ++d) {
+    if (d < tk.n_outer_dims) {
+      gdim[2 + d] = tk.outer_size[d];
+      gstride[1 + d] = static_cast<cuuint64_t>(tk.outer_stride[d]) * esz;
+      last = gstride[1 + d];
+    } else {
+      gdim[2 + d] = 1;
+      gstride[1 + d] = last;
+    }
+  }
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), gdim, gstride,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// G ([M, N] bf16, M = n_outer * S_in) seen as [n_outer][S_in][cols], cols <= N.
+CUresult encode_g_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, const void* G,
+                      const Prepared& pr, int N, int cols, cuuint32_t box0, cuuint32_t box1,
+                      CUtensorMapSwizzle sw) {
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(pr.tk.S_in),
+                        static_cast<cuuint64_t>(pr.tk.n_outer)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(N) * 2,
+                           static_cast<cuuint64_t>(pr.tk.S_in) * N * 2};
+  cuuint32_t box[3] = {box0, box1, 1}, estr[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(G), gdim, gstride, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, const void* base,
+                   CUtensorMapDataType dt, int esz, int64_t inner, int64_t outer, cuuint32_t box0,
+                   cuuint32_t box1, CUtensorMapSwizzle sw) {
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(inner) * esz};
+  cuuint32_t box[2] = {box0, box1}, estr[2] = {1, 1};
+  return encode(m, dt, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+size_t backward_workspace_bytes(int64_t M, int N) {
+  return (static_cast<size_t>(M) * static_cast<size_t>(N) * 2 + 255) / 256 * 256;
+}
+
+}  // namespace
+
+fp_status fp_backward_workspace_size(const fp_plan* p, const fp_layout* x_layout, size_t* bytes) {
+  if (!p || !x_layout || !bytes) return fail(FP_ERR_INVALID_ARG, "NULL argument");
+  const fp_layout& L = *x_layout;
+  if (L.ndim < 1 || L.ndim > FP_MAX_DIMS || L.channel_dim < 0 || L.channel_dim >= L.ndim)
+    return fail(FP_ERR_INVALID_ARG, "bad x_layout");
+  for (int d = 0; d < L.ndim; ++d)
+    if (L.sizes[d] < 0) return fail(FP_ERR_INVALID_ARG, "negative size");
+  const TokAxes ta = analyse_tokens(L);
+  *bytes = backward_workspace_bytes(ta.M, n_total(p));
+  return ok();
+}
+
+fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
+                      const int32_t* pos, const void* g_ff, const void* g_q, const void* g_k,
+                      const void* g_v, void* dx, float* dW, float* db, void* workspace,
+                      size_t workspace_bytes, void* stream_v) {
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  // the upstream gradients have the forward outputs' shapes: reuse its checks
+  const Args a{x, xl, W, b, pos, const_cast<void*>(g_ff), const_cast<void*>(g_q),
+               const_cast<void*>(g_k), const_cast<void*>(g_v)};
+  Prepared pr;
+  fp_status st = prepare(*p, a, pr);
+  if (st != FP_OK) return st;
+  if (!pr.tc_path)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                "the backward runs on the tensor-core path only (bf16, head_dim and ff_hidden "
+                "multiples of 16, x addressable by TMA)");
+  if (!dx || !dW) return fail(FP_ERR_INVALID_ARG, "dx and dW are required");
+  const int N = pr.N, C = p->C, F = p->F;
+  const int64_t M = pr.ta.M;
+  const void* ptrs[] = {dx, dW, db, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(FP_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  if (M == 0) {
+    p->last_launches = 0;
+    return ok();
+  }
+  if (!workspace || workspace_bytes < backward_workspace_bytes(M, N))
+    return fail(FP_ERR_INVALID_ARG, "workspace too small: %zu bytes needed",
+                backward_workspace_bytes(M, N));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0);
+  if (st != FP_OK) return st;
+  int launches = 0;
+  // rotary table: the forward's, rebuilt under the same rule
+  const bool build_table = pr.rope && (pos != nullptr || p->table_T != pr.ta.T);
+  if (pr.rope && !build_table && stream != p->table_stream) {
+    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
+  }
+  if (build_table) {
+    cudaError_t err = fp::launch_rope_table(p->d_table, pos, pr.ta.T, pr.rh, 2 * pr.rh,
+                                            static_cast<double>(p->rope_base), stream);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "rotary table launch: %s", cudaGetErrorString(err));
+    ++launches;
+    if (!p->table_ready &&
+        cudaEventCreateWithFlags(&p->table_ready, cudaEventDisableTiming) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event creation failed");
+    if (cudaEventRecord(p->table_ready, stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event record failed");
+    p->table_stream = stream;
+    p->table_T = pos ? -1 : pr.ta.T;
+  }
+  if (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
+      (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess))
+    return fail(FP_ERR_CUDA, "clearing dW / db failed");
+
+  p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
+  const int tag = static_cast<int>(p->launch_seq);
+  // 1. q|k|v part of G
+  if (p->heads > 0) {
+    fp::BwdGatherParams gp{};
+    gp.g_q = g_q;
+    gp.g_k = g_k;
+    gp.g_v = g_v;
+    gp.G = workspace;
+    gp.db = db;
+    gp.rope_cs = pr.rope ? p->d_table : nullptr;
+    gp.M = M;
+    gp.T = pr.ta.T;
+    gp.F = F;
+    gp.N = N;
+    gp.C = C;
+    gp.heads = p->heads;
+    gp.hd = p->hd;
+    gp.groups = p->groups;
+    gp.rope_half = pr.rh;
+    gp.k_transposed = p->k_transposed;
+    cudaError_t err = fp::launch_bwd_gather(gp, stream);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "gradient gather launch: %s", cudaGetErrorString(err));
+    ++launches;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  fp::BwdGemmParams base{};
+  base.tok = pr.tk;
+  base.group_m = p->group_m;
+  base.C = C;
+  base.F = F;
+  base.N = N;
+  base.act = p->act;
+  base.status = p->d_status;
+  base.wait_limit_ns = p->wait_limit_ns;
+  base.launch_tag = tag;
+  base.k_splits = 1;
+  const int mps = static_cast<int>((pr.tk.S_in + fp::kTcBM - 1) / fp::kTcBM);
+  const int ctas = p->max_ctas > 0 ? std::min(sm_count(p->device), p->max_ctas) : sm_count(p->device);
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  auto map_fail = [&](const char* what) {
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "backward: tensor map for %s rejected", what);
+  };
+  // 2. ff part of G: recompute x W_ff + b_ff, times act' and the upstream gradient
+  if (F > 0) {
+    fp::BwdGemmParams gp = base;
+    gp.mode = fp::BWD_GRADFF;
+    if (encode_x_map(encode, &gp.tmap_a, x, pr, C, pr.a_mn, 64, pr.a_mn ? 64 : 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return map_fail("x");
+    if (encode_2d(encode, &gp.tmap_b, W, BF, 2, N, C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
+      return map_fail("W");
+    if (encode_g_map(encode, &gp.tmap_out, workspace, pr, N, F, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+      return map_fail("G");
+    gp.m_tiles_per_slab = mps;
+    gp.num_m_tiles = static_cast<int>(pr.tk.n_outer) * mps;
+    gp.num_n_tiles = (F + fp::kTcBN - 1) / fp::kTcBN;
+    gp.num_k_blocks = (C + fp::kTcBK - 1) / fp::kTcBK;
+    gp.num_units = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
+    gp.bias = b;
+    gp.g_ff = g_ff;
+    gp.db = db;
+    cudaError_t err = fp::launch_bwd_gemm(gp, pr.a_mn, ctas, stream);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
+    ++launches;
+  }
+  // 3. dx = G W^T, stored in x's layout (dx^T = W G^T when tokens are innermost)
+  {
+    fp::BwdGemmParams gp = base;
+    if (encode_x_map(encode, &gp.tmap_out, dx, pr, C, pr.a_mn, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) !=
+        CUDA_SUCCESS)
+      return map_fail("dx");
+    gp.num_k_blocks = (N + fp::kTcBK - 1) / fp::kTcBK;
+    if (!pr.a_mn) {
+      gp.mode = fp::BWD_DX;
+      if (encode_g_map(encode, &gp.tmap_a, workspace, pr, N, N, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return map_fail("G");
+      if (encode_2d(encode, &gp.tmap_b, W, BF, 2, N, C, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) !=
+          CUDA_SUCCESS)
+        return map_fail("W");
+      gp.m_tiles_per_slab = mps;
+      gp.num_m_tiles = static_cast<int>(pr.tk.n_outer) * mps;
+      gp.num_n_tiles = (C + fp::kTcBN - 1) / fp::kTcBN;
+    } else {
+      gp.mode = fp::BWD_DXT;
+      if (encode_2d(encode, &gp.tmap_a, W, BF, 2, N, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
+          CUDA_SUCCESS)
+        return map_fail("W");
+      if (encode_g_map(encode, &gp.tmap_b, workspace, pr, N, N, 64, 256,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return map_fail("G");
+      gp.num_m_tiles = (C + fp::kTcBM - 1) / fp::kTcBM;
+      gp.n_tiles_per_slab = static_cast<int>((pr.tk.S_in + fp::kTcBN - 1) / fp::kTcBN);
+      gp.num_n_tiles = static_cast<int>(pr.tk.n_outer) * gp.n_tiles_per_slab;
+    }
+    gp.num_units = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
+    cudaError_t err = fp::launch_bwd_gemm(gp, false, ctas, stream);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
+    ++launches;
+  }
+  // 4. dW = X^T G (fp32), the token range split across CTAs, partials added by TMA
+  {
+    fp::BwdGemmParams gp = base;
+    gp.mode = fp::BWD_DW;
+    if (encode_x_map(encode, &gp.tmap_a, x, pr, C, pr.a_mn, 64, pr.a_mn ? 128 : 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return map_fail("x");
+    if (encode_g_map(encode, &gp.tmap_b, workspace, pr, N, N, 64, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return map_fail("G");
+    if (encode_2d(encode, &gp.tmap_out, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, N, C, 16, 32,
+                  CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+      return map_fail("dW");
+    gp.num_m_tiles = (C + fp::kTcBM - 1) / fp::kTcBM;
+    gp.num_n_tiles = (N + fp::kTcBN - 1) / fp::kTcBN;
+    gp.k_blocks_per_slab = static_cast<int>((pr.tk.S_in + fp::kTcBK - 1) / fp::kTcBK);
+    const int64_t kb = pr.tk.n_outer * gp.k_blocks_per_slab;
+    if (kb > INT32_MAX) return fail(FP_ERR_UNSUPPORTED_LAYOUT, "too many tokens");
+    gp.num_k_blocks = static_cast<int>(kb);
+    const int64_t tiles = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
+    // about four work items per SM, each a whole number of k-blocks
+    int64_t splits = (4 * static_cast<int64_t>(ctas) + tiles - 1) / tiles;
+    splits = std::max<int64_t>(1, std::min<int64_t>(splits, kb));
+    gp.k_splits = static_cast<int>(splits);
+    gp.num_units = tiles * splits;
+    cudaError_t err = fp::launch_bwd_gemm(gp, !pr.a_mn, ctas, stream);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
+    ++launches;
+  }
+  p->last_launches = launches;
+  return ok();
+}
+
 // ---------------------------------------------------------------- no-allocation entry point
 //
 // fp_forward_noalloc serves callers that must not allocate device memory

@@ -72,6 +72,50 @@ struct TcParams {
   int launch_tag;    // >= 1, unique per launch: marks this launch as aborted in status[1]
 };
 
+// Backward GEMMs on the tensor cores (gemm_bwd.cu). G is the gradient at the
+// pre-activation, pre-rotation fused output, [M, N] bf16 (workspace), viewed
+// as [n_outer][S_in][N].
+enum : int {
+  BWD_GRADFF = 0,  // G[:, :F] = g_ff * act'(x W_ff + b_ff): rows tokens, K = C
+  BWD_DX = 1,      // dx = G W^T for token-major x: rows tokens, cols channels, K = N
+  BWD_DXT = 2,     // dx^T = W G^T for channels-first x: rows channels, cols tokens, K = N
+  BWD_DW = 3,      // dW += X^T G (fp32, split over tokens): rows channels, cols N, K = tokens
+};
+
+struct BwdGemmParams {
+  CUtensorMap tmap_a, tmap_b, tmap_out;
+  TokenMap tok;             // token axes of x (S_in, outer axes)
+  int mode;
+  int num_m_tiles;          // row tiles (tokens: n_outer * m_tiles_per_slab; channels: C/128)
+  int m_tiles_per_slab;     // row tiles per slab when rows are tokens
+  int num_n_tiles;          // column tiles (tokens: n_outer * n_tiles_per_slab)
+  int n_tiles_per_slab;     // column tiles per slab when columns are tokens
+  int num_k_blocks;         // k-blocks of 64 (DW: all token blocks over all slabs)
+  int k_blocks_per_slab;    // DW: ceil(S_in / 64)
+  int k_splits;             // DW: the token range is split this many ways
+  int64_t num_units;
+  int group_m;
+  int C, F, N, act;
+  const void* bias;         // GRADFF: [N] bf16 or null
+  const void* g_ff;         // GRADFF: [M, F] bf16
+  float* db;                // GRADFF: [N] fp32 column sums, or null
+  int* status;
+  uint64_t wait_limit_ns;
+  int launch_tag;
+};
+
+// Gather of the q/k/v gradients into G (inverse rotation), with db column sums.
+struct BwdGatherParams {
+  const void* g_q;
+  const void* g_k;
+  const void* g_v;
+  void* G;                  // [M, N] bf16
+  float* db;                // [N] or null
+  const float2* rope_cs;    // [T][rope_half] (cos, sin), or null
+  int64_t M, T;
+  int F, N, C, heads, hd, groups, rope_half, k_transposed;
+};
+
 struct SimtParams {
   const void* x;  // float, or bf16 bits
   const void* W;
@@ -91,6 +135,9 @@ cudaError_t launch_rope_import(float4* dst, const void* cosv, const void* sinv, 
                                cudaStream_t stream);
 cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream);
 cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream);
+cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_ctas,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream);
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kSimtBM = 128, kSimtBN = 128;

@@ -1,0 +1,592 @@
+// Backward of the fused projection: the gradients of act/rotate/split(x W + b)
+// with respect to x, W and b, given the upstream gradients in the forward's
+// output layouts.
+//
+// The pages ("[perf] Fused linear", xformers PR #283) name the backward only
+// as the part of the fused linear left unfused and slow. Here it is the chain
+// rule in four device steps, every GEMM on the tensor cores:
+//
+//   gather   G[:, F:] = the q/k/v gradients gathered from their head-major
+//            buffers into token-major rows, q and k rotated back by the
+//            transpose of the rotation (bwd_gather_kernel, CUDA cores);
+//   GRADFF   G[:, :F] = g_ff * act'(x W_ff + b_ff): the pre-activation is
+//            recomputed by a forward GEMM whose epilogue multiplies the
+//            upstream gradient by the activation's derivative;
+//   DX/DXT   dx = G W^T. For token-major x the tile rows are tokens; for
+//            channels-first x the kernel computes dx^T = W G^T, whose rows are
+//            channels and whose columns are contiguous tokens, so either way
+//            the result is stored straight into x's own layout by TMA;
+//   DW       dW = X^T G in fp32, the token range split across CTAs, partial
+//            tiles added into dW by TMA reduce-add (cp.reduce.async.bulk).
+// db is the column sum of G, accumulated by the gather kernel and the GRADFF
+// epilogue (a 31-shuffle butterfly per warp, one atomic add per column).
+//
+// The GEMM kernel is a persistent single-CTA tcgen05 pipeline (M = 128,
+// N = 256, K = 64 per stage, 4 stages, two TMEM accumulators): warp 0 loads,
+// one thread of warp 1 issues tcgen05.mma, warps 2-9 drain the accumulators.
+// Every wait is bounded as in the forward kernel.
+#include "epilogue.cuh"
+#include "fp_internal.h"
+#include "tc_ptx.cuh"
+
+namespace fp {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int NUM_EPI_WARPS = 8;  // 2 per TMEM lane quarter
+constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int CHUNK_BYTES = 64 * BK * 2;       // one [64 k][64 mn] MN-major chunk, 8 KB
+constexpr int ACC_COLS = BN;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+// per epilogue warp, two 2 KB buffers staging [32 rows][64 B] for TMA stores
+constexpr int STAGING_BYTES_PER_WARP = 2 * 2048;
+constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
+// fp32 add of a staged tile into global memory
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Tile of one work item.
+struct Geo {
+  int o, s0;     // token slab and first token of the tile (token rows or columns)
+  int r0;        // first row when rows are channels (DXT, DW)
+  int c0;        // first column: ff column (GRADFF), channel (DX), fused column (DW)
+  int kb0, kb1;  // k-block range
+};
+
+// Work item -> tile. Groups of group_m row tiles sweep the column tiles, rows
+// fastest, so concurrently resident CTAs share operand tiles in L2. For DW
+// the k splits of one tile are num_m_tiles * num_n_tiles items apart.
+__device__ __forceinline__ Geo unit_geo(const BwdGemmParams& p, int64_t u64) {
+  const uint32_t u = static_cast<uint32_t>(u64);
+  const uint32_t tiles = static_cast<uint32_t>(p.num_m_tiles) * p.num_n_tiles;
+  const uint32_t split = u / tiles;
+  const uint32_t t = u - split * tiles;
+  const uint32_t gsz = static_cast<uint32_t>(p.group_m);
+  const uint32_t per_group = gsz * p.num_n_tiles;
+  const uint32_t g = t / per_group;
+  const uint32_t first = g * gsz;
+  const uint32_t left = p.num_m_tiles - first;
+  const uint32_t gm = left < gsz ? left : gsz;
+  const uint32_t rr = t - g * per_group;
+  const uint32_t n_tile = rr / gm;
+  const uint32_t m_tile = first + (rr - n_tile * gm);
+  Geo q;
+  q.o = q.s0 = q.r0 = q.c0 = 0;
+  q.kb0 = 0;
+  q.kb1 = p.num_k_blocks;
+  if (p.mode == BWD_GRADFF || p.mode == BWD_DX) {
+    const uint32_t mps = static_cast<uint32_t>(p.m_tiles_per_slab);
+    q.o = static_cast<int>(m_tile / mps);
+    q.s0 = static_cast<int>(m_tile - q.o * mps) * BM;
+    q.c0 = static_cast<int>(n_tile) * BN;
+  } else if (p.mode == BWD_DXT) {
+    const uint32_t nps = static_cast<uint32_t>(p.n_tiles_per_slab);
+    q.r0 = static_cast<int>(m_tile) * BM;
+    q.o = static_cast<int>(n_tile / nps);
+    q.s0 = static_cast<int>(n_tile - q.o * nps) * BN;
+  } else {
+    q.r0 = static_cast<int>(m_tile) * BM;
+    q.c0 = static_cast<int>(n_tile) * BN;
+    const int64_t kb = p.num_k_blocks;
+    q.kb0 = static_cast<int>(kb * split / p.k_splits);
+    q.kb1 = static_cast<int>(kb * (split + 1) / p.k_splits);
+  }
+  return q;
+}
+
+// Derivative of the ff activation (fp32, CUDA's math library).
+template <int ACT>
+__device__ __forceinline__ float act_deriv(float y) {
+  if (ACT == ACT_GELU_ERF) {
+    return normcdff(y) + y * 0.39894228040143268f * __expf(-0.5f * y * y);
+  } else if (ACT == ACT_GELU_TANH) {
+    constexpr float k0 = 0.79788456080286536f, k3 = 0.044715f;
+    const float th = tanhf(k0 * fmaf(k3 * y, y * y, y));
+    return 0.5f * (1.0f + th) + 0.5f * y * (1.0f - th * th) * k0 * fmaf(3.0f * k3, y * y, 1.0f);
+  } else if (ACT == ACT_SILU) {
+    const float sg = 1.0f / (1.0f + __expf(-y));
+    return sg * fmaf(y, 1.0f - sg, 1.0f);
+  } else if (ACT == ACT_RELU2) {
+    return y > 0.0f ? 2.0f * y : 0.0f;
+  }
+  return 1.0f;
+}
+
+// Column sums of a warp's [32 rows][32 columns] block (row = lane): a
+// butterfly that halves the columns each lane keeps at every step; after five
+// steps lane i holds the sum of column i.
+__device__ __forceinline__ float column_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int off = 16 >> step;
+    const int n = 32 >> step;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// 32 bf16 values (four 16-byte loads from a 16-byte aligned address), widened to fp32
+__device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = __ldg(s4 + q);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+      f[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int MODE, bool A_MN, bool B_MN, int ACT>
+__global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__ BwdGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - raw_addr);
+  const uint32_t staging0 = sbase + STAGES * STAGE_BYTES;
+  const uint32_t bar0 = staging0 + STAGING_BYTES;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + STAGING_BYTES +
+                                                    NUM_BARS * 8);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl wc{p.status, p.wait_limit_ns, p.launch_tag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t armed_mask = 0, armed_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Geo g = unit_geo(p, u);
+        int oc[3];
+        if (MODE != BWD_DW) outer_coords(p.tok, g.o, oc);
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a_dst = sbase + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const int k0 = kb * BK;
+          if (MODE == BWD_GRADFF) {
+            if (A_MN) {
+              tma_load_5d(a_dst, &p.tmap_a, fb, g.s0, k0, oc[0], oc[1], oc[2]);
+              tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, g.s0 + 64, k0, oc[0], oc[1], oc[2]);
+            } else {
+              tma_load_5d(a_dst, &p.tmap_a, fb, k0, g.s0, oc[0], oc[1], oc[2]);
+            }
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, g.c0 + 64 * j, k0);
+          } else if (MODE == BWD_DX) {
+            tma_load_3d(a_dst, &p.tmap_a, fb, k0, g.s0, g.o);   // G rows (tokens), K = N
+            tma_load_2d(b_dst, &p.tmap_b, fb, k0, g.c0);        // W rows (channels), K = N
+          } else if (MODE == BWD_DXT) {
+            tma_load_2d(a_dst, &p.tmap_a, fb, k0, g.r0);        // W rows (channels)
+            tma_load_3d(b_dst, &p.tmap_b, fb, k0, g.s0, g.o);   // G rows (tokens)
+          } else {
+            // K = tokens: block kb of slab ok
+            const int ok_slab = kb / p.k_blocks_per_slab;
+            const int sk = (kb - ok_slab * p.k_blocks_per_slab) * BK;
+            int ock[3];
+            outer_coords(p.tok, ok_slab, ock);
+            if (A_MN) {  // token-major x: channels contiguous
+              tma_load_5d(a_dst, &p.tmap_a, fb, g.r0, sk, ock[0], ock[1], ock[2]);
+              tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, g.r0 + 64, sk, ock[0], ock[1],
+                          ock[2]);
+            } else {     // channels-first x: tokens contiguous
+              tma_load_5d(a_dst, &p.tmap_a, fb, sk, g.r0, ock[0], ock[1], ock[2]);
+            }
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, g.c0 + 64 * j, sk, ok_slab);
+          }
+          armed_mask |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, wc, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(A_MN, B_MN, BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued = false;
+      int it = 0;
+      for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+        const Geo g = unit_geo(p, u);
+        const int buf = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!wait_bounded(tempty_bar(buf), acc_phase ^ 1u, wc, true)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * ACC_COLS;
+        bool ok = true;
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wc, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + stage * STAGE_BYTES;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t a_desc = A_MN ? sw128_desc(a_addr + k * 2048, CHUNK_BYTES, 1024)
+                                         : sw128_desc(a_addr + k * 32, 16, 1024);
+            const uint64_t b_desc = B_MN ? sw128_desc(b_addr + k * 2048, CHUNK_BYTES, 1024)
+                                         : sw128_desc(b_addr + k * 32, 16, 1024);
+            umma_bf16<1>(d_tmem, a_desc, b_desc, idesc, (kb != g.kb0 || k != 0) ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit<1>(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit<1>(tfull_bar(buf));
+      }
+      if (issued) {
+        umma_commit<1>(drain_bar);
+        wait_bounded(drain_bar, 0, wc, false);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;
+    const int part = (warp - 2) >> 2;  // 0 or 1: which of every 2 units
+    const uint32_t staging_warp = staging0 + (warp - 2) * STAGING_BYTES_PER_WARP;
+    const uint32_t sw64 = (lane >> 1) & 3u;  // 64-byte rows, 64-byte swizzle
+    uint32_t stage_sel = 0;
+    int turn = 0;
+    int it = 0;
+    // stage a [32 rows][16 words] block (one 64-byte row per lane)
+    auto stage_rows = [&](const uint32_t (&w)[16]) -> uint32_t {
+      const uint32_t stg = staging_warp + (stage_sel & 1) * 2048;
+      ++stage_sel;
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(stg + lane * 64 + ((q ^ sw64) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                     w[4 * q + 3]);
+      fence_async_shared();
+      __syncwarp();
+      return stg;
+    };
+    for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const int okw = wait_bounded(tfull_bar(buf), acc_phase, wc, true) ? 1 : 0;
+      if (!__all_sync(0xFFFFFFFFu, okw)) break;
+      tc_fence_after();
+      const Geo g = unit_geo(p, u);
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
+      int oc[3];
+      if (MODE != BWD_DW) outer_coords(p.tok, g.o, oc);
+      const int row0 = quarter * 32;  // the warp's first row in the tile
+      if (MODE == BWD_DW) {
+        // fp32 partial tile, 16 columns per unit, added into dW
+        for (int c = 0; c < BN; c += 16) {
+          const bool mine = turn == part;
+          turn ^= 1;
+          if (!mine) continue;
+          uint32_t v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_wait_ld();
+          // a store never starts past the tensor (loads may; stores are clipped, not skipped)
+          if (g.c0 + c >= p.N || g.r0 + row0 >= p.C) continue;
+          const uint32_t stg = stage_rows(v);
+          if (lane == 0) {
+            tma_reduce_add_2d(&p.tmap_out, stg, g.c0 + c, g.r0 + row0);
+            bulk_commit();
+          }
+        }
+      } else {
+        const int s = g.s0 + row0 + lane;  // GRADFF/DX: this lane's token in its slab
+        const bool valid = (MODE == BWD_DXT) || s < p.tok.S_in;
+        const int64_t m = static_cast<int64_t>(g.o) * p.tok.S_in + s;
+        for (int c = 0; c < BN; c += 32) {
+          const bool mine = turn == part;
+          turn ^= 1;
+          if (!mine) continue;
+          uint32_t v[32];
+          tmem_ld32(t_row + c, v);
+          tmem_wait_ld();
+          // a store never starts past the tensor (its far edge is clipped by TMA)
+          if (MODE == BWD_GRADFF && (g.c0 + c >= p.F || g.s0 + row0 >= p.tok.S_in)) continue;
+          if (MODE == BWD_DX && (g.c0 + c >= p.C || g.s0 + row0 >= p.tok.S_in)) continue;
+          if (MODE == BWD_DXT && (g.s0 + c >= p.tok.S_in || g.r0 + row0 >= p.C)) continue;
+          uint32_t w[16];
+          if (MODE == BWD_GRADFF) {
+            const int n = g.c0 + c;  // first ff column of the unit
+            float y[32], gg[32];
+            const uint16_t* bias = static_cast<const uint16_t*>(p.bias);
+            if (bias && n + 32 <= p.N) {
+              load32_bf16(bias + n, y);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                y[i] = (bias && n + i < p.N) ? bf16_bits_to_float(bias[n + i]) : 0.0f;
+            }
+            const uint16_t* grow = static_cast<const uint16_t*>(p.g_ff) + m * p.F + n;
+            if (valid && n + 32 <= p.F) {
+              load32_bf16(grow, gg);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                gg[i] = (valid && n + i < p.F) ? bf16_bits_to_float(grow[i]) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gg[i] *= act_deriv<ACT>(__uint_as_float(v[i]) + y[i]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(gg[2 * i], gg[2 * i + 1]);
+            if (p.db) {
+              const float cs = column_sum32(gg, lane);
+              if (n + lane < p.F) atomicAdd(p.db + n + lane, cs);
+            }
+            const uint32_t stg = stage_rows(w);
+            if (lane == 0) {  // [n_outer][S_in][F] view of G's ff columns: clips at S_in, F
+              tma_store_3d(&p.tmap_out, stg, n, g.s0 + row0, g.o);
+              bulk_commit();
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            const uint32_t stg = stage_rows(w);
+            if (lane == 0) {
+              if (MODE == BWD_DX)  // x token-major: [channels][tokens] box at (channel, token)
+                tma_store_5d(&p.tmap_out, stg, g.c0 + c, g.s0 + row0, oc[0], oc[1], oc[2]);
+              else                 // x channels-first: [tokens][channels] box at (token, channel)
+                tma_store_5d(&p.tmap_out, stg, g.s0 + c, g.r0 + row0, oc[0], oc[1], oc[2]);
+              bulk_commit();
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int MODE, bool A_MN, bool B_MN, int ACT>
+cudaError_t launch_one(const BwdGemmParams& p, int num_ctas, cudaStream_t stream) {
+  auto kernel = bwd_gemm_kernel<MODE, A_MN, B_MN, ACT>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_done[dev]) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_done[dev] = 1;
+  }
+  int ctas = num_ctas;
+  if (static_cast<int64_t>(ctas) > p.num_units) ctas = static_cast<int>(p.num_units);
+  if (ctas < 1) ctas = 1;
+  kernel<<<ctas, NT, SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool A_MN>
+cudaError_t launch_gradff(const BwdGemmParams& p, int num_ctas, cudaStream_t stream) {
+  switch (p.act) {
+    case ACT_GELU_ERF: return launch_one<BWD_GRADFF, A_MN, true, ACT_GELU_ERF>(p, num_ctas, stream);
+    case ACT_GELU_TANH: return launch_one<BWD_GRADFF, A_MN, true, ACT_GELU_TANH>(p, num_ctas, stream);
+    case ACT_SILU: return launch_one<BWD_GRADFF, A_MN, true, ACT_SILU>(p, num_ctas, stream);
+    case ACT_RELU2: return launch_one<BWD_GRADFF, A_MN, true, ACT_RELU2>(p, num_ctas, stream);
+    default: return launch_one<BWD_GRADFF, A_MN, true, ACT_NONE>(p, num_ctas, stream);
+  }
+}
+
+// ------------------------------------------------------------------ q/k/v gather
+
+// One thread per fused q|k|v column, 32 tokens per block row: reads the
+// upstream gradient of (head, lane) at each token (lanes of a head are
+// contiguous in the head-major buffers), rotates q and k back with the
+// transpose of the rotation, writes G and accumulates the column's sum.
+__global__ void __launch_bounds__(256) bwd_gather_kernel(const BwdGatherParams p) {
+  const int nq = p.N - p.F;
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  if (col >= nq) return;
+  // decode the column: block (1 q, 2 k, 3 v), head, lane
+  int seg, head, j;
+  if (p.groups > 0) {
+    const int qpk = p.heads / p.groups;
+    const int per = (qpk + 2) * p.hd;
+    const int gidx = col / per, r = col - gidx * per, slot = r / p.hd;
+    j = r - slot * p.hd;
+    if (slot < qpk) {
+      seg = 1;
+      head = gidx * qpk + slot;
+    } else {
+      seg = slot == qpk ? 2 : 3;
+      head = gidx;
+    }
+  } else {
+    seg = 1 + col / p.C;
+    const int r = col - (seg - 1) * p.C;
+    head = r / p.hd;
+    j = r - head * p.hd;
+  }
+  const int nkv = p.groups > 0 ? p.groups : p.heads;
+  const int rh = p.rope_half;
+  const bool rot = rh > 0 && seg < 3 && j < 2 * rh;
+  const int partner = j < rh ? j + rh : j - rh;
+  const uint16_t* src = static_cast<const uint16_t*>(seg == 1 ? p.g_q : seg == 2 ? p.g_k : p.g_v);
+  const int nh = seg == 1 ? p.heads : nkv;
+  const bool kt = seg == 2 && p.k_transposed;
+  uint16_t* G = static_cast<uint16_t*>(p.G);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * 32;
+  int64_t b = m0 / p.T, t = m0 - b * p.T;
+  float sum = 0.0f;
+  for (int r = 0; r < 32; ++r) {
+    const int64_t m = m0 + r;
+    if (m >= p.M) break;
+    const int64_t hrow = b * nh + head;
+    auto at = [&](int lane) -> float {
+      const int64_t idx = kt ? (hrow * p.hd + lane) * p.T + t : (hrow * p.T + t) * p.hd + lane;
+      return bf16_bits_to_float(src[idx]);
+    };
+    float gv = at(j);
+    if (rot) {
+      const float2 cs = p.rope_cs[t * rh + (j < rh ? j : j - rh)];
+      const float gp = at(partner);
+      gv = j < rh ? fmaf(gv, cs.x, gp * cs.y) : fmaf(gv, cs.x, -gp * cs.y);
+    }
+    sum += gv;
+    const __nv_bfloat16 hv = __float2bfloat16_rn(gv);
+    G[m * p.N + p.F + col] = *reinterpret_cast<const uint16_t*>(&hv);
+    if (++t == p.T) {
+      t = 0;
+      ++b;
+    }
+  }
+  if (p.db) atomicAdd(p.db + p.F + col, sum);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_ctas,
+                            cudaStream_t stream) {
+  switch (p.mode) {
+    case BWD_GRADFF:
+      return a_mn_major ? launch_gradff<true>(p, num_ctas, stream)
+                        : launch_gradff<false>(p, num_ctas, stream);
+    case BWD_DX: return launch_one<BWD_DX, false, false, ACT_NONE>(p, num_ctas, stream);
+    case BWD_DXT: return launch_one<BWD_DXT, false, false, ACT_NONE>(p, num_ctas, stream);
+    default:
+      return a_mn_major ? launch_one<BWD_DW, true, true, ACT_NONE>(p, num_ctas, stream)
+                        : launch_one<BWD_DW, false, true, ACT_NONE>(p, num_ctas, stream);
+  }
+}
+
+cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
+  const int nq = p.N - p.F;
+  if (nq <= 0 || p.M == 0) return cudaSuccess;
+  const dim3 grid((nq + 255) / 256, static_cast<unsigned>((p.M + 31) / 32));
+  bwd_gather_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp

@@ -40,6 +40,7 @@
 #ifndef FP_H
 #define FP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -188,6 +189,48 @@ fp_status fp_forward_rope_table(fp_plan* plan, const void* x, const fp_layout* x
                                 const void* W, const void* b, const void* rope_cos,
                                 const void* rope_sin, const fp_rope_table* layout, void* out_ff,
                                 void* out_q, void* out_k, void* out_v, void* stream);
+
+/*
+ * fp_backward_workspace_size — bytes of device workspace fp_backward needs for
+ * an activation of layout `x_layout`: the gradient G at the fused output before
+ * activation and rotation, [B*T, N] bf16 (rounded up to 256 bytes).
+ */
+fp_status fp_backward_workspace_size(const fp_plan* plan, const fp_layout* x_layout,
+                                     size_t* bytes);
+
+/*
+ * fp_backward — enqueue the gradients of fp_forward's outputs with respect to
+ * x, W and b on `stream`. The pages name this pass only as the part of the
+ * fused linear that is left unfused and slow ("[perf] Fused linear", xformers
+ * PR #283); it is the chain rule through the forward's steps in reverse:
+ *   G[m, ff col]  = g_ff * act'(x W + b) at the recomputed pre-activation,
+ *   G[m, q/k col] = the upstream gradient rotated back (the transpose of the
+ *                   rotation: lane i: g_i cos + g_{i+h} sin, lane i+h:
+ *                   g_{i+h} cos - g_i sin), v copied,
+ *   dx = G W^T,  dW = X^T G,  db = sum over tokens of G.
+ * Arguments:
+ *   x, x_layout, W, b, pos   as for fp_forward (the same values as the forward)
+ *   g_ff, g_q, g_k, g_v      upstream gradients, dtype of x, in the layouts of
+ *                            out_ff, out_q, out_k, out_v (g_k pre-transposed
+ *                            when the plan emits k that way); NULL exactly
+ *                            where the forward output is NULL
+ *   dx                       gradient of x, dtype of x, written through
+ *                            x_layout's strides (a buffer laid out like x)
+ *   dW                       float32 [C, N] row-major (overwritten)
+ *   db                       float32 [N] (overwritten), or NULL to skip
+ *   workspace                device buffer of fp_backward_workspace_size bytes,
+ *                            256-byte aligned, owned by the caller
+ * Runs on the tensor cores for bf16 layouts the forward's tcgen05 kernel
+ * takes; other layouts and f32 return FP_ERR_UNSUPPORTED_LAYOUT. dW and db
+ * are sums whose order varies between runs (atomic adds across CTAs), so they
+ * are reproducible to rounding, not bit for bit. Inputs must stay valid until
+ * the work completes; nothing is allocated except, on first use, the plan's
+ * status word and rotary table (as fp_forward). Returns FP_OK once enqueued.
+ */
+fp_status fp_backward(fp_plan* plan, const void* x, const fp_layout* x_layout, const void* W,
+                      const void* b, const int32_t* pos, const void* g_ff, const void* g_q,
+                      const void* g_k, const void* g_v, void* dx, float* dW, float* db,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fp_forward_noalloc — fp_forward for callers that may not allocate device

@@ -642,6 +642,13 @@ int oracle_backward(const void* x, int x_bf16, int ndim, const int64_t* sizes,
   bj.mode = mode;
   bj.cols = cols;
   bj.n_cols = n_cols;
+  if (mode == 1)
+    for (int64_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= j->M) return -9;
+  if (mode == 2)
+    for (int64_t k = 0; k < n_cols; ++k)
+      if (cols[k] < 0 || cols[k] >= j->N) return -9;
+  if ((F > 0 && !g_ff) || (heads > 0 && (!g_q || !g_k || !g_v))) return -10;
   const int64_t total = mode == 1 ? n_rows : j->M;
   const int64_t wcols = mode == 2 ? n_cols : j->N;
   if (n_threads < 1) n_threads = 1;

@@ -234,3 +234,15 @@ def test_planted_backward_mistake_is_caught(mutation):
     mid = oracle.BWD_MUTATIONS[mutation]
     caught = {p.__name__: b for p in PINS if (b := p(mid))}
     assert caught, f"planted mistake '{mutation}' passed every pin"
+
+
+def test_backward_rejects_bad_samples():
+    w = BWD_CASES["walrus_small"]
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+    with pytest.raises(ValueError):
+        _obwd(w, inp, grads, cols=[w.N])
+    with pytest.raises(ValueError):
+        _obwd(w, inp, grads, rows=[w.M])
+    with pytest.raises(ValueError):
+        _obwd(w, inp, {**grads, "q": None})
