@@ -5,6 +5,10 @@ One step = one fp_forward over one batch of synthetic input: the whole path
 split) on the Walrus-shaped channels-first workload by default.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--pass forward|backward]
+
+With --pass backward a step is one fp_backward (gradients of x, W and b from
+seeded upstream gradients) and the line reports its own metric.
 
 Prints one JSON line (rank 0). Under torchrun each rank projects its own copy
 of the workload (weak scaling, no data-path collective); the step time is the
@@ -36,6 +40,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["ff_input_projection_gb300/csrc/gemm_tc.cu",
                   "ff_input_projection_gb300/csrc/epilogue.cuh",
+                  "ff_input_projection_gb300/csrc/tc_ptx.cuh",
                   "ff_input_projection_gb300/csrc/gemm_simt.cu"]
 
 
@@ -50,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cluster", type=int, default=2, choices=[1, 2],
                     help="tensor-core path: CTA pairs sharing weight tiles (2) or single CTAs (1)")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                    help="time fp_forward (default) or fp_backward (gradients of x, W, b)")
     return ap.parse_args()
 
 
@@ -173,8 +180,8 @@ def cpu_baseline(w: fpsynth.Workload, inp, seconds: float):
     flops = 2.0 * done_rows * w.C * w.N
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "tokens_per_s": done_rows / elapsed,
-            "sample": f"{done_rows} of {w.M} token rows of {w.name} (all {w.N} fused columns), "
-                      f"fp64, {elapsed:.1f} s"}
+            "sample": f"{done_rows} token rows drawn from the {w.M} of {w.name} (all {w.N} "
+                      f"fused columns each), fp64, {elapsed:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -220,6 +227,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.which == "backward":
+        return main_backward(args, rank, world, local)
 
     import torch
     import ff_input_projection_gb300 as fpx
@@ -387,6 +396,175 @@ def main():
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def backward_algorithmic(w: fpsynth.Workload):
+    """FLOPs of one backward: the ff pre-activation recomputed (2 M C F), dx = G W^T
+    and dW = X^T G (2 M N C each); bytes: x, W, b and the upstream gradients read
+    once, dx, dW (fp32) and db (fp32) written once."""
+    flops = 2 * w.M * w.C * (w.F + 2 * w.N)
+    bytes_ = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0) + w.M * w.N + w.M * w.C) * 2 \
+        + (w.C * w.N + (w.N if w.bias else 0)) * 4
+    return flops, bytes_
+
+
+def main_backward(args, rank, world, local):
+    import torch
+    import ff_input_projection_gb300 as fpx
+    from ff_input_projection_gb300 import _build
+    from ff_input_projection_gb300.shard import max_over_ranks
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = fpsynth.WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("the backward takes bf16 workloads")
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+
+    def to_dev(a):
+        if a is None:
+            return None
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    flops, alg_bytes = backward_algorithmic(w)
+    in_bytes = (w.M * w.C + w.C * w.N + w.M * w.N) * 2
+    n_sets = max(1, int(np.ceil(2 * L2_BYTES / in_bytes)))
+    sets = [(to_dev(inp["x"]), to_dev(inp["W"]), to_dev(inp["b"]),
+             tuple(to_dev(grads[k]) for k in ("ff", "q", "k", "v"))) for _ in range(n_sets)]
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
+    proj.reserve(w.T)
+    stream = torch.cuda.Stream(device=dev)
+    L = fpx.make_layout(sets[0][0].shape, sets[0][0].stride(), w.channel_dim, w.n_batch_dims,
+                        fpx.FP_BF16)
+    st, ws_bytes = fpx.fp_backward_workspace_size(proj.plan, L)
+    fpx.check(st)
+    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+    dx = torch.empty_strided(sets[0][0].shape, sets[0][0].stride(), dtype=torch.bfloat16,
+                             device=dev)
+    res = None
+
+    def step(i):
+        nonlocal res
+        x, W, b, g = sets[i % n_sets]
+        res = proj.backward(x, W, b, g, None, channel_dim=w.channel_dim,
+                            n_batch_dims=w.n_batch_dims, dx=dx, workspace=ws,
+                            stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    launches_per_step = proj.last_launch_count
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk, torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    value = flops * world / (ms * 1e-3) / 1e12
+
+    # end to end: upstream gradients and x from pinned host memory, dx, dW, db back
+    x0, W0, b0, g0 = sets[0]
+    hx = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x0.cpu())
+    hg = [None if g is None else torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in g0]
+    for h, g in zip(hg, g0):
+        if h is not None:
+            h.copy_(g.cpu())
+    dxx = torch.empty_like(x0)
+    dg = [None if g is None else torch.empty_like(g) for g in g0]
+    hdx = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True)
+    hdW = torch.empty((w.C, w.N), dtype=torch.float32, pin_memory=True)
+    hdb = torch.empty((w.N,), dtype=torch.float32, pin_memory=True) if w.bias else None
+    h2d = hx.numel() * 2 + sum(h.numel() * 2 for h in hg if h is not None)
+    d2h = hdx.numel() * 2 + hdW.numel() * 4 + (hdb.numel() * 4 if hdb is not None else 0)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dxx.copy_(hx, non_blocking=True)
+        for d, h in zip(dg, hg):
+            if d is not None:
+                d.copy_(h, non_blocking=True)
+        ddx, ddW, ddb = proj.backward(dxx, W0, b0, tuple(dg), None, channel_dim=w.channel_dim,
+                                      n_batch_dims=w.n_batch_dims, dx=dx, workspace=ws,
+                                      stream=stream.cuda_stream)
+        hdx.copy_(ddx, non_blocking=True)
+        hdW.copy_(ddW, non_blocking=True)
+        if hdb is not None:
+            hdb.copy_(ddb, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dev)
+
+    pk, pk_src = peaks()
+    roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "traffic": None, "peak_source": f"{pk_src} (burst)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": "fused-proj backward TFLOP/s & tokens/s on 1 GB300; % of TC roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": w.M * world / (ms * 1e-3),
+        "config": {"workload": w.name, "pass": "backward", "x": list(w.x_shape),
+                   "channel_dim": w.channel_dim, "C": w.C, "F": w.F, "heads": w.heads,
+                   "head_dim": w.head_dim, "N": w.N, "tokens": w.M,
+                   "act": fpsynth.ACT_NAMES[w.act], "bias": w.bias,
+                   "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs rotate over {n_sets} sets ({n_sets * in_bytes / 1e6:.0f} MB) > L2 "
+                         f"129 MB", "timing": "eager loop of fp_backward calls"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        cores = os.cpu_count() or 1
+        rows = list(range(0, w.M, max(1, w.M // 32)))[:32]
+        t = time.perf_counter()
+        oracle.backward_workload(w, inp, grads, rows=rows, threads=cores)
+        el = time.perf_counter() - t
+        fl = 2.0 * len(rows) * w.C * (w.F + w.N)
+        line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"dx of {len(rows)} token rows of {w.M} (ff recompute "
+                                          f"+ G W^T per row), fp64, {el:.1f} s"}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
