@@ -144,6 +144,33 @@ __device__ __forceinline__ float act_deriv(float y) {
   return 1.0f;
 }
 
+// GELU'(y) = Phi(y) + y phi(y) for two values on packed fp32 pairs, with the
+// same Abramowitz & Stegun 7.1.26 erf as the forward: for a = |y|,
+// t = 1 / (1 + p a / sqrt 2), erfc(a / sqrt 2) = t P(t) exp(-a^2/2), so
+// Phi(y) = h or 1 - h with h = (1/2) t P(t) e, e = exp(-y^2/2), and
+// phi(y) = e / sqrt(2 pi). Absolute error about 1e-7.
+__device__ __forceinline__ void gelu_erf_deriv2(float y0, float y1, float& d0, float& d1) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float a0 = fabsf(y0), a1 = fabsf(y1);
+  const uint64_t A = f2_pack(a0, a1);
+  float q0, q1;
+  f2_unpack(f2_fma(A, f2_splat(0.3275911f * 0.70710678118654752f), f2_splat(1.0f)), q0, q1);
+  const uint64_t T = f2_pack(rcp_approx(q0), rcp_approx(q1));
+  uint64_t P = f2_fma(f2_splat(0.5f * 1.061405429f), T, f2_splat(0.5f * -1.453152027f));
+  P = f2_fma(P, T, f2_splat(0.5f * 1.421413741f));
+  P = f2_fma(P, T, f2_splat(0.5f * -0.284496736f));
+  P = f2_fma(P, T, f2_splat(0.5f * 0.254829592f));
+  float e0, e1;
+  f2_unpack(f2_mul(f2_mul(A, f2_splat(-0.5f * kLog2e)), A), e0, e1);
+  const uint64_t E = f2_pack(ex2_approx(e0), ex2_approx(e1));
+  float h0, h1;
+  f2_unpack(f2_mul(f2_mul(P, T), E), h0, h1);  // (1/2) erfc(|y| / sqrt 2)
+  const uint64_t PHI = f2_pack(y0 >= 0.0f ? 1.0f - h0 : h0, y1 >= 0.0f ? 1.0f - h1 : h1);
+  const uint64_t R =
+      f2_fma(f2_mul(f2_pack(y0, y1), f2_splat(0.39894228040143268f)), E, PHI);
+  f2_unpack(R, d0, d1);
+}
+
 // Column sums of a warp's [32 rows][32 columns] block (row = lane): a
 // butterfly that halves the columns each lane keeps at every step; after five
 // steps lane i holds the sum of column i.
@@ -422,8 +449,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
               for (int i = 0; i < 32; ++i)
                 gg[i] = (valid && n + i < p.F) ? bf16_bits_to_float(grow[i]) : 0.0f;
             }
+            if (ACT == ACT_GELU_ERF) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) gg[i] *= act_deriv<ACT>(__uint_as_float(v[i]) + y[i]);
+              for (int i = 0; i < 16; ++i) {
+                float d0, d1;
+                gelu_erf_deriv2(__uint_as_float(v[2 * i]) + y[2 * i],
+                                __uint_as_float(v[2 * i + 1]) + y[2 * i + 1], d0, d1);
+                gg[2 * i] *= d0;
+                gg[2 * i + 1] *= d1;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) gg[i] *= act_deriv<ACT>(__uint_as_float(v[i]) + y[i]);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(gg[2 * i], gg[2 * i + 1]);
             if (p.db) {
@@ -501,21 +539,32 @@ cudaError_t launch_gradff(const BwdGemmParams& p, int num_ctas, cudaStream_t str
 
 // ------------------------------------------------------------------ q/k/v gather
 
-// One thread per fused q|k|v column, 32 tokens per block row: reads the
-// upstream gradient of (head, lane) at each token (lanes of a head are
-// contiguous in the head-major buffers), rotates q and k back with the
-// transpose of the rotation, writes G and accumulates the column's sum.
-__global__ void __launch_bounds__(256) bwd_gather_kernel(const BwdGatherParams p) {
+// One thread per 8 consecutive lanes of one head (16 bytes) and 64 tokens:
+// reads the upstream gradient of those lanes at each token (lanes of a head
+// are contiguous in the head-major buffers; a warp covers 4 heads of 64
+// lanes), rotates q and k back with the transpose of the rotation, writes 16
+// bytes of G and adds the 8 column sums into db at the end.
+constexpr int GATHER_TOKENS = 64;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(128) bwd_gather_kernel(const BwdGatherParams p) {
   const int nq = p.N - p.F;
-  const int col = blockIdx.x * 256 + threadIdx.x;
-  if (col >= nq) return;
-  // decode the column: block (1 q, 2 k, 3 v), head, lane
-  int seg, head, j;
+  const int col0 = (blockIdx.x * 128 + threadIdx.x) * 8;  // first of 8 columns
+  if (col0 >= nq) return;
+  int seg, head, j0;
   if (p.groups > 0) {
     const int qpk = p.heads / p.groups;
     const int per = (qpk + 2) * p.hd;
-    const int gidx = col / per, r = col - gidx * per, slot = r / p.hd;
-    j = r - slot * p.hd;
+    const int gidx = col0 / per, r = col0 - gidx * per, slot = r / p.hd;
+    j0 = r - slot * p.hd;
     if (slot < qpk) {
       seg = 1;
       head = gidx * qpk + slot;
@@ -524,45 +573,79 @@ __global__ void __launch_bounds__(256) bwd_gather_kernel(const BwdGatherParams p
       head = gidx;
     }
   } else {
-    seg = 1 + col / p.C;
-    const int r = col - (seg - 1) * p.C;
+    seg = 1 + col0 / p.C;
+    const int r = col0 - (seg - 1) * p.C;
     head = r / p.hd;
-    j = r - head * p.hd;
+    j0 = r - head * p.hd;
   }
   const int nkv = p.groups > 0 ? p.groups : p.heads;
   const int rh = p.rope_half;
-  const bool rot = rh > 0 && seg < 3 && j < 2 * rh;
-  const int partner = j < rh ? j + rh : j - rh;
+  const bool rot = rh > 0 && seg < 3 && j0 < 2 * rh;
+  // the 8 lanes and their partners are each one 16-byte group when rh is a
+  // multiple of 8; otherwise (rh < 8) lanes are fetched one by one
+  const bool grouped = (rh & 7) == 0;
   const uint16_t* src = static_cast<const uint16_t*>(seg == 1 ? p.g_q : seg == 2 ? p.g_k : p.g_v);
   const int nh = seg == 1 ? p.heads : nkv;
   const bool kt = seg == 2 && p.k_transposed;
   uint16_t* G = static_cast<uint16_t*>(p.G);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS;
   int64_t b = m0 / p.T, t = m0 - b * p.T;
-  float sum = 0.0f;
-  for (int r = 0; r < 32; ++r) {
+  float sum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
+  for (int r = 0; r < GATHER_TOKENS; ++r) {
     const int64_t m = m0 + r;
     if (m >= p.M) break;
     const int64_t hrow = b * nh + head;
-    auto at = [&](int lane) -> float {
+    auto lane_at = [&](int lane) -> float {
       const int64_t idx = kt ? (hrow * p.hd + lane) * p.T + t : (hrow * p.T + t) * p.hd + lane;
       return bf16_bits_to_float(src[idx]);
     };
-    float gv = at(j);
-    if (rot) {
-      const float2 cs = p.rope_cs[t * rh + (j < rh ? j : j - rh)];
-      const float gp = at(partner);
-      gv = j < rh ? fmaf(gv, cs.x, gp * cs.y) : fmaf(gv, cs.x, -gp * cs.y);
+    float g[8];
+    if (!kt) {
+      unpack8(*reinterpret_cast<const uint4*>(src + (hrow * p.T + t) * p.hd + j0), g);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = lane_at(j0 + i);
     }
-    sum += gv;
-    const __nv_bfloat16 hv = __float2bfloat16_rn(gv);
-    G[m * p.N + p.F + col] = *reinterpret_cast<const uint16_t*>(&hv);
+    if (rot) {
+      float gp[8];
+      if (grouped && !kt) {
+        const int pj = j0 < rh ? j0 + rh : j0 - rh;
+        unpack8(*reinterpret_cast<const uint4*>(src + (hrow * p.T + t) * p.hd + pj), gp);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = j0 + i;
+          gp[i] = j < 2 * rh ? lane_at(j < rh ? j + rh : j - rh) : 0.0f;
+        }
+      }
+      const float2* cs = p.rope_cs + t * rh;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        if (j < 2 * rh) {
+          const float2 c = __ldg(cs + (j < rh ? j : j - rh));
+          g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
+        }
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(g[0], g[1]);
+    o.y = pack_bf16x2(g[2], g[3]);
+    o.z = pack_bf16x2(g[4], g[5]);
+    o.w = pack_bf16x2(g[6], g[7]);
+    *reinterpret_cast<uint4*>(G + m * p.N + p.F + col0) = o;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum[i] += g[i];
     if (++t == p.T) {
       t = 0;
       ++b;
     }
   }
-  if (p.db) atomicAdd(p.db + p.F + col, sum);
+  if (p.db)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) atomicAdd(p.db + p.F + col0 + i, sum[i]);
 }
 
 }  // namespace
@@ -584,8 +667,9 @@ cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_cta
 cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
   const int nq = p.N - p.F;
   if (nq <= 0 || p.M == 0) return cudaSuccess;
-  const dim3 grid((nq + 255) / 256, static_cast<unsigned>((p.M + 31) / 32));
-  bwd_gather_kernel<<<grid, 256, 0, stream>>>(p);
+  const dim3 grid((nq / 8 + 127) / 128,
+                  static_cast<unsigned>((p.M + GATHER_TOKENS - 1) / GATHER_TOKENS));
+  bwd_gather_kernel<<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
