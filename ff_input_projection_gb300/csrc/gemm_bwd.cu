@@ -539,12 +539,17 @@ cudaError_t launch_gradff(const BwdGemmParams& p, int num_ctas, cudaStream_t str
 
 // ------------------------------------------------------------------ q/k/v gather
 
-// One thread per 8 consecutive lanes of one head (16 bytes) and 64 tokens:
-// reads the upstream gradient of those lanes at each token (lanes of a head
-// are contiguous in the head-major buffers; a warp covers 4 heads of 64
-// lanes), rotates q and k back with the transpose of the rotation, writes 16
-// bytes of G and adds the 8 column sums into db at the end.
-constexpr int GATHER_TOKENS = 64;
+// A block covers 32 groups of 8 consecutive lanes (16 bytes of one head each;
+// a warp spans 4 heads of 64 lanes) and 64 tokens: thread (x, y) takes group x
+// and tokens y, y + 8, ..., loading the upstream gradients of 4 tokens (and
+// their rotation partners) before using any, so several requests per thread
+// are in flight. q and k are rotated back with the transpose of the rotation;
+// each token's 8 values go to G as one 16-byte store; the 8 token rows' column
+// sums are reduced in shared memory and added into db once per block.
+constexpr int GATHER_ROWS = 8;     // token rows of threads per block
+constexpr int GATHER_PER_ROW = 8;  // tokens per thread
+constexpr int GATHER_TOKENS = GATHER_ROWS * GATHER_PER_ROW;
+constexpr int GATHER_BATCH = 4;    // tokens whose loads are issued together
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -555,97 +560,122 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   }
 }
 
-__global__ void __launch_bounds__(128) bwd_gather_kernel(const BwdGatherParams p) {
+// VEC: every column group is read as 16-byte vectors (k not pre-transposed,
+// rotated half-width a multiple of 8); otherwise lane by lane.
+template <bool VEC>
+__global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const BwdGatherParams p) {
+  __shared__ float part[GATHER_ROWS][32][8];
   const int nq = p.N - p.F;
-  const int col0 = (blockIdx.x * 128 + threadIdx.x) * 8;  // first of 8 columns
-  if (col0 >= nq) return;
-  int seg, head, j0;
-  if (p.groups > 0) {
-    const int qpk = p.heads / p.groups;
-    const int per = (qpk + 2) * p.hd;
-    const int gidx = col0 / per, r = col0 - gidx * per, slot = r / p.hd;
-    j0 = r - slot * p.hd;
-    if (slot < qpk) {
-      seg = 1;
-      head = gidx * qpk + slot;
+  const int col0 = (blockIdx.x * 32 + threadIdx.x) * 8;  // first of 8 columns
+  const bool active = col0 < nq;
+  int seg = 3, head = 0, j0 = 0;
+  if (active) {
+    if (p.groups > 0) {
+      const int qpk = p.heads / p.groups;
+      const int per = (qpk + 2) * p.hd;
+      const int gidx = col0 / per, r = col0 - gidx * per, slot = r / p.hd;
+      j0 = r - slot * p.hd;
+      if (slot < qpk) {
+        seg = 1;
+        head = gidx * qpk + slot;
+      } else {
+        seg = slot == qpk ? 2 : 3;
+        head = gidx;
+      }
     } else {
-      seg = slot == qpk ? 2 : 3;
-      head = gidx;
+      seg = 1 + col0 / p.C;
+      const int r = col0 - (seg - 1) * p.C;
+      head = r / p.hd;
+      j0 = r - head * p.hd;
     }
-  } else {
-    seg = 1 + col0 / p.C;
-    const int r = col0 - (seg - 1) * p.C;
-    head = r / p.hd;
-    j0 = r - head * p.hd;
   }
   const int nkv = p.groups > 0 ? p.groups : p.heads;
   const int rh = p.rope_half;
   const bool rot = rh > 0 && seg < 3 && j0 < 2 * rh;
   // the 8 lanes and their partners are each one 16-byte group when rh is a
-  // multiple of 8; otherwise (rh < 8) lanes are fetched one by one
-  const bool grouped = (rh & 7) == 0;
+  // multiple of 8; otherwise (rh < 8) and for pre-transposed k, lane by lane
+  const bool kt = seg == 2 && p.k_transposed;
+  const int pj0 = j0 < rh ? j0 + rh : j0 - rh;
   const uint16_t* src = static_cast<const uint16_t*>(seg == 1 ? p.g_q : seg == 2 ? p.g_k : p.g_v);
   const int nh = seg == 1 ? p.heads : nkv;
-  const bool kt = seg == 2 && p.k_transposed;
   uint16_t* G = static_cast<uint16_t*>(p.G);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS;
-  int64_t b = m0 / p.T, t = m0 - b * p.T;
   float sum[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
-  for (int r = 0; r < GATHER_TOKENS; ++r) {
-    const int64_t m = m0 + r;
-    if (m >= p.M) break;
-    const int64_t hrow = b * nh + head;
-    auto lane_at = [&](int lane) -> float {
-      const int64_t idx = kt ? (hrow * p.hd + lane) * p.T + t : (hrow * p.T + t) * p.hd + lane;
-      return bf16_bits_to_float(src[idx]);
-    };
-    float g[8];
-    if (!kt) {
-      unpack8(*reinterpret_cast<const uint4*>(src + (hrow * p.T + t) * p.hd + j0), g);
-    } else {
+  const int64_t mb = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS + threadIdx.y;
+#pragma unroll 1
+  for (int i0 = 0; i0 < GATHER_PER_ROW && active; i0 += GATHER_BATCH) {
+    int64_t roff[GATHER_BATCH];  // element offset of the token's row of its head
+    int tt[GATHER_BATCH];        // position of the token in its batch element
+    uint4 gv[GATHER_BATCH] = {}, pv[GATHER_BATCH] = {};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) g[i] = lane_at(j0 + i);
+    for (int k = 0; k < GATHER_BATCH; ++k) {
+      const int64_t m = mb + static_cast<int64_t>(i0 + k) * GATHER_ROWS;
+      const int64_t bb = m < p.M ? m / p.T : 0;
+      const int64_t t = m < p.M ? m - bb * p.T : 0;
+      tt[k] = static_cast<int>(t);
+      roff[k] = ((bb * nh + head) * p.T + t) * p.hd;
+      if (VEC && m < p.M) {
+        gv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + j0);
+        pv[k] = rot ? *reinterpret_cast<const uint4*>(src + roff[k] + pj0) : make_uint4(0, 0, 0, 0);
+      }
     }
-    if (rot) {
-      float gp[8];
-      if (grouped && !kt) {
-        const int pj = j0 < rh ? j0 + rh : j0 - rh;
-        unpack8(*reinterpret_cast<const uint4*>(src + (hrow * p.T + t) * p.hd + pj), gp);
+#pragma unroll
+    for (int k = 0; k < GATHER_BATCH; ++k) {
+      const int64_t m = mb + static_cast<int64_t>(i0 + k) * GATHER_ROWS;
+      if (m >= p.M) continue;
+      const int t = tt[k];
+      float g[8], gp[8];
+      if constexpr (VEC) {
+        unpack8(gv[k], g);
+        unpack8(pv[k], gp);
       } else {
+        // lane by lane: pre-transposed k is [B*kv, hd, T]; or rh < 8
+        const int64_t hrow = (m / p.T) * nh + head;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int j = j0 + i;
-          gp[i] = j < 2 * rh ? lane_at(j < rh ? j + rh : j - rh) : 0.0f;
+          const int jp = j < rh ? j + rh : j - rh;
+          const int64_t ij = kt ? (hrow * p.hd + j) * p.T + t : roff[k] + j;
+          const int64_t ip = kt ? (hrow * p.hd + jp) * p.T + t : roff[k] + jp;
+          g[i] = bf16_bits_to_float(src[ij]);
+          gp[i] = (rot && j < 2 * rh) ? bf16_bits_to_float(src[ip]) : 0.0f;
         }
       }
-      const float2* cs = p.rope_cs + t * rh;
+      if (rot) {
+        const float2* cs = p.rope_cs + static_cast<int64_t>(t) * rh;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = j0 + i;
-        if (j < 2 * rh) {
-          const float2 c = __ldg(cs + (j < rh ? j : j - rh));
-          g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
+        for (int i = 0; i < 8; ++i) {
+          const int j = j0 + i;
+          if (j < 2 * rh) {
+            const float2 c = __ldg(cs + (j < rh ? j : j - rh));
+            g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
+          }
         }
       }
-    }
-    uint4 o;
-    o.x = pack_bf16x2(g[0], g[1]);
-    o.y = pack_bf16x2(g[2], g[3]);
-    o.z = pack_bf16x2(g[4], g[5]);
-    o.w = pack_bf16x2(g[6], g[7]);
-    *reinterpret_cast<uint4*>(G + m * p.N + p.F + col0) = o;
+      uint4 o;
+      o.x = pack_bf16x2(g[0], g[1]);
+      o.y = pack_bf16x2(g[2], g[3]);
+      o.z = pack_bf16x2(g[4], g[5]);
+      o.w = pack_bf16x2(g[6], g[7]);
+      *reinterpret_cast<uint4*>(G + m * p.N + p.F + col0) = o;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sum[i] += g[i];
-    if (++t == p.T) {
-      t = 0;
-      ++b;
+      for (int i = 0; i < 8; ++i) sum[i] += g[i];
     }
   }
-  if (p.db)
+  if (!p.db) return;  // uniform across the block
 #pragma unroll
-    for (int i = 0; i < 8; ++i) atomicAdd(p.db + p.F + col0 + i, sum[i]);
+  for (int i = 0; i < 8; ++i) part[threadIdx.y][threadIdx.x][i] = sum[i];
+  __syncthreads();
+  if (threadIdx.y == 0 && active) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int r = 0; r < GATHER_ROWS; ++r) acc += part[r][threadIdx.x][i];
+      atomicAdd(p.db + p.F + col0 + i, acc);
+    }
+  }
 }
 
 }  // namespace
@@ -667,9 +697,12 @@ cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_cta
 cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
   const int nq = p.N - p.F;
   if (nq <= 0 || p.M == 0) return cudaSuccess;
-  const dim3 grid((nq / 8 + 127) / 128,
+  const dim3 grid((nq / 8 + 31) / 32,
                   static_cast<unsigned>((p.M + GATHER_TOKENS - 1) / GATHER_TOKENS));
-  bwd_gather_kernel<<<grid, 128, 0, stream>>>(p);
+  if (!p.k_transposed && p.rope_half % 8 == 0)
+    bwd_gather_kernel<true><<<grid, dim3(32, GATHER_ROWS), 0, stream>>>(p);
+  else
+    bwd_gather_kernel<false><<<grid, dim3(32, GATHER_ROWS), 0, stream>>>(p);
   return cudaGetLastError();
 }
 
