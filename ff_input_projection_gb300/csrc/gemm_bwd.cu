@@ -250,6 +250,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above touches no global memory: it overlaps the previous
+  // launch's tail; from here on its results are visible
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -262,6 +266,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
         const Geo g = unit_geo(p, u);
         int oc[3];
         if (MODE != BWD_DW) outer_coords(p.tok, g.o, oc);
+        // DW walks K over tokens: (slab, block in slab) advances incrementally and
+        // the slab's outer coordinates are recomputed only when the slab changes
+        int ok_slab = 0, kb_in = 0;
+        int ock[3] = {0, 0, 0};
+        if (MODE == BWD_DW) {
+          ok_slab = g.kb0 / p.k_blocks_per_slab;
+          kb_in = g.kb0 - ok_slab * p.k_blocks_per_slab;
+          outer_coords(p.tok, ok_slab, ock);
+        }
         for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wc, true)) {
             ok = false;
@@ -289,11 +302,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
             tma_load_2d(a_dst, &p.tmap_a, fb, k0, g.r0);        // W rows (channels)
             tma_load_3d(b_dst, &p.tmap_b, fb, k0, g.s0, g.o);   // G rows (tokens)
           } else {
-            // K = tokens: block kb of slab ok
-            const int ok_slab = kb / p.k_blocks_per_slab;
-            const int sk = (kb - ok_slab * p.k_blocks_per_slab) * BK;
-            int ock[3];
-            outer_coords(p.tok, ok_slab, ock);
+            // K = tokens: block kb_in of slab ok_slab
+            const int sk = kb_in * BK;
             if (A_MN) {  // token-major x: channels contiguous
               tma_load_5d(a_dst, &p.tmap_a, fb, g.r0, sk, ock[0], ock[1], ock[2]);
               tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, g.r0 + 64, sk, ock[0], ock[1],
@@ -310,6 +320,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (MODE == BWD_DW && ++kb_in == p.k_blocks_per_slab) {
+            kb_in = 0;
+            ++ok_slab;
+            if (kb + 1 < g.kb1) outer_coords(p.tok, ok_slab, ock);
           }
         }
       }
@@ -522,8 +537,18 @@ cudaError_t launch_one(const BwdGemmParams& p, int num_ctas, cudaStream_t stream
   int ctas = num_ctas;
   if (static_cast<int64_t>(ctas) > p.num_units) ctas = static_cast<int>(p.num_units);
   if (ctas < 1) ctas = 1;
-  kernel<<<ctas, NT, SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kernel, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <bool A_MN>

@@ -283,6 +283,10 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = p.num_k_blocks;
+  // everything above touches no global memory: it overlaps the previous
+  // launch's tail; from here on its results are visible
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (every CTA)
@@ -813,27 +817,36 @@ cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream)
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
-  if (CL == 1) {
-    kernel<<<num_ctas, NT, Cfg<CL>::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = Cfg<CL>::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the prologue may overlap the previous
+  // launch's tail (the kernel waits on it before touching global memory)
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  if (CL == 1) {
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(num_ctas, 1, 1);
+    err = cudaLaunchKernelEx(&cfg, kernel, p);
+    return err != cudaSuccess ? err : cudaGetLastError();
+  }
+  cfg.numAttrs = 2;
   // persistent: as many clusters as can be resident at once (one CTA per SM)
   static int max_clusters[64] = {0};
   if (dev >= 64 || !max_clusters[dev]) {
     cfg.gridDim = dim3(num_ctas, 1, 1);
+    cudaLaunchConfig_t q = cfg;  // the query sees the cluster shape only
+    q.attrs = attr + 1;
+    q.numAttrs = 1;
     int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
     if (err != cudaSuccess) return err;
     if (n < 1) return cudaErrorInvalidConfiguration;
     if (dev < 64) max_clusters[dev] = n;

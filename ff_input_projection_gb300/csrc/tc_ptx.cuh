@@ -268,6 +268,16 @@ __device__ __forceinline__ void umma_commit_all(uint32_t bar) {
   }
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible (a no-op without such a grid),
+// and let the next dependent launch start its prologue on SMs this grid frees.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
