@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cluster", type=int, default=2, choices=[1, 2],
                     help="tensor-core path: CTA pairs sharing weight tiles (2) or single CTAs (1)")
+    ap.add_argument("--group-m", type=int, default=0,
+                    help="tensor-core tile rasterisation: M-tiles per group (0: the library's default)")
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
                     help="time fp_forward (default) or fp_backward (gradients of x, W, b)")
     return ap.parse_args()
@@ -262,6 +264,8 @@ def main():
     proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
                                w.n_query_groups, w.rope_n_elem, w.k_transposed)
     proj.set_option(fpx.FP_OPT_CLUSTER, args.cluster)
+    if args.group_m:
+        proj.set_option(fpx.FP_OPT_GROUP_M, args.group_m)
     proj.reserve(w.T)
     stream = torch.cuda.Stream(device=dev)
     outs = None

@@ -594,7 +594,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->last_launches = 0;
   p->wait_limit_ns = 2000000000ull;
   p->inject_stall = 0;
-  p->group_m = 8;
+  p->group_m = 32;
   p->max_ctas = 0;
   p->cluster = 2;
   p->launch_seq = 0;

@@ -34,8 +34,9 @@ struct Epilogue {
   int N, F, C, heads, hd, groups;  // groups > 0: grouped-query column order
   int act;
   int rope_half;      // 0: no rotation, else rotated lanes / 2
-  const float2* rope_cs;  // [T][rope_half] (cos, sin) of theta_i, shared by lanes i and i+half
-  const float4* rope_cs4; // per-lane tables: [T][rope_half] (cos_i, sin_i, cos_i+h, sin_i+h)
+  // rotary tables, frequency-major: entry (i, t) at i * T + t
+  const float2* rope_cs;  // [rope_half][T] (cos, sin) of theta_i, shared by lanes i and i+half
+  const float4* rope_cs4; // per-lane tables: [rope_half][T] (cos_i, sin_i, cos_i+h, sin_i+h)
   int rope_per_lane;      // 1: use rope_cs4
   const void* bias;   // [N] or null, dtype of x
   void* out_ff;
@@ -111,7 +112,7 @@ struct BwdGatherParams {
   const void* g_v;
   void* G;                  // [M, N] bf16
   float* db;                // [N] or null
-  const float2* rope_cs;    // [T][rope_half] (cos, sin), or null
+  const float2* rope_cs;    // [rope_half][T] (cos, sin), frequency-major, or null
   int64_t M, T;
   int F, N, C, heads, hd, groups, rope_half, k_transposed;
 };

@@ -590,6 +590,10 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 template <bool VEC>
 __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const BwdGatherParams p) {
   __shared__ float part[GATHER_ROWS][32][8];
+  // the block's slice of the frequency-major rotary table, token-major here
+  // ([64 tokens][rope_half]): filled by runs of consecutive tokens per
+  // frequency, read by a warp as different frequencies of one token
+  extern __shared__ float2 tab[];
   const int nq = p.N - p.F;
   const int col0 = (blockIdx.x * 32 + threadIdx.x) * 8;  // first of 8 columns
   const bool active = col0 < nq;
@@ -627,7 +631,17 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
   float sum[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
-  const int64_t mb = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS + threadIdx.y;
+  const int64_t mblk = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS;
+  if (rh > 0) {
+    const int tid = threadIdx.y * 32 + threadIdx.x;
+    for (int e = tid; e < rh * GATHER_TOKENS; e += 32 * GATHER_ROWS) {
+      const int f = e / GATHER_TOKENS, r = e - f * GATHER_TOKENS;
+      const int64_t m = mblk + r;
+      if (m < p.M) tab[r * rh + f] = __ldg(p.rope_cs + f * p.T + m % p.T);
+    }
+    __syncthreads();
+  }
+  const int64_t mb = mblk + threadIdx.y;
 #pragma unroll 1
   for (int i0 = 0; i0 < GATHER_PER_ROW && active; i0 += GATHER_BATCH) {
     int64_t roff[GATHER_BATCH];  // element offset of the token's row of its head
@@ -668,12 +682,12 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
         }
       }
       if (rot) {
-        const float2* cs = p.rope_cs + static_cast<int64_t>(t) * rh;
+        const float2* cs = tab + (threadIdx.y + (i0 + k) * GATHER_ROWS) * rh;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int j = j0 + i;
           if (j < 2 * rh) {
-            const float2 c = __ldg(cs + (j < rh ? j : j - rh));
+            const float2 c = cs[j < rh ? j : j - rh];
             g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
           }
         }
@@ -724,10 +738,12 @@ cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
   if (nq <= 0 || p.M == 0) return cudaSuccess;
   const dim3 grid((nq / 8 + 31) / 32,
                   static_cast<unsigned>((p.M + GATHER_TOKENS - 1) / GATHER_TOKENS));
+  const size_t smem = static_cast<size_t>(p.rope_half) * GATHER_TOKENS * sizeof(float2);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;  // rope_half <= 64 (head_dim <= 128)
   if (!p.k_transposed && p.rope_half % 8 == 0)
-    bwd_gather_kernel<true><<<grid, dim3(32, GATHER_ROWS), 0, stream>>>(p);
+    bwd_gather_kernel<true><<<grid, dim3(32, GATHER_ROWS), smem, stream>>>(p);
   else
-    bwd_gather_kernel<false><<<grid, dim3(32, GATHER_ROWS), 0, stream>>>(p);
+    bwd_gather_kernel<false><<<grid, dim3(32, GATHER_ROWS), smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -126,11 +126,11 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
       if (in && rot) {
         pv[q] = Cs[r * CS_LD + pc] + pbv;
         if (e.rope_per_lane) {
-          const float4 c4 = e.rope_cs4[row_t[r] * half + f];
+          const float4 c4 = e.rope_cs4[static_cast<int64_t>(f) * e.T + row_t[r]];
           cc[q] = lo ? c4.x : c4.z;
           ss[q] = lo ? c4.y : c4.w;
         } else {
-          const float2 cs = e.rope_cs[row_t[r] * half + f];
+          const float2 cs = e.rope_cs[static_cast<int64_t>(f) * e.T + row_t[r]];
           cc[q] = cs.x;
           ss[q] = cs.y;
         }

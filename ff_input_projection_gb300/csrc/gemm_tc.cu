@@ -133,12 +133,14 @@ __device__ __forceinline__ void store16_packed_strided(uint16_t* dst, int64_t st
 
 // Rotation of lanes [0, 2*RH) of a head held in one 16-column granule (partial
 // rotary, rope_n_elem = 2*RH <= 16): pair (i, i + RH) with (cos, sin) of
-// frequency i.
+// frequency i. cs points at the token's entry of frequency 0 of the
+// frequency-major table; frequency i is T entries further.
 template <int RH>
-__device__ __forceinline__ void rotate_in_granule(float (&v)[16], const float2* __restrict__ cs) {
+__device__ __forceinline__ void rotate_in_granule(float (&v)[16], const float2* __restrict__ cs,
+                                                  int64_t T) {
 #pragma unroll
   for (int i = 0; i < RH; ++i) {
-    const float2 c = __ldg(cs + i);
+    const float2 c = __ldg(cs + i * T);
     const float x = v[i], y = v[i + RH];
     v[i] = x * c.x - y * c.y;
     v[i + RH] = y * c.x + x * c.y;
@@ -147,40 +149,41 @@ __device__ __forceinline__ void rotate_in_granule(float (&v)[16], const float2* 
 
 // Per-lane tables: lane i uses (cos_i, sin_i), lane i+RH uses (cos_i+RH, sin_i+RH).
 template <int RH>
-__device__ __forceinline__ void rotate_in_granule4(float (&v)[16], const float4* __restrict__ cs) {
+__device__ __forceinline__ void rotate_in_granule4(float (&v)[16], const float4* __restrict__ cs,
+                                                   int64_t T) {
 #pragma unroll
   for (int i = 0; i < RH; ++i) {
-    const float4 c = __ldg(cs + i);
+    const float4 c = __ldg(cs + i * T);
     const float x = v[i], y = v[i + RH];
     v[i] = x * c.x - y * c.y;
     v[i + RH] = y * c.z + x * c.w;
   }
 }
 
-__device__ __forceinline__ void rotate_small4(float (&v)[16], const float4* cs, int rh) {
+__device__ __forceinline__ void rotate_small4(float (&v)[16], const float4* cs, int rh, int64_t T) {
   switch (rh) {
-    case 1: rotate_in_granule4<1>(v, cs); break;
-    case 2: rotate_in_granule4<2>(v, cs); break;
-    case 3: rotate_in_granule4<3>(v, cs); break;
-    case 4: rotate_in_granule4<4>(v, cs); break;
-    case 5: rotate_in_granule4<5>(v, cs); break;
-    case 6: rotate_in_granule4<6>(v, cs); break;
-    case 7: rotate_in_granule4<7>(v, cs); break;
-    case 8: rotate_in_granule4<8>(v, cs); break;
+    case 1: rotate_in_granule4<1>(v, cs, T); break;
+    case 2: rotate_in_granule4<2>(v, cs, T); break;
+    case 3: rotate_in_granule4<3>(v, cs, T); break;
+    case 4: rotate_in_granule4<4>(v, cs, T); break;
+    case 5: rotate_in_granule4<5>(v, cs, T); break;
+    case 6: rotate_in_granule4<6>(v, cs, T); break;
+    case 7: rotate_in_granule4<7>(v, cs, T); break;
+    case 8: rotate_in_granule4<8>(v, cs, T); break;
     default: break;
   }
 }
 
-__device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, int rh) {
+__device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, int rh, int64_t T) {
   switch (rh) {
-    case 1: rotate_in_granule<1>(v, cs); break;
-    case 2: rotate_in_granule<2>(v, cs); break;
-    case 3: rotate_in_granule<3>(v, cs); break;
-    case 4: rotate_in_granule<4>(v, cs); break;
-    case 5: rotate_in_granule<5>(v, cs); break;
-    case 6: rotate_in_granule<6>(v, cs); break;
-    case 7: rotate_in_granule<7>(v, cs); break;
-    case 8: rotate_in_granule<8>(v, cs); break;
+    case 1: rotate_in_granule<1>(v, cs, T); break;
+    case 2: rotate_in_granule<2>(v, cs, T); break;
+    case 3: rotate_in_granule<3>(v, cs, T); break;
+    case 4: rotate_in_granule<4>(v, cs, T); break;
+    case 5: rotate_in_granule<5>(v, cs, T); break;
+    case 6: rotate_in_granule<6>(v, cs, T); break;
+    case 7: rotate_in_granule<7>(v, cs, T); break;
+    case 8: rotate_in_granule<8>(v, cs, T); break;
     default: break;
   }
 }
@@ -592,13 +595,15 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               tmem_ld16(t_head + j + rh, hi_u);
               tmem_wait_ld();
               uint32_t lo_w[8], hi_w[8];
+              // frequency-major tables: lane (token t) reads entry (f, t) at f * T + t,
+              // so a warp's 32 consecutive tokens read one contiguous run per f
               if (e.rope_per_lane) {
-                const float4* t4 = e.rope_cs4 + t * rh + j;
+                const float4* t4 = e.rope_cs4 + t + j * e.T;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
                   for (int i = 4 * h; i < 4 * h + 4; ++i) {
-                    const float4 c0 = __ldg(t4 + 2 * i), c1 = __ldg(t4 + 2 * i + 1);
+                    const float4 c0 = __ldg(t4 + (2 * i) * e.T), c1 = __ldg(t4 + (2 * i + 1) * e.T);
                     const float x0 = __uint_as_float(lo_u[2 * i]);
                     const float y0 = __uint_as_float(hi_u[2 * i]);
                     const float x1 = __uint_as_float(lo_u[2 * i + 1]);
@@ -609,15 +614,16 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                   asm volatile("" ::: "memory");
                 }
               } else {
-                const float4* cs4 = reinterpret_cast<const float4*>(e.rope_cs + t * rh + j);
+                const float2* csf = e.rope_cs + t + j * e.T;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const float4 cs = __ldg(cs4 + i);  // (cos, sin) of frequencies 2i and 2i+1
+                  // (cos, sin) of frequencies j + 2i and j + 2i + 1
+                  const float2 ca = __ldg(csf + (2 * i) * e.T), cb = __ldg(csf + (2 * i + 1) * e.T);
                   const float x0 = __uint_as_float(lo_u[2 * i]), y0 = __uint_as_float(hi_u[2 * i]);
                   const float x1 = __uint_as_float(lo_u[2 * i + 1]);
                   const float y1 = __uint_as_float(hi_u[2 * i + 1]);
-                  lo_w[i] = pack_bf16x2(x0 * cs.x - y0 * cs.y, x1 * cs.z - y1 * cs.w);
-                  hi_w[i] = pack_bf16x2(y0 * cs.x + x0 * cs.y, y1 * cs.z + x1 * cs.w);
+                  lo_w[i] = pack_bf16x2(x0 * ca.x - y0 * ca.y, x1 * cb.x - y1 * cb.y);
+                  hi_w[i] = pack_bf16x2(y0 * ca.x + x0 * ca.y, y1 * cb.x + x1 * cb.y);
                 }
               }
               stage_store(map, j, static_cast<int>(t), z, true, lo_w);
@@ -654,7 +660,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         uint16_t* const v_row = static_cast<uint16_t*>(e.out_v) + (bidx * nkv * e.T + t) * e.hd;
         // pre-transposed k: element (b, head, lane j, token t) at ((b*nkv + head)*hd + j)*T + t
         uint16_t* const kt_row = static_cast<uint16_t*>(e.out_k) + bidx * nkv * head_stride + t;
-        const float2* const cs_row = e.rope_cs + t * rh;
+        const float2* const cs_t = e.rope_cs + t;  // entry (0, t) of the frequency-major table
         auto put16 = [&](int seg, int head, int j, uint16_t* dst, const uint32_t (&w)[8]) {
           if (!(seg == 0 ? tma_ff : tma_heads)) {
             if (valid) {
@@ -698,15 +704,16 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             tmem_wait_ld();
             uint32_t lo_w[8], hi_w[8];  // results, two bf16 per word
             if (e.rope_per_lane) {
-              const float4* t4 = e.rope_cs4 + t * rh + ci.j;
+              const float4* t4 = e.rope_cs4 + t + ci.j * e.T;
               // two halves, so that at most eight table entries are in flight
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
 #pragma unroll
                 for (int i = 4 * h; i < 4 * h + 4; ++i) {
-                  const float4 c0 = valid ? __ldg(t4 + 2 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  const float4 c0 =
+                      valid ? __ldg(t4 + (2 * i) * e.T) : make_float4(0.f, 0.f, 0.f, 0.f);
                   const float4 c1 =
-                      valid ? __ldg(t4 + 2 * i + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                      valid ? __ldg(t4 + (2 * i + 1) * e.T) : make_float4(0.f, 0.f, 0.f, 0.f);
                   const float x0 = __uint_as_float(lo_u[2 * i]);
                   const float y0 = __uint_as_float(hi_u[2 * i]);
                   const float x1 = __uint_as_float(lo_u[2 * i + 1]);
@@ -717,16 +724,17 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                 asm volatile("" ::: "memory");
               }
             } else {
-              const float4* cs4 = reinterpret_cast<const float4*>(cs_row + ci.j);
+              const float2* csf = cs_t + ci.j * e.T;
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                // (cos, sin) of frequencies 2i and 2i+1
-                const float4 cs = valid ? __ldg(cs4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                // (cos, sin) of frequencies j + 2i and j + 2i + 1
+                const float2 ca = valid ? __ldg(csf + (2 * i) * e.T) : make_float2(0.f, 0.f);
+                const float2 cb = valid ? __ldg(csf + (2 * i + 1) * e.T) : make_float2(0.f, 0.f);
                 const float x0 = __uint_as_float(lo_u[2 * i]), y0 = __uint_as_float(hi_u[2 * i]);
                 const float x1 = __uint_as_float(lo_u[2 * i + 1]);
                 const float y1 = __uint_as_float(hi_u[2 * i + 1]);
-                lo_w[i] = pack_bf16x2(x0 * cs.x - y0 * cs.y, x1 * cs.z - y1 * cs.w);
-                hi_w[i] = pack_bf16x2(y0 * cs.x + x0 * cs.y, y1 * cs.z + x1 * cs.w);
+                lo_w[i] = pack_bf16x2(x0 * ca.x - y0 * ca.y, x1 * cb.x - y1 * cb.y);
+                hi_w[i] = pack_bf16x2(y0 * ca.x + x0 * ca.y, y1 * cb.x + x1 * cb.y);
               }
             }
             if (kt) {  // pre-transposed k is stored directly, one lane column at a time
@@ -752,9 +760,9 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(v_u[i]);
               if (e.rope_per_lane)
-                rotate_small4(v, e.rope_cs4 + t * rh, rh);
+                rotate_small4(v, e.rope_cs4 + t, rh, e.T);
               else
-                rotate_small(v, cs_row, rh);
+                rotate_small(v, cs_t, rh, e.T);
 #pragma unroll
               for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
             } else {

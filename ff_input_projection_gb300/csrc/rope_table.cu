@@ -1,9 +1,11 @@
-// Rotary table kernel: cs[t, i] = (cos, sin)(pos[t] * base^(-2 i / n_elem)).
+// Rotary table kernel: cs[i, t] = (cos, sin)(pos[t] * base^(-2 i / n_elem)).
 //
 // The rotate-half embedding of nvFuser issue #1597 "Improve performance on
 // RoPE" (rope_one_entry listing) takes cos/sin tables [T, rope_n_elem] as
 // inputs. Both halves of a head use the same angle theta_i, so one (cos, sin)
-// pair per (position, frequency) is stored: T * n_elem/2 float2.
+// pair per (frequency, position) is stored: n_elem/2 * T float2, frequency-major
+// so that the 32 lanes of a warp (32 consecutive tokens) read one contiguous
+// run per frequency.
 //
 // Accuracy: the angle is formed and reduced to [-pi, pi] in fp64 (Cody-Waite
 // reduction with 2*pi split into a head and a tail), then cos/sin are taken in
@@ -17,8 +19,8 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, const int32_t* __rest
                                   int64_t T, int half, int n_elem, double log2_base) {
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= T * half) return;
-  int64_t t = i / half;
-  int f = static_cast<int>(i - t * half);
+  const int f = static_cast<int>(i / T);
+  const int64_t t = i - static_cast<int64_t>(f) * T;
   double p = pos ? static_cast<double>(pos[t]) : static_cast<double>(t);
   double inv_freq = exp2(-(2.0 * f / n_elem) * log2_base);
   double a = p * inv_freq;
@@ -34,7 +36,8 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, const int32_t* __rest
 
 // Caller-given tables (the rope_one_entry listing's cos/sin inputs, [T, n_rot],
 // any strides, bf16 or f32): repacked per rotated pair as (cos_i, sin_i,
-// cos_{i+half}, sin_{i+half}) in fp32, so the epilogue reads one float4 per pair.
+// cos_{i+half}, sin_{i+half}) in fp32, so the epilogue reads one float4 per pair;
+// frequency-major, [half][T], like the computed table.
 __device__ __forceinline__ float load_any(const void* p, bool bf16, int64_t i) {
   if (bf16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16);
   return static_cast<const float*>(p)[i];
@@ -44,8 +47,8 @@ __global__ void rope_import_kernel(float4* __restrict__ dst, const void* cosv, c
                                    bool bf16, int64_t T, int half, int64_t st_t, int64_t st_i) {
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= T * half) return;
-  int64_t t = i / half;
-  int64_t f = i - t * half;
+  const int64_t f = i / T;
+  const int64_t t = i - f * T;
   const int64_t lo = t * st_t + f * st_i, hi = t * st_t + (f + half) * st_i;
   dst[i] = make_float4(load_any(cosv, bf16, lo), load_any(sinv, bf16, lo), load_any(cosv, bf16, hi),
                        load_any(sinv, bf16, hi));
