@@ -560,15 +560,20 @@ def main_backward(args, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         import oracle
         cores = os.cpu_count() or 1
-        rows = list(range(0, w.M, max(1, w.M // 32)))[:32]
-        t = time.perf_counter()
-        oracle.backward_workload(w, inp, grads, rows=rows, threads=cores)
-        el = time.perf_counter() - t
-        fl = 2.0 * len(rows) * w.C * (w.F + w.N)
+        rng = np.random.default_rng(0)
+        el, done = 0.0, 0
+        while el < args.cpu_seconds and done < 64 * w.M:
+            rows = np.sort(rng.choice(w.M, size=min(64, w.M), replace=False))
+            t = time.perf_counter()
+            oracle.backward_workload(w, inp, grads, rows=rows, threads=cores)
+            el += time.perf_counter() - t
+            done += len(rows)
+        rows = range(done)
+        fl = 2.0 * done * w.C * (w.F + w.N)
         line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores,
                                 "kind": "oracle",
-                                "sample": f"dx of {len(rows)} token rows of {w.M} (ff recompute "
-                                          f"+ G W^T per row), fp64, {el:.1f} s"}
+                                "sample": f"dx of {done} token rows drawn from the {w.M} (ff "
+                                          f"recompute + G W^T per row), fp64, {el:.1f} s"}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
