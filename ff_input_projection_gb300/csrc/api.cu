@@ -375,6 +375,7 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
   e.status = sc.status;
   e.bn_eff = bn_eff;
   e.k_transposed = p->k_transposed;
+  e.ff_ld = p->F;
   const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
 
   if (pr.tc_path) {
@@ -958,8 +959,62 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   auto map_fail = [&](const char* what) {
     return fail(FP_ERR_UNSUPPORTED_LAYOUT, "backward: tensor map for %s rejected", what);
   };
-  // 2. ff part of G: recompute x W_ff + b_ff, times act' and the upstream gradient
-  if (F > 0) {
+  // 2. ff part of G: recompute x W_ff + b_ff, times act' and the upstream gradient.
+  // CTA pairs of the forward kernel in its gradient mode when every tile is a
+  // whole number of 32-column units; the single-CTA backward kernel otherwise.
+  const int64_t fwd_m_tiles = pr.tk.n_outer * mps;
+  if (F > 0 && F % 32 == 0 && fwd_m_tiles >= 2) {
+    fp::TcParams tp;
+    memset(&tp, 0, sizeof tp);
+    if (encode_x_map(encode, &tp.tmap_a, x, pr, C, pr.a_mn, 64, pr.a_mn ? 64 : 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return map_fail("x");
+    if (encode_2d(encode, &tp.tmap_b, W, BF, 2, N, C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
+      return map_fail("W");
+    if (b && encode_2d(encode, &tp.tmap_bias, b, BF, 2, N, 1, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE) !=
+                 CUDA_SUCCESS)
+      return map_fail("b");
+    {  // G's ff columns, [M][F] with row stride N, 32 x 32 boxes
+      cuuint64_t d[2] = {static_cast<cuuint64_t>(F), static_cast<cuuint64_t>(M)};
+      cuuint64_t st[1] = {static_cast<cuuint64_t>(N) * 2};
+      cuuint32_t bx[2] = {32, 32}, es[2] = {1, 1};
+      if (encode(&tp.tmap_ff32, BF, 2, workspace, d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return map_fail("G");
+    }
+    tp.tma_store = 1;
+    tp.tok = pr.tk;
+    fp::Epilogue& e = tp.epi;
+    e.M = M;
+    e.T = pr.ta.T;
+    e.N = F;  // only the ff columns
+    e.F = F;
+    e.C = C;
+    e.act = p->act;
+    e.bias = b;
+    e.out_ff = workspace;
+    e.ff_ld = N;
+    e.g_ff = g_ff;
+    e.db = db;
+    e.status = p->d_status;
+    e.bn_eff = fp::kTcBN;
+    tp.C = C;
+    tp.num_k_blocks = (C + fp::kTcBK - 1) / fp::kTcBK;
+    tp.m_tiles_per_slab = mps;
+    tp.num_m_tiles = fwd_m_tiles;
+    tp.num_n_tiles = (F + fp::kTcBN - 1) / fp::kTcBN;
+    tp.num_tiles = tp.num_m_tiles * tp.num_n_tiles;
+    tp.cluster = 2;
+    tp.num_units = (tp.num_m_tiles + 1) / 2 * tp.num_n_tiles;
+    tp.group_m = p->group_m;
+    tp.wait_limit_ns = p->wait_limit_ns;
+    tp.launch_tag = tag;
+    cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, ctas, stream, true);
+    if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
+    ++launches;
+  } else if (F > 0) {
     fp::BwdGemmParams gp = base;
     gp.mode = fp::BWD_GRADFF;
     if (encode_x_map(encode, &gp.tmap_a, x, pr, C, pr.a_mn, 64, pr.a_mn ? 64 : 128,

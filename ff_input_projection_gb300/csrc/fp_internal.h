@@ -46,6 +46,11 @@ struct Epilogue {
   int* status;
   int bn_eff;         // columns of an N-tile that this tile owns
   int k_transposed;   // 1: k is written [B*kv, hd, T]
+  int64_t ff_ld;      // row stride of out_ff (F; N when out_ff is the backward's G)
+  // backward ff gradient (tensor-core kernel, grad mode): out_ff receives
+  // g_ff * act'(x W + b) instead of act(x W + b), its column sums go to db
+  const void* g_ff;   // [M, F] upstream gradient, dtype of x
+  float* db;          // [N] or null
 };
 
 struct TcParams {
@@ -134,7 +139,8 @@ cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int hal
 cudaError_t launch_rope_import(float4* dst, const void* cosv, const void* sinv, bool bf16,
                                int64_t T, int half, int64_t stride_t, int64_t stride_i,
                                cudaStream_t stream);
-cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream);
+cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream,
+                           bool grad = false);
 cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_ctas,
                             cudaStream_t stream);

@@ -126,70 +126,6 @@ __device__ __forceinline__ Geo unit_geo(const BwdGemmParams& p, int64_t u64) {
   return q;
 }
 
-// Derivative of the ff activation (fp32, CUDA's math library).
-template <int ACT>
-__device__ __forceinline__ float act_deriv(float y) {
-  if (ACT == ACT_GELU_ERF) {
-    return normcdff(y) + y * 0.39894228040143268f * __expf(-0.5f * y * y);
-  } else if (ACT == ACT_GELU_TANH) {
-    constexpr float k0 = 0.79788456080286536f, k3 = 0.044715f;
-    const float th = tanhf(k0 * fmaf(k3 * y, y * y, y));
-    return 0.5f * (1.0f + th) + 0.5f * y * (1.0f - th * th) * k0 * fmaf(3.0f * k3, y * y, 1.0f);
-  } else if (ACT == ACT_SILU) {
-    const float sg = 1.0f / (1.0f + __expf(-y));
-    return sg * fmaf(y, 1.0f - sg, 1.0f);
-  } else if (ACT == ACT_RELU2) {
-    return y > 0.0f ? 2.0f * y : 0.0f;
-  }
-  return 1.0f;
-}
-
-// GELU'(y) = Phi(y) + y phi(y) for two values on packed fp32 pairs, with the
-// same Abramowitz & Stegun 7.1.26 erf as the forward: for a = |y|,
-// t = 1 / (1 + p a / sqrt 2), erfc(a / sqrt 2) = t P(t) exp(-a^2/2), so
-// Phi(y) = h or 1 - h with h = (1/2) t P(t) e, e = exp(-y^2/2), and
-// phi(y) = e / sqrt(2 pi). Absolute error about 1e-7.
-__device__ __forceinline__ void gelu_erf_deriv2(float y0, float y1, float& d0, float& d1) {
-  constexpr float kLog2e = 1.4426950408889634f;
-  const float a0 = fabsf(y0), a1 = fabsf(y1);
-  const uint64_t A = f2_pack(a0, a1);
-  float q0, q1;
-  f2_unpack(f2_fma(A, f2_splat(0.3275911f * 0.70710678118654752f), f2_splat(1.0f)), q0, q1);
-  const uint64_t T = f2_pack(rcp_approx(q0), rcp_approx(q1));
-  uint64_t P = f2_fma(f2_splat(0.5f * 1.061405429f), T, f2_splat(0.5f * -1.453152027f));
-  P = f2_fma(P, T, f2_splat(0.5f * 1.421413741f));
-  P = f2_fma(P, T, f2_splat(0.5f * -0.284496736f));
-  P = f2_fma(P, T, f2_splat(0.5f * 0.254829592f));
-  float e0, e1;
-  f2_unpack(f2_mul(f2_mul(A, f2_splat(-0.5f * kLog2e)), A), e0, e1);
-  const uint64_t E = f2_pack(ex2_approx(e0), ex2_approx(e1));
-  float h0, h1;
-  f2_unpack(f2_mul(f2_mul(P, T), E), h0, h1);  // (1/2) erfc(|y| / sqrt 2)
-  const uint64_t PHI = f2_pack(y0 >= 0.0f ? 1.0f - h0 : h0, y1 >= 0.0f ? 1.0f - h1 : h1);
-  const uint64_t R =
-      f2_fma(f2_mul(f2_pack(y0, y1), f2_splat(0.39894228040143268f)), E, PHI);
-  f2_unpack(R, d0, d1);
-}
-
-// Column sums of a warp's [32 rows][32 columns] block (row = lane): a
-// butterfly that halves the columns each lane keeps at every step; after five
-// steps lane i holds the sum of column i.
-__device__ __forceinline__ float column_sum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int off = 16 >> step;
-    const int n = 32 >> step;
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
-    }
-  }
-  return v[0];
-}
-
 // 32 bf16 values (four 16-byte loads from a 16-byte aligned address), widened to fp32
 __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32]) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);

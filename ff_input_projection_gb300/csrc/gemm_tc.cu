@@ -202,7 +202,10 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 // relay of the odd CTA's completions through a second thread, or a second
 // barrier per stage, each measured 20-100 % slower.)
 // One CTA per SM (its shared-memory footprint allows no second one).
-template <bool A_MN_MAJOR, int ACT, int CL>
+// GRAD: the backward's ff gradient instead of the forward: every tile lies in
+// the ff block and its output is g_ff * act'(x W + b) (same GEMM, bias in the
+// MMA), with column sums into db.
+template <bool A_MN_MAJOR, int ACT, int CL, bool GRAD = false>
 __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using G = Cfg<CL>;
   constexpr int STAGES = G::STAGES;
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
       if (tc.n0 + cols <= e.F && (cols & 31) == 0) {
         // ---- a tile inside the ff block: activation, then [M, F] row-major,
         // 32 columns per work unit (the tile's width is a multiple of 32)
-        uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.F + tc.n0;
+        uint16_t* const ff_row = static_cast<uint16_t*>(e.out_ff) + m * e.ff_ld + tc.n0;
         // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)
         const uint32_t sw64 = (lane >> 1) & 3u;
         for (int c = 0; c < cols; c += 32) {
@@ -544,8 +547,44 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           tmem_ld32(t_row + c, v_u);
           tmem_wait_ld();
           uint32_t w[16];
+          if constexpr (GRAD) {
+            // upstream gradient of the lane's token, 32 columns (zero past M)
+            float gg[32];
+            const uint4* g4 = reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(e.g_ff) + m * e.F + tc.n0 + c);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
+            for (int q = 0; q < 4; ++q) {
+              const uint4 u = valid ? __ldg(g4 + q) : make_uint4(0, 0, 0, 0);
+              const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                gg[8 * q + 2 * i] = __uint_as_float(uw[i] << 16);
+                gg[8 * q + 2 * i + 1] = __uint_as_float(uw[i] & 0xFFFF0000u);
+              }
+            }
+            if (ACT == ACT_GELU_ERF) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float d0, d1;
+                gelu_erf_deriv2(__uint_as_float(v_u[2 * i]), __uint_as_float(v_u[2 * i + 1]), d0,
+                                d1);
+                gg[2 * i] *= d0;
+                gg[2 * i + 1] *= d1;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) gg[i] *= act_deriv<ACT>(__uint_as_float(v_u[i]));
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(gg[2 * i], gg[2 * i + 1]);
+            if (e.db) {
+              const float cs = column_sum32(gg, lane);
+              atomicAdd(e.db + tc.n0 + c + lane, cs);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = activate2_bf16<ACT>(v_u[2 * i], v_u[2 * i + 1]);
+          }
           if (tma_ff) {
             const uint32_t stg = staging_warp + (stage_sel & 1) * 2048;
             ++stage_sel;
@@ -812,9 +851,9 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
   }
 }
 
-template <bool A_MN, int ACT, int CL>
+template <bool A_MN, int ACT, int CL, bool GRAD = false>
 cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream) {
-  auto kernel = tc_gemm_kernel<A_MN, ACT, CL>;
+  auto kernel = tc_gemm_kernel<A_MN, ACT, CL, GRAD>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -869,21 +908,27 @@ cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream)
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-template <bool A_MN, int CL>
+template <bool A_MN, int CL, bool GRAD = false>
 cudaError_t launch_act(const TcParams& p, int num_ctas, cudaStream_t stream) {
   switch (p.epi.act) {
-    case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF, CL>(p, num_ctas, stream);
-    case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH, CL>(p, num_ctas, stream);
-    case ACT_SILU: return launch_variant<A_MN, ACT_SILU, CL>(p, num_ctas, stream);
-    case ACT_RELU2: return launch_variant<A_MN, ACT_RELU2, CL>(p, num_ctas, stream);
-    default: return launch_variant<A_MN, ACT_NONE, CL>(p, num_ctas, stream);
+    case ACT_GELU_ERF: return launch_variant<A_MN, ACT_GELU_ERF, CL, GRAD>(p, num_ctas, stream);
+    case ACT_GELU_TANH: return launch_variant<A_MN, ACT_GELU_TANH, CL, GRAD>(p, num_ctas, stream);
+    case ACT_SILU: return launch_variant<A_MN, ACT_SILU, CL, GRAD>(p, num_ctas, stream);
+    case ACT_RELU2: return launch_variant<A_MN, ACT_RELU2, CL, GRAD>(p, num_ctas, stream);
+    default: return launch_variant<A_MN, ACT_NONE, CL, GRAD>(p, num_ctas, stream);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_tc_gemm(const TcParams& p, bool a_mn_major, int num_ctas, cudaStream_t stream,
+                           bool grad) {
   if (p.num_units == 0) return cudaSuccess;
+  if (grad) {  // CTA pairs only
+    if (p.cluster != 2) return cudaErrorInvalidValue;
+    return a_mn_major ? launch_act<true, 2, true>(p, num_ctas, stream)
+                      : launch_act<false, 2, true>(p, num_ctas, stream);
+  }
   if (p.cluster == 2)
     return a_mn_major ? launch_act<true, 2>(p, num_ctas, stream)
                       : launch_act<false, 2>(p, num_ctas, stream);

@@ -266,3 +266,30 @@ def test_caller_rope_tables(w, cuda_ok):
     out2 = run(w, {**inp, "rope_cos": None, "rope_sin": None}, proj=proj)
     for k in ("q", "k"):
         assert_close(host(out2[k]), ref2[k], w.dtype, f"{w.name}:default:{k}")
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[5]], ids=lambda w: w.name)
+def test_back_to_back_launches_keep_order(w, cuda_ok):
+    """Launches may start their prologue while the previous kernel finishes
+    (programmatic dependent launch); they must still read and write in stream
+    order: a forward, a torch copy of its output, and a second forward into the
+    same buffers, all enqueued without synchronising."""
+    inp1 = fpsynth.make_inputs(w)
+    inp2 = fpsynth.make_inputs(w, seed=w.seed + 1000)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    x1, x2 = to_device(inp1["x"], w.dtype), to_device(inp2["x"], w.dtype)
+    W, b = to_device(inp1["W"], w.dtype), to_device(inp1["b"], w.dtype)
+    out = proj.forward(x1, W, b, None, channel_dim=w.channel_dim)
+    snap = [None if o is None else o.clone() for o in out]
+    out = proj.forward(x2, W, b, None, channel_dim=w.channel_dim, out=out)
+    snap2 = [None if o is None else o.clone() for o in out]
+    proj.forward(x1, W, b, None, channel_dim=w.channel_dim, out=out)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK
+    ref1 = oracle.forward_workload(w, inp1)
+    ref2 = oracle.forward_workload(w, {**inp2, "W": inp1["W"], "b": inp1["b"]})
+    for i, k in enumerate(("ff", "q", "k", "v")):
+        if snap[i] is not None:
+            assert_close(host(snap[i]), ref1[k], w.dtype, f"first:{k}")
+            assert_close(host(snap2[i]), ref2[k], w.dtype, f"second:{k}")
+            assert_close(host(out[i]), ref1[k], w.dtype, f"third:{k}")
