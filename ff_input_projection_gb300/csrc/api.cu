@@ -1010,6 +1010,7 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     tp.num_units = (tp.num_m_tiles + 1) / 2 * tp.num_n_tiles;
     tp.group_m = p->group_m;
     tp.wait_limit_ns = p->wait_limit_ns;
+    tp.inject_stall = p->inject_stall;
     tp.launch_tag = tag;
     cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, ctas, stream, true);
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
@@ -1102,6 +1103,7 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
     ++launches;
   }
+  p->inject_stall = 0;
   p->last_launches = launches;
   return ok();
 }

@@ -36,3 +36,25 @@ def test_timeout_is_reported_and_context_survives(cuda_ok):
     out = run(w, inp, proj=proj)
     for k in ("ff", "q", "k", "v"):
         assert_close(host(out[k]), ref[k], w.dtype, f"after-timeout:{k}")
+
+
+def test_backward_timeout_is_reported_and_context_survives(cuda_ok):
+    """The same hook in the backward's first tensor-core GEMM (the ff gradient)."""
+    import torch
+    from tests.test_gpu_backward import run_backward
+    w = CASE
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    proj.set_option(fpx.FP_OPT_WAIT_LIMIT_NS, 200_000_000)  # 0.2 s
+    proj.set_option(fpx.FP_OPT_INJECT_STALL, 1)
+    x, W, b = (to_device(inp[k], w.dtype) for k in ("x", "W", "b"))
+    g = tuple(to_device(grads[k], w.dtype) for k in ("ff", "q", "k", "v"))
+    proj.backward(x, W, b, g, channel_dim=w.channel_dim)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_ERR_TIMEOUT
+    assert proj.device_status() == fpx.FP_OK
+    dx, dW, db = run_backward(w, inp, grads, proj=proj)
+    ref = oracle.backward_workload(w, inp, grads)
+    assert_close(dx, ref["dx"], "bf16", "after-timeout:dx")
+    assert_close(dW, ref["dW"], "bf16", "after-timeout:dW")
