@@ -1094,8 +1094,27 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     if (kb > INT32_MAX) return fail(FP_ERR_UNSUPPORTED_LAYOUT, "too many tokens");
     gp.num_k_blocks = static_cast<int>(kb);
     const int64_t tiles = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
-    // about four work items per SM, each a whole number of k-blocks
-    int64_t splits = (4 * static_cast<int64_t>(ctas) + tiles - 1) / tiles;
+    // k splits: at least one full wave of work items, and the count whose
+    // waves are fullest (a last, partly idle wave costs a whole wave); ties
+    // take fewer splits (less reduce-add traffic)
+    // Large outputs are not split (each split adds a read-modify-write of dW),
+    // and every split keeps at least 16 k-blocks.
+    int64_t splits = 1;
+    double best_fill = -1.0;
+    const int64_t max_splits = tiles >= 4 * static_cast<int64_t>(ctas)
+                                   ? 1
+                                   : std::max<int64_t>(1, std::min<int64_t>(kb / 16, 32));
+    for (int64_t sp = std::min(max_splits, std::max<int64_t>(1, (ctas + tiles - 1) / tiles));
+         sp <= max_splits; ++sp) {
+      const int64_t units = tiles * sp;
+      const double fill = static_cast<double>(units) /
+                          static_cast<double>((units + ctas - 1) / ctas * ctas);
+      if (fill > best_fill + 1e-9) {
+        best_fill = fill;
+        splits = sp;
+      }
+      if (fill > 0.97) break;
+    }
     splits = std::max<int64_t>(1, std::min<int64_t>(splits, kb));
     gp.k_splits = static_cast<int>(splits);
     gp.num_units = tiles * splits;
