@@ -502,15 +502,14 @@ cudaError_t launch_gradff(const BwdGemmParams& p, int num_ctas, cudaStream_t str
 
 // A block covers 32 groups of 8 consecutive lanes (16 bytes of one head each;
 // a warp spans 4 heads of 64 lanes) and 64 tokens: thread (x, y) takes group x
-// and tokens y, y + 8, ..., loading the upstream gradients of 4 tokens (and
-// their rotation partners) before using any, so several requests per thread
-// are in flight. q and k are rotated back with the transpose of the rotation;
+// and tokens y, y + 8, ..., y + 56, loading the upstream gradients of all 8
+// (and their rotation partners) before the block fills its rotary-table slice,
+// so the loads and the fill are in flight together. q and k are rotated back with the transpose of the rotation;
 // each token's 8 values go to G as one 16-byte store; the 8 token rows' column
 // sums are reduced in shared memory and added into db once per block.
 constexpr int GATHER_ROWS = 8;     // token rows of threads per block
 constexpr int GATHER_PER_ROW = 8;  // tokens per thread
 constexpr int GATHER_TOKENS = GATHER_ROWS * GATHER_PER_ROW;
-constexpr int GATHER_BATCH = 4;    // tokens whose loads are issued together
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -568,6 +567,37 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
 #pragma unroll
   for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
   const int64_t mblk = static_cast<int64_t>(blockIdx.y) * GATHER_TOKENS;
+  const int64_t mb = mblk + threadIdx.y;
+  // the thread's tokens mb, mb + ROWS, ...: batch element and position walked
+  // from one division
+  int64_t roff[GATHER_PER_ROW];  // element offset of the token's row of its head
+  int tt[GATHER_PER_ROW];        // position of the token in its batch element
+  {
+    int64_t bb = mb / p.T;
+    int64_t t = mb - bb * p.T;
+#pragma unroll
+    for (int k = 0; k < GATHER_PER_ROW; ++k) {
+      tt[k] = static_cast<int>(t);
+      roff[k] = ((bb * nh + head) * p.T + t) * p.hd;
+      t += GATHER_ROWS;
+      while (t >= p.T) {
+        t -= p.T;
+        ++bb;
+      }
+    }
+  }
+  // the 16-byte gradient loads go out before the table fill and its barrier,
+  // so the two latencies overlap
+  uint4 gv[GATHER_PER_ROW] = {}, pv[GATHER_PER_ROW] = {};
+  if (VEC && active) {
+#pragma unroll
+    for (int k = 0; k < GATHER_PER_ROW; ++k) {
+      if (mb + static_cast<int64_t>(k) * GATHER_ROWS < p.M) {
+        gv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + j0);
+        if (rot) pv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + pj0);
+      }
+    }
+  }
   if (rh > 0) {
     const int tid = threadIdx.y * 32 + threadIdx.x;
     for (int e = tid; e < rh * GATHER_TOKENS; e += 32 * GATHER_ROWS) {
@@ -577,66 +607,47 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
     }
     __syncthreads();
   }
-  const int64_t mb = mblk + threadIdx.y;
-#pragma unroll 1
-  for (int i0 = 0; i0 < GATHER_PER_ROW && active; i0 += GATHER_BATCH) {
-    int64_t roff[GATHER_BATCH];  // element offset of the token's row of its head
-    int tt[GATHER_BATCH];        // position of the token in its batch element
-    uint4 gv[GATHER_BATCH] = {}, pv[GATHER_BATCH] = {};
 #pragma unroll
-    for (int k = 0; k < GATHER_BATCH; ++k) {
-      const int64_t m = mb + static_cast<int64_t>(i0 + k) * GATHER_ROWS;
-      const int64_t bb = m < p.M ? m / p.T : 0;
-      const int64_t t = m < p.M ? m - bb * p.T : 0;
-      tt[k] = static_cast<int>(t);
-      roff[k] = ((bb * nh + head) * p.T + t) * p.hd;
-      if (VEC && m < p.M) {
-        gv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + j0);
-        pv[k] = rot ? *reinterpret_cast<const uint4*>(src + roff[k] + pj0) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < GATHER_PER_ROW && active; ++k) {
+    const int64_t m = mb + static_cast<int64_t>(k) * GATHER_ROWS;
+    if (m >= p.M) continue;
+    const int t = tt[k];
+    float g[8], gp[8];
+    if constexpr (VEC) {
+      unpack8(gv[k], g);
+      unpack8(pv[k], gp);
+    } else {
+      // lane by lane: pre-transposed k is [B*kv, hd, T]; or rh < 8
+      const int64_t hrow = (m / p.T) * nh + head;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        const int jp = j < rh ? j + rh : j - rh;
+        const int64_t ij = kt ? (hrow * p.hd + j) * p.T + t : roff[k] + j;
+        const int64_t ip = kt ? (hrow * p.hd + jp) * p.T + t : roff[k] + jp;
+        g[i] = bf16_bits_to_float(src[ij]);
+        gp[i] = (rot && j < 2 * rh) ? bf16_bits_to_float(src[ip]) : 0.0f;
       }
     }
+    if (rot) {
+      const float2* cs = tab + (threadIdx.y + k * GATHER_ROWS) * rh;
 #pragma unroll
-    for (int k = 0; k < GATHER_BATCH; ++k) {
-      const int64_t m = mb + static_cast<int64_t>(i0 + k) * GATHER_ROWS;
-      if (m >= p.M) continue;
-      const int t = tt[k];
-      float g[8], gp[8];
-      if constexpr (VEC) {
-        unpack8(gv[k], g);
-        unpack8(pv[k], gp);
-      } else {
-        // lane by lane: pre-transposed k is [B*kv, hd, T]; or rh < 8
-        const int64_t hrow = (m / p.T) * nh + head;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j = j0 + i;
-          const int jp = j < rh ? j + rh : j - rh;
-          const int64_t ij = kt ? (hrow * p.hd + j) * p.T + t : roff[k] + j;
-          const int64_t ip = kt ? (hrow * p.hd + jp) * p.T + t : roff[k] + jp;
-          g[i] = bf16_bits_to_float(src[ij]);
-          gp[i] = (rot && j < 2 * rh) ? bf16_bits_to_float(src[ip]) : 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        if (j < 2 * rh) {
+          const float2 c = cs[j < rh ? j : j - rh];
+          g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
         }
       }
-      if (rot) {
-        const float2* cs = tab + (threadIdx.y + (i0 + k) * GATHER_ROWS) * rh;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j = j0 + i;
-          if (j < 2 * rh) {
-            const float2 c = cs[j < rh ? j : j - rh];
-            g[i] = j < rh ? fmaf(g[i], c.x, gp[i] * c.y) : fmaf(g[i], c.x, -gp[i] * c.y);
-          }
-        }
-      }
-      uint4 o;
-      o.x = pack_bf16x2(g[0], g[1]);
-      o.y = pack_bf16x2(g[2], g[3]);
-      o.z = pack_bf16x2(g[4], g[5]);
-      o.w = pack_bf16x2(g[6], g[7]);
-      *reinterpret_cast<uint4*>(G + m * p.N + p.F + col0) = o;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum[i] += g[i];
     }
+    uint4 o;
+    o.x = pack_bf16x2(g[0], g[1]);
+    o.y = pack_bf16x2(g[2], g[3]);
+    o.z = pack_bf16x2(g[4], g[5]);
+    o.w = pack_bf16x2(g[6], g[7]);
+    *reinterpret_cast<uint4*>(G + m * p.N + p.F + col0) = o;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum[i] += g[i];
   }
   if (!p.db) return;  // uniform across the block
 #pragma unroll
