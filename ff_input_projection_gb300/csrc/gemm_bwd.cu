@@ -8,7 +8,8 @@
 //
 //   gather   G[:, F:] = the q/k/v gradients gathered from their head-major
 //            buffers into token-major rows, q and k rotated back by the
-//            transpose of the rotation (bwd_gather_kernel, CUDA cores);
+//            transpose of the rotation (bwd_gather_pairs_kernel, or
+//            bwd_gather_kernel for the layouts it does not cover; CUDA cores);
 //   GRADFF   G[:, :F] = g_ff * act'(x W_ff + b_ff): the pre-activation is
 //            recomputed by a forward GEMM whose epilogue multiplies the
 //            upstream gradient by the activation's derivative;
@@ -25,6 +26,8 @@
 // N = 256, K = 64 per stage, 4 stages, two TMEM accumulators): warp 0 loads,
 // one thread of warp 1 issues tcgen05.mma, warps 2-9 drain the accumulators.
 // Every wait is bounded as in the forward kernel.
+#include <algorithm>
+
 #include "epilogue.cuh"
 #include "fp_internal.h"
 #include "tc_ptx.cuh"
@@ -500,13 +503,19 @@ cudaError_t launch_gradff(const BwdGemmParams& p, int num_ctas, cudaStream_t str
 
 // ------------------------------------------------------------------ q/k/v gather
 
-// A block covers 32 groups of 8 consecutive lanes (16 bytes of one head each;
-// a warp spans 4 heads of 64 lanes) and 64 tokens: thread (x, y) takes group x
-// and tokens y, y + 8, ..., y + 56, loading the upstream gradients of all 8
-// (and their rotation partners) before the block fills its rotary-table slice,
-// so the loads and the fill are in flight together. q and k are rotated back with the transpose of the rotation;
-// each token's 8 values go to G as one 16-byte store; the 8 token rows' column
-// sums are reduced in shared memory and added into db once per block.
+// Two gather kernels, both over blocks of 256 threads in token rows (thread
+// row y takes tokens y, y + rows, ...), each block staging its slice of the
+// rotary table in shared memory and adding its column sums into db once:
+//  - bwd_gather_pairs_kernel (16-byte path): a thread owns 16 columns of one
+//    head, the rotation pair (j .. j+7, j+rh .. j+rh+7) or two adjacent
+//    unrotated groups, so each token costs it two 16-byte loads and two
+//    16-byte stores and no partner is loaded twice;
+//  - bwd_gather_kernel (lane by lane): 8 columns per thread, element loads,
+//    8 rows of 32 threads, 8 tokens per thread; pre-transposed k, or a
+//    rotated half-width that is not a multiple of 8.
+// Both issue all of a thread's loads before the table fill and its barrier,
+// so the two are in flight together. q and k are rotated back with the transpose
+// of the rotation.
 constexpr int GATHER_ROWS = 8;     // token rows of threads per block
 constexpr int GATHER_PER_ROW = 8;  // tokens per thread
 constexpr int GATHER_TOKENS = GATHER_ROWS * GATHER_PER_ROW;
@@ -520,15 +529,12 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   }
 }
 
-// VEC: every column group is read as 16-byte vectors (k not pre-transposed,
-// rotated half-width a multiple of 8); otherwise lane by lane.
-template <bool VEC>
 __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const BwdGatherParams p) {
-  __shared__ float part[GATHER_ROWS][32][8];
+  __shared__ __align__(16) float part[GATHER_ROWS][32][8];
   // the block's slice of the frequency-major rotary table, token-major here
-  // ([64 tokens][rope_half]): filled by runs of consecutive tokens per
+  // ([64 tokens][rope_half + 2]): filled by runs of consecutive tokens per
   // frequency, read by a warp as different frequencies of one token
-  extern __shared__ float2 tab[];
+  extern __shared__ __align__(16) float2 tab[];
   const int nq = p.N - p.F;
   const int col0 = (blockIdx.x * 32 + threadIdx.x) * 8;  // first of 8 columns
   const bool active = col0 < nq;
@@ -556,10 +562,7 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
   const int nkv = p.groups > 0 ? p.groups : p.heads;
   const int rh = p.rope_half;
   const bool rot = rh > 0 && seg < 3 && j0 < 2 * rh;
-  // the 8 lanes and their partners are each one 16-byte group when rh is a
-  // multiple of 8; otherwise (rh < 8) and for pre-transposed k, lane by lane
   const bool kt = seg == 2 && p.k_transposed;
-  const int pj0 = j0 < rh ? j0 + rh : j0 - rh;
   const uint16_t* src = static_cast<const uint16_t*>(seg == 1 ? p.g_q : seg == 2 ? p.g_k : p.g_v);
   const int nh = seg == 1 ? p.heads : nkv;
   uint16_t* G = static_cast<uint16_t*>(p.G);
@@ -586,24 +589,19 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
       }
     }
   }
-  // the 16-byte gradient loads go out before the table fill and its barrier,
-  // so the two latencies overlap
-  uint4 gv[GATHER_PER_ROW] = {}, pv[GATHER_PER_ROW] = {};
-  if (VEC && active) {
-#pragma unroll
-    for (int k = 0; k < GATHER_PER_ROW; ++k) {
-      if (mb + static_cast<int64_t>(k) * GATHER_ROWS < p.M) {
-        gv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + j0);
-        if (rot) pv[k] = *reinterpret_cast<const uint4*>(src + roff[k] + pj0);
-      }
-    }
-  }
+  // table rows are rh + 2 entries apart: 16-byte aligned, and the fill's
+  // token-strided stores fall in distinct bank pairs
+  const int tab_ld = rh + 2;
   if (rh > 0) {
     const int tid = threadIdx.y * 32 + threadIdx.x;
+    const int64_t t_blk = mblk % p.T;  // position of the block's first token
     for (int e = tid; e < rh * GATHER_TOKENS; e += 32 * GATHER_ROWS) {
       const int f = e / GATHER_TOKENS, r = e - f * GATHER_TOKENS;
-      const int64_t m = mblk + r;
-      if (m < p.M) tab[r * rh + f] = __ldg(p.rope_cs + f * p.T + m % p.T);
+      if (mblk + r < p.M) {
+        int64_t t = t_blk + r;
+        if (t >= p.T) t = p.T >= GATHER_TOKENS ? t - p.T : t % p.T;
+        tab[r * tab_ld + f] = __ldg(p.rope_cs + f * p.T + t);
+      }
     }
     __syncthreads();
   }
@@ -612,25 +610,20 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
     const int64_t m = mb + static_cast<int64_t>(k) * GATHER_ROWS;
     if (m >= p.M) continue;
     const int t = tt[k];
+    // pre-transposed k is [B*kv, hd, T]
+    const int64_t hrow = (m / p.T) * nh + head;
     float g[8], gp[8];
-    if constexpr (VEC) {
-      unpack8(gv[k], g);
-      unpack8(pv[k], gp);
-    } else {
-      // lane by lane: pre-transposed k is [B*kv, hd, T]; or rh < 8
-      const int64_t hrow = (m / p.T) * nh + head;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = j0 + i;
-        const int jp = j < rh ? j + rh : j - rh;
-        const int64_t ij = kt ? (hrow * p.hd + j) * p.T + t : roff[k] + j;
-        const int64_t ip = kt ? (hrow * p.hd + jp) * p.T + t : roff[k] + jp;
-        g[i] = bf16_bits_to_float(src[ij]);
-        gp[i] = (rot && j < 2 * rh) ? bf16_bits_to_float(src[ip]) : 0.0f;
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int j = j0 + i;
+      const int jp = j < rh ? j + rh : j - rh;
+      const int64_t ij = kt ? (hrow * p.hd + j) * p.T + t : roff[k] + j;
+      const int64_t ip = kt ? (hrow * p.hd + jp) * p.T + t : roff[k] + jp;
+      g[i] = bf16_bits_to_float(src[ij]);
+      gp[i] = (rot && j < 2 * rh) ? bf16_bits_to_float(src[ip]) : 0.0f;
     }
     if (rot) {
-      const float2* cs = tab + (threadIdx.y + k * GATHER_ROWS) * rh;
+      const float2* cs = tab + (threadIdx.y + k * GATHER_ROWS) * tab_ld;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int j = j0 + i;
@@ -650,16 +643,172 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
     for (int i = 0; i < 8; ++i) sum[i] += g[i];
   }
   if (!p.db) return;  // uniform across the block
-#pragma unroll
-  for (int i = 0; i < 8; ++i) part[threadIdx.y][threadIdx.x][i] = sum[i];
+  float4* mine = reinterpret_cast<float4*>(part[threadIdx.y][threadIdx.x]);
+  mine[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
+  mine[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
   __syncthreads();
   if (threadIdx.y == 0 && active) {
+    float acc[8] = {};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float acc = 0.0f;
+    for (int r = 0; r < GATHER_ROWS; ++r) {
+      const float4* q = reinterpret_cast<const float4*>(part[r][threadIdx.x]);
+      const float4 a = q[0], b = q[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
 #pragma unroll
-      for (int r = 0; r < GATHER_ROWS; ++r) acc += part[r][threadIdx.x][i];
-      atomicAdd(p.db + p.F + col0 + i, acc);
+    for (int i = 0; i < 8; ++i) atomicAdd(p.db + p.F + col0 + i, acc[i]);
+  }
+}
+
+// 16-byte path. Every head's hd columns split into hd / 16 items of 16
+// columns: for a rotated head (q, k with rh > 0) items 0 .. rh/8 - 1 are the
+// rotation pairs (j .. j+7, j+rh .. j+rh+7), j = 8 i, and the rest pairs of
+// adjacent groups past the rotated part; for v (or no rotation) every item is
+// two adjacent groups. Heads lie side by side in G's q|k|v columns in both
+// column orders, so item k covers G columns F + 16 k .. with a per-item offset
+// of its second group. Needs hd % 16 == 0, rh % 8 == 0, k not pre-transposed.
+// XW items per token row of threads (32 or 16), 256 / XW token rows, TPT
+// tokens per thread.
+template <int XW, int TPT>
+__global__ void __launch_bounds__(256, TPT == 4 ? 3 : 2)
+    bwd_gather_pairs_kernel(const BwdGatherParams p) {
+  constexpr int ROWS = 256 / XW;
+  constexpr int TOKENS = ROWS * TPT;
+  // the block's slice of the rotary table ([64 tokens][rope_half + 2]), then
+  // (after a barrier) the token rows' column sums [ROWS][XW threads][16]
+  extern __shared__ __align__(16) float2 tab[];
+  const int hd = p.hd, rh = p.rope_half;
+  const int per_head = hd / 16;
+  const int n_items = (p.N - p.F) / 16;
+  const int item = blockIdx.x * XW + threadIdx.x;
+  const bool active = item < n_items;
+  const int hall = active ? item / per_head : 0;  // head in G's q|k|v order
+  const int i = item - hall * per_head;
+  int seg, head;
+  if (p.groups > 0) {
+    const int qpk = p.heads / p.groups;
+    const int g = hall / (qpk + 2), slot = hall - g * (qpk + 2);
+    seg = slot < qpk ? 0 : slot == qpk ? 1 : 2;
+    head = slot < qpk ? g * qpk + slot : g;
+  } else {
+    seg = hall / p.heads;
+    head = hall - seg * p.heads;
+  }
+  const int nrot = seg < 2 ? rh / 8 : 0;  // rotation pairs in this head
+  const bool rot = i < nrot;
+  const int ja = rot ? 8 * i : 16 * nrot + 16 * (i - nrot);  // first group's column
+  const int jb = rot ? ja + rh : ja + 8;                     // second group's column
+  const uint16_t* src = static_cast<const uint16_t*>(seg == 0 ? p.g_q : seg == 1 ? p.g_k : p.g_v);
+  const int nh = seg == 0 ? p.heads : (p.groups > 0 ? p.groups : p.heads);
+  uint16_t* const Gcol = static_cast<uint16_t*>(p.G) + p.F + static_cast<int64_t>(hall) * hd;
+  const int64_t mblk = static_cast<int64_t>(blockIdx.y) * TOKENS;
+  const int64_t mb = mblk + threadIdx.y;
+  // all TPT tokens' loads before the table fill: batch element and position
+  // walked from one division
+  uint4 va[TPT], vb[TPT];
+  {
+    int64_t bb = mb / p.T;
+    int64_t t = mb - bb * p.T;
+#pragma unroll
+    for (int k = 0; k < TPT; ++k) {
+      va[k] = make_uint4(0, 0, 0, 0);
+      vb[k] = make_uint4(0, 0, 0, 0);
+      if (active && mb + static_cast<int64_t>(k) * ROWS < p.M) {
+        const uint16_t* row = src + ((bb * nh + head) * p.T + t) * hd;
+        va[k] = *reinterpret_cast<const uint4*>(row + ja);
+        vb[k] = *reinterpret_cast<const uint4*>(row + jb);
+      }
+      t += ROWS;
+      while (t >= p.T) {
+        t -= p.T;
+        ++bb;
+      }
+    }
+  }
+  // rows rh + 2 entries apart: 16-byte aligned, and the fill's token-strided
+  // stores fall in distinct bank pairs
+  const int tab_ld = rh + 2;
+  if (rh > 0) {
+    const int tid = threadIdx.y * XW + threadIdx.x;
+    const int64_t t_blk = mblk % p.T;
+    for (int e = tid; e < rh * TOKENS; e += 256) {
+      const int f = e / TOKENS, r = e - f * TOKENS;
+      if (mblk + r < p.M) {
+        int64_t t = t_blk + r;
+        if (t >= p.T) t = p.T >= TOKENS ? t - p.T : t % p.T;
+        tab[r * tab_ld + f] = __ldg(p.rope_cs + f * p.T + t);
+      }
+    }
+    __syncthreads();
+  }
+  float sa[8], sb[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) sa[q] = sb[q] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < TPT; ++k) {
+    const int64_t m = mb + static_cast<int64_t>(k) * ROWS;
+    if (!active || m >= p.M) continue;
+    float a[8], b[8];
+    unpack8(va[k], a);
+    unpack8(vb[k], b);
+    if (rot) {
+      // (cos, sin) of frequencies ja .. ja + 7: the transpose of the rotation,
+      // a' = a c + b s, b' = b c - a s
+      const float4* c4 =
+          reinterpret_cast<const float4*>(tab + (threadIdx.y + k * ROWS) * tab_ld + ja);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 c = c4[q];
+        const float a0 = a[2 * q], b0 = b[2 * q], a1 = a[2 * q + 1], b1 = b[2 * q + 1];
+        a[2 * q] = fmaf(a0, c.x, b0 * c.y);
+        b[2 * q] = fmaf(b0, c.x, -a0 * c.y);
+        a[2 * q + 1] = fmaf(a1, c.z, b1 * c.w);
+        b[2 * q + 1] = fmaf(b1, c.z, -a1 * c.w);
+      }
+    }
+    uint16_t* const grow = Gcol + m * p.N;
+    *reinterpret_cast<uint4*>(grow + ja) =
+        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                   pack_bf16x2(a[6], a[7]));
+    *reinterpret_cast<uint4*>(grow + jb) =
+        make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]),
+                   pack_bf16x2(b[6], b[7]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      sa[q] += a[q];
+      sb[q] += b[q];
+    }
+  }
+  if (!p.db) return;  // uniform across the block
+  // column sums: the table slice is dead, its space takes the partial sums
+  if (rh > 0) __syncthreads();
+  float4* part = reinterpret_cast<float4*>(tab);
+  float4* mine = part + (threadIdx.y * XW + threadIdx.x) * 4;
+  mine[0] = make_float4(sa[0], sa[1], sa[2], sa[3]);
+  mine[1] = make_float4(sa[4], sa[5], sa[6], sa[7]);
+  mine[2] = make_float4(sb[0], sb[1], sb[2], sb[3]);
+  mine[3] = make_float4(sb[4], sb[5], sb[6], sb[7]);
+  __syncthreads();
+  if (threadIdx.y == 0 && active) {
+    float acc[16] = {};
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      const float4* q4 = part + (r * XW + threadIdx.x) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = q4[q];
+        acc[4 * q] += v.x;
+        acc[4 * q + 1] += v.y;
+        acc[4 * q + 2] += v.z;
+        acc[4 * q + 3] += v.w;
+      }
+    }
+    float* const dcol = p.db + p.F + static_cast<int64_t>(hall) * hd;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      atomicAdd(dcol + ja + q, acc[q]);
+      atomicAdd(dcol + jb + q, acc[8 + q]);
     }
   }
 }
@@ -683,14 +832,55 @@ cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_cta
 cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
   const int nq = p.N - p.F;
   if (nq <= 0 || p.M == 0) return cudaSuccess;
-  const dim3 grid((nq / 8 + 31) / 32,
-                  static_cast<unsigned>((p.M + GATHER_TOKENS - 1) / GATHER_TOKENS));
-  const size_t smem = static_cast<size_t>(p.rope_half) * GATHER_TOKENS * sizeof(float2);
-  if (smem > 48 * 1024) return cudaErrorInvalidValue;  // rope_half <= 64 (head_dim <= 128)
-  if (!p.k_transposed && p.rope_half % 8 == 0)
-    bwd_gather_kernel<true><<<grid, dim3(32, GATHER_ROWS), smem, stream>>>(p);
-  else
-    bwd_gather_kernel<false><<<grid, dim3(32, GATHER_ROWS), smem, stream>>>(p);
+  if (!p.k_transposed && p.rope_half % 8 == 0 && p.hd % 16 == 0 && nq % 16 == 0) {
+    // 16-byte path: 32 items a row of threads; 16 when there is no rotary
+    // table and the count is an odd multiple of 16 (with a table, 16-wide
+    // blocks fill twice the table per thread and share it over half the
+    // heads: walrus 74 us against 66 us for 32-wide blocks, the last of them
+    // half idle); 4 tokens a thread when 8 would leave fewer than 8 blocks per
+    // SM
+    const int n_items = nq / 16;
+    const int xw = p.rope_half == 0 && n_items % 32 == 16 ? 16 : 32;
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 152;
+    }
+    const int64_t x_blocks = (n_items + xw - 1) / xw;
+    const int64_t tok8 = (256 / xw) * 8;
+    const int tpt = x_blocks * ((p.M + tok8 - 1) / tok8) < 8LL * sms ? 4 : 8;
+    const int64_t tokens = (256 / xw) * tpt;
+    const dim3 grid2(static_cast<unsigned>(x_blocks),
+                     static_cast<unsigned>((p.M + tokens - 1) / tokens));
+    // shared memory: the table slice, later the 16 column sums of 256 threads
+    const size_t tab_bytes =
+        p.rope_half > 0 ? static_cast<size_t>(p.rope_half + 2) * tokens * sizeof(float2) : 0;
+    const size_t smem = std::max<size_t>(tab_bytes, 256 * 16 * sizeof(float));
+    auto go = [&](auto kernel) {
+      if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+      }
+      kernel<<<grid2, dim3(xw, 256 / xw), smem, stream>>>(p);
+      return cudaSuccess;
+    };
+    cudaError_t e;
+    if (xw == 32)
+      e = tpt == 8 ? go(bwd_gather_pairs_kernel<32, 8>) : go(bwd_gather_pairs_kernel<32, 4>);
+    else
+      e = tpt == 8 ? go(bwd_gather_pairs_kernel<16, 8>) : go(bwd_gather_pairs_kernel<16, 4>);
+    if (e != cudaSuccess) return e;
+  } else {
+    const dim3 grid((nq / 8 + 31) / 32,
+                    static_cast<unsigned>((p.M + GATHER_TOKENS - 1) / GATHER_TOKENS));
+    const size_t tab_bytes =
+        p.rope_half > 0 ? static_cast<size_t>(p.rope_half + 2) * GATHER_TOKENS * sizeof(float2) : 0;
+    if (tab_bytes > 48 * 1024) return cudaErrorInvalidValue;  // rope_half <= 64 (head_dim <= 128)
+    bwd_gather_kernel<<<grid, dim3(32, GATHER_ROWS), tab_bytes, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

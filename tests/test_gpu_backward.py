@@ -41,6 +41,11 @@ SMALL = [
        72, rope_n_elem=16, n_query_groups=2),
     W_("bwd_k_transposed", (2, 3, 64, 8, 16, 1), 2, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 10000.0,
        True, "bf16", 73, k_transposed=True),
+    # rotated half-width 2: the lane-by-lane gather
+    W_("bwd_rope_n4", (2, 90, 64), 2, 1, 64, 0, 2, 32, A.ACT_NONE, 10000.0, True, "bf16", 74,
+       rope_n_elem=4),
+    # head_dim 16, fully rotated: one rotation-pair item per head
+    W_("bwd_hd16_rope", (2, 150, 64), 2, 1, 64, 0, 4, 16, A.ACT_NONE, 10000.0, True, "bf16", 75),
 ]
 
 
