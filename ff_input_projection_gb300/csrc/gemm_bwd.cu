@@ -529,6 +529,30 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   }
 }
 
+// The block's slice of the frequency-major rotary table, token-major in
+// shared memory (row r = the block's token r, tab_ld entries apart). Thread
+// tid of 256 always fills token tid % TOKENS, frequencies tid / TOKENS,
+// + 256 / TOKENS, ...: consecutive threads read consecutive tokens of one
+// frequency row, and the wrap of the position and the source address are
+// worked out once.
+template <int TOKENS>
+__device__ __forceinline__ void fill_table_slice(float2* tab, int tab_ld, const float2* cs,
+                                                 int64_t T, int64_t M, int64_t mblk, int rh,
+                                                 int tid) {
+  static_assert(256 % TOKENS == 0, "a whole number of frequencies per pass");
+  constexpr int FSTEP = 256 / TOKENS;
+  const int r = tid % TOKENS;
+  if (mblk + r >= M) return;
+  int64_t t = mblk % T + r;
+  if (t >= T) t = T >= TOKENS ? t - T : t % T;
+  const int f0 = tid / TOKENS;
+  const float2* src = cs + f0 * T + t;
+  float2* dst = tab + r * tab_ld + f0;
+  const int64_t sstep = FSTEP * T;
+#pragma unroll 4
+  for (int f = f0; f < rh; f += FSTEP, src += sstep, dst += FSTEP) *dst = __ldg(src);
+}
+
 __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const BwdGatherParams p) {
   __shared__ __align__(16) float part[GATHER_ROWS][32][8];
   // the block's slice of the frequency-major rotary table, token-major here
@@ -593,16 +617,8 @@ __global__ void __launch_bounds__(32 * GATHER_ROWS, 2) bwd_gather_kernel(const B
   // token-strided stores fall in distinct bank pairs
   const int tab_ld = rh + 2;
   if (rh > 0) {
-    const int tid = threadIdx.y * 32 + threadIdx.x;
-    const int64_t t_blk = mblk % p.T;  // position of the block's first token
-    for (int e = tid; e < rh * GATHER_TOKENS; e += 32 * GATHER_ROWS) {
-      const int f = e / GATHER_TOKENS, r = e - f * GATHER_TOKENS;
-      if (mblk + r < p.M) {
-        int64_t t = t_blk + r;
-        if (t >= p.T) t = p.T >= GATHER_TOKENS ? t - p.T : t % p.T;
-        tab[r * tab_ld + f] = __ldg(p.rope_cs + f * p.T + t);
-      }
-    }
+    fill_table_slice<GATHER_TOKENS>(tab, tab_ld, p.rope_cs, p.T, p.M, mblk, rh,
+                                    threadIdx.y * 32 + threadIdx.x);
     __syncthreads();
   }
 #pragma unroll
@@ -730,16 +746,8 @@ __global__ void __launch_bounds__(256, TPT == 4 ? 3 : 2)
   // stores fall in distinct bank pairs
   const int tab_ld = rh + 2;
   if (rh > 0) {
-    const int tid = threadIdx.y * XW + threadIdx.x;
-    const int64_t t_blk = mblk % p.T;
-    for (int e = tid; e < rh * TOKENS; e += 256) {
-      const int f = e / TOKENS, r = e - f * TOKENS;
-      if (mblk + r < p.M) {
-        int64_t t = t_blk + r;
-        if (t >= p.T) t = p.T >= TOKENS ? t - p.T : t % p.T;
-        tab[r * tab_ld + f] = __ldg(p.rope_cs + f * p.T + t);
-      }
-    }
+    fill_table_slice<TOKENS>(tab, tab_ld, p.rope_cs, p.T, p.M, mblk, rh,
+                             threadIdx.y * XW + threadIdx.x);
     __syncthreads();
   }
   float sa[8], sb[8];
