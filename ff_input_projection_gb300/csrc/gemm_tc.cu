@@ -533,26 +533,6 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           bulk_commit();
         }
       };
-      // the two halves of a rotated pair: [32 rows][16 lanes] blocks at 0 and
-      // 1 KB of one staging buffer, one fence, two stores in one group
-      auto stage_store_pair = [&](const CUtensorMap* map, int ca, int cb, int c1, int c2,
-                                  const uint32_t (&wa)[8], const uint32_t (&wb)[8]) {
-        const uint32_t stg = staging_warp + (stage_sel & 1) * 2048;
-        ++stage_sel;
-        if (lane == 0) bulk_wait_read_1();  // this buffer's previous store group has read it
-        __syncwarp();
-        st_shared_v4(stg + lane * 32 + swz, wa[0], wa[1], wa[2], wa[3]);
-        st_shared_v4(stg + lane * 32 + (swz ^ 16u), wa[4], wa[5], wa[6], wa[7]);
-        st_shared_v4(stg + 1024 + lane * 32 + swz, wb[0], wb[1], wb[2], wb[3]);
-        st_shared_v4(stg + 1024 + lane * 32 + (swz ^ 16u), wb[4], wb[5], wb[6], wb[7]);
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(map, stg, ca, c1, c2);
-          tma_store_3d(map, stg + 1024, cb, c1, c2);
-          bulk_commit();
-        }
-      };
       if (tc.n0 + cols <= e.F && (cols & 31) == 0) {
         // ---- a tile inside the ff block: activation, then [M, F] row-major,
         // 32 columns per work unit (the tile's width is a multiple of 32)
@@ -652,16 +632,10 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               uint32_t lo_u[16], hi_u[16];
               tmem_ld16(t_head + j, lo_u);
               tmem_ld16(t_head + j + rh, hi_u);
-              // frequency-major tables: lane (token t) reads entry (f, t) at f * T + t,
-              // so a warp's 32 consecutive tokens read one contiguous run per f; the
-              // plan's table is fetched into L1 while the accumulator loads are in flight
-              const float2* const csf = e.rope_cs + t + j * e.T;
-              if (!e.rope_per_lane) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) prefetch_l1(csf + i * e.T);
-              }
               tmem_wait_ld();
               uint32_t lo_w[8], hi_w[8];
+              // frequency-major tables: lane (token t) reads entry (f, t) at f * T + t,
+              // so a warp's 32 consecutive tokens read one contiguous run per f
               if (e.rope_per_lane) {
                 const float4* t4 = e.rope_cs4 + t + j * e.T;
 #pragma unroll
@@ -679,6 +653,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                   asm volatile("" ::: "memory");
                 }
               } else {
+                const float2* csf = e.rope_cs + t + j * e.T;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   // (cos, sin) of frequencies j + 2i and j + 2i + 1
@@ -690,7 +665,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                   hi_w[i] = pack_bf16x2(y0 * ca.x + x0 * ca.y, y1 * cb.x + x1 * cb.y);
                 }
               }
-              stage_store_pair(map, j, j + rh, static_cast<int>(t), z, lo_w, hi_w);
+              stage_store(map, j, static_cast<int>(t), z, true, lo_w);
+              stage_store(map, j + rh, static_cast<int>(t), z, true, hi_w);
             }
             j0 = 2 * rh;  // lanes past the rotated ones pass through
           }

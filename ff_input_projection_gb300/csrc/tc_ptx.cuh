@@ -310,11 +310,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-// fetch the line holding *ptr into L1 (no register written)
-__device__ __forceinline__ void prefetch_l1(const void* ptr) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
