@@ -953,6 +953,7 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   base.wait_limit_ns = p->wait_limit_ns;
   base.launch_tag = tag;
   base.k_splits = 1;
+  base.cluster = 1;
   const int mps = static_cast<int>((pr.tk.S_in + fp::kTcBM - 1) / fp::kTcBM);
   const int ctas = p->max_ctas > 0 ? std::min(sm_count(p->device), p->max_ctas) : sm_count(p->device);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1039,6 +1040,8 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
     ++launches;
   }
+  // CTA pairs for the dx GEMM (the plan's cluster option), whole clusters
+  const int bwd_cl = p->cluster == 2 && ctas >= 2 ? 2 : 1;
   // 3. dx = G W^T, stored in x's layout (dx^T = W G^T when tokens are innermost)
   {
     fp::BwdGemmParams gp = base;
@@ -1048,28 +1051,33 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     gp.num_k_blocks = (N + fp::kTcBK - 1) / fp::kTcBK;
     if (!pr.a_mn) {
       gp.mode = fp::BWD_DX;
-      if (encode_g_map(encode, &gp.tmap_a, workspace, pr, N, N, 64, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-        return map_fail("G");
-      if (encode_2d(encode, &gp.tmap_b, W, BF, 2, N, C, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) !=
-          CUDA_SUCCESS)
-        return map_fail("W");
       gp.m_tiles_per_slab = mps;
       gp.num_m_tiles = static_cast<int>(pr.tk.n_outer) * mps;
       gp.num_n_tiles = (C + fp::kTcBN - 1) / fp::kTcBN;
-    } else {
-      gp.mode = fp::BWD_DXT;
-      if (encode_2d(encode, &gp.tmap_a, W, BF, 2, N, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
-          CUDA_SUCCESS)
-        return map_fail("W");
-      if (encode_g_map(encode, &gp.tmap_b, workspace, pr, N, N, 64, 256,
+      gp.cluster = gp.num_m_tiles >= 2 ? bwd_cl : 1;
+      if (encode_g_map(encode, &gp.tmap_a, workspace, pr, N, N, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return map_fail("G");
+      // B: this CTA's share of the tile's 256 channel rows
+      if (encode_2d(encode, &gp.tmap_b, W, BF, 2, N, C, 64, fp::kTcBN / gp.cluster,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return map_fail("W");
+    } else {
+      gp.mode = fp::BWD_DXT;
       gp.num_m_tiles = (C + fp::kTcBM - 1) / fp::kTcBM;
       gp.n_tiles_per_slab = static_cast<int>((pr.tk.S_in + fp::kTcBN - 1) / fp::kTcBN);
       gp.num_n_tiles = static_cast<int>(pr.tk.n_outer) * gp.n_tiles_per_slab;
+      gp.cluster = gp.num_m_tiles >= 2 ? bwd_cl : 1;
+      if (encode_2d(encode, &gp.tmap_a, W, BF, 2, N, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
+          CUDA_SUCCESS)
+        return map_fail("W");
+      // B: this CTA's share of the tile's 256 token rows
+      if (encode_g_map(encode, &gp.tmap_b, workspace, pr, N, N, 64, fp::kTcBN / gp.cluster,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return map_fail("G");
     }
-    gp.num_units = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
+    gp.num_units = static_cast<int64_t>((gp.num_m_tiles + gp.cluster - 1) / gp.cluster) *
+                   gp.num_n_tiles;
     cudaError_t err = fp::launch_bwd_gemm(gp, false, ctas, stream);
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
     ++launches;
@@ -1089,26 +1097,33 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
       return map_fail("dW");
     gp.num_m_tiles = (C + fp::kTcBM - 1) / fp::kTcBM;
     gp.num_n_tiles = (N + fp::kTcBN - 1) / fp::kTcBN;
+    // single CTAs: on CTA pairs this GEMM measured slower (walrus 148 -> 163 us,
+    // the LLM shape 630 -> 733 us) while the dx GEMMs gained
+    gp.cluster = 1;
     gp.k_blocks_per_slab = static_cast<int>((pr.tk.S_in + fp::kTcBK - 1) / fp::kTcBK);
     const int64_t kb = pr.tk.n_outer * gp.k_blocks_per_slab;
     if (kb > INT32_MAX) return fail(FP_ERR_UNSUPPORTED_LAYOUT, "too many tokens");
     gp.num_k_blocks = static_cast<int>(kb);
-    const int64_t tiles = static_cast<int64_t>(gp.num_m_tiles) * gp.num_n_tiles;
-    // k splits: at least one full wave of work items, and the count whose
-    // waves are fullest (a last, partly idle wave costs a whole wave); ties
-    // take fewer splits (less reduce-add traffic)
-    // Large outputs are not split (each split adds a read-modify-write of dW),
-    // and every split keeps at least 16 k-blocks.
+    // work items are (row-tile group of `cluster`, column tile, split); a wave
+    // is one item per cluster
+    const int64_t tiles =
+        static_cast<int64_t>((gp.num_m_tiles + gp.cluster - 1) / gp.cluster) * gp.num_n_tiles;
+    const int64_t slots = std::max<int64_t>(1, ctas / gp.cluster);
+    // k splits: counting up from one item per cluster, the first count whose
+    // waves are at least 97 % full (a last, partly idle wave costs a whole
+    // one), else the fullest; ties take fewer splits (less reduce-add
+    // traffic). Large outputs are not split (each split adds a
+    // read-modify-write of dW), and every split keeps at least 16 k-blocks.
     int64_t splits = 1;
     double best_fill = -1.0;
-    const int64_t max_splits = tiles >= 4 * static_cast<int64_t>(ctas)
+    const int64_t max_splits = tiles >= 4 * slots
                                    ? 1
                                    : std::max<int64_t>(1, std::min<int64_t>(kb / 16, 32));
-    for (int64_t sp = std::min(max_splits, std::max<int64_t>(1, (ctas + tiles - 1) / tiles));
+    for (int64_t sp = std::min(max_splits, std::max<int64_t>(1, (slots + tiles - 1) / tiles));
          sp <= max_splits; ++sp) {
       const int64_t units = tiles * sp;
       const double fill = static_cast<double>(units) /
-                          static_cast<double>((units + ctas - 1) / ctas * ctas);
+                          static_cast<double>((units + slots - 1) / slots * slots);
       if (fill > best_fill + 1e-9) {
         best_fill = fill;
         splits = sp;

@@ -36,21 +36,42 @@ namespace fp {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int NUM_EPI_WARPS = 8;  // 2 per TMEM lane quarter
 constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
-constexpr int A_BYTES = BM * BK * 2;           // 16 KB
-constexpr int B_BYTES = BN * BK * 2;           // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB: this CTA's 128 rows
 constexpr int CHUNK_BYTES = 64 * BK * 2;       // one [64 k][64 mn] MN-major chunk, 8 KB
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 // per epilogue warp, two 2 KB buffers staging [32 rows][64 B] for TMA stores
 constexpr int STAGING_BYTES_PER_WARP = 2 * 2048;
 constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// Per cluster size. A single CTA holds the tile's 128 rows and all 256
+// columns of B (48 KB a k-step, 4 stages). A CTA pair runs 2-SM MMAs
+// (M = 256): each CTA holds its own 128 rows and its own 128 of the 256 B
+// columns, 32 KB a k-step, so the same shared memory keeps 6 k-steps in flight.
+template <int CL>
+struct BwdCfg {
+  static constexpr int B_COLS = BN / CL;
+  static constexpr int B_BYTES = B_COLS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = CL == 2 ? 6 : 4;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARS * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// The odd CTA of a pair: a 3-D tiled load into its own shared memory whose
+// bytes complete on an mbarrier of the even CTA (`bar`, a cluster address).
+__device__ __forceinline__ void tma_load_3d_peer(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {
@@ -86,26 +107,33 @@ struct Geo {
   int r0;        // first row when rows are channels (DXT, DW)
   int c0;        // first column: ff column (GRADFF), channel (DX), fused column (DW)
   int kb0, kb1;  // k-block range
+  bool phantom;  // row tile past the end (odd row-tile count in a pair): compute, store nothing
 };
 
-// Work item -> tile. Groups of group_m row tiles sweep the column tiles, rows
-// fastest, so concurrently resident CTAs share operand tiles in L2. For DW
-// the k splits of one tile are num_m_tiles * num_n_tiles items apart.
-__device__ __forceinline__ Geo unit_geo(const BwdGemmParams& p, int64_t u64) {
+// Work item -> this CTA's tile. A cluster of CL CTAs takes CL consecutive row
+// tiles with the same column tile (they share its B tile). Groups of group_m
+// row tiles sweep the column tiles, rows fastest, so concurrently resident
+// CTAs share operand tiles in L2. For DW the k splits of one tile are
+// (row-tile groups of CL) * num_n_tiles items apart.
+template <int CL>
+__device__ __forceinline__ Geo unit_geo(const BwdGemmParams& p, int64_t u64, int rank) {
   const uint32_t u = static_cast<uint32_t>(u64);
-  const uint32_t tiles = static_cast<uint32_t>(p.num_m_tiles) * p.num_n_tiles;
+  const uint32_t m_units = (static_cast<uint32_t>(p.num_m_tiles) + CL - 1) / CL;
+  const uint32_t tiles = m_units * p.num_n_tiles;
   const uint32_t split = u / tiles;
   const uint32_t t = u - split * tiles;
-  const uint32_t gsz = static_cast<uint32_t>(p.group_m);
+  const uint32_t gsz = p.group_m >= CL ? static_cast<uint32_t>(p.group_m) / CL : 1u;
   const uint32_t per_group = gsz * p.num_n_tiles;
   const uint32_t g = t / per_group;
   const uint32_t first = g * gsz;
-  const uint32_t left = p.num_m_tiles - first;
+  const uint32_t left = m_units - first;
   const uint32_t gm = left < gsz ? left : gsz;
   const uint32_t rr = t - g * per_group;
   const uint32_t n_tile = rr / gm;
-  const uint32_t m_tile = first + (rr - n_tile * gm);
+  const uint32_t m_raw = (first + (rr - n_tile * gm)) * CL + rank;
   Geo q;
+  q.phantom = m_raw >= static_cast<uint32_t>(p.num_m_tiles);
+  const uint32_t m_tile = q.phantom ? static_cast<uint32_t>(p.num_m_tiles) - 1 : m_raw;
   q.o = q.s0 = q.r0 = q.c0 = 0;
   q.kb0 = 0;
   q.kb1 = p.num_k_blocks;
@@ -144,8 +172,16 @@ __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32])
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN, int ACT>
+// CL: CTAs per cluster. With CL == 2 the even CTA issues 2-SM MMAs (M = 256)
+// reading each CTA's own 128 rows and each CTA's half of the B tile; the odd
+// CTA's copies complete on the even CTA's full barriers, which the even CTA's
+// producer arms for both halves; commits go to both CTAs' barriers; the odd
+// CTA's epilogue releases the accumulator on the even CTA's barrier.
+template <int MODE, bool A_MN, bool B_MN, int ACT, int CL>
 __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__ BwdGemmParams p) {
+  using G = BwdCfg<CL>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -158,10 +194,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + STAGES * STAGE_BYTES + STAGING_BYTES +
-                                                    NUM_BARS * 8);
+                                                    G::NUM_BARS * 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl wc{p.status, p.wait_limit_ns, p.launch_tag};
+  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t first_unit = blockIdx.x / CL;
+  const int64_t unit_step = gridDim.x / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -170,7 +209,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+      mbar_init(tempty_bar(b), CL * NUM_EPI_WARPS);  // every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -179,14 +218,24 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
     prefetch_tmap(&p.tmap_b);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // a pair allocates collectively: one warp of each CTA, 512 columns in each
+    if constexpr (CL == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // the peer signals our barriers only after they exist
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // everything above touches no global memory: it overlaps the previous
@@ -201,8 +250,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Geo g = unit_geo(p, u);
+      const bool peer = CL > 1 && rank != 0;
+      const int bcol = rank * G::B_COLS;  // first of the B tile's columns this CTA holds
+      for (int64_t u = first_unit; u < p.num_units && ok; u += unit_step) {
+        const Geo g = unit_geo<CL>(p, u, rank);
         int oc[3];
         if (MODE != BWD_DW) outer_coords(p.tok, g.o, oc);
         // DW walks K over tokens: (slab, block in slab) advances incrementally and
@@ -219,11 +270,31 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          // the even CTA's full barrier takes both CTAs' bytes
+          const uint32_t fb = peer ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+          if (!peer) mbar_arrive_expect_tx(fb, CL * STAGE_BYTES);
           const uint32_t a_dst = sbase + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           const int k0 = kb * BK;
+          auto ld2 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+            if (peer)
+              tma_load_2d_peer(dst, map, fb, c0, c1);
+            else
+              tma_load_2d(dst, map, fb, c0, c1);
+          };
+          auto ld3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+            if (peer)
+              tma_load_3d_peer(dst, map, fb, c0, c1, c2);
+            else
+              tma_load_3d(dst, map, fb, c0, c1, c2);
+          };
+          auto ld5 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                         int c4) {
+            if (peer)
+              tma_load_5d_peer(dst, map, fb, c0, c1, c2, c3, c4);
+            else
+              tma_load_5d(dst, map, fb, c0, c1, c2, c3, c4);
+          };
           if (MODE == BWD_GRADFF) {
             if (A_MN) {
               tma_load_5d(a_dst, &p.tmap_a, fb, g.s0, k0, oc[0], oc[1], oc[2]);
@@ -235,27 +306,28 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
             for (int j = 0; j < BN / 64; ++j)
               tma_load_2d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, g.c0 + 64 * j, k0);
           } else if (MODE == BWD_DX) {
-            tma_load_3d(a_dst, &p.tmap_a, fb, k0, g.s0, g.o);   // G rows (tokens), K = N
-            tma_load_2d(b_dst, &p.tmap_b, fb, k0, g.c0);        // W rows (channels), K = N
+            ld3(a_dst, &p.tmap_a, k0, g.s0, g.o);       // G rows (tokens), K = N
+            ld2(b_dst, &p.tmap_b, k0, g.c0 + bcol);     // W rows (channels), K = N
           } else if (MODE == BWD_DXT) {
-            tma_load_2d(a_dst, &p.tmap_a, fb, k0, g.r0);        // W rows (channels)
-            tma_load_3d(b_dst, &p.tmap_b, fb, k0, g.s0, g.o);   // G rows (tokens)
+            ld2(a_dst, &p.tmap_a, k0, g.r0);            // W rows (channels)
+            ld3(b_dst, &p.tmap_b, k0, g.s0 + bcol, g.o);  // G rows (tokens)
           } else {
             // K = tokens: block kb_in of slab ok_slab
             const int sk = kb_in * BK;
             if (A_MN) {  // token-major x: channels contiguous
-              tma_load_5d(a_dst, &p.tmap_a, fb, g.r0, sk, ock[0], ock[1], ock[2]);
-              tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, g.r0 + 64, sk, ock[0], ock[1],
-                          ock[2]);
+              ld5(a_dst, &p.tmap_a, g.r0, sk, ock[0], ock[1], ock[2]);
+              ld5(a_dst + CHUNK_BYTES, &p.tmap_a, g.r0 + 64, sk, ock[0], ock[1], ock[2]);
             } else {     // channels-first x: tokens contiguous
-              tma_load_5d(a_dst, &p.tmap_a, fb, sk, g.r0, ock[0], ock[1], ock[2]);
+              ld5(a_dst, &p.tmap_a, sk, g.r0, ock[0], ock[1], ock[2]);
             }
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(b_dst + j * CHUNK_BYTES, &p.tmap_b, fb, g.c0 + 64 * j, sk, ok_slab);
+            for (int j = 0; j < G::B_COLS / 64; ++j)
+              ld3(b_dst + j * CHUNK_BYTES, &p.tmap_b, g.c0 + bcol + 64 * j, sk, ok_slab);
           }
-          armed_mask |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (!peer) {
+            armed_mask |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -267,19 +339,32 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
           }
         }
       }
+      // drain: this CTA's copies land before it exits. The even CTA waits on
+      // the barriers it armed (an armed phase whose peer half never came runs
+      // out after 10 ms: nothing is then in flight). The odd CTA's copies
+      // complete on the even CTA's barriers, which the even CTA's MMA thread
+      // waits for in a normal run; after an abort the odd CTA allows its last
+      // copies a bounded grace period instead.
+      const WaitCtl dc{wc.status, wc.limit_ns < 10000000ull ? wc.limit_ns : 10000000ull,
+                       wc.launch_tag};
       for (int s = 0; s < STAGES; ++s)
-        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, wc, false);
+        if (armed_mask & (1u << s)) wait_bounded(full_bar(s), (armed_parity >> s) & 1u, dc, false);
+      if (peer && !ok) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000ull) {
+        }
+      }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 && rank == 0) {
+    // ------------------------------------------------ MMA issuer (the even CTA's)
     if (lane == 0) {
-      const uint32_t idesc = make_idesc(A_MN, B_MN, BM, BN);
+      const uint32_t idesc = make_idesc(A_MN, B_MN, BM * CL, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool issued = false;
       int it = 0;
-      for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-        const Geo g = unit_geo(p, u);
+      for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
+        const Geo g = unit_geo<CL>(p, u, rank);
         const int buf = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!wait_bounded(tempty_bar(buf), acc_phase ^ 1u, wc, true)) break;
@@ -300,24 +385,24 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
                                          : sw128_desc(a_addr + k * 32, 16, 1024);
             const uint64_t b_desc = B_MN ? sw128_desc(b_addr + k * 2048, CHUNK_BYTES, 1024)
                                          : sw128_desc(b_addr + k * 32, 16, 1024);
-            umma_bf16<1>(d_tmem, a_desc, b_desc, idesc, (kb != g.kb0 || k != 0) ? 1u : 0u);
+            umma_bf16<CL>(d_tmem, a_desc, b_desc, idesc, (kb != g.kb0 || k != 0) ? 1u : 0u);
           }
           issued = true;
-          umma_commit<1>(empty_bar(stage));
+          umma_commit_all<CL>(empty_bar(stage));  // frees the stage in every CTA of the pair
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit<1>(tfull_bar(buf));
+        umma_commit_all<CL>(tfull_bar(buf));  // accumulators ready for both CTAs' epilogues
       }
       if (issued) {
-        umma_commit<1>(drain_bar);
+        umma_commit<CL>(drain_bar);  // all MMAs retired before TMEM is freed
         wait_bounded(drain_bar, 0, wc, false);
       }
     }
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
     const int part = (warp - 2) >> 2;  // 0 or 1: which of every 2 units
@@ -340,13 +425,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
       __syncwarp();
       return stg;
     };
-    for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+    for (int64_t u = first_unit; u < p.num_units; u += unit_step, ++it) {
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       const int okw = wait_bounded(tfull_bar(buf), acc_phase, wc, true) ? 1 : 0;
       if (!__all_sync(0xFFFFFFFFu, okw)) break;
       tc_fence_after();
-      const Geo g = unit_geo(p, u);
+      const Geo g = unit_geo<CL>(p, u, rank);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
       int oc[3];
       if (MODE != BWD_DW) outer_coords(p.tok, g.o, oc);
@@ -361,7 +446,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
           tmem_ld16(t_row + c, v);
           tmem_wait_ld();
           // a store never starts past the tensor (loads may; stores are clipped, not skipped)
-          if (g.c0 + c >= p.N || g.r0 + row0 >= p.C) continue;
+          if (g.phantom || g.c0 + c >= p.N || g.r0 + row0 >= p.C) continue;
           const uint32_t stg = stage_rows(v);
           if (lane == 0) {
             tma_reduce_add_2d(&p.tmap_out, stg, g.c0 + c, g.r0 + row0);
@@ -380,6 +465,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
           tmem_ld32(t_row + c, v);
           tmem_wait_ld();
           // a store never starts past the tensor (its far edge is clipped by TMA)
+          if (g.phantom) continue;
           if (MODE == BWD_GRADFF && (g.c0 + c >= p.F || g.s0 + row0 >= p.tok.S_in)) continue;
           if (MODE == BWD_DX && (g.c0 + c >= p.C || g.s0 + row0 >= p.tok.S_in)) continue;
           if (MODE == BWD_DXT && (g.s0 + c >= p.tok.S_in || g.r0 + row0 >= p.C)) continue;
@@ -444,7 +530,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      // release the accumulator: the even CTA's MMA thread waits on every
+      // epilogue warp of the pair
+      if (lane == 0) {
+        if (CL == 1 || rank == 0)
+          mbar_arrive(tempty_bar(buf));
+        else
+          mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));
+      }
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -452,40 +545,55 @@ __global__ void __launch_bounds__(NT, 1) bwd_gemm_kernel(const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer may still write into its shared memory or
+  // arrive on its barriers
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    if constexpr (CL == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN, int ACT>
+template <int MODE, bool A_MN, bool B_MN, int ACT, int CL = 1>
 cudaError_t launch_one(const BwdGemmParams& p, int num_ctas, cudaStream_t stream) {
-  auto kernel = bwd_gemm_kernel<MODE, A_MN, B_MN, ACT>;
+  static_assert(MODE != BWD_GRADFF || CL == 1, "the ff-gradient fallback runs single CTAs");
+  auto kernel = bwd_gemm_kernel<MODE, A_MN, B_MN, ACT, CL>;
+  constexpr int smem = BwdCfg<CL>::SMEM_BYTES;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
-  int ctas = num_ctas;
-  if (static_cast<int64_t>(ctas) > p.num_units) ctas = static_cast<int>(p.num_units);
-  if (ctas < 1) ctas = 1;
+  // whole clusters, no more than there are work items (a unit is one cluster's)
+  int64_t ctas = num_ctas / CL * CL;
+  if (ctas > p.num_units * CL) ctas = p.num_units * CL;
+  if (ctas < CL) ctas = CL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
   err = cudaLaunchKernelEx(&cfg, kernel, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
@@ -829,11 +937,18 @@ cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_cta
     case BWD_GRADFF:
       return a_mn_major ? launch_gradff<true>(p, num_ctas, stream)
                         : launch_gradff<false>(p, num_ctas, stream);
-    case BWD_DX: return launch_one<BWD_DX, false, false, ACT_NONE>(p, num_ctas, stream);
-    case BWD_DXT: return launch_one<BWD_DXT, false, false, ACT_NONE>(p, num_ctas, stream);
+    case BWD_DX:
+      return p.cluster == 2 ? launch_one<BWD_DX, false, false, ACT_NONE, 2>(p, num_ctas, stream)
+                            : launch_one<BWD_DX, false, false, ACT_NONE, 1>(p, num_ctas, stream);
+    case BWD_DXT:
+      return p.cluster == 2 ? launch_one<BWD_DXT, false, false, ACT_NONE, 2>(p, num_ctas, stream)
+                            : launch_one<BWD_DXT, false, false, ACT_NONE, 1>(p, num_ctas, stream);
     default:
-      return a_mn_major ? launch_one<BWD_DW, true, true, ACT_NONE>(p, num_ctas, stream)
-                        : launch_one<BWD_DW, false, true, ACT_NONE>(p, num_ctas, stream);
+      if (p.cluster == 2)
+        return a_mn_major ? launch_one<BWD_DW, true, true, ACT_NONE, 2>(p, num_ctas, stream)
+                          : launch_one<BWD_DW, false, true, ACT_NONE, 2>(p, num_ctas, stream);
+      return a_mn_major ? launch_one<BWD_DW, true, true, ACT_NONE, 1>(p, num_ctas, stream)
+                        : launch_one<BWD_DW, false, true, ACT_NONE, 1>(p, num_ctas, stream);
   }
 }
 
