@@ -46,6 +46,10 @@ SMALL = [
        rope_n_elem=4),
     # head_dim 16, fully rotated: one rotation-pair item per head
     W_("bwd_hd16_rope", (2, 150, 64), 2, 1, 64, 0, 4, 16, A.ACT_NONE, 10000.0, True, "bf16", 75),
+    # channels-first, three 128-channel row tiles: the dx^T GEMM on CTA pairs
+    # with a phantom tile in the second pair, ragged token tiles
+    W_("bwd_cf_c384", (2, 384, 10, 16, 1), 1, 1, 384, 128, 6, 64, A.ACT_SILU, 10000.0, True,
+       "bf16", 76),
 ]
 
 
