@@ -961,7 +961,9 @@ cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
     // blocks fill twice the table per thread and share it over half the
     // heads: walrus 74 us against 66 us for 32-wide blocks, the last of them
     // half idle); 4 tokens a thread when 8 would leave fewer than 8 blocks per
-    // SM
+    // SM, or when the table has 64 or more frequencies (its fill and shared
+    // memory grow with the tokens of a block: the LLM shape's gather, rh 64,
+    // 91 us at 8 tokens against 79 us at 4; walrus, rh 32, 53 against 80)
     const int n_items = nq / 16;
     const int xw = p.rope_half == 0 && n_items % 32 == 16 ? 16 : 32;
     static int sms = 0;
@@ -973,7 +975,8 @@ cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream) {
     }
     const int64_t x_blocks = (n_items + xw - 1) / xw;
     const int64_t tok8 = (256 / xw) * 8;
-    const int tpt = x_blocks * ((p.M + tok8 - 1) / tok8) < 8LL * sms ? 4 : 8;
+    const int tpt =
+        x_blocks * ((p.M + tok8 - 1) / tok8) < 8LL * sms || p.rope_half >= 64 ? 4 : 8;
     const int64_t tokens = (256 / xw) * tpt;
     const dim3 grid2(static_cast<unsigned>(x_blocks),
                      static_cast<unsigned>((p.M + tokens - 1) / tokens));
