@@ -100,7 +100,7 @@ struct BwdGemmParams {
   int k_blocks_per_slab;    // DW: ceil(S_in / 64)
   int k_splits;             // DW: the token range is split this many ways
   int64_t num_units;        // work items: (row-tile group of `cluster`, column tile, k split)
-  int cluster;              // CTAs per cluster sharing one B tile (1, or 2: DX/DXT, DW)
+  int cluster;              // CTAs per cluster sharing one B tile (1; 2 for DX/DXT)
   int group_m;
   int C, F, N, act;
   const void* bias;         // GRADFF: [N] bf16 or null
