@@ -29,6 +29,10 @@ struct fp_plan {
   int64_t table_T;   // T of the default-position table held in d_table (-1: none)
   cudaStream_t table_stream;  // stream that last wrote the table
   cudaEvent_t table_ready;    // recorded after that write
+  // backward: the q/k/v gather runs beside the ff-gradient GEMM on this stream,
+  // forked from and joined back to the caller's stream by the two events
+  cudaStream_t side_stream;
+  cudaEvent_t ev_fork, ev_join;
   int last_launches;
   uint64_t wait_limit_ns;
   int inject_stall;
@@ -477,7 +481,7 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
                             CU_TENSOR_MAP_L2_PROMOTION_NONE,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
       }
-      tp.tma_store = okm ? 1 : 0;
+      tp.tma_store = okm && ta.M <= INT32_MAX ? 1 : 0;  // TMA coordinates are 32-bit
     }
     tp.tok = tk;
     tp.epi = e;
@@ -592,6 +596,9 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->table_T = -1;
   p->table_stream = nullptr;
   p->table_ready = nullptr;
+  p->side_stream = nullptr;
+  p->ev_fork = nullptr;
+  p->ev_join = nullptr;
   p->last_launches = 0;
   p->wait_limit_ns = 2000000000ull;
   p->inject_stall = 0;
@@ -618,6 +625,9 @@ void fp_destroy(fp_plan* plan) {
     if (plan->d_status) cudaFree(plan->d_status);
     if (plan->d_table) cudaFree(plan->d_table);
     if (plan->table_ready) cudaEventDestroy(plan->table_ready);
+    if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
+    if (plan->ev_join) cudaEventDestroy(plan->ev_join);
+    if (plan->side_stream) cudaStreamDestroy(plan->side_stream);
     if (prev >= 0) cudaSetDevice(prev);
   }
   delete plan;
@@ -917,8 +927,9 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
 
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const int tag = static_cast<int>(p->launch_seq);
-  // 1. q|k|v part of G
-  if (p->heads > 0) {
+  // 1. q|k|v part of G (launched in step 2: beside the ff gradient when that
+  // runs on the tensor-core forward kernel, else before it)
+  auto launch_gather = [&](cudaStream_t gs) -> fp_status {
     fp::BwdGatherParams gp{};
     gp.g_q = g_q;
     gp.g_k = g_k;
@@ -936,10 +947,11 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     gp.groups = p->groups;
     gp.rope_half = pr.rh;
     gp.k_transposed = p->k_transposed;
-    cudaError_t err = fp::launch_bwd_gather(gp, stream);
+    cudaError_t err = fp::launch_bwd_gather(gp, gs);
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "gradient gather launch: %s", cudaGetErrorString(err));
     ++launches;
-  }
+    return FP_OK;
+  };
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
   if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   fp::BwdGemmParams base{};
@@ -964,7 +976,34 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   // CTA pairs of the forward kernel in its gradient mode when every tile is a
   // whole number of 32-column units; the single-CTA backward kernel otherwise.
   const int64_t fwd_m_tiles = pr.tk.n_outer * mps;
-  if (F > 0 && F % 32 == 0 && fwd_m_tiles >= 2) {
+  // (TMA coordinates are 32-bit: the gradient mode's stores need M < 2^31)
+  const bool tc_grad = F > 0 && F % 32 == 0 && fwd_m_tiles >= 2 && M <= INT32_MAX;
+  // The gather (HBM-bound) and the ff gradient (tensor- and latency-bound)
+  // write disjoint columns of G and of db. With both present the ff gradient
+  // runs on all but kGatherSMs SMs and the gather on a second stream fills
+  // the rest: a gradient CTA holds nearly all of an SM's shared memory, so
+  // no gather block lands beside it. The gradient is launched first so its
+  // CTAs claim their SMs before the gather's blocks are queued. SMs left to
+  // the gather, walrus backward: 12 -> 470 us, 24 -> 465, 36 -> 462, 48 -> 469
+  // (471 with the two in sequence).
+  constexpr int kGatherSMs = 36;
+  const bool fork = tc_grad && p->heads > 0 && ctas >= kGatherSMs + 16;
+  if (p->heads > 0 && !fork) {
+    st = launch_gather(stream);
+    if (st != FP_OK) return st;
+  }
+  if (fork) {
+    if (!p->side_stream &&
+        cudaStreamCreateWithFlags(&p->side_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "side stream creation failed");
+    if ((!p->ev_fork && cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess) ||
+        (!p->ev_join && cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess))
+      return fail(FP_ERR_CUDA, "event creation failed");
+    if (cudaEventRecord(p->ev_fork, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(p->side_stream, p->ev_fork, 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "forking the gather stream failed");
+  }
+  if (tc_grad) {
     fp::TcParams tp;
     memset(&tp, 0, sizeof tp);
     if (encode_x_map(encode, &tp.tmap_a, x, pr, C, pr.a_mn, 64, pr.a_mn ? 64 : 128,
@@ -1013,9 +1052,17 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     tp.wait_limit_ns = p->wait_limit_ns;
     tp.inject_stall = p->inject_stall;
     tp.launch_tag = tag;
-    cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, ctas, stream, true);
+    cudaError_t err = fp::launch_tc_gemm(tp, pr.a_mn, fork ? (ctas - kGatherSMs) & ~1 : ctas,
+                                         stream, true);
     if (err != cudaSuccess) return fail(FP_ERR_CUDA, "backward GEMM launch: %s", cudaGetErrorString(err));
     ++launches;
+    if (fork) {
+      st = launch_gather(p->side_stream);
+      if (st != FP_OK) return st;
+      if (cudaEventRecord(p->ev_join, p->side_stream) != cudaSuccess ||
+          cudaStreamWaitEvent(stream, p->ev_join, 0) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "joining the gather stream failed");
+    }
   } else if (F > 0) {
     fp::BwdGemmParams gp = base;
     gp.mode = fp::BWD_GRADFF;
