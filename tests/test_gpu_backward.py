@@ -127,3 +127,26 @@ def test_backward_rejects_f32(cuda_ok):
         proj.backward(x, to_device(inp["W"], "f32"), None,
                       tuple(to_device(grads[k], "f32") for k in ("ff", "q", "k", "v")),
                       channel_dim=w.channel_dim)
+
+
+@pytest.mark.parametrize("max_ctas,cluster", [(40, 2), (152, 1), (7, 2)],
+                         ids=["ctas40", "single_cta", "ctas7"])
+def test_backward_launch_shapes(max_ctas, cluster, cuda_ok):
+    """Other launch shapes than the default grid: with fewer than 52 CTAs the
+    gather runs before the ff gradient on one stream instead of beside it; with
+    the cluster option at 1 the dx and dW GEMMs run on single CTAs; an odd CTA
+    cap rounds the pair grids down to whole clusters."""
+    w = W_("bwd_shapes", (2, 3, 64, 16, 16, 1), 2, 1, 64, 128, 2, 32, A.ACT_GELU_ERF, 10000.0,
+           True, "bf16", 77)
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+    pos = (np.arange(w.T, dtype=np.int32) * 5 + 1) % 997
+    inp = {**inp, "pos": pos}
+    proj = _proj(w)
+    proj.set_option(fpx.FP_OPT_MAX_CTAS, max_ctas)
+    proj.set_option(fpx.FP_OPT_CLUSTER, cluster)
+    dx, dW, db = run_backward(w, inp, grads, proj=proj, pos=pos)
+    ref = oracle.backward_workload(w, inp, grads)
+    assert_close(dx, ref["dx"], "bf16", "dx")
+    assert_close(dW, ref["dW"], "bf16", "dW")
+    assert_close(db, ref["db"], "f32", "db")
