@@ -225,7 +225,12 @@ fp_status fp_backward_workspace_size(const fp_plan* plan, const fp_layout* x_lay
  * are sums whose order varies between runs (atomic adds across CTAs), so they
  * are reproducible to rounding, not bit for bit. Inputs must stay valid until
  * the work completes; nothing is allocated except, on first use, the plan's
- * status word and rotary table (as fp_forward). Returns FP_OK once enqueued.
+ * status word and rotary table (as fp_forward) and, when both the ff
+ * gradient and the q/k/v gather run, a second stream and two events of the
+ * plan: the gather runs there beside the ff gradient, forked from `stream`
+ * and joined back to it before the dx GEMM, so the call's work still
+ * completes in `stream` order. A plan's calls are issued from one host
+ * thread at a time. Returns FP_OK once enqueued.
  */
 fp_status fp_backward(fp_plan* plan, const void* x, const fp_layout* x_layout, const void* W,
                       const void* b, const int32_t* pos, const void* g_ff, const void* g_q,
