@@ -879,19 +879,26 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   Prepared pr;
   fp_status st = prepare(*p, a, pr);
   if (st != FP_OK) return st;
-  if (!pr.tc_path)
+  if (xl->dtype != FP_BF16)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "the backward takes bf16 activations");
+  const int N = pr.N, C = p->C, F = p->F;
+  const int64_t M = pr.ta.M;
+  if (M > 0 && !pr.tc_path)
     return fail(FP_ERR_UNSUPPORTED_LAYOUT,
                 "the backward runs on the tensor-core path only (bf16, head_dim and ff_hidden "
                 "multiples of 16, x addressable by TMA)");
-  if (!dx || !dW) return fail(FP_ERR_INVALID_ARG, "dx and dW are required");
-  const int N = pr.N, C = p->C, F = p->F;
-  const int64_t M = pr.ta.M;
+  if (!dW || (M > 0 && !dx)) return fail(FP_ERR_INVALID_ARG, "dx and dW are required");
   const void* ptrs[] = {dx, dW, db, workspace};
   for (const void* q : ptrs)
     if (q && !aligned16(q)) return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(FP_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   if (M == 0) {
+    // no tokens: the gradients of W and b are zero, dx is empty
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
+        (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess))
+      return fail(FP_ERR_CUDA, "clearing dW / db failed");
     p->last_launches = 0;
     return ok();
   }

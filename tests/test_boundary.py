@@ -123,6 +123,34 @@ def test_create_ex_grouped_query(lib):
     fpx.fp_destroy(h)
 
 
+def test_backward_rejects_on_host(lib):
+    """fp_backward's argument checks run on the host, before any CUDA call."""
+    h = _plan()  # C 64, F 64, 4 heads of 16: N = 256
+    L = _cf_layout()  # 2 x 64 tokens
+    st, need = fpx.fp_backward_workspace_size(h, L)
+    assert st == fpx.FP_OK and need == 128 * 256 * 2  # G [M, N] bf16, 256-byte rounded
+    DX, DW, DB, WS = (0x30000000 + i * 0x1000000 for i in range(4))
+
+    def bwd(plan=h, L=L, dx=DX, dW=DW, ws=WS, wsb=need):
+        return fpx.fp_backward(plan, X, L, WP, BP, None, O1, O2, O3, O4, dx, dW, DB, ws, wsb, None)
+
+    assert bwd(plan=None) == fpx.FP_ERR_INVALID_ARG
+    assert bwd(dx=None) == fpx.FP_ERR_INVALID_ARG
+    assert bwd(dW=None) == fpx.FP_ERR_INVALID_ARG
+    assert bwd(dx=DX + 2) == fpx.FP_ERR_MISALIGNED
+    assert bwd(ws=WS + 16) == fpx.FP_ERR_MISALIGNED       # workspace wants 256 bytes
+    assert bwd(wsb=need - 256) == fpx.FP_ERR_INVALID_ARG  # workspace too small
+    assert "workspace" in fpx.fp_last_error()
+    assert bwd(L=_cf_layout(dtype=fpx.FP_F32)) == fpx.FP_ERR_UNSUPPORTED_LAYOUT
+    st, _ = fpx.fp_backward_workspace_size(None, L)
+    assert st == fpx.FP_ERR_INVALID_ARG
+    E = fpx.make_layout([0, 64, 8, 8], [4096, 64, 8, 1], 1, 1, fpx.FP_BF16)
+    st, need0 = fpx.fp_backward_workspace_size(h, E)
+    assert st == fpx.FP_OK and need0 == 0
+    assert bwd(L=E, dW=None) == fpx.FP_ERR_INVALID_ARG  # dW is written even with no tokens
+    fpx.fp_destroy(h)
+
+
 def test_empty_input_is_a_no_op(lib):
     h = _plan()
     L = fpx.make_layout([0, 64, 8, 8], [4096, 64, 8, 1], 1, 1, fpx.FP_BF16)

@@ -150,3 +150,19 @@ def test_backward_launch_shapes(max_ctas, cluster, cuda_ok):
     assert_close(dx, ref["dx"], "bf16", "dx")
     assert_close(dW, ref["dW"], "bf16", "dW")
     assert_close(db, ref["db"], "f32", "db")
+
+
+def test_backward_empty_input_zeroes_dw_db(cuda_ok):
+    """No tokens: dx is empty, dW and db come back zero (they are overwritten)."""
+    w = W_("bwd_empty", (0, 64, 8, 8), 1, 1, 64, 64, 4, 16, A.ACT_GELU_ERF, 0.0, True, "bf16", 78)
+    proj = _proj(w)
+    x = torch.empty((0, 64, 8, 8), dtype=torch.bfloat16, device="cuda")
+    W = torch.randn((64, proj.N), device="cuda").to(torch.bfloat16)
+    b = torch.randn((proj.N,), device="cuda").to(torch.bfloat16)
+    g = (torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"),) + tuple(
+        torch.empty((0, 64, 16), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    dx, dW, db = proj.backward(x, W, b, g, channel_dim=1)
+    torch.cuda.synchronize()
+    assert dx.numel() == 0
+    assert torch.count_nonzero(dW).item() == 0 and torch.count_nonzero(db).item() == 0
+    assert proj.last_launch_count == 0
