@@ -221,7 +221,9 @@ fp_status fp_backward_workspace_size(const fp_plan* plan, const fp_layout* x_lay
  *   workspace                device buffer of fp_backward_workspace_size bytes,
  *                            256-byte aligned, owned by the caller
  * Runs on the tensor cores for bf16 layouts the forward's tcgen05 kernel
- * takes; other layouts and f32 return FP_ERR_UNSUPPORTED_LAYOUT. dW and db
+ * takes; other layouts and f32 return FP_ERR_UNSUPPORTED_LAYOUT. With no
+ * tokens nothing is launched: dx (which may then be NULL) is empty and dW and
+ * db are set to zero. dW and db
  * are sums whose order varies between runs (atomic adds across CTAs), so they
  * are reproducible to rounding, not bit for bit. Inputs must stay valid until
  * the work completes; nothing is allocated except, on first use, the plan's
