@@ -50,6 +50,11 @@ SMALL = [
     # with a phantom tile in the second pair, ragged token tiles
     W_("bwd_cf_c384", (2, 384, 10, 16, 1), 1, 1, 384, 128, 6, 64, A.ACT_SILU, 10000.0, True,
        "bf16", 76),
+    # sequences shorter than a gather block's tokens: positions wrap several
+    # times inside one block (16-byte gather, then the lane-by-lane one)
+    W_("bwd_short_seq", (7, 20, 128), 2, 1, 128, 0, 2, 64, A.ACT_NONE, 10000.0, True, "bf16", 79),
+    W_("bwd_short_seq_n4", (9, 11, 64), 2, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 500.0, True, "bf16",
+       80, rope_n_elem=4),
 ]
 
 
