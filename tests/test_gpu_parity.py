@@ -39,6 +39,10 @@ SMALL = [
     W_("fp32_rope_silu", (2, 24, 6, 10), 1, 1, 24, 36, 2, 12, A.ACT_SILU, 10000.0, True, "f32", 31),
     W_("fp32_rowmajor", (3, 50, 48), 2, 1, 48, 96, 3, 16, A.ACT_GELU_ERF, 10000.0, True, "f32", 32),
     W_("one_token", (1, 1, 64), 2, 1, 64, 64, 1, 64, A.ACT_GELU_ERF, 10000.0, True, "bf16", 33),
+    # tensor-core path with sequences shorter than a tile and a warp: rows of one
+    # tile span several batch elements, head stores leave the whole-head path
+    W_("short_seq_tc", (7, 20, 128), 2, 1, 128, 128, 2, 64, A.ACT_GELU_ERF, 10000.0, True, "bf16",
+       81),
     W_("k_tail_c48", (2, 70, 48), 2, 1, 48, 0, 1, 48, A.ACT_NONE, 0.0, True, "bf16", 34),
     # bf16 shapes the TMA path cannot describe run on the FFMA kernel
     W_("bf16_odd_spatial", (2, 64, 5, 7), 1, 1, 64, 64, 2, 32, A.ACT_GELU_ERF, 10000.0, True,
