@@ -12,7 +12,9 @@
 //            bwd_gather_kernel for the layouts it does not cover; CUDA cores);
 //   GRADFF   G[:, :F] = g_ff * act'(x W_ff + b_ff): the pre-activation is
 //            recomputed by a forward GEMM whose epilogue multiplies the
-//            upstream gradient by the activation's derivative;
+//            upstream gradient by the activation's derivative (the forward
+//            kernel's gradient mode when F is a multiple of 32, else this
+//            file's GEMM kernel);
 //   DX/DXT   dx = G W^T. For token-major x the tile rows are tokens; for
 //            channels-first x the kernel computes dx^T = W G^T, whose rows are
 //            channels and whose columns are contiguous tokens, so either way
@@ -22,10 +24,11 @@
 // db is the column sum of G, accumulated by the gather kernel and the GRADFF
 // epilogue (a 31-shuffle butterfly per warp, one atomic add per column).
 //
-// The GEMM kernel is a persistent single-CTA tcgen05 pipeline (M = 128,
-// N = 256, K = 64 per stage, 4 stages, two TMEM accumulators): warp 0 loads,
-// one thread of warp 1 issues tcgen05.mma, warps 2-9 drain the accumulators.
-// Every wait is bounded as in the forward kernel.
+// The GEMM kernel is a persistent tcgen05 pipeline with two TMEM accumulators:
+// warp 0 loads, one thread of warp 1 issues tcgen05.mma, warps 2-9 drain the
+// accumulators. It runs on single CTAs (M = 128, N = 256, K = 64 per stage, 4
+// stages of 48 KB) or, for DX and DXT, on CTA pairs (2-SM MMAs with M = 256,
+// 6 stages of 32 KB per CTA). Every wait is bounded as in the forward kernel.
 #include <algorithm>
 
 #include "epilogue.cuh"
