@@ -11,17 +11,20 @@
 // [batch*heads, tokens, head_dim] layout).
 //
 // Structure (one persistent CTA per SM, 14 warps; CTA pairs by default):
-//   warp 0     TMA producer: loads x and W tiles into a shared ring (6 stages
-//              of 32 KB in a pair, 4 of 48 KB alone), and each tile's bias
+//   warp 0     TMA producer: loads x and W tiles into a shared ring (5 stages
+//              of 32 KB in a pair, 3 of 48 KB alone), and each tile's bias
 //              row into a bias operand
 //   warp 1     allocates 512 TMEM columns; in the even CTA one thread issues
 //              tcgen05.mma (2-SM M=256 or 1-SM M=128; N=256, K=16, bf16 in,
 //              fp32 accumulate) and commits completion to mbarriers
 //   warps 2-13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //              per thread), activation / rotation in registers, bf16
-//              round-to-nearest-even, TMA tensor stores of 32 x 16 blocks
+//              round-to-nearest-even, TMA tensor stores of 32 x 32 (ff) and
+//              32 x 16 (q/k/v) blocks
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the
-// epilogue of tile i overlaps the main loop of tile i+1.
+// epilogue of tile i overlaps the main loop of tile i+1. In its gradient mode
+// the same kernel computes the backward's ff part, g_ff * act'(x W + b), with
+// column sums into db.
 //
 // The bias enters through the tensor core: each tile starts with one K=16 MMA
 // (accumulate off) whose A operand is a constant atom with 0.5 in k-row 0 and
