@@ -20,6 +20,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "attn_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
@@ -31,6 +32,9 @@ MUTATIONS = {
     "pos_global": 10, "rope_on_v": 11, "qk_swapped": 12, "gelu_scale": 13,
     "relu2_unsquared": 14,
 }
+# planted mistakes of the attention oracle
+ATTN_MUTATIONS = {"no_merge_rescale": 1, "no_scale": 2, "k_index_swap": 3,
+                  "softmax_over_queries": 4, "sum_not_rescaled": 5}
 # planted mistakes of the backward
 BWD_MUTATIONS = {
     "bwd_rope_forward": 21, "bwd_act_value": 22, "bwd_no_recompute_bias": 23,
@@ -41,11 +45,11 @@ BWD_MUTATIONS = {
 def build(force: bool = False) -> str:
     """Compile fp_oracle.c into liboracle.so (plain C, no CUDA)."""
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
-           _SRC, "-o", tmp, "-lm"]
+           *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -66,6 +70,9 @@ def _load():
         g.restype = ctypes.c_int
         g.argtypes = [P, I, I, P, P, I, I, P, P, P, P, P, I, I, I, I, I, I, I, I,
                       ctypes.c_double, P, P, P, P, I, P, I64, P, I64, P, P, P, I, I]
+        h = lib.oracle_attention
+        h.restype = ctypes.c_int
+        h.argtypes = [P, P, P, I, I64, I64, I64, I, I, ctypes.c_double, I64, I64, P, I, I]
         _lib = lib
     return _lib
 
@@ -229,3 +236,35 @@ def backward_workload(w, inputs: Dict[str, np.ndarray], grads: Dict[str, np.ndar
                     pos=inputs.get("pos"), rope_cos=inputs.get("rope_cos"),
                     rope_sin=inputs.get("rope_sin"), groups=w.n_query_groups,
                     rope_n_elem=w.rope_n_elem, k_transposed=w.k_transposed, **kw)
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, dtype: str,
+              k_transposed: bool = False, scale: Optional[float] = None,
+              q_chunk: Optional[int] = None, kv_chunk: Optional[int] = None,
+              threads: Optional[int] = None, mutate: int = 0) -> np.ndarray:
+    """Attention over the projection's outputs, in fp64 (attn_oracle.c).
+
+    ``q`` [BH, Tq, hd], ``k`` [BH, Tk, hd] (or [BH, hd, Tk] with
+    ``k_transposed``), ``v`` [BH, Tk, hd], stored values (uint16 bf16 bits or
+    float32). ``scale`` defaults to hd**-0.5; ``q_chunk`` / ``kv_chunk`` default
+    to one chunk (the page's fast paths). Returns [BH, Tq, hd] float64.
+    """
+    lib = _load()
+    is_bf16 = dtype == "bf16"
+    want = np.uint16 if is_bf16 else np.float32
+    qc, kc, vc = (np.ascontiguousarray(a) for a in (q, k, v))
+    for a in (qc, kc, vc):
+        if a.dtype != want:
+            raise TypeError(f"inputs must be {want}")
+    BH, Tq, hd = qc.shape
+    Tk = kc.shape[2] if k_transposed else kc.shape[1]
+    if scale is None:
+        scale = hd ** -0.5
+    out = np.zeros((BH, Tq, hd))
+    rc = lib.oracle_attention(_ptr(qc), _ptr(kc), _ptr(vc), int(is_bf16), BH, Tq, Tk, hd,
+                              int(bool(k_transposed)), float(scale),
+                              int(q_chunk or max(Tq, 1)), int(kv_chunk or Tk), _ptr(out),
+                              int(threads or os.cpu_count() or 1), int(mutate))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
