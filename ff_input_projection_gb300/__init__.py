@@ -34,10 +34,11 @@ FP_OPT_INJECT_STALL = 2
 FP_OPT_GROUP_M = 3
 FP_OPT_MAX_CTAS = 4
 FP_OPT_CLUSTER = 5
+FP_OPT_BOUNDS_CHECK = 6
 
 # the C ABI's entry points, as declared in include/fp.h
 EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_rope_table",
-           "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward",
+           "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward", "fp_attention",
            "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
@@ -102,6 +103,8 @@ def load():
     lib.fp_backward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P, P, P, P,
                                 ctypes.c_size_t, P]
     lib.fp_backward.restype = I
+    lib.fp_attention.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, P]
+    lib.fp_attention.restype = I
     lib.fp_reserve.argtypes = [P, I64]
     lib.fp_reserve.restype = I
     lib.fp_get_device_status.argtypes = [P, P]
@@ -182,11 +185,17 @@ def fp_backward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
                               dW, db, workspace, workspace_bytes, stream)
 
 
+def fp_attention(plan: int, q: int, k: int, v: int, out: int, batch: int, T_q: int, T_k: int,
+                 scale: float, stream: Optional[int]) -> int:
+    return load().fp_attention(plan, q, k, v, out, batch, T_q, T_k, scale, stream)
+
+
 def fp_reserve(plan: int, max_tokens_per_batch: int) -> int:
     return load().fp_reserve(plan, max_tokens_per_batch)
 
 
-def fp_get_device_status(plan: int, stream: Optional[int]) -> int:
+def fp_get_device_status(plan: Optional[int], stream: Optional[int]) -> int:
+    """plan None: the status words of fp_forward_noalloc on the current device."""
     return load().fp_get_device_status(plan, stream)
 
 
@@ -343,6 +352,33 @@ class FusedProjection:
             st = fp_forward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
                             ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
         check(st)
+        return out
+
+    def attention(self, q, k, v, *, batch: int, scale: float = 0.0, out=None, stream=None):
+        """Softmax attention over this plan's q, k, v outputs (k pre-transposed when
+        the plan emits it so). Returns out [batch*heads, T_q, head_dim], bf16, on
+        torch's current stream."""
+        import torch
+        for t in (q, k, v):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != q.device:
+                raise ValueError("q, k, v must be contiguous bfloat16 tensors on one device")
+        hd = self.head_dim
+        if q.dim() != 3 or q.shape[0] != batch * self.heads or q.shape[2] != hd:
+            raise ValueError(f"q must be [{batch * self.heads}, T_q, {hd}]")
+        T_q = q.shape[1]
+        kvn = batch * self.kv_heads
+        T_k = v.shape[1]
+        k_want = (kvn, hd, T_k) if self.k_transposed else (kvn, T_k, hd)
+        if tuple(v.shape) != (kvn, T_k, hd) or tuple(k.shape) != k_want:
+            raise ValueError(f"k must be {k_want} and v {(kvn, T_k, hd)}")
+        if out is None:
+            out = torch.empty_like(q)
+        elif tuple(out.shape) != tuple(q.shape) or not out.is_contiguous() or out.dtype != q.dtype:
+            raise ValueError("out must be a contiguous tensor shaped like q")
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+        check(fp_attention(self.plan, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           batch, T_q, T_k, scale, stream))
         return out
 
     def backward(self, x, W, b, grads, pos=None, *, channel_dim: int, n_batch_dims: int = 1,

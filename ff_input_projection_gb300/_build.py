@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfp.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_bwd.cu", "gemm_simt.cu", "rope_table.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_bwd.cu", "gemm_simt.cu", "rope_table.cu", "attention.cu"]
 HEADERS = ["fp_internal.h", "epilogue.cuh", "tc_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -5,6 +5,7 @@
 // adds none). Checks run on the host before any CUDA call, so a rejected call
 // has launched nothing.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -13,6 +14,9 @@
 #include <new>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
+
+#include <vector>
 
 #include "../../include/fp.h"
 #include "fp_internal.h"
@@ -39,10 +43,31 @@ struct fp_plan {
   int group_m;
   int max_ctas;
   int cluster;  // CTAs per cluster on the tensor-core path (1 or 2)
+  int bounds_check;  // FP_OPT_BOUNDS_CHECK
   uint32_t launch_seq;
+  // Scratch grown inside a call is allocated in stream order on that call's
+  // stream (scratch_stream); scratch_ready is recorded there after the growth,
+  // and calls on other streams wait for it. Tables it replaced may still be
+  // read by queued work, so they are kept here until fp_destroy or fp_reserve.
+  cudaStream_t scratch_stream;
+  cudaEvent_t scratch_ready;
+  bool scratch_pending;
+  std::vector<void*> retired;
 };
 
 namespace {
+
+// Launch knobs shared by plans (their defaults) and the no-allocation entry point.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+constexpr int kDefaultGroupM = 32;   // M-tiles per rasterisation group
+constexpr int kDefaultCluster = 2;   // CTA pairs on the tensor-core path
+
+// NVTX range over one entry-point call (visible in Nsight timelines; a no-op
+// when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 thread_local char g_err[512];
 
@@ -139,36 +164,81 @@ TokAxes analyse_tokens(const fp_layout& L) {
   return ta;
 }
 
-fp_status ensure_device_state(fp_plan* p, int64_t table_entries) {
+// Make `stream` wait for `ev`. Inside a stream capture an event recorded
+// outside the capture is waited on as an external event node, which is legal
+// there and orders graph replays after the recorded work.
+cudaError_t wait_event(cudaStream_t stream, cudaEvent_t ev) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+  return cudaStreamWaitEvent(stream, ev,
+                             cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0);
+}
+
+// Grows the plan's device scratch (status words, rotary table) to hold
+// `table_entries` (cos, sin) pairs. Inside a call (`in_stream` true) nothing
+// synchronises: the memory comes from cudaMallocAsync and is cleared by
+// cudaMemsetAsync on `stream`, scratch_ready is recorded after it, and a table
+// it replaces is retired (queued work on any stream may still read it). From
+// fp_reserve (`in_stream` false) the growth completes before returning and
+// retired tables are freed once the device is idle.
+fp_status ensure_device_state(fp_plan* p, int64_t table_entries, cudaStream_t stream,
+                              bool in_stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
   if (p->d_status && p->device != dev)
     return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
                 p->device, dev);
+  const cudaStream_t s = in_stream ? stream : nullptr;
+  bool grew = false;
   if (!p->d_status) {
-    int* s = nullptr;
-    if (cudaMalloc(&s, 2 * sizeof(int)) != cudaSuccess)
+    void* st = nullptr;
+    if (cudaMallocAsync(&st, 2 * sizeof(int), s) != cudaSuccess)
       return fail(FP_ERR_OUT_OF_MEMORY, "status word allocation failed");
-    if (cudaMemset(s, 0, 2 * sizeof(int)) != cudaSuccess) {
-      cudaFree(s);
+    if (cudaMemsetAsync(st, 0, 2 * sizeof(int), s) != cudaSuccess) {
+      cudaFreeAsync(st, s);
       return fail(FP_ERR_CUDA, "status word initialisation failed");
     }
-    p->d_status = s;
+    p->d_status = static_cast<int*>(st);
     p->device = dev;
+    grew = true;
   }
   if (table_entries > p->table_cap) {
-    float2* t = nullptr;
-    if (cudaMalloc(&t, static_cast<size_t>(table_entries) * sizeof(float2)) != cudaSuccess)
+    // at least double, so that a slowly growing T retires little memory
+    const int64_t cap = std::max(table_entries, 2 * p->table_cap);
+    void* t = nullptr;
+    if (cudaMallocAsync(&t, static_cast<size_t>(cap) * sizeof(float2), s) != cudaSuccess)
       return fail(FP_ERR_OUT_OF_MEMORY, "rotary table allocation (%lld entries) failed",
-                  static_cast<long long>(table_entries));
-    if (p->d_table) {
-      // the old table may still be read by work queued on any stream
-      cudaDeviceSynchronize();
-      cudaFree(p->d_table);
-    }
-    p->d_table = t;
-    p->table_cap = table_entries;
+                  static_cast<long long>(cap));
+    if (p->d_table) p->retired.push_back(p->d_table);
+    p->d_table = static_cast<float2*>(t);
+    p->table_cap = cap;
     p->table_T = -1;
+    grew = true;
+  }
+  if (!in_stream) {
+    if (cudaStreamSynchronize(nullptr) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "scratch allocation failed: %s",
+                  cudaGetErrorString(cudaGetLastError()));
+    if (!p->retired.empty()) {
+      cudaDeviceSynchronize();  // nothing queued reads a retired table any more
+      for (void* q : p->retired) cudaFreeAsync(q, nullptr);
+      p->retired.clear();
+    }
+    p->scratch_pending = false;
+    return FP_OK;
+  }
+  if (grew) {
+    if (!p->scratch_ready &&
+        cudaEventCreateWithFlags(&p->scratch_ready, cudaEventDisableTiming) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event creation failed");
+    if (cudaEventRecord(p->scratch_ready, stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "event record failed");
+    p->scratch_stream = stream;
+    p->scratch_pending = true;
+  } else if (p->scratch_pending && stream != p->scratch_stream) {
+    // scratch allocated in another stream's order: this stream waits for it
+    if (wait_event(stream, p->scratch_ready) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "stream wait on the plan's scratch failed");
   }
   return FP_OK;
 }
@@ -220,6 +290,7 @@ struct Scratch {
   int group_m;
   int max_ctas;
   int cluster;
+  int bounds_check;  // 0 off, 1 on, 2 on against half-size extents (test of the check)
 };
 
 // Every check of a forward call; touches no GPU.
@@ -380,6 +451,13 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
   e.bn_eff = bn_eff;
   e.k_transposed = p->k_transposed;
   e.ff_ld = p->F;
+  e.bounds_check = sc.bounds_check ? 1 : 0;
+  {
+    const int nkv = p->groups > 0 ? p->groups : p->heads;
+    const int64_t ext[4] = {ta.M * p->F, ta.M * p->heads * p->hd, ta.M * nkv * p->hd,
+                            ta.M * nkv * p->hd};
+    for (int i = 0; i < 4; ++i) e.extent[i] = sc.bounds_check == 2 ? ext[i] / 2 : ext[i];
+  }
   const int num_n_tiles = (N + bn_eff - 1) / bn_eff;
 
   if (pr.tc_path) {
@@ -526,6 +604,10 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
   return FP_OK;
 }
 
+// Device address of the no-allocation entry point's static scratch (defined
+// with that entry point at the end of this file).
+fp_status noalloc_scratch(int dev, unsigned char** out);
+
 }  // namespace
 
 extern "C" {
@@ -600,12 +682,16 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->ev_fork = nullptr;
   p->ev_join = nullptr;
   p->last_launches = 0;
-  p->wait_limit_ns = 2000000000ull;
+  p->wait_limit_ns = kDefaultWaitLimitNs;
   p->inject_stall = 0;
-  p->group_m = 32;
+  p->group_m = kDefaultGroupM;
   p->max_ctas = 0;
-  p->cluster = 2;
+  p->cluster = kDefaultCluster;
+  p->bounds_check = 0;
   p->launch_seq = 0;
+  p->scratch_stream = nullptr;
+  p->scratch_ready = nullptr;
+  p->scratch_pending = false;
   *plan = p;
   return ok();
 }
@@ -622,9 +708,14 @@ void fp_destroy(fp_plan* plan) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (plan->device >= 0) cudaSetDevice(plan->device);
-    if (plan->d_status) cudaFree(plan->d_status);
-    if (plan->d_table) cudaFree(plan->d_table);
+    // queued work may still use the scratch: free it once the device is idle
+    cudaDeviceSynchronize();
+    if (plan->d_status) cudaFreeAsync(plan->d_status, nullptr);
+    if (plan->d_table) cudaFreeAsync(plan->d_table, nullptr);
+    for (void* q : plan->retired) cudaFreeAsync(q, nullptr);
+    cudaStreamSynchronize(nullptr);
     if (plan->table_ready) cudaEventDestroy(plan->table_ready);
+    if (plan->scratch_ready) cudaEventDestroy(plan->scratch_ready);
     if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
     if (plan->ev_join) cudaEventDestroy(plan->ev_join);
     if (plan->side_stream) cudaStreamDestroy(plan->side_stream);
@@ -657,6 +748,10 @@ fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value) {
       if (value != 1 && value != 2) return fail(FP_ERR_INVALID_ARG, "cluster must be 1 or 2");
       plan->cluster = static_cast<int>(value);
       return ok();
+    case FP_OPT_BOUNDS_CHECK:
+      if (value < 0 || value > 2) return fail(FP_ERR_INVALID_ARG, "bounds check must be 0, 1 or 2");
+      plan->bounds_check = static_cast<int>(value);
+      return ok();
   }
   return fail(FP_ERR_INVALID_ARG, "unknown option %d", static_cast<int>(opt));
 }
@@ -664,22 +759,32 @@ fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value) {
 fp_status fp_reserve(fp_plan* plan, int64_t max_tokens_per_batch) {
   if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   if (max_tokens_per_batch < 0) return fail(FP_ERR_INVALID_ARG, "negative size");
-  fp_status st = ensure_device_state(plan, max_tokens_per_batch * rope_half_of(plan));
+  fp_status st = ensure_device_state(plan, max_tokens_per_batch * rope_half_of(plan), nullptr,
+                                     false);
   return st == FP_OK ? ok() : st;
 }
 
 fp_status fp_get_device_status(fp_plan* plan, void* stream) {
-  if (!plan) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
-  if (!plan->d_status) return ok();
+  int* words = plan ? plan->d_status : nullptr;
+  if (!plan) {
+    // the no-allocation entry point's status words, on the current device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+    unsigned char* base = nullptr;
+    const fp_status st = noalloc_scratch(dev, &base);
+    if (st != FP_OK) return st;
+    words = reinterpret_cast<int*>(base);
+  }
+  if (!words) return ok();
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return fail(FP_ERR_CUDA, "stream synchronisation failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
   int h[2] = {0, 0};
-  if (cudaMemcpy(h, plan->d_status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(h, words, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
     return fail(FP_ERR_CUDA, "status read failed");
   if (h[0] != 0) {
     int zero[2] = {0, 0};
-    cudaMemcpy(plan->d_status, zero, sizeof zero, cudaMemcpyHostToDevice);
+    cudaMemcpy(words, zero, sizeof zero, cudaMemcpyHostToDevice);
     return fail(static_cast<fp_status>(h[0]), "device reported: %s",
                 fp_status_string(static_cast<fp_status>(h[0])));
   }
@@ -689,6 +794,7 @@ fp_status fp_get_device_status(fp_plan* plan, void* stream) {
 fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
                      const int32_t* pos, void* out_ff, void* out_q, void* out_k, void* out_v,
                      void* stream_v) {
+  const NvtxRange range("fp_forward");
   if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   const Args a{x, xl, W, b, pos, out_ff, out_q, out_k, out_v};
   Prepared pr;
@@ -699,7 +805,7 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
     return ok();  // no tokens: nothing to do
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0);
+  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0, stream, true);
   if (st != FP_OK) return st;
   // The table depends only on (positions, base, rotated width). With the
   // default positions 0..T-1 it is a constant of the plan and of T, so it is
@@ -707,12 +813,13 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   const bool build_table = pr.rope && (pos != nullptr || p->table_T != pr.ta.T);
   if (pr.rope && !build_table && stream != p->table_stream) {
     // cached table written on another stream: order this call after that write
-    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
+    if (wait_event(stream, p->table_ready) != cudaSuccess)
       return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
   }
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
-                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster};
+                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster,
+                   p->bounds_check};
   int launches = 0;
   st = launch(*p, pr, a, sc, build_table, stream, &launches);
   if (st != FP_OK) return st;
@@ -734,6 +841,7 @@ fp_status fp_forward_rope_table(fp_plan* p, const void* x, const fp_layout* x_la
                                 const void* W, const void* b, const void* rope_cos,
                                 const void* rope_sin, const fp_rope_table* tl, void* out_ff,
                                 void* out_q, void* out_k, void* out_v, void* stream_v) {
+  const NvtxRange range("fp_forward_rope_table");
   if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   if (rope_half_of(p) == 0) return fail(FP_ERR_INVALID_ARG, "the plan has no rotary embedding");
   if (!rope_cos || !rope_sin || !tl)
@@ -771,12 +879,13 @@ fp_status fp_forward_rope_table(fp_plan* p, const void* x, const fp_layout* x_la
       if (overlaps(o, t)) return fail(FP_ERR_INVALID_ARG, "an output overlaps a rotary table");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   // the imported table is one float4 per (position, pair): two float2 entries
-  st = ensure_device_state(p, 2 * pr.ta.T * pr.rh);
+  st = ensure_device_state(p, 2 * pr.ta.T * pr.rh, stream, true);
   if (st != FP_OK) return st;
   p->table_T = -1;  // the default-position table (if any) is overwritten
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
-                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster};
+                   p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster,
+                   p->bounds_check};
   const ExtTable ext{rope_cos, rope_sin, tl->dtype == FP_BF16, tl->stride_t, tl->stride_i};
   int launches = 0;
   st = launch(*p, pr, a, sc, false, stream, &launches, &ext);
@@ -872,6 +981,7 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
                       const int32_t* pos, const void* g_ff, const void* g_q, const void* g_k,
                       const void* g_v, void* dx, float* dW, float* db, void* workspace,
                       size_t workspace_bytes, void* stream_v) {
+  const NvtxRange range("fp_backward");
   if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   // the upstream gradients have the forward outputs' shapes: reuse its checks
   const Args a{x, xl, W, b, pos, const_cast<void*>(g_ff), const_cast<void*>(g_q),
@@ -906,13 +1016,13 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     return fail(FP_ERR_INVALID_ARG, "workspace too small: %zu bytes needed",
                 backward_workspace_bytes(M, N));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0);
+  st = ensure_device_state(p, pr.rope ? pr.ta.T * pr.rh : 0, stream, true);
   if (st != FP_OK) return st;
   int launches = 0;
   // rotary table: the forward's, rebuilt under the same rule
   const bool build_table = pr.rope && (pos != nullptr || p->table_T != pr.ta.T);
   if (pr.rope && !build_table && stream != p->table_stream) {
-    if (cudaStreamWaitEvent(stream, p->table_ready, 0) != cudaSuccess)
+    if (wait_event(stream, p->table_ready) != cudaSuccess)
       return fail(FP_ERR_CUDA, "stream wait on the rotary table failed");
   }
   if (build_table) {
@@ -1196,6 +1306,86 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   return ok();
 }
 
+// ---------------------------------------------------------------- attention over the outputs
+
+extern "C" fp_status fp_attention(fp_plan* p, const void* q, const void* k, const void* v,
+                                  void* out, int64_t batch, int64_t T_q, int64_t T_k, float scale,
+                                  void* stream_v) {
+  const NvtxRange range("fp_attention");
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (p->heads == 0) return fail(FP_ERR_INVALID_ARG, "the plan has no attention heads");
+  if (batch < 0 || T_q < 0 || T_k < 0) return fail(FP_ERR_INVALID_ARG, "negative size");
+  const int hd = p->hd, heads = p->heads;
+  const int kvh = p->groups > 0 ? p->groups : p->heads;
+  if (hd != 64 && hd != 128)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "attention takes head_dim 64 or 128 (plan has %d)", hd);
+  if (batch == 0 || T_q == 0) return ok();
+  if (T_k == 0) return fail(FP_ERR_INVALID_ARG, "attention needs at least one key");
+  if (!q || !k || !v || !out) return fail(FP_ERR_INVALID_ARG, "q, k, v and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(FP_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
+  if (p->k_transposed && T_k % 8)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                "pre-transposed k needs T_k a multiple of 8 (its rows are TMA strides)");
+  const int64_t BH = batch * heads, BHkv = batch * kvh;
+  if (BH > INT32_MAX || T_q > INT32_MAX || T_k > INT32_MAX ||
+      BH * ((T_q + 127) / 128) > INT32_MAX)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "attention sizes beyond 32-bit grid coordinates");
+  auto rng = [](const void* a, int64_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(a);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+  };
+  const Range ro = rng(out, BH * T_q * hd * 2);
+  if (overlaps(ro, rng(q, BH * T_q * hd * 2)) || overlaps(ro, rng(k, BHkv * T_k * hd * 2)) ||
+      overlaps(ro, rng(v, BHkv * T_k * hd * 2)))
+    return fail(FP_ERR_INVALID_ARG, "out overlaps an input");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  fp_status st = ensure_device_state(p, 0, stream, true);
+  if (st != FP_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  fp::AttnParams ap;
+  memset(&ap, 0, sizeof ap);
+  const cuuint32_t es[3] = {1, 1, 1};
+  auto map3 = [&](CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+                  cuuint32_t b0, cuuint32_t b1) {
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  CUresult r = map3(&ap.tmap_q, q, hd, T_q, BH, 64, 128);
+  if (r == CUDA_SUCCESS)
+    r = p->k_transposed ? map3(&ap.tmap_k, k, T_k, hd, BHkv, 64, 64)
+                        : map3(&ap.tmap_k, k, hd, T_k, BHkv, 64, 128);
+  if (r == CUDA_SUCCESS) r = map3(&ap.tmap_v, v, hd, T_k, BHkv, 64, 64);
+  if (r != CUDA_SUCCESS)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "attention tensor map rejected (CUresult %d)",
+                static_cast<int>(r));
+  ap.out = out;
+  ap.Tq = T_q;
+  ap.Tk = T_k;
+  ap.BH = static_cast<int>(BH);
+  ap.hd = hd;
+  ap.heads = heads;
+  ap.kv_heads = kvh;
+  ap.k_transposed = p->k_transposed;
+  ap.num_q_blocks = static_cast<int>((T_q + 127) / 128);
+  const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / sqrt(static_cast<double>(hd));
+  ap.scale_log2e = static_cast<float>(sc * 1.4426950408889634);
+  p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
+  ap.status = p->d_status;
+  ap.wait_limit_ns = p->wait_limit_ns;
+  ap.launch_tag = static_cast<int>(p->launch_seq);
+  const cudaError_t err = fp::launch_attention(ap, stream);
+  if (err != cudaSuccess)
+    return fail(FP_ERR_CUDA, "attention launch: %s", cudaGetErrorString(err));
+  p->last_launches = 1;
+  return ok();
+}
+
 // ---------------------------------------------------------------- no-allocation entry point
 //
 // fp_forward_noalloc serves callers that must not allocate device memory
@@ -1314,7 +1504,8 @@ extern "C" fp_status fp_forward_noalloc(const fp_config* config, const void* x,
     return fail(FP_ERR_CUDA, "clearing the static status words failed");
   const uint32_t tag = g_noalloc_seq.fetch_add(1) % 0x7FFFFFFEu + 1u;
   const Scratch sc{status, reinterpret_cast<float2*>(base + kNoAllocHeaderBytes), dev,
-                   static_cast<int>(tag), 2000000000ull, 0, 8, 0, 2};
+                   static_cast<int>(tag), kDefaultWaitLimitNs, 0, kDefaultGroupM, 0,
+                   kDefaultCluster, 0};
   int launches = 0;
   // the shared table may hold another call's positions: always rebuild it
   st = launch(pl, pr, a, sc, pr.rope, stream, &launches);

@@ -324,4 +324,15 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// With bounds checking on: may `n` elements, `stride` apart, starting at
+// element `off` of output `seg` (0 ff, 1 q, 2 k, 3 v) be stored? A store that
+// would leave the buffer is recorded (ST_BOUNDS) and must be skipped.
+__device__ __forceinline__ bool store_in_bounds(const Epilogue& e, int seg, int64_t off,
+                                                int64_t n, int64_t stride = 1) {
+  if (!e.bounds_check) return true;
+  if (off >= 0 && off + (n - 1) * stride < e.extent[seg]) return true;
+  record_status(e.status, ST_BOUNDS);
+  return false;
+}
+
 }  // namespace fp

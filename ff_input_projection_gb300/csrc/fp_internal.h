@@ -51,6 +51,12 @@ struct Epilogue {
   // g_ff * act'(x W + b) instead of act(x W + b), its column sums go to db
   const void* g_ff;   // [M, F] upstream gradient, dtype of x
   float* db;          // [N] or null
+  // opt-in check of every directly addressed output store (stores by TMA are
+  // confined to their tensor map): the element extents of out_ff, out_q,
+  // out_k, out_v. A store that would leave its buffer is skipped and recorded
+  // as ST_BOUNDS in the status word.
+  int bounds_check;
+  int64_t extent[4];
 };
 
 struct TcParams {
@@ -134,6 +140,21 @@ struct SimtParams {
   int num_n_tiles;
 };
 
+// Softmax attention over the projection's outputs (attention.cu): q [BH, Tq, hd],
+// k [BHkv, Tk, hd] or pre-transposed [BHkv, hd, Tk], v [BHkv, Tk, hd], out
+// [BH, Tq, hd], bf16; BH = batch * heads, BHkv = batch * kv_heads.
+struct AttnParams {
+  CUtensorMap tmap_q, tmap_k, tmap_v;
+  void* out;
+  int64_t Tq, Tk;
+  int BH, hd, heads, kv_heads, k_transposed;
+  int num_q_blocks;     // ceil(Tq / 128)
+  float scale_log2e;    // softmax scale times log2(e): exp(s * scale) = 2^(s * scale_log2e)
+  int* status;
+  uint64_t wait_limit_ns;
+  int launch_tag;
+};
+
 // Launchers (defined in the .cu files). Return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
                               double rope_base, cudaStream_t stream);
@@ -146,6 +167,7 @@ cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream
 cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_ctas,
                             cudaStream_t stream);
 cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream);
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kSimtBM = 128, kSimtBN = 128;

@@ -146,7 +146,7 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
       else if (rot)
         // rotate-half: lane i gets x_i cos - x_{i+half} sin, lane i+half gets x_{i+half} cos + x_i sin
         out = lo ? out * cc[q] - pv[q] * ss[q] : out * cc[q] + pv[q] * ss[q];
-      st_elem(base, rb[r] + col_off, out);
+      if (store_in_bounds(e, ci.seg, rb[r] + col_off, 1)) st_elem(base, rb[r] + col_off, out);
     }
   }
 }

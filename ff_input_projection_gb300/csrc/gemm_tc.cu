@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               tma_store_2d(&p.tmap_ff32, stg, tc.n0 + c, static_cast<int>(m));
               bulk_commit();
             }
-          } else if (valid) {
+          } else if (valid && store_in_bounds(e, 0, m * e.ff_ld + tc.n0 + c, 32)) {
             uint4* d4 = reinterpret_cast<uint4*>(ff_row + c);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -705,7 +705,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         const float2* const cs_t = e.rope_cs + t;  // entry (0, t) of the frequency-major table
         auto put16 = [&](int seg, int head, int j, uint16_t* dst, const uint32_t (&w)[8]) {
           if (!(seg == 0 ? tma_ff : tma_heads)) {
-            if (valid) {
+            if (valid &&
+                store_in_bounds(e, seg, dst - static_cast<uint16_t*>(out_base(e, seg)), 16)) {
               uint4* d4 = reinterpret_cast<uint4*>(dst);
               d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
               d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -780,10 +781,11 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
               }
             }
             if (kt) {  // pre-transposed k is stored directly, one lane column at a time
-              if (valid) {
+              const int64_t off = dst_t - static_cast<uint16_t*>(e.out_k);
+              if (valid && store_in_bounds(e, 2, off, 16, e.T))
                 store16_packed_strided(dst_t, e.T, lo_w);
+              if (valid && store_in_bounds(e, 2, off + rh * e.T, 16, e.T))
                 store16_packed_strided(dst_t + rh * e.T, e.T, hi_w);
-              }
             } else {
               put16(ci.seg, ci.head, ci.j, dst, lo_w);
               put16(ci.seg, ci.head, ci.j + rh, dst + rh, hi_w);
@@ -813,7 +815,8 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
                 w[i] = pack_bf16x2(__uint_as_float(v_u[2 * i]), __uint_as_float(v_u[2 * i + 1]));
             }
             if (kt) {
-              if (valid) store16_packed_strided(dst_t, e.T, w);
+              if (valid && store_in_bounds(e, 2, dst_t - static_cast<uint16_t*>(e.out_k), 16, e.T))
+                store16_packed_strided(dst_t, e.T, w);
             } else {
               put16(ci.seg, ci.head, ci.j, dst, w);
             }

@@ -34,8 +34,11 @@
  *  - Argument checks run on the host before any launch; a rejected call
  *    launches nothing and returns a non-zero fp_status. fp_last_error()
  *    then gives a one-line reason (thread-local).
- *  - Errors raised on the device (a bounded wait that ran out) are recorded
- *    in a per-plan status word and reported by fp_get_device_status.
+ *  - Errors raised on the device (a bounded wait that ran out; with
+ *    FP_OPT_BOUNDS_CHECK, a store that would leave its output buffer) are
+ *    recorded in a per-plan status word and reported by fp_get_device_status.
+ *  - Each call is bracketed by an NVTX range named after the entry point, so
+ *    it shows in Nsight timelines; without an attached tool this costs nothing.
  */
 #ifndef FP_H
 #define FP_H
@@ -55,7 +58,7 @@ typedef enum {
   FP_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
   FP_ERR_OUT_OF_MEMORY = 5,      /* plan scratch could not be allocated */
   FP_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out */
-  FP_ERR_DEVICE_BOUNDS = 7       /* a device-side bounds check failed */
+  FP_ERR_DEVICE_BOUNDS = 7       /* a store was stopped by FP_OPT_BOUNDS_CHECK */
 } fp_status;
 
 typedef enum {
@@ -157,9 +160,15 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* config);
  * plan and T; it is built by the first such call and reused by later ones
  * (calls on another stream are ordered after that build with an event).
  * Caller-given positions rebuild the table on every call, so such calls on
- * different streams must be ordered by the caller. The first call that needs
- * more table room than the plan holds allocates it (see fp_reserve); every
- * other call allocates nothing.
+ * different streams must be ordered by the caller.
+ * Device scratch: the first call on a plan, and a call that needs more table
+ * room than the plan holds, grow the plan's scratch in stream order
+ * (cudaMallocAsync and cudaMemsetAsync on `stream`, at least doubling the
+ * table); later calls on other streams are ordered after that growth by an
+ * event, and a replaced table is freed by fp_reserve or fp_destroy. Every other
+ * call allocates nothing; fp_reserve sizes the scratch up front, and must be
+ * used (or one call made) before the first call inside a stream capture. Inside
+ * a capture, waits on events recorded outside it become external-event nodes.
  * Returns FP_OK once the work is enqueued.
  */
 fp_status fp_forward(fp_plan* plan, const void* x, const fp_layout* x_layout, const void* W,
@@ -261,24 +270,60 @@ fp_status fp_backward(fp_plan* plan, const void* x, const fp_layout* x_layout, c
  *   contents; each call clears the status words and rebuilds the table on its
  *   stream. Calls whose work overlaps on the GPU (other streams, other host
  *   threads) race on the array and must be serialised by the caller.
- *   Device-side timeouts still stop the kernels cleanly but are not reported
- *   here (there is no plan to hold the status); use fp_forward for that.
+ *   Device-side timeouts still stop the kernels cleanly; the call cannot
+ *   report them (it returns once the work is enqueued), but
+ *   fp_get_device_status(NULL, stream) reads and clears these status words.
+ *   The device address is cached per device ordinal for the life of the
+ *   process: it assumes the device's primary context is not reset
+ *   (cudaDeviceReset) while the library is loaded.
  */
 fp_status fp_forward_noalloc(const fp_config* config, const void* x, const fp_layout* x_layout,
                              const void* W, const void* b, const int32_t* pos, void* out_ff,
                              void* out_q, void* out_k, void* out_v, void* stream);
 
 /*
+ * fp_attention — enqueue softmax attention over this plan's q, k, v outputs:
+ *     out[z, i, :] = sum_t softmax_t(scale * q[z, i, :] . k[z', t, :]) v[z', t, :]
+ * for every batch*head index z and query i, in the [batch*heads, tokens,
+ * head_dim] layout of memory-efficient-attention issue #7 ("Improve
+ * performance via batched-matmul and fused multiplies": the scaled scores of
+ * its baddbmm, the softmax over the keys, its bmm with the values). The
+ * queries are taken in chunks of 128 and the keys in chunks of 128 merged
+ * under the running row maximum, as that page chunks them; with at most 128
+ * keys there is one key chunk (the page's fast path). Both products run on
+ * the tcgen05 tensor cores; bf16 in and out, fp32 scores and accumulation.
+ *   q     [batch*heads, T_q, head_dim]
+ *   k     [batch*kv, T_k, head_dim], or [batch*kv, head_dim, T_k] when the plan
+ *         emits k pre-transposed (kv = n_query_groups, else heads; query head
+ *         h uses k/v head h / (heads/kv) of its batch element)
+ *   v     [batch*kv, T_k, head_dim]
+ *   out   [batch*heads, T_q, head_dim], may not overlap q, k or v
+ *   scale > 0: the softmax scale; <= 0: head_dim^(-1/2)
+ * head_dim must be 64 or 128 (else FP_ERR_UNSUPPORTED_LAYOUT); with
+ * pre-transposed k, T_k must be a multiple of 8 (its rows are TMA strides).
+ * All pointers 16-byte aligned. Uses the plan's status word (device-side
+ * timeouts surface through fp_get_device_status) and allocates only as
+ * fp_forward does on a plan's first use. Returns FP_OK once enqueued.
+ */
+fp_status fp_attention(fp_plan* plan, const void* q, const void* k, const void* v, void* out,
+                       int64_t batch, int64_t T_q, int64_t T_k, float scale, void* stream);
+
+/*
  * fp_reserve — allocate, on the current device, the plan's device scratch
  * (status word and a rotary table for up to max_tokens_per_batch positions) so
  * that later fp_forward calls with T <= max_tokens_per_batch allocate nothing.
+ * Unlike the calls that enqueue work, it waits for the allocation to complete;
+ * if it replaces a table it first waits for the device to go idle and frees
+ * every table the plan has retired.
  */
 fp_status fp_reserve(fp_plan* plan, int64_t max_tokens_per_batch);
 
 /*
  * fp_get_device_status — synchronise `stream`, then report and clear the
  * device-side status word: FP_OK, FP_ERR_TIMEOUT or FP_ERR_DEVICE_BOUNDS.
- * Returns FP_ERR_CUDA if the synchronisation itself failed.
+ * With plan == NULL it reads the status words of fp_forward_noalloc on the
+ * current device (allocating nothing). Returns FP_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 fp_status fp_get_device_status(fp_plan* plan, void* stream);
 
@@ -300,15 +345,27 @@ const char* fp_last_error(void);
  *                          error path; the GPU stays usable). Cleared after use.
  *   FP_OPT_GROUP_M         tile rasterisation: M-tiles per group (>= 1)
  *   FP_OPT_MAX_CTAS        cap on the persistent grid (0 = one CTA per SM)
- *   FP_OPT_CLUSTER         2 (default): CTA pairs share each weight tile by
- *                          multicast; 1: every CTA loads its own
+ *   FP_OPT_CLUSTER         2 (default): CTA pairs run 2-SM MMAs over one
+ *                          256-column weight tile, each CTA loading its own half
+ *                          of it and its own 128 token rows; 1: single CTAs,
+ *                          each loading the whole weight tile
+ *   FP_OPT_BOUNDS_CHECK    1: every output store whose address the kernels
+ *                          compute themselves (ragged or batch-crossing tiles,
+ *                          pre-transposed k, the FFMA kernel) is first checked
+ *                          against its buffer; one that would leave it is
+ *                          skipped and reported as FP_ERR_DEVICE_BOUNDS (stores
+ *                          by TMA are confined by their tensor maps). 2: the same
+ *                          against half of each buffer, a test of the check
+ *                          itself (stores past the middle are reported, never
+ *                          made). 0 (default): off. Forward calls only.
  */
 typedef enum {
   FP_OPT_WAIT_LIMIT_NS = 1,
   FP_OPT_INJECT_STALL = 2,
   FP_OPT_GROUP_M = 3,
   FP_OPT_MAX_CTAS = 4,
-  FP_OPT_CLUSTER = 5
+  FP_OPT_CLUSTER = 5,
+  FP_OPT_BOUNDS_CHECK = 6
 } fp_option;
 fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value);
 

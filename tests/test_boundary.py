@@ -165,6 +165,9 @@ def test_options_and_status_without_device(lib):
     assert fpx.fp_set_option(h, fpx.FP_OPT_GROUP_M, 16) == fpx.FP_OK
     assert fpx.fp_set_option(h, fpx.FP_OPT_WAIT_LIMIT_NS, -5) == fpx.FP_ERR_INVALID_ARG
     assert fpx.fp_set_option(h, 77, 1) == fpx.FP_ERR_INVALID_ARG
+    for v, want in ((-1, fpx.FP_ERR_INVALID_ARG), (3, fpx.FP_ERR_INVALID_ARG), (0, fpx.FP_OK),
+                    (1, fpx.FP_OK), (2, fpx.FP_OK)):
+        assert fpx.fp_set_option(h, fpx.FP_OPT_BOUNDS_CHECK, v) == want, v
     # no device state yet: nothing to report, no CUDA call made
     assert fpx.fp_get_device_status(h, None) == fpx.FP_OK
     fpx.fp_destroy(h)

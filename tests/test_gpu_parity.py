@@ -1,8 +1,7 @@
 """GPU path vs the CPU oracle, through the C ABI (needs a GB300).
 
-Small shapes compare every output element; the full-size workloads compare
-sampled token rows (the oracle computes them one by one) and properties that
-hold at any size. Tolerances: bf16 |d| <= max(1e-2 |ref|, 2e-2 rms(ref)),
+Small shapes and the full-size workloads compare every output element;
+properties that hold at any size are checked at the largest shape. Tolerances: bf16 |d| <= max(1e-2 |ref|, 2e-2 rms(ref)),
 f32 |d| <= max(1e-4 |ref|, 2e-4 rms(ref)); layout/scatter with an identity
 weight is bit-exact.
 """
@@ -13,7 +12,7 @@ import torch
 import ff_input_projection_gb300 as fpx
 import fpsynth
 import oracle
-from tests.gpu_util import assert_close, gather_rows, host, run, to_device
+from tests.gpu_util import assert_close, host, run, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -140,30 +139,23 @@ def test_identity_weight_nchw_fp32_bit_exact(cuda_ok):
 
 
 FULL = ["tiny_fp32", "walrus_bf16", "bert_ff_bf16", "bert_qkv_bf16", "llm_qkv_rope_bf16",
-        "unet_qkv_bf16", "unet_qkv_fp32"]
-
-
-def _sample_rows(w, n=24, seed=0):
-    rng = np.random.default_rng(seed)
-    fixed = [0, 1, 127, 128, w.T - 1, w.T, w.M - 129, w.M - 1]
-    rows = sorted(set([r for r in fixed if 0 <= r < w.M] + list(rng.integers(0, w.M, n))))
-    return rows
+        "unet_qkv_bf16", "unet_qkv_fp32", "gqa_rope_toy_bf16"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(name, cuda_ok):
+def test_full_size_every_element(name, cuda_ok):
+    """Each workload at its full size, every output element against the oracle
+    (the oracle runs on all host cores). The outputs start as NaN, so an element
+    the kernels never wrote fails."""
     w = fpsynth.WORKLOADS[name]
     inp = fpsynth.make_inputs(w)
     out = run(w, inp)
-    rows = _sample_rows(w)
-    ref = oracle.forward_workload(w, inp, rows=rows)
-    got = gather_rows(out, w, rows)
+    ref = oracle.forward_workload(w, inp)
     for k in ("ff", "q", "k", "v"):
-        assert_close(got[k], ref[k], w.dtype, f"{name}:{k}")
-    # every output element is finite and written (outputs start as uninitialised memory)
-    for k, t in out.items():
-        if t is not None:
-            assert torch.isfinite(t.float()).all(), k
+        if out[k] is None:
+            assert ref[k].size == 0
+            continue
+        assert_close(host(out[k]), ref[k], w.dtype, f"{name}:{k}")
 
 
 def test_full_size_rope_invariants(cuda_ok):
@@ -209,8 +201,8 @@ def test_empty_tokens_on_device(cuda_ok):
 
 @pytest.mark.parametrize("w", [SMALL[1], SMALL[3], SMALL[5], SMALL[8]], ids=lambda w: w.name)
 def test_cluster_pairs_match_single_ctas(w, cuda_ok):
-    """CTA pairs that multicast the shared weight tile (default) and single
-    CTAs give identical bits; odd M-tile counts leave one CTA of the last pair
+    """CTA pairs (2-SM MMAs over one weight tile, the default) and single CTAs
+    give identical bits; odd M-tile counts leave one CTA of the last pair
     with nothing to store."""
     inp = fpsynth.make_inputs(w)
     outs = []

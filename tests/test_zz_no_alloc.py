@@ -17,6 +17,7 @@ import torch
 
 import ff_input_projection_gb300 as fpx
 import fpsynth
+import oracle
 from tests.gpu_util import assert_close, host, run, to_device
 
 pytestmark = pytest.mark.gpu
@@ -55,11 +56,48 @@ def test_noalloc_matches_fp_forward_two_calls(cuda_ok):
         inp = fpsynth.make_inputs(w)
         ref = run(w, inp, pos=pos)
         got = _noalloc(w, inp, pos)
+        # the oracle too, so the check does not rest on the other entry point alone
+        ref_o = oracle.forward_workload(w, dict(inp, pos=pos))
         for k in ("ff", "q", "k", "v"):
             if ref[k] is None:
                 assert got[k] is None
                 continue
             assert_close(host(got[k]), host(ref[k]), w.dtype, f"{w.name}:{k}")
+            assert_close(host(got[k]), ref_o[k], w.dtype, f"{w.name}:{k} (oracle)")
+        # the status words of the static array: nothing went wrong, and reading
+        # them allocates nothing either
+        assert fpx.fp_get_device_status(None, torch.cuda.current_stream().cuda_stream) == \
+            fpx.FP_OK, fpx.fp_last_error()
+
+
+def test_noalloc_leaves_free_device_memory_unchanged(cuda_ok):
+    """After a first call has loaded the kernels, a call with another sequence
+    length and other positions changes the device's free memory by nothing."""
+    w = FIRST
+    inp = fpsynth.make_inputs(w)
+    _noalloc(w, inp, None)  # loads the kernel variants this configuration uses
+    w2 = w.scaled(name="noalloc_walrus_2", x_shape=(2, 5, 64, 16, 16, 1))
+    inp2 = fpsynth.make_inputs(w2)
+    pos2 = (np.arange(w2.T) * 3 + 5) % 7000
+    x, W, b = (to_device(inp2[k], w2.dtype) for k in ("x", "W", "b"))
+    pos_t = torch.from_numpy(pos2.astype(np.int32)).cuda()
+    ff = torch.empty((w2.Bb * w2.T, w2.F), dtype=torch.bfloat16, device="cuda")
+    qkv = [torch.empty((w2.Bb * w2.heads, w2.T, w2.head_dim), dtype=torch.bfloat16,
+                       device="cuda") for _ in range(3)]
+    cfg = fpx.fp_config(w2.C, w2.F, w2.heads, w2.head_dim, 0, 0, w2.act, w2.rope_base, 0)
+    L = fpx.make_layout(x.shape, x.stride(), w2.channel_dim, w2.n_batch_dims, fpx.FP_BF16)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    st = fpx.fp_forward_noalloc(cfg, x.data_ptr(), L, W.data_ptr(), b.data_ptr(), pos_t.data_ptr(),
+                                ff.data_ptr(), *[t.data_ptr() for t in qkv],
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == fpx.FP_OK, fpx.fp_last_error()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    ref = oracle.forward_workload(w2, dict(inp2, pos=pos2))
+    for k, o in zip(("ff", "q", "k", "v"), [ff] + qkv):
+        assert_close(host(o), ref[k], "bf16", f"noalloc second call:{k}")
 
 
 def test_noalloc_rejects_a_table_beyond_its_maximum(cuda_ok):
