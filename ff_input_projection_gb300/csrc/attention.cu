@@ -1,0 +1,389 @@
+// Softmax attention over the fused projection's q, k, v on the 5th-generation
+// tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes, per batch*head index z and query i:
+//     out[z, i, :] = sum_t softmax_t(scale * q[z, i, :] . k[z', t, :]) v[z', t, :]
+// in the [batch*heads, tokens, head_dim] layout of memory-efficient-attention
+// issue #7 ("Improve performance via batched-matmul and fused multiplies"):
+// its baddbmm (the scaled scores q k^T, the scale fused into the multiply),
+// the softmax over the keys and its bmm with the values, chunked as that page
+// chunks them. Each CTA takes one chunk of 128 queries and walks the keys in
+// chunks of 128, merging the chunks under the running row maximum; with 128
+// keys or fewer there is a single key chunk and nothing to merge (the page's
+// fast path). k arrives pre-transposed, [batch*heads, head_dim, tokens] (the
+// same page's comments on transposing the key once), or as [batch*heads,
+// tokens, head_dim]. z' is the k/v head of query head z: grouped-query
+// layouts share one k/v head among heads / kv_heads query heads.
+//
+// Structure (one CTA per 128-query chunk, 8 warps):
+//   warp 0     TMA producer: the q chunk once, then k and v chunks into
+//              two-stage rings
+//   warp 1     MMA issuer (one thread): S = q k^T into one of two TMEM score
+//              buffers (M 128, N 128, K head_dim), then O += P v into the TMEM
+//              output accumulator (M 128, N head_dim, K 128); the next chunk's
+//              scores are issued before this chunk's P v, so the tensor core
+//              works while the softmax runs
+//   warps 4-7  softmax, one query row per thread (TMEM lane = row): scores
+//              from TMEM, running maximum m and sum l, P = 2^(s c - m) rounded
+//              to bf16 into shared memory (the A operand of P v); when m grows
+//              the output accumulator is rescaled in TMEM first. At the end
+//              O / l is rounded to bf16 and stored.
+// Shared-memory operands use the 128-byte swizzle TMA writes and the MMA reads;
+// P is written by the softmax threads in the same swizzled K-major layout.
+// Every mbarrier wait is bounded: a wait that runs out records a timeout in
+// the status word, tags the launch as aborted, drains its own copies and MMAs
+// and returns, so the GPU stays usable.
+#include "epilogue.cuh"
+#include "fp_internal.h"
+#include "tc_ptx.cuh"
+
+namespace fp {
+namespace {
+
+constexpr int QB = 128;   // queries per CTA: one per softmax thread and TMEM lane
+constexpr int KB = 128;   // keys per chunk: the N of S and the K of P v
+constexpr int ANT = 256;  // 8 warps
+constexpr int RING = 2;   // k and v stages
+constexpr int ATOM = QB * 128;  // a [128 rows][64 bf16] 128-byte-swizzled atom: 16 KB
+constexpr int CHUNK = 64 * 128; // a [64 rows][64 bf16] atom: 8 KB
+
+template <int HD>
+struct ACfg {
+  static constexpr int Q_BYTES = QB * HD * 2;
+  static constexpr int K_BYTES = KB * HD * 2;
+  static constexpr int V_BYTES = KB * HD * 2;
+  static constexpr int P_BYTES = QB * KB * 2;
+  // q_full; k full/empty and v full/empty per stage; s full/empty per score
+  // buffer; p_full; o_done; drain
+  static constexpr int NUM_BARS = 1 + 4 * RING + 4 + 3;
+  static constexpr int SMEM_BYTES =
+      1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + P_BYTES + NUM_BARS * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static constexpr int O_COL = 2 * KB;  // TMEM: scores in [0, 256), output in [256, 256 + HD)
+};
+
+template <int HD, bool KT>
+__global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant__ AttnParams p) {
+  using G = ACfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - raw);
+  const uint32_t q_s = sbase;
+  const uint32_t k_s = q_s + G::Q_BYTES;                   // RING stages
+  const uint32_t v_s = k_s + RING * G::K_BYTES;            // RING stages
+  const uint32_t p_s = v_s + RING * G::V_BYTES;
+  const uint32_t bar0 = p_s + G::P_BYTES;
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + RING + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * RING + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * RING + s); };
+  const uint32_t bar1 = bar0 + 8u * (1 + 4 * RING);
+  auto s_full = [&](int b) { return bar1 + 8u * b; };
+  auto s_empty = [&](int b) { return bar1 + 8u * (2 + b); };
+  const uint32_t p_full = bar1 + 8u * 4;
+  const uint32_t o_done = bar1 + 8u * 5;
+  const uint32_t drain = bar1 + 8u * 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 7 - sbase));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl wc{p.status, p.wait_limit_ns, p.launch_tag};
+  const int z = static_cast<int>(blockIdx.x / p.num_q_blocks);
+  const int q0 = static_cast<int>(blockIdx.x - static_cast<int64_t>(z) * p.num_q_blocks) * QB;
+  const int qpk = p.heads / p.kv_heads;
+  const int zkv = (z / p.heads) * p.kv_heads + (z % p.heads) / qpk;
+  const int nkb = static_cast<int>((p.Tk + KB - 1) / KB);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 4);  // the four softmax warps
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    prefetch_tmap(&p.tmap_q);
+    prefetch_tmap(&p.tmap_k);
+    prefetch_tmap(&p.tmap_v);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t armed = 0, armed_par = 0;  // bit per barrier slot: 0 q, 1+s k, 1+RING+s v
+      auto arm = [&](int slot, uint32_t par) {
+        armed |= 1u << slot;
+        armed_par = (armed_par & ~(1u << slot)) | (par << slot);
+      };
+      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
+#pragma unroll
+      for (int a = 0; a < HD / 64; ++a) tma_load_3d(q_s + a * ATOM, &p.tmap_q, q_full, 64 * a, q0, z);
+      arm(0, 0);
+      for (int j = 0; j < nkb; ++j) {
+        const int s = j % RING;
+        const uint32_t ph = (j / RING) & 1;
+        const int key0 = j * KB;
+        if (!wait_bounded(k_empty(s), ph ^ 1u, wc, true)) break;
+        mbar_arrive_expect_tx(k_full(s), G::K_BYTES);
+        const uint32_t kd = k_s + s * G::K_BYTES;
+        if (KT) {
+          // [hd][Tk] rows of the head: chunk (h, n) holds hd rows 64h.. and keys 64n..
+#pragma unroll
+          for (int h = 0; h < HD / 64; ++h)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+              tma_load_3d(kd + (h * 2 + n) * CHUNK, &p.tmap_k, k_full(s), key0 + 64 * n, 64 * h,
+                          zkv);
+        } else {
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            tma_load_3d(kd + a * ATOM, &p.tmap_k, k_full(s), 64 * a, key0, zkv);
+        }
+        arm(1 + s, ph);
+        if (!wait_bounded(v_empty(s), ph ^ 1u, wc, true)) break;
+        mbar_arrive_expect_tx(v_full(s), G::V_BYTES);
+        const uint32_t vd = v_s + s * G::V_BYTES;
+        // chunk (h, n) holds keys 64h.. and head lanes 64n..
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int n = 0; n < HD / 64; ++n)
+            tma_load_3d(vd + (h * (HD / 64) + n) * CHUNK, &p.tmap_v, v_full(s), 64 * n,
+                        key0 + 64 * h, zkv);
+        arm(1 + RING + s, ph);
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      const WaitCtl dc{wc.status, wc.limit_ns < 10000000ull ? wc.limit_ns : 10000000ull,
+                       wc.launch_tag};
+      if (armed & 1u) wait_bounded(q_full, armed_par & 1u, dc, false);
+      for (int s = 0; s < RING; ++s) {
+        if (armed & (1u << (1 + s))) wait_bounded(k_full(s), (armed_par >> (1 + s)) & 1u, dc, false);
+        if (armed & (1u << (1 + RING + s)))
+          wait_bounded(v_full(s), (armed_par >> (1 + RING + s)) & 1u, dc, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = make_idesc(false, KT, QB, KB);
+      const uint32_t idesc_o = make_idesc(false, true, QB, HD);
+      bool issued = false, ok = wait_bounded(q_full, 0, wc, true);
+      tc_fence_after();
+      auto issue_scores = [&](int j) -> bool {
+        const int s = j % RING, b = j & 1;
+        if (!wait_bounded(k_full(s), (j / RING) & 1, wc, true)) return false;
+        if (!wait_bounded(s_empty(b), ((j >> 1) & 1) ^ 1u, wc, true)) return false;
+        tc_fence_after();
+        const uint32_t kd = k_s + s * G::K_BYTES;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t a_desc = sw128_desc(q_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+          // pre-transposed k: MN-major B, two 64-key chunks per 64 head lanes;
+          // else K-major B, like q
+          const uint64_t b_desc = KT ? sw128_desc(kd + (k / 4) * 2 * CHUNK + (k % 4) * 2048, CHUNK, 1024)
+                                     : sw128_desc(kd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+          umma_bf16<1>(tmem + b * KB, a_desc, b_desc, idesc_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit<1>(s_full(b));
+        umma_commit<1>(k_empty(s));
+        issued = true;
+        return true;
+      };
+      if (ok && nkb > 0) ok = issue_scores(0);
+      for (int j = 0; ok && j < nkb; ++j) {
+        if (j + 1 < nkb && !issue_scores(j + 1)) break;
+        const int s = j % RING;
+        if (!wait_bounded(p_full, j & 1, wc, true)) break;
+        if (!wait_bounded(v_full(s), (j / RING) & 1, wc, true)) break;
+        tc_fence_after();
+        const uint32_t vd = v_s + s * G::V_BYTES;
+#pragma unroll
+        for (int k = 0; k < KB / 16; ++k) {
+          const uint64_t a_desc = sw128_desc(p_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+          const uint64_t b_desc =
+              sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
+          umma_bf16<1>(tmem + G::O_COL, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
+        }
+        umma_commit<1>(o_done);
+        umma_commit<1>(v_empty(s));
+      }
+      if (issued) {
+        umma_commit<1>(drain);  // every MMA retired before TMEM is freed
+        wait_bounded(drain, 0, wc, false);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax and output
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c = p.scale_log2e;
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool alive = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int b = j & 1;
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(s_full(b), (j >> 1) & 1, wc, true) ? 1 : 0)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[KB];
+#pragma unroll
+      for (int q = 0; q < KB / 32; ++q)
+        tmem_ld32(t_lane + b * KB + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty(b));  // the score buffer may be overwritten
+      // scores in log2 units, keys past Tk masked out
+      const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(j) * KB);
+      float t[KB];
+      float m_blk = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        t[i] = i < valid ? __uint_as_float(sv[i]) * c : -INFINITY;
+        m_blk = fmaxf(m_blk, t[i]);
+      }
+      const float m_new = fmaxf(m_run, m_blk);
+      const float alpha = ex2_approx(m_run - m_new);  // 0 on the first chunk
+      // P = 2^(t - m), rounded to bf16; the row sum takes the rounded values
+      uint32_t pw[KB / 2];
+      float sum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < KB / 2; ++i) {
+        pw[i] = pack_bf16x2(ex2_approx(t[2 * i] - m_new), ex2_approx(t[2 * i + 1] - m_new));
+        sum += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      if (j > 0) {
+        // P and the output accumulator are free once the previous P v has run
+        if (!__all_sync(0xFFFFFFFFu, wait_bounded(o_done, (j - 1) & 1, wc, true) ? 1 : 0)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // P row into the swizzled K-major atoms: 16-byte chunk ch of row r at ch ^ (r & 7)
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t addr = p_s + a * ATOM + row * 128 + ((ch ^ (row & 7)) << 4);
+          const int w0 = a * 32 + ch * 4;
+          st_shared_v4(addr, pw[w0], pw[w0 + 1], pw[w0 + 2], pw[w0 + 3]);
+        }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+        // the running maximum grew: scale the output accumulated so far
+#pragma unroll
+        for (int q = 0; q < HD / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(t_lane + G::O_COL + 32 * q, o);
+        }
+        tmem_wait_st();
+      }
+      fence_async_shared();  // P visible to the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (alive && nkb > 0 &&
+        __all_sync(0xFFFFFFFFu, wait_bounded(o_done, (nkb - 1) & 1, wc, true) ? 1 : 0)) {
+      tc_fence_after();
+      const float inv = 1.0f / l_run;
+      const int64_t qi = q0 + row;
+      uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(z) * p.Tq + qi) * HD;
+#pragma unroll
+      for (int q = 0; q < HD / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (qi < p.Tq) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
+}
+
+template <int HD, bool KT>
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
+  auto kernel = attention_kernel<HD, KT>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_done[dev]) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ACfg<HD>::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_done[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.num_q_blocks), 1, 1);
+  cfg.blockDim = dim3(ANT, 1, 1);
+  cfg.dynamicSmemBytes = ACfg<HD>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kernel, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
+  if (p.BH == 0 || p.num_q_blocks == 0) return cudaSuccess;
+  if (p.hd == 64) return p.k_transposed ? launch_attn<64, true>(p, stream) : launch_attn<64, false>(p, stream);
+  if (p.hd == 128)
+    return p.k_transposed ? launch_attn<128, true>(p, stream) : launch_attn<128, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fp
