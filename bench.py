@@ -38,6 +38,8 @@ METRIC = "fused-proj TFLOP/s & tokens/s on 1 GB300; % of min(TC peak, HBM) roofl
 DEFAULT_WORKLOAD = "walrus_bf16"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 data-sheet figures: dense bf16 tensor throughput and HBM3e bandwidth
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 KERNEL_SOURCES = ["ff_input_projection_gb300/csrc/gemm_tc.cu",
                   "ff_input_projection_gb300/csrc/epilogue.cuh",
                   "ff_input_projection_gb300/csrc/tc_ptx.cuh",
@@ -52,6 +54,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fpsynth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (no per_config key)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cluster", type=int, default=2, choices=[1, 2],
                     help="tensor-core path: CTA pairs sharing weight tiles (2) or single CTAs (1)")
@@ -222,6 +226,247 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+PER_CONFIG = ["bert_ff_bf16", "bert_qkv_bf16", "llm_qkv_rope_bf16", "unet_qkv_bf16",
+              "unet_qkv_fp32", "gqa_rope_toy_bf16", "tiny_fp32"]
+MAX_SETS = 64
+
+
+def to_device_fn(torch, dev, dtype):
+    def to_dev(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
+            if dtype == "bf16" else torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(dev)
+    return to_dev
+
+
+def ffma_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FP32 FFMA peak: SMs x 128 FP32 lanes x 2 FLOP per FMA x SM clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def roofline(w, ms, pk, pk_src, sm_count, flops=None, bytes_=None):
+    """Roofline of one timed configuration: bf16 against the tensor or HBM bound
+    (whichever takes longer at the measured peaks), f32 (TF32 off) against the
+    FFMA peak. frac_nominal: the same achieved figure over the data-sheet peak."""
+    if flops is None:
+        flops, bytes_ = algorithmic(w)
+    t = ms * 1e-3
+    if w.dtype == "bf16":
+        tensor_time = flops / (pk["bf16_tflops"] * 1e12)
+        hbm_time = bytes_ / (pk["hbm_gbs"] * 1e9)
+        if tensor_time >= hbm_time:
+            r = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": pk["bf16_tflops"],
+                 "unit": "TFLOP/s", "peak_source": f"{pk_src} (cuBLAS bf16 burst)",
+                 "nominal_peak": NOMINAL["bf16_tflops"]}
+        else:
+            r = {"bound": "hbm", "achieved": bytes_ / t / 1e9, "peak": pk["hbm_gbs"],
+                 "unit": "GB/s", "peak_source": f"{pk_src} (copy)",
+                 "nominal_peak": NOMINAL["hbm_gbs"]}
+    else:
+        mhz = float(pk.get("sm_max_mhz") or 2070.0)
+        r = {"bound": "alu", "achieved": flops / t / 1e12, "peak": ffma_peak_tflops(sm_count, mhz),
+             "unit": "TFLOP/s",
+             "peak_source": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 FLOP x {mhz:.0f} MHz",
+             "nominal_peak": ffma_peak_tflops(sm_count, mhz)}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["frac_nominal"] = r["achieved"] / r["nominal_peak"]
+    return r
+
+
+class ForwardRun:
+    """One forward configuration set up for timing: input and output sets
+    rotated so that one pass over them exceeds twice the L2."""
+
+    def __init__(self, torch, fpx, dev, w, *, explicit_pos=False, cluster=2, group_m=0):
+        self.torch, self.w, self.dev = torch, w, dev
+        inp = fpsynth.make_inputs(w)
+        self.inp = inp
+        to_dev = to_device_fn(torch, dev, w.dtype)
+        esz = 2 if w.dtype == "bf16" else 4
+        self.in_bytes = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0)) * esz
+        self.out_bytes = w.M * w.N * esz
+        per_set = self.in_bytes + self.out_bytes
+        self.n_sets = int(min(MAX_SETS, max(2, np.ceil(2 * L2_BYTES / per_set))))
+        self.xs = [to_dev(inp["x"]) for _ in range(self.n_sets)]
+        self.Ws = [to_dev(inp["W"]) for _ in range(self.n_sets)]
+        self.bs = [to_dev(inp["b"]) for _ in range(self.n_sets)]
+        self.proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                                        w.n_query_groups, w.rope_n_elem, w.k_transposed)
+        self.proj.set_option(fpx.FP_OPT_CLUSTER, cluster)
+        if group_m:
+            self.proj.set_option(fpx.FP_OPT_GROUP_M, group_m)
+        self.proj.reserve(w.T)
+        self.pos = torch.arange(w.T, dtype=torch.int32, device=dev) if explicit_pos else None
+        self.stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(self.stream):
+            self.outs = [self.proj.forward(self.xs[0], self.Ws[0], self.bs[0], self.pos,
+                                           channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims,
+                                           stream=self.stream.cuda_stream)
+                         for _ in range(self.n_sets)]
+        self.fpx = fpx
+
+    def step(self, i):
+        j = i % self.n_sets
+        w = self.w
+        return self.proj.forward(self.xs[j], self.Ws[j], self.bs[j], self.pos,
+                                 channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims,
+                                 out=self.outs[j], stream=self.stream.cuda_stream)
+
+    def l2_note(self):
+        tot = self.n_sets * (self.in_bytes + self.out_bytes)
+        cap = " (capped)" if self.n_sets == MAX_SETS and tot < 2 * L2_BYTES else ""
+        return (f"inputs and outputs rotate over {self.n_sets} sets{cap} "
+                f"({tot / 1e6:.0f} MB; L2 129 MB)")
+
+    def time(self, steps, warmup, uuid, dist=None):
+        """Mean ms per step over `steps` steps replayed from a CUDA graph, after
+        `warmup` eager steps; clocks sampled during the timed region."""
+        torch, fpx = self.torch, self.fpx
+        with torch.cuda.stream(self.stream):
+            for i in range(max(3, warmup)):
+                self.step(i)
+        torch.cuda.synchronize(self.dev)
+        fpx.check(self.proj.device_status(self.stream.cuda_stream))
+        self.launches_per_step = self.proj.last_launch_count
+        G = max(d for d in range(1, min(steps, 64) + 1) if steps % d == 0)
+        graph = None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=self.stream):
+                for i in range(G):
+                    self.step(i)
+            with torch.cuda.stream(self.stream):
+                graph.replay()
+            torch.cuda.synchronize(self.dev)
+        except Exception as exc:  # capture unsupported here: time the eager loop instead
+            graph = None
+            self.timing_note = f"eager (graph capture failed: {type(exc).__name__})"
+        else:
+            self.timing_note = f"CUDA graph of {G} steps replayed {steps // G} times"
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        # graph.replay() launches on torch's current stream: make that the timed stream
+        with ClockSampler(uuid) as clk, torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            if graph is not None:
+                for _ in range(steps // G):
+                    graph.replay()
+            else:
+                for i in range(steps):
+                    self.step(i)
+            ev1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+        if dist:
+            dist.barrier()
+        fpx.check(self.proj.device_status(self.stream.cuda_stream))
+        self.clocks = clk.summary()
+        return ev0.elapsed_time(ev1) / steps
+
+    def close(self):
+        self.proj.close()
+        del self.xs, self.Ws, self.bs, self.outs
+        self.torch.cuda.empty_cache()
+
+
+def steps_for(run, target_s=0.25, lo=20, hi=4000):
+    """Steps whose timed region lasts about target_s, from a short eager trial."""
+    torch = run.torch
+    with torch.cuda.stream(run.stream):
+        run.step(0)
+        torch.cuda.synchronize(run.dev)
+        t = time.perf_counter()
+        for i in range(5):
+            run.step(i)
+        torch.cuda.synchronize(run.dev)
+    per = max((time.perf_counter() - t) / 5, 1e-6)
+    n = int(min(hi, max(lo, target_s / per)))
+    return max(lo, n // 20 * 20)
+
+
+def time_attention(torch, fpx, dev, uuid, pk, pk_src, sm_count):
+    """fp_attention over the outputs of the diffusion-UNet projection (k emitted
+    pre-transposed): per_config entry with its own timing, clocks and roofline."""
+    w = fpsynth.WORKLOADS["unet_qkv_bf16"].scaled(k_transposed=True)
+    inp = fpsynth.make_inputs(w)
+    to_dev = to_device_fn(torch, dev, "bf16")
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base, 0, 0, True)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        _, q, kT, v = proj.forward(to_dev(inp["x"]), to_dev(inp["W"]), None, None,
+                                   channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims,
+                                   stream=stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    per_set = 4 * q.numel() * 2
+    n_sets = int(min(MAX_SETS, max(2, np.ceil(2 * L2_BYTES / per_set))))
+    sets = [(q.clone(), kT.clone(), v.clone(), torch.empty_like(q)) for _ in range(n_sets)]
+    B, T = w.Bb, w.T
+
+    def step(i):
+        a, b, c, o = sets[i % n_sets]
+        proj.attention(a, b, c, batch=B, out=o, stream=stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            step(i)
+    torch.cuda.synchronize(dev)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    steps = 200
+    G = 20
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            step(i)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk, torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps // G):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    ms = ev0.elapsed_time(ev1) / steps
+    BH = B * w.heads
+    flops = 4 * BH * T * T * w.head_dim
+    bytes_ = 4 * BH * T * w.head_dim * 2
+    roof = roofline(w, ms, pk, pk_src, sm_count, flops, bytes_)
+    entry = {"workload": "unet_attention_bf16", "pass": "attention", "ms_per_step": ms,
+             "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": BH * T / (ms * 1e-3),
+             "steps": steps, "timing": f"CUDA graph of {G} steps replayed {steps // G} times",
+             "gpu_launches_per_step": 1, "dtype": "bf16",
+             "shape": {"batch_heads": BH, "T_q": T, "T_k": T, "head_dim": w.head_dim,
+                       "k": "pre-transposed [B*heads, head_dim, T] from fp_forward"},
+             "flops_per_step": flops,
+             "l2": f"q, k, v, out rotate over {n_sets} sets ({n_sets * per_set / 1e6:.0f} MB)",
+             "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                               "frac_nominal", "peak_source")},
+             "clocks": clk.summary()}
+    proj.close()
+    del sets
+    torch.cuda.empty_cache()
+    return entry
+
+
+def config_entry(w, ms, roof, clocks, steps, timing, launches, extra=None):
+    e = {"workload": w.name, "ms_per_step": ms, "tflops": 2.0 * w.M * w.C * w.N / (ms * 1e-3) / 1e12,
+         "tokens_per_s": w.M / (ms * 1e-3), "steps": steps, "timing": timing,
+         "gpu_launches_per_step": launches, "dtype": w.dtype,
+         "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                           "frac_nominal", "peak_source")},
+         "clocks": clocks}
+    if extra:
+        e.update(extra)
+    return e
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -243,110 +488,45 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-
-    w = fpsynth.WORKLOADS[args.workload]
-    inp = fpsynth.make_inputs(w)
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-
-    def to_dev(a):
-        if a is None:
-            return None
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
-            if w.dtype == "bf16" else torch.from_numpy(np.ascontiguousarray(a))
-        return t.to(dev)
-
-    flops, alg_bytes = algorithmic(w)
-    in_bytes = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0)) * (2 if w.dtype == "bf16" else 4)
-    n_sets = max(2, int(np.ceil(2 * L2_BYTES / in_bytes)))
-    xs = [to_dev(inp["x"]) for _ in range(n_sets)]
-    Ws = [to_dev(inp["W"]) for _ in range(n_sets)]
-    bs = [to_dev(inp["b"]) for _ in range(n_sets)]
-    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
-                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
-    proj.set_option(fpx.FP_OPT_CLUSTER, args.cluster)
-    if args.group_m:
-        proj.set_option(fpx.FP_OPT_GROUP_M, args.group_m)
-    proj.reserve(w.T)
-    stream = torch.cuda.Stream(device=dev)
-    outs = None
-
-    def step(i):
-        nonlocal outs
-        j = i % n_sets
-        outs = proj.forward(xs[j], Ws[j], bs[j], None, channel_dim=w.channel_dim,
-                            n_batch_dims=w.n_batch_dims, out=outs, stream=stream.cuda_stream)
-
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            step(i)
-    torch.cuda.synchronize(dev)
-    fpx.check(proj.device_status(stream.cuda_stream))
-    launches_per_step = proj.last_launch_count
-
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = str(local)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    # The K timed steps replay a CUDA graph of G steps (G divides K), so the
-    # host's per-call cost (Python, ctypes, argument checks) is off the timeline.
-    G = max(d for d in range(1, min(args.steps, 64) + 1) if args.steps % d == 0)
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(G):
-                step(i)
-        with torch.cuda.stream(stream):
-            graph.replay()
-        torch.cuda.synchronize(dev)
-    except Exception as exc:  # capture unsupported here: time the eager loop instead
-        graph = None
-        timing_note = f"eager (graph capture failed: {type(exc).__name__})"
-    else:
-        timing_note = f"CUDA graph of {G} steps replayed {args.steps // G} times"
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    # graph.replay() launches on torch's current stream: make that the timed stream
-    with ClockSampler(uuid) as clk, torch.cuda.stream(stream):
-        ev0.record(stream)
-        if graph is not None:
-            for _ in range(args.steps // G):
-                graph.replay()
-        else:
-            for i in range(args.steps):
-                step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    fpx.check(proj.device_status(stream.cuda_stream))
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    pk, pk_src = peaks()
+
+    w = fpsynth.WORKLOADS[args.workload]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    flops, alg_bytes = algorithmic(w)
+    run = ForwardRun(torch, fpx, dev, w, cluster=args.cluster, group_m=args.group_m)
+    ms = run.time(args.steps, args.warmup, uuid, dist)
     ms = max_over_ranks(ms, dev)
     total_flops = flops * world
     value = total_flops / (ms * 1e-3) / 1e12
     tokens_per_s = w.M * world / (ms * 1e-3)
+    clocks = run.clocks
 
     # ---- end to end through the public API with pinned host buffers
-    hx = torch.empty(xs[0].shape, dtype=tdt, pin_memory=True)
-    hx.copy_(xs[0].cpu())
+    proj, outs, stream = run.proj, run.outs[0], run.stream
+    hx = torch.empty(run.xs[0].shape, dtype=tdt, pin_memory=True)
+    hx.copy_(run.xs[0].cpu())
     host_outs = [None if o is None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
                  for o in outs]
-    dx = torch.empty_like(xs[0])
+    dx = torch.empty_like(run.xs[0])
     h2d = hx.numel() * hx.element_size()
     d2h = sum(o.numel() * o.element_size() for o in host_outs if o is not None)
     e2e_steps = max(3, min(args.steps, 30))
 
     def e2e_step():
         dx.copy_(hx, non_blocking=True)
-        o = proj.forward(dx, Ws[0], bs[0], None, channel_dim=w.channel_dim,
+        o = proj.forward(dx, run.Ws[0], run.bs[0], None, channel_dim=w.channel_dim,
                          n_batch_dims=w.n_batch_dims, out=outs, stream=stream.cuda_stream)
         for h, d in zip(host_outs, o):
             if h is not None:
                 h.copy_(d, non_blocking=True)
 
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -359,25 +539,9 @@ def main():
         torch.cuda.synchronize(dev)
     e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
-
-    pk, pk_src = peaks()
-    tensor_time = flops / (pk["bf16_tflops"] * 1e12)
-    hbm_time = alg_bytes / (pk["hbm_gbs"] * 1e9)
-    if w.dtype == "bf16" and tensor_time >= hbm_time:
-        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": alg_bytes / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(w, ms, pk, pk_src, sm_count)
     roof["traffic"] = recorded_traffic(w.name)
-    roof["peak_source"] = f"{pk_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})"
     roof["kernel_hash"] = kernel_hash()
-
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -388,18 +552,47 @@ def main():
                    "C": w.C, "F": w.F, "heads": w.heads, "head_dim": w.head_dim, "N": w.N,
                    "tokens": w.M, "act": fpsynth.ACT_NAMES[w.act], "rope_base": w.rope_base,
                    "bias": w.bias, "parallelism": f"replicas x{world}",
-                   "cta_cluster": args.cluster,
-                   "l2": f"inputs rotate over {n_sets} copies ({n_sets * in_bytes / 1e6:.0f} MB) "
-                         f"> L2 129 MB; each step also writes {w.M * w.N * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB",
-                   "timing": timing_note},
-        "gpu_launches": launches_per_step * args.steps,
+                   "cta_cluster": args.cluster, "l2": run.l2_note(), "timing": run.timing_note},
+        "gpu_launches": run.launches_per_step * args.steps,
         "roofline": roof,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
+    run.close()
+
+    # ---- every other configuration, each with its own timing, clocks and roofline
+    if not args.no_per_config and world == 1 and rank == 0:
+        per = []
+        names = [(n, False) for n in PER_CONFIG if n != w.name] + [(w.name, True)]
+        for name, explicit_pos in names:
+            cw = fpsynth.WORKLOADS[name]
+            if explicit_pos and cw.rope_base <= 0:
+                continue
+            r = ForwardRun(torch, fpx, dev, cw, explicit_pos=explicit_pos, cluster=args.cluster)
+            n = steps_for(r)
+            cms = r.time(n, 5, uuid)
+            extra = {"positions": "caller int32 [T] (rotary table rebuilt every call)"} \
+                if explicit_pos else None
+            per.append(config_entry(cw, cms, roofline(cw, cms, pk, pk_src, sm_count), r.clocks, n,
+                                    r.timing_note, r.launches_per_step, extra))
+            r.close()
+        if w.dtype == "bf16":
+            bms, bclk, bn, blaunch = time_backward_run(torch, fpx, dev, w, uuid)
+            bfl, bby = backward_algorithmic(w)
+            e = config_entry(w, bms, roofline(w, bms, pk, pk_src, sm_count, bfl, bby),
+                             bclk, bn, "eager loop of fp_backward calls", blaunch,
+                             {"pass": "backward", "flops_per_step": bfl})
+            e["tflops"] = bfl / (bms * 1e-3) / 1e12
+            per.append(e)
+        per.append(time_attention(torch, fpx, dev, uuid, pk, pk_src, sm_count))
+        line["per_config"] = per
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, run.inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -413,6 +606,77 @@ def backward_algorithmic(w: fpsynth.Workload):
     bytes_ = (w.M * w.C + w.C * w.N + (w.N if w.bias else 0) + w.M * w.N + w.M * w.C) * 2 \
         + (w.C * w.N + (w.N if w.bias else 0)) * 4
     return flops, bytes_
+
+
+class BackwardRun:
+    """fp_backward on one workload, set up for timing: input and upstream
+    gradient sets rotated so that one pass over them exceeds twice the L2."""
+
+    def __init__(self, torch, fpx, dev, w):
+        self.torch, self.fpx, self.dev, self.w = torch, fpx, dev, w
+        self.inp = inp = fpsynth.make_inputs(w)
+        self.grads = grads = fpsynth.make_grads(w)
+        to_dev = to_device_fn(torch, dev, "bf16")
+        self.in_bytes = (w.M * w.C + w.C * w.N + w.M * w.N) * 2
+        self.n_sets = max(1, int(np.ceil(2 * L2_BYTES / self.in_bytes)))
+        self.sets = [(to_dev(inp["x"]), to_dev(inp["W"]), to_dev(inp["b"]),
+                      tuple(to_dev(grads[k]) for k in ("ff", "q", "k", "v")))
+                     for _ in range(self.n_sets)]
+        self.proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                                        w.n_query_groups, w.rope_n_elem, w.k_transposed)
+        self.proj.reserve(w.T)
+        self.stream = torch.cuda.Stream(device=dev)
+        x0 = self.sets[0][0]
+        L = fpx.make_layout(x0.shape, x0.stride(), w.channel_dim, w.n_batch_dims, fpx.FP_BF16)
+        st, ws_bytes = fpx.fp_backward_workspace_size(self.proj.plan, L)
+        fpx.check(st)
+        self.ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+        self.dx = torch.empty_strided(x0.shape, x0.stride(), dtype=torch.bfloat16, device=dev)
+
+    def step(self, i):
+        x, W, b, g = self.sets[i % self.n_sets]
+        w = self.w
+        return self.proj.backward(x, W, b, g, None, channel_dim=w.channel_dim,
+                                  n_batch_dims=w.n_batch_dims, dx=self.dx, workspace=self.ws,
+                                  stream=self.stream.cuda_stream)
+
+    def time(self, steps, warmup, uuid, dist=None):
+        torch, fpx = self.torch, self.fpx
+        with torch.cuda.stream(self.stream):
+            for i in range(max(3, warmup)):
+                self.step(i)
+        torch.cuda.synchronize(self.dev)
+        fpx.check(self.proj.device_status(self.stream.cuda_stream))
+        self.launches_per_step = self.proj.last_launch_count
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        with ClockSampler(uuid) as clk, torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            for i in range(steps):
+                self.step(i)
+            ev1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+        if dist:
+            dist.barrier()
+        fpx.check(self.proj.device_status(self.stream.cuda_stream))
+        self.clocks = clk.summary()
+        return ev0.elapsed_time(ev1) / steps
+
+    def close(self):
+        self.proj.close()
+        del self.sets, self.ws, self.dx
+        self.torch.cuda.empty_cache()
+
+
+def time_backward_run(torch, fpx, dev, w, uuid, steps=100):
+    r = BackwardRun(torch, fpx, dev, w)
+    ms = r.time(steps, 5, uuid)
+    out = (ms, r.clocks, steps, r.launches_per_step)
+    r.close()
+    return out
 
 
 def main_backward(args, rank, world, local):
@@ -430,68 +694,19 @@ def main_backward(args, rank, world, local):
     w = fpsynth.WORKLOADS[args.workload]
     if w.dtype != "bf16":
         raise SystemExit("the backward takes bf16 workloads")
-    inp = fpsynth.make_inputs(w)
-    grads = fpsynth.make_grads(w)
-
-    def to_dev(a):
-        if a is None:
-            return None
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    flops, alg_bytes = backward_algorithmic(w)
-    in_bytes = (w.M * w.C + w.C * w.N + w.M * w.N) * 2
-    n_sets = max(1, int(np.ceil(2 * L2_BYTES / in_bytes)))
-    sets = [(to_dev(inp["x"]), to_dev(inp["W"]), to_dev(inp["b"]),
-             tuple(to_dev(grads[k]) for k in ("ff", "q", "k", "v"))) for _ in range(n_sets)]
-    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
-                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
-    proj.reserve(w.T)
-    stream = torch.cuda.Stream(device=dev)
-    L = fpx.make_layout(sets[0][0].shape, sets[0][0].stride(), w.channel_dim, w.n_batch_dims,
-                        fpx.FP_BF16)
-    st, ws_bytes = fpx.fp_backward_workspace_size(proj.plan, L)
-    fpx.check(st)
-    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
-    dx = torch.empty_strided(sets[0][0].shape, sets[0][0].stride(), dtype=torch.bfloat16,
-                             device=dev)
-    res = None
-
-    def step(i):
-        nonlocal res
-        x, W, b, g = sets[i % n_sets]
-        res = proj.backward(x, W, b, g, None, channel_dim=w.channel_dim,
-                            n_batch_dims=w.n_batch_dims, dx=dx, workspace=ws,
-                            stream=stream.cuda_stream)
-
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            step(i)
-    torch.cuda.synchronize(dev)
-    fpx.check(proj.device_status(stream.cuda_stream))
-    launches_per_step = proj.last_launch_count
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = str(local)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(uuid) as clk, torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dev)
-    fpx.check(proj.device_status(stream.cuda_stream))
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    flops, alg_bytes = backward_algorithmic(w)
+    run = BackwardRun(torch, fpx, dev, w)
+    ms = max_over_ranks(run.time(args.steps, args.warmup, uuid, dist), dev)
     value = flops * world / (ms * 1e-3) / 1e12
+    proj, stream, dx, ws = run.proj, run.stream, run.dx, run.ws
 
     # end to end: upstream gradients and x from pinned host memory, dx, dW, db back
-    x0, W0, b0, g0 = sets[0]
+    x0, W0, b0, g0 = run.sets[0]
     hx = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True)
     hx.copy_(x0.cpu())
     hg = [None if g is None else torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in g0]
@@ -520,6 +735,8 @@ def main_backward(args, rank, world, local):
         if hdb is not None:
             hdb.copy_(ddb, non_blocking=True)
 
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -531,9 +748,8 @@ def main_backward(args, rank, world, local):
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dev)
 
     pk, pk_src = peaks()
-    roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
-            "unit": "TFLOP/s", "traffic": None, "peak_source": f"{pk_src} (burst)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(w, ms, pk, pk_src, sm_count, flops, alg_bytes)
+    roof["traffic"] = None
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -549,11 +765,12 @@ def main_backward(args, rank, world, local):
                    "head_dim": w.head_dim, "N": w.N, "tokens": w.M,
                    "act": fpsynth.ACT_NAMES[w.act], "bias": w.bias,
                    "flops_per_step": flops, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs rotate over {n_sets} sets ({n_sets * in_bytes / 1e6:.0f} MB) > L2 "
-                         f"129 MB", "timing": "eager loop of fp_backward calls"},
-        "gpu_launches": launches_per_step * args.steps,
+                   "l2": f"inputs rotate over {run.n_sets} sets "
+                         f"({run.n_sets * run.in_bytes / 1e6:.0f} MB) > L2 129 MB",
+                   "timing": "eager loop of fp_backward calls"},
+        "gpu_launches": run.launches_per_step * args.steps,
         "roofline": roof,
-        "clocks": clk.summary(),
+        "clocks": run.clocks,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
@@ -565,15 +782,15 @@ def main_backward(args, rank, world, local):
         while el < args.cpu_seconds and done < 64 * w.M:
             rows = np.sort(rng.choice(w.M, size=min(64, w.M), replace=False))
             t = time.perf_counter()
-            oracle.backward_workload(w, inp, grads, rows=rows, threads=cores)
+            oracle.backward_workload(w, run.inp, run.grads, rows=rows, threads=cores)
             el += time.perf_counter() - t
             done += len(rows)
-        rows = range(done)
         fl = 2.0 * done * w.C * (w.F + w.N)
         line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"dx of {done} token rows drawn from the {w.M} (ff "
                                           f"recompute + G W^T per row), fp64, {el:.1f} s"}
+    run.close()
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
