@@ -495,6 +495,34 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
       }
       box[2 + d] = 1;
     }
+    if (pr.a_mn && ta.S_in % 64 == 0 && tk.n_outer_dims <= 2) {
+      // unit token stride, whole 64-token blocks: tokens become (64 inside a
+      // block, S_in/64 blocks), and one [2 blocks][64 ch][64 tok] box is a stage
+      // (the same shared-memory image as two [64 ch][64 tok] boxes; one TMA
+      // instruction instead of two measured 3 % faster on the Walrus shape)
+      gdim[0] = 64;
+      gdim[1] = p->C;
+      gdim[2] = ta.S_in / 64;
+      gstride[0] = static_cast<cuuint64_t>(tk.c_stride) * esz;
+      gstride[1] = 64ull * esz;
+      cuuint64_t prev = gstride[1];
+      for (int d = 0; d < 2; ++d) {
+        if (d < tk.n_outer_dims) {
+          gdim[3 + d] = tk.outer_size[d];
+          gstride[2 + d] = static_cast<cuuint64_t>(tk.outer_stride[d]) * esz;
+          prev = gstride[2 + d];
+        } else {
+          gdim[3 + d] = 1;
+          gstride[2 + d] = prev;
+        }
+      }
+      if (gstride[0] == 0 || gstride[0] % 16) gstride[0] = 16 * ((64 * esz + 15) / 16);
+      box[0] = 64;
+      box[1] = fp::kTcBK;
+      box[2] = 2;
+      box[3] = box[4] = 1;
+      tp.a_split = 1;
+    }
     CUresult r = encode(&tp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a.x),
                         gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -17,17 +17,21 @@
 //
 // Structure (one CTA per 128-query chunk, 8 warps):
 //   warp 0     TMA producer: the q chunk once, then k and v chunks into
-//              two-stage rings
+//              rings of 4 stages (head_dim 64) or 2 (head_dim 128)
 //   warp 1     MMA issuer (one thread): S = q k^T into one of two TMEM score
 //              buffers (M 128, N 128, K head_dim), then O += P v into the TMEM
 //              output accumulator (M 128, N head_dim, K 128); the next chunk's
 //              scores are issued before this chunk's P v, so the tensor core
 //              works while the softmax runs
 //   warps 4-7  softmax, one query row per thread (TMEM lane = row): scores
-//              from TMEM, running maximum m and sum l, P = 2^(s c - m) rounded
-//              to bf16 into shared memory (the A operand of P v); when m grows
-//              the output accumulator is rescaled in TMEM first. At the end
-//              O / l is rounded to bf16 and stored.
+//              from TMEM, a reference maximum m and the sum l, P = 2^(s c - m)
+//              rounded to bf16 into one of two shared-memory buffers (the A
+//              operand of P v), so the next chunk's P is written while the
+//              tensor core still reads this one. m is raised only when a
+//              chunk's maximum exceeds it by more than 8 (log2 units): P then
+//              stays below 2^8, and the output accumulator is rescaled in TMEM
+//              only at those rare steps. At the end O / l is rounded to bf16
+//              and stored.
 // Shared-memory operands use the 128-byte swizzle TMA writes and the MMA reads;
 // P is written by the softmax threads in the same swizzled K-major layout.
 // Every mbarrier wait is bounded: a wait that runs out records a timeout in
@@ -43,21 +47,25 @@ namespace {
 constexpr int QB = 128;   // queries per CTA: one per softmax thread and TMEM lane
 constexpr int KB = 128;   // keys per chunk: the N of S and the K of P v
 constexpr int ANT = 256;  // 8 warps
-constexpr int RING = 2;   // k and v stages
 constexpr int ATOM = QB * 128;  // a [128 rows][64 bf16] 128-byte-swizzled atom: 16 KB
 constexpr int CHUNK = 64 * 128; // a [64 rows][64 bf16] atom: 8 KB
 
 template <int HD>
 struct ACfg {
+  // k and v stages: a chunk's loads are requested about one chunk's softmax
+  // ahead of their use, less than the L2 latency under load, so the ring is
+  // as deep as shared memory allows
+  static constexpr int RING = HD == 64 ? 4 : 2;
   static constexpr int Q_BYTES = QB * HD * 2;
   static constexpr int K_BYTES = KB * HD * 2;
   static constexpr int V_BYTES = KB * HD * 2;
-  static constexpr int P_BYTES = QB * KB * 2;
+  static constexpr int P_BYTES = QB * KB * 2;  // one P buffer; there are two
   // q_full; k full/empty and v full/empty per stage; s full/empty per score
-  // buffer; p_full; o_done; drain
-  static constexpr int NUM_BARS = 1 + 4 * RING + 4 + 3;
+  // buffer; p full and P v done per P buffer; drain
+  static constexpr int NUM_BARS = 1 + 4 * RING + 4 + 4 + 1;
+  static_assert(RING <= 4, "armed-barrier bit masks hold 1 + 2 * RING slots");
   static constexpr int SMEM_BYTES =
-      1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + P_BYTES + NUM_BARS * 8 + 16;
+      1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + 2 * P_BYTES + NUM_BARS * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static constexpr int O_COL = 2 * KB;  // TMEM: scores in [0, 256), output in [256, 256 + HD)
 };
@@ -65,6 +73,7 @@ struct ACfg {
 template <int HD, bool KT>
 __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant__ AttnParams p) {
   using G = ACfg<HD>;
+  constexpr int RING = G::RING;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const uint32_t k_s = q_s + G::Q_BYTES;                   // RING stages
   const uint32_t v_s = k_s + RING * G::K_BYTES;            // RING stages
   const uint32_t p_s = v_s + RING * G::V_BYTES;
-  const uint32_t bar0 = p_s + G::P_BYTES;
+  const uint32_t bar0 = p_s + 2 * G::P_BYTES;
   const uint32_t q_full = bar0;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto k_empty = [&](int s) { return bar0 + 8u * (1 + RING + s); };
@@ -82,10 +91,11 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const uint32_t bar1 = bar0 + 8u * (1 + 4 * RING);
   auto s_full = [&](int b) { return bar1 + 8u * b; };
   auto s_empty = [&](int b) { return bar1 + 8u * (2 + b); };
-  const uint32_t p_full = bar1 + 8u * 4;
-  const uint32_t o_done = bar1 + 8u * 5;
-  const uint32_t drain = bar1 + 8u * 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 7 - sbase));
+  // P buffer b: full once the softmax wrote it, done once P v has read it
+  auto p_full = [&](int b) { return bar1 + 8u * (4 + b); };
+  auto pv_done = [&](int b) { return bar1 + 8u * (6 + b); };
+  const uint32_t drain = bar1 + 8u * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 9 - sbase));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,8 +118,10 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), 4);  // the four softmax warps
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(p_full(b), 4);
+      mbar_init(pv_done(b), 1);
+    }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -216,19 +228,20 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       if (ok && nkb > 0) ok = issue_scores(0);
       for (int j = 0; ok && j < nkb; ++j) {
         if (j + 1 < nkb && !issue_scores(j + 1)) break;
-        const int s = j % RING;
-        if (!wait_bounded(p_full, j & 1, wc, true)) break;
+        const int s = j % RING, pb = j & 1;
+        if (!wait_bounded(p_full(pb), (j >> 1) & 1, wc, true)) break;
         if (!wait_bounded(v_full(s), (j / RING) & 1, wc, true)) break;
         tc_fence_after();
         const uint32_t vd = v_s + s * G::V_BYTES;
+        const uint32_t pd = p_s + pb * G::P_BYTES;
 #pragma unroll
         for (int k = 0; k < KB / 16; ++k) {
-          const uint64_t a_desc = sw128_desc(p_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+          const uint64_t a_desc = sw128_desc(pd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
           const uint64_t b_desc =
               sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
           umma_bf16<1>(tmem + G::O_COL, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
         }
-        umma_commit<1>(o_done);
+        umma_commit<1>(pv_done(pb));
         umma_commit<1>(v_empty(s));
       }
       if (issued) {
@@ -242,7 +255,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = p.scale_log2e;
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_ref = -INFINITY, l_run = 0.0f;
     bool alive = true;
     for (int j = 0; j < nkb; ++j) {
       const int b = j & 1;
@@ -259,46 +272,76 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty(b));  // the score buffer may be overwritten
-      // scores in log2 units, keys past Tk masked out
+      // keys past Tk masked out (only the last chunk can hold any); the maxima
+      // are taken on the raw scores (the scale c is positive), eight
+      // independent partial maxima and sums keep the dependency chains short
       const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(j) * KB);
-      float t[KB];
-      float m_blk = -INFINITY;
+      if (valid < KB) {
 #pragma unroll
-      for (int i = 0; i < KB; ++i) {
-        t[i] = i < valid ? __uint_as_float(sv[i]) * c : -INFINITY;
-        m_blk = fmaxf(m_blk, t[i]);
+        for (int i = 0; i < KB; ++i)
+          if (i >= valid) sv[i] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m_run, m_blk);
-      const float alpha = ex2_approx(m_run - m_new);  // 0 on the first chunk
-      // P = 2^(t - m), rounded to bf16; the row sum takes the rounded values
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < KB; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]));
+      const float m_blk = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // the reference maximum (log2 units) moves only when this chunk's maximum
+      // exceeds it by more than 8 (P <= 2^8); the first chunk sets it
+      const bool raise = j == 0 || m_blk > m_ref + 8.0f;
+      const float m_new = raise ? fmaxf(m_ref, m_blk) : m_ref;
+      const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.0f;  // 0 on the first chunk
+      // P = 2^(s c - m) on packed pairs (one fma.f32x2 per two scores), rounded
+      // to bf16 for the tensor core; the row sum adds the fp32 values
       uint32_t pw[KB / 2];
-      float sum = 0.0f;
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ps[k] = 0.0f;
+      const uint64_t c2 = f2_splat(c), nm2 = f2_splat(-m_new);
 #pragma unroll
       for (int i = 0; i < KB / 2; ++i) {
-        pw[i] = pack_bf16x2(ex2_approx(t[2 * i] - m_new), ex2_approx(t[2 * i + 1] - m_new));
-        sum += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2,
+                         nm2),
+                  x0, x1);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        pw[i] = pack_bf16x2(e0, e1);
+        ps[i & 7] += e0 + e1;
       }
+      const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_run = l_run * alpha + sum;
-      m_run = m_new;
-      if (j > 0) {
-        // P and the output accumulator are free once the previous P v has run
-        if (!__all_sync(0xFFFFFFFFu, wait_bounded(o_done, (j - 1) & 1, wc, true) ? 1 : 0)) {
+      m_ref = m_new;
+      const int pb = j & 1;
+      if (j >= 2) {
+        // this P buffer is free once the P v of two chunks ago has read it
+        if (!__all_sync(0xFFFFFFFFu,
+                        wait_bounded(pv_done(pb), ((j - 2) >> 1) & 1, wc, true) ? 1 : 0)) {
           alive = false;
           break;
         }
         tc_fence_after();
       }
       // P row into the swizzled K-major atoms: 16-byte chunk ch of row r at ch ^ (r & 7)
+      const uint32_t pd = p_s + pb * G::P_BYTES;
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t addr = p_s + a * ATOM + row * 128 + ((ch ^ (row & 7)) << 4);
+          const uint32_t addr = pd + a * ATOM + row * 128 + ((ch ^ (row & 7)) << 4);
           const int w0 = a * 32 + ch * 4;
           st_shared_v4(addr, pw[w0], pw[w0 + 1], pw[w0 + 2], pw[w0 + 3]);
         }
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-        // the running maximum grew: scale the output accumulated so far
+        // a raised maximum: the output accumulated so far is scaled once the
+        // previous chunk's P v has landed in it
+        if (!__all_sync(0xFFFFFFFFu,
+                        wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int q = 0; q < HD / 32; ++q) {
           uint32_t o[32];
@@ -313,10 +356,11 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       fence_async_shared();  // P visible to the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(pb));
     }
     if (alive && nkb > 0 &&
-        __all_sync(0xFFFFFFFFu, wait_bounded(o_done, (nkb - 1) & 1, wc, true) ? 1 : 0)) {
+        __all_sync(0xFFFFFFFFu,
+                   wait_bounded(pv_done((nkb - 1) & 1), ((nkb - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
       tc_fence_after();
       const float inv = 1.0f / l_run;
       const int64_t qi = q0 + row;

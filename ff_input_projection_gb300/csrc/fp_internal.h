@@ -68,6 +68,9 @@ struct TcParams {
   // bias [N] as a 1-row 2-D map (64-column boxes), when there is a bias
   CUtensorMap tmap_bias;
   int tma_store;  // 1: the output maps are valid
+  // 1: the MN-major x map views each slab's tokens as (64 inside a block,
+  // S_in/64 blocks), so one box loads both 64-token chunks of a stage
+  int a_split;
   TokenMap tok;
   Epilogue epi;
   int C;

@@ -11,7 +11,7 @@
 // multiples of 16.
 //
 // Tile: 128 tokens x 128 fused columns, k-steps of 16, 256 threads with an
-// 8x8 register block each (rows ty*4+{0..3} and 64+ty*4+{0..3}, columns
+// 8x8 register block each (accumulated on packed fp32 pairs) (rows ty*4+{0..3} and 64+ty*4+{0..3}, columns
 // likewise), operands double-buffered in shared memory with a register
 // prefetch of the next k-step. The epilogue stages the fp32 tile in shared
 // memory so a rotary pair (lane i, lane i + half) can be read by whichever
@@ -218,11 +218,16 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
     }
   };
 
-  float acc[8][8];
+  // accumulators as packed fp32 pairs along the column index: acc2[i][t] holds
+  // columns 2t and 2t+1 of row i. One fma.rn.f32x2 is two IEEE fp32 FMAs (the
+  // same results as two scalar ones), so the 8 x 8 outer product of a k-step
+  // issues as 32 packed FMAs and 8 splats instead of 64 FMAs: the FMA pipe,
+  // not instruction issue, becomes the limit.
+  uint64_t acc2[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int t = 0; t < 4; ++t) acc2[i][t] = 0ull;
 
   const int num_k = (C + BK - 1) / BK;
   load_regs(0);
@@ -239,12 +244,15 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
       float4 a1 = *reinterpret_cast<const float4*>(a + kk * BM + 64 + ty * 4);
       float4 b0 = *reinterpret_cast<const float4*>(b + kk * BN + tx * 4);
       float4 b1 = *reinterpret_cast<const float4*>(b + kk * BN + 64 + tx * 4);
-      float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint64_t bv2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                               f2_pack(b1.z, b1.w)};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t ai = f2_splat(av[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int t = 0; t < 4; ++t) acc2[i][t] = f2_fma(ai, bv2[t], acc2[i][t]);
+      }
     }
     if (kb + 1 < num_k) store_regs(buf ^ 1);
     __syncthreads();
@@ -255,10 +263,11 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
-    *reinterpret_cast<float4*>(Cs + r * CS_LD + tx * 4) =
-        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    *reinterpret_cast<float4*>(Cs + r * CS_LD + 64 + tx * 4) =
-        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    float c[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) f2_unpack(acc2[i][t], c[2 * t], c[2 * t + 1]);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + tx * 4) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + 64 + tx * 4) = make_float4(c[4], c[5], c[6], c[7]);
   }
   __syncthreads();
 

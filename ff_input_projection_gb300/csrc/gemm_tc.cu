@@ -10,14 +10,14 @@
 // q/k/v [B*heads, T, head_dim] (memory-efficient-attention issue #7, the
 // [batch*heads, tokens, head_dim] layout).
 //
-// Structure (one persistent CTA per SM, 14 warps; CTA pairs by default):
+// Structure (one persistent CTA per SM, 10 warps; CTA pairs by default):
 //   warp 0     TMA producer: loads x and W tiles into a shared ring (5 stages
 //              of 32 KB in a pair, 3 of 48 KB alone), and each tile's bias
 //              row into a bias operand
 //   warp 1     allocates 512 TMEM columns; in the even CTA one thread issues
 //              tcgen05.mma (2-SM M=256 or 1-SM M=128; N=256, K=16, bf16 in,
 //              fp32 accumulate) and commits completion to mbarriers
-//   warps 2-13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
+//   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //              per thread), activation / rotation in registers, bf16
 //              round-to-nearest-even, TMA tensor stores of 32 x 32 (ff) and
 //              32 x 16 (q/k/v) blocks
@@ -35,7 +35,8 @@
 //
 // Operand layouts (128-byte swizzle, as written by TMA and read by the MMA):
 //   A, row-major x (unit channel stride): K-major, [128 rows][64 ch] per stage.
-//   A, channels-first x (unit token stride): MN-major, two [64 ch][64 tok] chunks.
+//   A, channels-first x (unit token stride): MN-major, two [64 ch][64 tok] chunks
+//      (one TMA box of [2][64][64] when the slab length is a multiple of 64).
 //   B, W [C, N] row-major: MN-major (N contiguous), four [64 ch][64 col] chunks.
 //
 // Every mbarrier wait is bounded (%globaltimer); a wait that runs out records
@@ -51,10 +52,21 @@ namespace {
 
 constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK;
 constexpr int UMMA_K = 16;
-constexpr int NUM_EPI_WARPS = 12;  // 3 per SM sub-partition (one per TMEM lane quarter each)
-constexpr int NT = 32 * (2 + NUM_EPI_WARPS);
-// registers are granted per 4 warps: 14 warps count as 16, so 128 a thread fit
-static_assert(((NT / 32 + 3) / 4 * 4) * 32 * 128 <= 65536, "register budget");
+// Epilogue warps per SM sub-partition, each reading one TMEM lane quarter.
+// Forward: two per quarter (168 registers each) measured faster than three
+// (128 registers) on every bf16 workload and one (184) slower: the epilogue
+// keeps up with the main loop, and fewer warps put fewer stores in flight
+// beside the MMAs. The backward's ff-gradient mode (upstream-gradient loads,
+// act', column sums) keeps three: with two it measured 2 % slower.
+template <bool GRAD>
+struct Warps {
+  static constexpr int EPQ = GRAD ? 3 : 2;
+  static constexpr int EPI = 4 * EPQ;
+  static constexpr int NT = 32 * (2 + EPI);
+  static constexpr int REGS = GRAD ? 128 : 168;
+  // registers are granted per 4 warps (10 warps count as 12, 14 as 16)
+  static_assert(((NT / 32 + 3) / 4 * 4) * 32 * REGS <= 65536, "register budget");
+};
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB: this CTA's 128 token rows
 constexpr int CHUNK_BYTES = 64 * BK * 2;         // one [64 ch][64 elems] MN-major chunk, 8 KB
 constexpr int ACC_COLS = BN;                     // fp32 accumulator: one TMEM column per output column
@@ -65,14 +77,14 @@ constexpr int BIAS_A_BYTES = 2 * 1024;
 // per epilogue warp, two 2 KB buffers staging a [32 rows][32 bf16] block (ff)
 // or a [32 rows][16 bf16] block (q/k/v, mixed tiles) for a TMA store
 constexpr int STAGING_BYTES_PER_WARP = 2 * 2048;
-constexpr int STAGING_BYTES = NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
 static_assert(TMEM_COLS == 512, "TMEM holds 512 columns");
 
 // Per cluster size: a single CTA holds all 256 W columns of its tile; a CTA
 // pair runs 2-SM MMAs (M = 256), each CTA holding its own 128 token rows and
 // its own 128 of the 256 W columns, so a stage is 32 KB instead of 48 KB.
-template <int CL>
+template <int CL, int EPI>
 struct Cfg {
+  static constexpr int STAGING_BYTES = EPI * STAGING_BYTES_PER_WARP;
   static constexpr int B_COLS = BN / CL;
   static constexpr int B_BYTES = B_COLS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -209,8 +221,13 @@ __device__ __forceinline__ void rotate_small(float (&v)[16], const float2* cs, i
 // the ff block and its output is g_ff * act'(x W + b) (same GEMM, bias in the
 // MMA), with column sums into db.
 template <bool A_MN_MAJOR, int ACT, int CL, bool GRAD = false>
-__global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using G = Cfg<CL>;
+__global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  constexpr int NT = Warps<GRAD>::NT;
+  constexpr int NUM_EPI_WARPS = Warps<GRAD>::EPI;
+  constexpr int EPI_PER_QUARTER = Warps<GRAD>::EPQ;
+  using G = Cfg<CL, NUM_EPI_WARPS>;
+  constexpr int STAGING_BYTES = G::STAGING_BYTES;
   constexpr int STAGES = G::STAGES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -345,7 +362,10 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           if (peer) {
             // the even CTA armed its full barrier for these bytes too
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (A_MN_MAJOR) {
+            if (A_MN_MAJOR && p.a_split) {
+              tma_load_5d_peer(a_dst, &p.tmap_a, fb, 0, k0, static_cast<int>(tc.s0 >> 6), oc[0],
+                               oc[1]);
+            } else if (A_MN_MAJOR) {
               tma_load_5d_peer(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1],
                                oc[2]);
               tma_load_5d_peer(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64,
@@ -363,7 +383,10 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             } else {
               const uint32_t fb = full_bar(stage);
               mbar_arrive_expect_tx(fb, CL * STAGE_BYTES);  // both CTAs' halves
-              if (A_MN_MAJOR) {
+              if (A_MN_MAJOR && p.a_split) {
+                tma_load_5d(a_dst, &p.tmap_a, fb, 0, k0, static_cast<int>(tc.s0 >> 6), oc[0],
+                            oc[1]);
+              } else if (A_MN_MAJOR) {
                 tma_load_5d(a_dst, &p.tmap_a, fb, static_cast<int>(tc.s0), k0, oc[0], oc[1],
                             oc[2]);
                 tma_load_5d(a_dst + CHUNK_BYTES, &p.tmap_a, fb, static_cast<int>(tc.s0) + 64, k0,
@@ -468,7 +491,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     // ------------------------------------------------ epilogue warps
     const Epilogue& e = p.epi;
     const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    const int part = (warp - 2) >> 2;              // which of every 3 work units it takes
+    const int part = (warp - 2) >> 2;              // which of a quarter's work units it takes
     const int row = quarter * 32 + lane;
     const int rh = e.rope_half;
     const int nkv = e.groups > 0 ? e.groups : e.heads;
@@ -479,7 +502,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
     // quarter-warp stores at once fall in distinct banks
     const uint32_t swz = ((lane >> 2) & 1u) * 16u;
     uint32_t stage_sel = 0;  // alternates this warp's two staging buffers
-    // a quarter's three warps take its work units round-robin; the count runs
+    // a quarter's warps take its work units round-robin; the count runs
     // on across tiles, so a tile whose unit count is not a multiple of 3 does
     // not always load the same warp
     int turn = 0;
@@ -544,7 +567,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
         const uint32_t sw64 = (lane >> 1) & 3u;
         for (int c = 0; c < cols; c += 32) {
           const bool mine = turn == part;
-          turn = turn == 2 ? 0 : turn + 1;
+          turn = turn + 1 == EPI_PER_QUARTER ? 0 : turn + 1;
           if (!mine) continue;
           uint32_t v_u[32];
           tmem_ld32(t_row + c, v_u);
@@ -630,7 +653,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
             // rotated pairs (j, j + rh), 16 lanes at a time
             for (int j = 0; j < rh; j += 16) {
               const bool mine = turn == part;
-              turn = turn == 2 ? 0 : turn + 1;
+              turn = turn + 1 == EPI_PER_QUARTER ? 0 : turn + 1;
               if (!mine) continue;
               uint32_t lo_u[16], hi_u[16];
               tmem_ld16(t_head + j, lo_u);
@@ -675,7 +698,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           }
           for (int j = j0; j < e.hd; j += 16) {
             const bool mine = turn == part;
-            turn = turn == 2 ? 0 : turn + 1;
+            turn = turn + 1 == EPI_PER_QUARTER ? 0 : turn + 1;
             if (!mine) continue;
             uint32_t v_u[16];
             tmem_ld16(t_head + j, v_u);
@@ -732,7 +755,7 @@ __global__ void __launch_bounds__(NT, 1) tc_gemm_kernel(const __grid_constant__ 
           const bool rope_small = rh > 0 && rh <= 8 && qk && ci.j == 0;
           if (rope && ci.j >= rh) continue;  // the high half is written with its low partner
           const bool mine = turn == part;
-          turn = turn == 2 ? 0 : turn + 1;
+          turn = turn + 1 == EPI_PER_QUARTER ? 0 : turn + 1;
           if (!mine) continue;
           uint16_t* const dst =
               ci.seg == 0 ? ff_row + ci.j
@@ -866,13 +889,13 @@ cudaError_t launch_variant(const TcParams& p, int num_ctas, cudaStream_t stream)
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<CL>::SMEM_BYTES);
+                               Cfg<CL, Warps<GRAD>::EPI>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<CL>::SMEM_BYTES;
+  cfg.blockDim = dim3(Warps<GRAD>::NT, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<CL, Warps<GRAD>::EPI>::SMEM_BYTES;
   cfg.stream = stream;
   // programmatic dependent launch: the prologue may overlap the previous
   // launch's tail (the kernel waits on it before touching global memory)

@@ -15,23 +15,27 @@
 
 namespace fp {
 
+// One block row per frequency (blockIdx.y = f): the inverse frequency
+// base^(-2f/n_elem) is formed once per block in fp64 (FP64 throughput is low
+// on this part), each thread then forms and reduces its token's angle.
 __global__ void rope_table_kernel(float2* __restrict__ cs, const int32_t* __restrict__ pos,
-                                  int64_t T, int half, int n_elem, double log2_base) {
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= T * half) return;
-  const int f = static_cast<int>(i / T);
-  const int64_t t = i - static_cast<int64_t>(f) * T;
-  double p = pos ? static_cast<double>(pos[t]) : static_cast<double>(t);
-  double inv_freq = exp2(-(2.0 * f / n_elem) * log2_base);
-  double a = p * inv_freq;
+                                  int64_t T, int n_elem, double log2_base) {
+  __shared__ double inv_freq_s;
+  const int f = static_cast<int>(blockIdx.y);
+  if (threadIdx.x == 0) inv_freq_s = exp2(-(2.0 * f / n_elem) * log2_base);
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const double p = pos ? static_cast<double>(pos[t]) : static_cast<double>(t);
+  const double a = p * inv_freq_s;
   const double two_pi_hi = 6.283185307179586232;      // nearest double to 2*pi
   const double two_pi_lo = 2.4492935982947064e-16;    // 2*pi - two_pi_hi
-  double k = rint(a * 0.15915494309189533577);        // a / (2*pi), nearest integer
+  const double k = rint(a * 0.15915494309189533577);  // a / (2*pi), nearest integer
   double r = fma(-k, two_pi_hi, a);
   r = fma(-k, two_pi_lo, r);
   float s, c;
   sincosf(static_cast<float>(r), &s, &c);
-  cs[i] = make_float2(c, s);
+  cs[static_cast<int64_t>(f) * T + t] = make_float2(c, s);
 }
 
 // Caller-given tables (the rope_one_entry listing's cos/sin inputs, [T, n_rot],
@@ -68,12 +72,10 @@ cudaError_t launch_rope_import(float4* dst, const void* cosv, const void* sinv, 
 
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
                               double rope_base, cudaStream_t stream) {
-  int64_t n = T * half;
-  if (n == 0) return cudaSuccess;
-  int threads = 256;
-  int64_t blocks = (n + threads - 1) / threads;
-  rope_table_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(cs, pos, T, half, n_elem,
-                                                                            log2(rope_base));
+  if (T == 0 || half == 0) return cudaSuccess;
+  const int threads = 256;
+  const dim3 grid(static_cast<unsigned>((T + threads - 1) / threads), static_cast<unsigned>(half));
+  rope_table_kernel<<<grid, threads, 0, stream>>>(cs, pos, T, n_elem, log2(rope_base));
   return cudaGetLastError();
 }
 
