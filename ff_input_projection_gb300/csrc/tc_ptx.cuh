@@ -74,12 +74,24 @@ __device__ __forceinline__ void abort_launch(const WaitCtl& w) {
   atomicExch(w.status + 1, w.launch_tag);
 }
 
-// Wait for phase `parity` of an mbarrier, for at most limit_ns. Returns false
-// when the limit ran out (recorded as a timeout) or, if honor_abort, when
-// another role or CTA has aborted this launch.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& w,
-                                          bool honor_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The slow path of wait_bounded: poll for at most limit_ns. Returns false when
+// the limit ran out (recorded as a timeout) or, if honor_abort, when another
+// role or CTA has aborted this launch. Out of line, so the loop does not weigh
+// on the caller's registers.
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                               bool honor_abort) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -91,6 +103,16 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const W
       }
     }
   }
+}
+
+// Wait for phase `parity` of an mbarrier, for at most limit_ns (see the slow
+// path). The common case, a phase that has already completed, is one inline
+// non-blocking probe: a call of the out-of-line loop costs a few hundred cycles
+// even then (the caller's live registers are saved around it), which measured
+// 7 % of the forward kernel's time (Walrus 163 -> 152 us, same output bits).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                             bool honor_abort) {
+  return mbar_test_wait(bar, parity) || wait_bounded_slow(bar, parity, w, honor_abort);
 }
 
 // 5-D tiled TMA load into shared memory, completing on an mbarrier.
