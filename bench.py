@@ -61,6 +61,8 @@ def parse():
                     help="tensor-core path: CTA pairs sharing weight tiles (2) or single CTAs (1)")
     ap.add_argument("--group-m", type=int, default=0,
                     help="tensor-core tile rasterisation: M-tiles per group (0: the library's default)")
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 192, 256],
+                    help="tensor-core tile width without rotation (0: the library's choice)")
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
                     help="time fp_forward (default) or fp_backward (gradients of x, W, b)")
     return ap.parse_args()
@@ -279,7 +281,8 @@ class ForwardRun:
     """One forward configuration set up for timing: input and output sets
     rotated so that one pass over them exceeds twice the L2."""
 
-    def __init__(self, torch, fpx, dev, w, *, explicit_pos=False, cluster=2, group_m=0):
+    def __init__(self, torch, fpx, dev, w, *, explicit_pos=False, cluster=2, group_m=0,
+                 tile_n=0):
         self.torch, self.w, self.dev = torch, w, dev
         inp = fpsynth.make_inputs(w)
         self.inp = inp
@@ -297,6 +300,8 @@ class ForwardRun:
         self.proj.set_option(fpx.FP_OPT_CLUSTER, cluster)
         if group_m:
             self.proj.set_option(fpx.FP_OPT_GROUP_M, group_m)
+        if tile_n:
+            self.proj.set_option(fpx.FP_OPT_TILE_N, tile_n)
         self.proj.reserve(w.T)
         self.pos = torch.arange(w.T, dtype=torch.int32, device=dev) if explicit_pos else None
         self.stream = torch.cuda.Stream(device=dev)
@@ -498,7 +503,8 @@ def main():
     w = fpsynth.WORKLOADS[args.workload]
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     flops, alg_bytes = algorithmic(w)
-    run = ForwardRun(torch, fpx, dev, w, cluster=args.cluster, group_m=args.group_m)
+    run = ForwardRun(torch, fpx, dev, w, cluster=args.cluster, group_m=args.group_m,
+                     tile_n=args.tile_n)
     ms = run.time(args.steps, args.warmup, uuid, dist)
     ms = max_over_ranks(ms, dev)
     total_flops = flops * world
@@ -552,7 +558,7 @@ def main():
                    "C": w.C, "F": w.F, "heads": w.heads, "head_dim": w.head_dim, "N": w.N,
                    "tokens": w.M, "act": fpsynth.ACT_NAMES[w.act], "rope_base": w.rope_base,
                    "bias": w.bias, "parallelism": f"replicas x{world}",
-                   "cta_cluster": args.cluster, "l2": run.l2_note(), "timing": run.timing_note},
+                   "cta_cluster": args.cluster, "tile_n": args.tile_n or "auto", "l2": run.l2_note(), "timing": run.timing_note},
         "gpu_launches": run.launches_per_step * args.steps,
         "roofline": roof,
         "clocks": clocks,
@@ -569,7 +575,8 @@ def main():
             cw = fpsynth.WORKLOADS[name]
             if explicit_pos and cw.rope_base <= 0:
                 continue
-            r = ForwardRun(torch, fpx, dev, cw, explicit_pos=explicit_pos, cluster=args.cluster)
+            r = ForwardRun(torch, fpx, dev, cw, explicit_pos=explicit_pos, cluster=args.cluster,
+                           tile_n=args.tile_n)
             n = steps_for(r)
             cms = r.time(n, 5, uuid)
             extra = {"positions": "caller int32 [T] (rotary table rebuilt every call)"} \

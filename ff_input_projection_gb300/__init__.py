@@ -35,6 +35,7 @@ FP_OPT_GROUP_M = 3
 FP_OPT_MAX_CTAS = 4
 FP_OPT_CLUSTER = 5
 FP_OPT_BOUNDS_CHECK = 6
+FP_OPT_TILE_N = 7
 
 # the C ABI's entry points, as declared in include/fp.h
 EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_rope_table",

@@ -44,6 +44,7 @@ struct fp_plan {
   int max_ctas;
   int cluster;  // CTAs per cluster on the tensor-core path (1 or 2)
   int bounds_check;  // FP_OPT_BOUNDS_CHECK
+  int tile_n;        // FP_OPT_TILE_N
   uint32_t launch_seq;
   // Scratch grown inside a call is allocated in stream order on that call's
   // stream (scratch_stream); scratch_ready is recorded there after the growth,
@@ -291,6 +292,7 @@ struct Scratch {
   int max_ctas;
   int cluster;
   int bounds_check;  // 0 off, 1 on, 2 on against half-size extents (test of the check)
+  int tile_n;        // 0 automatic, 256 or 192 (tensor-core tiles without rotation)
 };
 
 // Every check of a forward call; touches no GPU.
@@ -600,6 +602,24 @@ fp_status launch(const fp_plan& P, const Prepared& pr, const Args& a, const Scra
     // two CTAs share each W tile when there are M-tiles to pair
     tp.cluster = (sc.cluster == 2 && tp.num_m_tiles >= 2) ? 2 : 1;
     tp.num_units = (tp.num_m_tiles + tp.cluster - 1) / tp.cluster * num_n_tiles;
+    tp.bn_mma = fp::kTcBN;
+    if (!pr.rope && tp.cluster == 2) {
+      // 192-column tiles only where 256-column tiles would compute at least
+      // 15 % more columns than N (N = 384: 512 against 384). Measured on the
+      // wave-quantised shapes instead (BERT ff, N = 3072 on 384 units of 256),
+      // 192 was 5-40 % slower: the operand traffic per FLOP grows by a third
+      // and the kernel runs at the rate the loads arrive, not at the wave fill.
+      const int64_t m_units = (tp.num_m_tiles + 1) / 2;
+      const int64_t c256 = (N + 255) / 256 * 256, c192 = (N + 191) / 192 * 192;
+      const bool use192 = sc.tile_n == 192 || (sc.tile_n == 0 && c192 * 100 <= c256 * 85);
+      if (use192) {
+        tp.bn_mma = 192;
+        tp.epi.bn_eff = 192;
+        tp.num_n_tiles = (N + 191) / 192;
+        tp.num_tiles = tp.num_m_tiles * tp.num_n_tiles;
+        tp.num_units = m_units * tp.num_n_tiles;
+      }
+    }
     if (tp.num_units * tp.cluster > INT32_MAX)
       return fail(FP_ERR_UNSUPPORTED_LAYOUT, "more than 2^31 output tiles");
     tp.group_m = sc.group_m;
@@ -716,6 +736,7 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->max_ctas = 0;
   p->cluster = kDefaultCluster;
   p->bounds_check = 0;
+  p->tile_n = 0;
   p->launch_seq = 0;
   p->scratch_stream = nullptr;
   p->scratch_ready = nullptr;
@@ -775,6 +796,11 @@ fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value) {
     case FP_OPT_CLUSTER:
       if (value != 1 && value != 2) return fail(FP_ERR_INVALID_ARG, "cluster must be 1 or 2");
       plan->cluster = static_cast<int>(value);
+      return ok();
+    case FP_OPT_TILE_N:
+      if (value != 0 && value != 256 && value != 192)
+        return fail(FP_ERR_INVALID_ARG, "tile width must be 0, 256 or 192");
+      plan->tile_n = static_cast<int>(value);
       return ok();
     case FP_OPT_BOUNDS_CHECK:
       if (value < 0 || value > 2) return fail(FP_ERR_INVALID_ARG, "bounds check must be 0, 1 or 2");
@@ -847,7 +873,7 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
                    p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster,
-                   p->bounds_check};
+                   p->bounds_check, p->tile_n};
   int launches = 0;
   st = launch(*p, pr, a, sc, build_table, stream, &launches);
   if (st != FP_OK) return st;
@@ -913,7 +939,7 @@ fp_status fp_forward_rope_table(fp_plan* p, const void* x, const fp_layout* x_la
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
   const Scratch sc{p->d_status, p->d_table, p->device, static_cast<int>(p->launch_seq),
                    p->wait_limit_ns, p->inject_stall, p->group_m, p->max_ctas, p->cluster,
-                   p->bounds_check};
+                   p->bounds_check, p->tile_n};
   const ExtTable ext{rope_cos, rope_sin, tl->dtype == FP_BF16, tl->stride_t, tl->stride_i};
   int launches = 0;
   st = launch(*p, pr, a, sc, false, stream, &launches, &ext);
@@ -1533,7 +1559,7 @@ extern "C" fp_status fp_forward_noalloc(const fp_config* config, const void* x,
   const uint32_t tag = g_noalloc_seq.fetch_add(1) % 0x7FFFFFFEu + 1u;
   const Scratch sc{status, reinterpret_cast<float2*>(base + kNoAllocHeaderBytes), dev,
                    static_cast<int>(tag), kDefaultWaitLimitNs, 0, kDefaultGroupM, 0,
-                   kDefaultCluster, 0};
+                   kDefaultCluster, 0, 0};
   int launches = 0;
   // the shared table may hold another call's positions: always rebuild it
   st = launch(pl, pr, a, sc, pr.rope, stream, &launches);

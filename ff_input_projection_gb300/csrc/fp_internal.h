@@ -71,6 +71,10 @@ struct TcParams {
   // 1: the MN-major x map views each slab's tokens as (64 inside a block,
   // S_in/64 blocks), so one box loads both 64-token chunks of a stage
   int a_split;
+  // N of the MMAs: 256, or 192 when tiles of 192 columns fill the waves of CTA
+  // pairs better (0 reads as 256). Each CTA of a pair then holds bn_mma / 2
+  // columns, from column n0 + rank * bn_mma / 2, in its two 64-column chunks.
+  int bn_mma;
   TokenMap tok;
   Epilogue epi;
   int C;

@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
       uint32_t bias_phase = 0;
       bool bias_armed = false, aborted = false;
       const bool peer = CL > 1 && rank != 0;
-      const int col0 = rank * G::B_COLS;  // first tile column this CTA holds
+      // first tile column this CTA holds: its half of the MMA's N
+      const int col0 = rank * ((p.bn_mma ? p.bn_mma : BN) / CL);
       for (int64_t u = first_unit; u < p.num_units && !aborted; u += unit_step) {
         const TileCoord tc = tile_coord<CL>(p, u, rank);
         int oc[3];
@@ -428,10 +429,11 @@ __global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
   } else if (warp == 1 && rank == 0) {
     // ------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
-      const uint32_t idesc = make_idesc(A_MN_MAJOR, true, BM * CL);
+      const int bn_mma = p.bn_mma ? p.bn_mma : BN;
+      const uint32_t idesc = make_idesc(A_MN_MAJOR, true, BM * CL, bn_mma);
       // bias MMA: both operands MN-major; m (n) chunks 1 KB apart, and a k-group
       // stride of 0 so k-rows 8-15 read the same atom as k-rows 0-7
-      const uint32_t idesc_bias = make_idesc(true, true, BM * CL);
+      const uint32_t idesc_bias = make_idesc(true, true, BM * CL, bn_mma);
       const uint64_t bias_a_desc = sw128_desc(bias_a, 1024, 0);
       const uint64_t bias_b_desc = sw128_desc(bias_b, 1024, 0);
       int stage = 0;

@@ -358,6 +358,11 @@ const char* fp_last_error(void);
  *                          against half of each buffer, a test of the check
  *                          itself (stores past the middle are reported, never
  *                          made). 0 (default): off. Forward calls only.
+ *   FP_OPT_TILE_N          width of the tensor-core tiles without rotation: 0
+ *                          (default) takes 256, or 192 where 256-column tiles
+ *                          would compute at least 15 % more columns than N
+ *                          (N = 384, 576, 960 ...); 256 or 192 forces it. CTA
+ *                          pairs only; rotated layouts keep whole heads per tile
  */
 typedef enum {
   FP_OPT_WAIT_LIMIT_NS = 1,
@@ -365,7 +370,8 @@ typedef enum {
   FP_OPT_GROUP_M = 3,
   FP_OPT_MAX_CTAS = 4,
   FP_OPT_CLUSTER = 5,
-  FP_OPT_BOUNDS_CHECK = 6
+  FP_OPT_BOUNDS_CHECK = 6,
+  FP_OPT_TILE_N = 7
 } fp_option;
 fp_status fp_set_option(fp_plan* plan, fp_option opt, int64_t value);
 

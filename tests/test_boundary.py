@@ -168,6 +168,9 @@ def test_options_and_status_without_device(lib):
     for v, want in ((-1, fpx.FP_ERR_INVALID_ARG), (3, fpx.FP_ERR_INVALID_ARG), (0, fpx.FP_OK),
                     (1, fpx.FP_OK), (2, fpx.FP_OK)):
         assert fpx.fp_set_option(h, fpx.FP_OPT_BOUNDS_CHECK, v) == want, v
+    for v, want in ((128, fpx.FP_ERR_INVALID_ARG), (-1, fpx.FP_ERR_INVALID_ARG),
+                    (192, fpx.FP_OK), (256, fpx.FP_OK), (0, fpx.FP_OK)):
+        assert fpx.fp_set_option(h, fpx.FP_OPT_TILE_N, v) == want, v
     # no device state yet: nothing to report, no CUDA call made
     assert fpx.fp_get_device_status(h, None) == fpx.FP_OK
     fpx.fp_destroy(h)

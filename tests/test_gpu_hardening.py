@@ -7,6 +7,9 @@
   each buffer are reported and never made.
 * Guard bands: each output sits between two bands of a sentinel value, which
   must be untouched after the call (no kernel writes outside its outputs).
+* 192-column tensor-core tiles (FP_OPT_TILE_N): forced on small shapes that
+  cover ragged column tails, whole and straddled heads, the bias MMA and the
+  pre-transposed k; identical bits to 256-column tiles and to the oracle.
 * Scratch grown in stream order on one stream and used from others, and a
   forward captured into a CUDA graph on a stream other than the one that built
   the rotary table.
@@ -47,6 +50,40 @@ def test_many_tiles_per_cta(w, cluster, max_ctas, cuda_ok):
     for k in ("ff", "q", "k", "v"):
         if out[k] is not None:
             assert_close(host(out[k]), ref[k], w.dtype, f"{w.name}/{cluster}/{max_ctas}:{k}")
+
+
+TILE192 = [
+    # ff only, N = 1000: five full tiles of 192 and a 40-column tail
+    W_("t192_ff_ragged", (3, 200, 256), 2, 1, 256, 1000, 0, 0, A.ACT_GELU_ERF, 0.0, True, "bf16",
+       81),
+    # q|k|v of 64-wide heads (three heads per tile) after a 192-column ff block
+    W_("t192_ff_qkv", (2, 150, 256), 2, 1, 256, 192, 4, 64, A.ACT_SILU, 0.0, True, "bf16", 82),
+    # 128-wide heads straddle the 192-column tiles; grouped k/v
+    W_("t192_hd128_gqa", (2, 130, 512), 2, 1, 512, 0, 4, 128, A.ACT_NONE, 0.0, False, "bf16", 83,
+       n_query_groups=2),
+    # channels-first x (the A operand MN-major) and k pre-transposed: one tile
+    W_("t192_nchw_kt", (2, 64, 12, 20), 1, 1, 64, 0, 1, 64, A.ACT_NONE, 0.0, True, "bf16", 84,
+       k_transposed=True),
+]
+
+
+@pytest.mark.parametrize("max_ctas", [0, 4])
+@pytest.mark.parametrize("w", TILE192, ids=lambda w: w.name)
+def test_tile_192_matches_256(w, max_ctas, cuda_ok):
+    inp = fpsynth.make_inputs(w)
+    outs = []
+    for tile_n in (256, 192):
+        proj = _proj(w)
+        proj.set_option(fpx.FP_OPT_TILE_N, tile_n)
+        if max_ctas:
+            proj.set_option(fpx.FP_OPT_MAX_CTAS, max_ctas)
+        outs.append(run(w, inp, proj=proj))
+        assert proj.device_status() == fpx.FP_OK, fpx.fp_last_error()
+    ref = oracle.forward_workload(w, inp)
+    for k in ("ff", "q", "k", "v"):
+        if outs[0][k] is not None:
+            assert torch.equal(outs[0][k], outs[1][k]), f"{w.name}:{k}"
+            assert_close(host(outs[1][k]), ref[k], w.dtype, f"{w.name}/192:{k}")
 
 
 # workloads whose stores are (partly) addressed by the kernels themselves
