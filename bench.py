@@ -43,7 +43,8 @@ NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 KERNEL_SOURCES = ["ff_input_projection_gb300/csrc/gemm_tc.cu",
                   "ff_input_projection_gb300/csrc/epilogue.cuh",
                   "ff_input_projection_gb300/csrc/tc_ptx.cuh",
-                  "ff_input_projection_gb300/csrc/gemm_simt.cu"]
+                  "ff_input_projection_gb300/csrc/gemm_simt.cu",
+                  "ff_input_projection_gb300/csrc/attention.cu"]
 
 
 def parse():
@@ -63,8 +64,11 @@ def parse():
                     help="tensor-core tile rasterisation: M-tiles per group (0: the library's default)")
     ap.add_argument("--tile-n", type=int, default=0, choices=[0, 192, 256],
                     help="tensor-core tile width without rotation (0: the library's choice)")
-    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
-                    help="time fp_forward (default) or fp_backward (gradients of x, W, b)")
+    ap.add_argument("--pass", dest="which", default="forward",
+                    choices=["forward", "backward", "attention", "library-gemm"],
+                    help="time fp_forward (default), fp_backward (gradients of x, W, b), or "
+                         "fp_attention over the UNet projection's outputs, or the workload's "
+                         "plain GEMM through this library and through cuBLAS")
     return ap.parse_args()
 
 
@@ -93,11 +97,15 @@ def kernel_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    """DRAM bytes per launch of the workload's dominant kernel from a committed
+    ncu summary (tensor-core GEMM, FFMA GEMM or attention), if it was taken on
     the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"tc_gemm_{workload}.md")
-    if not os.path.exists(path):
+    paths = [os.path.join(ROOT, "profiles", f"{k}_{workload}.md")
+             for k in ("tc_gemm", "simt_gemm", "attention")]
+    paths = [q for q in paths if os.path.exists(q)]
+    if not paths:
         return None
+    path = paths[0]
     text = open(path).read()
     mh = re.search(r"kernel_hash:\s*([0-9a-f]+)", text)
     mt = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
@@ -454,6 +462,7 @@ def time_attention(torch, fpx, dev, uuid, pk, pk_src, sm_count):
              "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                "frac_nominal", "peak_source")},
              "clocks": clk.summary()}
+    entry["roofline"]["traffic"] = recorded_traffic("unet_attention_bf16")
     proj.close()
     del sets
     torch.cuda.empty_cache()
@@ -467,6 +476,8 @@ def config_entry(w, ms, roof, clocks, steps, timing, launches, extra=None):
          "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                            "frac_nominal", "peak_source")},
          "clocks": clocks}
+    if not (extra and extra.get("pass") == "backward"):
+        e["roofline"]["traffic"] = recorded_traffic(w.name)
     if extra:
         e.update(extra)
     return e
@@ -481,6 +492,10 @@ def main():
         return run_reference(args, rank, world)
     if args.which == "backward":
         return main_backward(args, rank, world, local)
+    if args.which == "library-gemm":
+        return main_library_gemm(args, local)
+    if args.which == "attention":
+        return main_attention(local)
 
     import torch
     import ff_input_projection_gb300 as fpx
@@ -801,6 +816,99 @@ def main_backward(args, rank, world, local):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def main_attention(local):
+    """The attention consumer alone (its per_config entry), for profiling."""
+    import torch
+    import ff_input_projection_gb300 as fpx
+    from ff_input_projection_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    pk, pk_src = peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    print(json.dumps(time_attention(torch, fpx, dev, uuid, pk, pk_src, sm_count)), flush=True)
+
+
+def main_library_gemm(args, local):
+    """Context line, not the headline: the workload's contraction as a plain
+    bf16 GEMM [M, C] x [C, N] (channels-last x, no bias, activation, rotation or
+    head split) through fp_forward and through torch.matmul (cuBLAS), both on
+    the same rotated operand sets, CUDA-graph replays timed with CUDA events."""
+    import torch
+    import ff_input_projection_gb300 as fpx
+    from ff_input_projection_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = fpsynth.WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("the library comparison takes bf16 workloads")
+    M, C, N = w.M, w.C, w.N
+    per_set = (M * C + C * N + M * N) * 2
+    n_sets = int(min(MAX_SETS, max(2, np.ceil(2 * L2_BYTES / per_set))))
+    gen = torch.Generator(device=dev).manual_seed(1)
+    xs = [torch.randn(M, C, device=dev, generator=gen).to(torch.bfloat16) for _ in range(n_sets)]
+    Ws = [(torch.randn(C, N, device=dev, generator=gen) * C ** -0.5).to(torch.bfloat16)
+          for _ in range(n_sets)]
+    ys = [torch.empty(M, N, device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
+    proj = fpx.FusedProjection(C, N, 0, 0, "none", 0.0)
+    stream = torch.cuda.Stream(device=dev)
+
+    def ours(i):
+        j = i % n_sets
+        proj.forward(xs[j].view(1, M, C), Ws[j], None, None, channel_dim=2,
+                     out=(ys[j], None, None, None), stream=stream.cuda_stream)
+
+    def cublas(i):
+        j = i % n_sets
+        torch.matmul(xs[j], Ws[j], out=ys[j])
+
+    def timed(step, steps):
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                step(i)
+        torch.cuda.synchronize(dev)
+        G = max(d for d in range(1, min(steps, 64) + 1) if steps % d == 0)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(G):
+                step(i)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            for _ in range(steps // G):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / steps
+
+    steps = max(20, args.steps // 20 * 20)
+    ms_ours = timed(ours, steps)
+    fpx.check(proj.device_status(stream.cuda_stream))
+    ms_cb = timed(cublas, steps)
+    ref = torch.matmul(xs[0], Ws[0])
+    ours(0)
+    torch.cuda.synchronize(dev)
+    err = (ys[0].float() - ref.float()).abs().max().item()
+    flops = 2.0 * M * C * N
+    print(json.dumps({
+        "metric": "plain bf16 GEMM, this library against cuBLAS (context, not the headline)",
+        "workload": w.name, "shape_MxCxN": [M, C, N], "steps": steps,
+        "ours_us": ms_ours * 1e3, "cublas_us": ms_cb * 1e3,
+        "ours_tflops": flops / (ms_ours * 1e-3) / 1e12,
+        "cublas_tflops": flops / (ms_cb * 1e-3) / 1e12,
+        "ours_over_cublas_time": ms_ours / ms_cb, "max_abs_diff_vs_cublas": err,
+        "l2": f"operands rotate over {n_sets} sets ({n_sets * per_set / 1e6:.0f} MB; L2 129 MB)",
+    }), flush=True)
+    proj.close()
 
 
 if __name__ == "__main__":
