@@ -454,7 +454,7 @@ def time_attention(torch, fpx, dev, uuid, pk, pk_src, sm_count):
     entry = {"workload": "unet_attention_bf16", "pass": "attention", "ms_per_step": ms,
              "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": BH * T / (ms * 1e-3),
              "steps": steps, "timing": f"CUDA graph of {G} steps replayed {steps // G} times",
-             "gpu_launches_per_step": 1, "dtype": "bf16",
+             "gpu_launches_per_step": proj.last_launch_count, "dtype": "bf16",
              "shape": {"batch_heads": BH, "T_q": T, "T_k": T, "head_dim": w.head_dim,
                        "k": "pre-transposed [B*heads, head_dim, T] from fp_forward"},
              "flops_per_step": flops,

@@ -29,6 +29,8 @@ struct fp_plan {
   int device;
   int* d_status;     // [2]: sticky device error, tag of an aborted launch
   float2* d_table;   // rotary (cos, sin) table
+  float* d_attn;     // partial results of the attention's split tail
+  int64_t attn_cap;  // bytes
   int64_t table_cap; // entries
   int64_t table_T;   // T of the default-position table held in d_table (-1: none)
   cudaStream_t table_stream;  // stream that last wrote the table
@@ -183,7 +185,7 @@ cudaError_t wait_event(cudaStream_t stream, cudaEvent_t ev) {
 // fp_reserve (`in_stream` false) the growth completes before returning and
 // retired tables are freed once the device is idle.
 fp_status ensure_device_state(fp_plan* p, int64_t table_entries, cudaStream_t stream,
-                              bool in_stream) {
+                              bool in_stream, int64_t attn_bytes = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
   if (p->d_status && p->device != dev)
@@ -214,6 +216,17 @@ fp_status ensure_device_state(fp_plan* p, int64_t table_entries, cudaStream_t st
     p->d_table = static_cast<float2*>(t);
     p->table_cap = cap;
     p->table_T = -1;
+    grew = true;
+  }
+  if (attn_bytes > p->attn_cap) {
+    const int64_t cap = std::max(attn_bytes, 2 * p->attn_cap);
+    void* a = nullptr;
+    if (cudaMallocAsync(&a, static_cast<size_t>(cap), s) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "attention scratch allocation (%lld bytes) failed",
+                  static_cast<long long>(cap));
+    if (p->d_attn) p->retired.push_back(p->d_attn);
+    p->d_attn = static_cast<float*>(a);
+    p->attn_cap = cap;
     grew = true;
   }
   if (!in_stream) {
@@ -722,6 +735,8 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* cfg) {
   p->device = -1;
   p->d_status = nullptr;
   p->d_table = nullptr;
+  p->d_attn = nullptr;
+  p->attn_cap = 0;
   p->table_cap = 0;
   p->table_T = -1;
   p->table_stream = nullptr;
@@ -753,7 +768,7 @@ fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_di
 
 void fp_destroy(fp_plan* plan) {
   if (!plan) return;
-  if (plan->d_status || plan->d_table) {
+  if (plan->d_status || plan->d_table || plan->d_attn) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (plan->device >= 0) cudaSetDevice(plan->device);
@@ -761,6 +776,7 @@ void fp_destroy(fp_plan* plan) {
     cudaDeviceSynchronize();
     if (plan->d_status) cudaFreeAsync(plan->d_status, nullptr);
     if (plan->d_table) cudaFreeAsync(plan->d_table, nullptr);
+    if (plan->d_attn) cudaFreeAsync(plan->d_attn, nullptr);
     for (void* q : plan->retired) cudaFreeAsync(q, nullptr);
     cudaStreamSynchronize(nullptr);
     if (plan->table_ready) cudaEventDestroy(plan->table_ready);
@@ -1394,7 +1410,11 @@ extern "C" fp_status fp_attention(fp_plan* p, const void* q, const void* k, cons
       overlaps(ro, rng(v, BHkv * T_k * hd * 2)))
     return fail(FP_ERR_INVALID_ARG, "out overlaps an input");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  fp_status st = ensure_device_state(p, 0, stream, true);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  const int64_t q_blocks = BH * ((T_q + 127) / 128);
+  const fp::AttnSplit split = fp::attention_split(q_blocks, T_k, hd, sm_count(dev));
+  fp_status st = ensure_device_state(p, 0, stream, true, split.part_bytes);
   if (st != FP_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
   if (!encode) return fail(FP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -1433,10 +1453,14 @@ extern "C" fp_status fp_attention(fp_plan* p, const void* q, const void* k, cons
   ap.status = p->d_status;
   ap.wait_limit_ns = p->wait_limit_ns;
   ap.launch_tag = static_cast<int>(p->launch_seq);
-  const cudaError_t err = fp::launch_attention(ap, stream);
+  ap.full = split.full;
+  ap.splits = split.splits;
+  ap.part = p->d_attn;
+  int launches = 0;
+  const cudaError_t err = fp::launch_attention(ap, stream, &launches);
+  p->last_launches = launches;
   if (err != cudaSuccess)
     return fail(FP_ERR_CUDA, "attention launch: %s", cudaGetErrorString(err));
-  p->last_launches = 1;
   return ok();
 }
 

@@ -37,6 +37,8 @@
 // Every mbarrier wait is bounded: a wait that runs out records a timeout in
 // the status word, tags the launch as aborted, drains its own copies and MMAs
 // and returns, so the GPU stays usable.
+#include <algorithm>
+
 #include "epilogue.cuh"
 #include "fp_internal.h"
 #include "tc_ptx.cuh"
@@ -100,11 +102,22 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl wc{p.status, p.wait_limit_ns, p.launch_tag};
-  const int z = static_cast<int>(blockIdx.x / p.num_q_blocks);
-  const int q0 = static_cast<int>(blockIdx.x - static_cast<int64_t>(z) * p.num_q_blocks) * QB;
+  // this CTA's work: a whole query block, or one key range of a block of the
+  // split tail (chunks [j0, j0 + nkb) of the block's keys, partial results
+  // into slot `slot`)
+  const int nkb_all = static_cast<int>((p.Tk + KB - 1) / KB);
+  int qb = static_cast<int>(blockIdx.x), j0 = 0, nkb = nkb_all, slot = -1;
+  if (qb >= p.full) {
+    const int r = (qb - p.full) / p.splits, sp = qb - p.full - r * p.splits;
+    j0 = static_cast<int>(static_cast<int64_t>(sp) * nkb_all / p.splits);
+    nkb = static_cast<int>(static_cast<int64_t>(sp + 1) * nkb_all / p.splits) - j0;
+    slot = r * p.splits + sp;
+    qb = p.full + r;
+  }
+  const int z = qb / p.num_q_blocks;
+  const int q0 = (qb - z * p.num_q_blocks) * QB;
   const int qpk = p.heads / p.kv_heads;
   const int zkv = (z / p.heads) * p.kv_heads + (z % p.heads) / qpk;
-  const int nkb = static_cast<int>((p.Tk + KB - 1) / KB);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       for (int j = 0; j < nkb; ++j) {
         const int s = j % RING;
         const uint32_t ph = (j / RING) & 1;
-        const int key0 = j * KB;
+        const int key0 = (j0 + j) * KB;
         if (!wait_bounded(k_empty(s), ph ^ 1u, wc, true)) break;
         mbar_arrive_expect_tx(k_full(s), G::K_BYTES);
         const uint32_t kd = k_s + s * G::K_BYTES;
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       // keys past Tk masked out (only the last chunk can hold any); the maxima
       // are taken on the raw scores (the scale c is positive), eight
       // independent partial maxima and sums keep the dependency chains short
-      const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(j) * KB);
+      const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(j0 + j) * KB);
       if (valid < KB) {
 #pragma unroll
         for (int i = 0; i < KB; ++i)
@@ -362,8 +375,25 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         __all_sync(0xFFFFFFFFu,
                    wait_bounded(pv_done((nkb - 1) & 1), ((nkb - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
       tc_fence_after();
+      if (slot >= 0) {
+        // a split: unnormalised O, m and l for the merge (every row, also past Tq)
+        float* pp = p.part + static_cast<int64_t>(slot) * (QB * (HD + 2));
+#pragma unroll
+        for (int q = 0; q < HD / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+          tmem_wait_ld();
+          float4* d4 = reinterpret_cast<float4*>(pp + row * HD + 32 * q);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        }
+        pp[QB * HD + row] = m_ref;
+        pp[QB * HD + QB + row] = l_run;
+      }
       const float inv = 1.0f / l_run;
-      const int64_t qi = q0 + row;
+      const int64_t qi = slot >= 0 ? p.Tq : q0 + row;  // a split stores no output itself
       uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(z) * p.Tq + qi) * HD;
 #pragma unroll
       for (int q = 0; q < HD / 32; ++q) {
@@ -393,6 +423,76 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   }
 }
 
+// Merge of the split tail: per query row, the splits' partial results under
+// one maximum, m = max m_s, l = sum 2^(m_s - m) l_s, O = sum 2^(m_s - m) O_s / l,
+// rounded to bf16. One CTA per (tail block, 8 output columns), one thread per
+// row; every split's loads are issued together (at most kMaxSplits of them).
+constexpr int kMaxSplits = 16;
+
+template <int HD>
+__global__ void __launch_bounds__(QB) attention_merge_kernel(const AttnParams p) {
+  grid_dependency_wait();  // the partial results of the attention launch before it
+  grid_launch_dependents();
+  const int r = static_cast<int>(blockIdx.x);
+  const int c0 = static_cast<int>(blockIdx.y) * 8;
+  const int row = static_cast<int>(threadIdx.x);
+  const int qb = p.full + r;
+  const int z = qb / p.num_q_blocks;
+  const int64_t qi = static_cast<int64_t>(qb - z * p.num_q_blocks) * QB + row;
+  if (qi >= p.Tq) return;
+  constexpr int U = QB * (HD + 2);
+  const float* base = p.part + static_cast<int64_t>(r) * p.splits * U;
+  float ms[kMaxSplits], ls[kMaxSplits];
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp) {
+    const bool in = sp < p.splits;
+    ms[sp] = in ? base[sp * U + QB * HD + row] : -INFINITY;
+    ls[sp] = in ? base[sp * U + QB * HD + QB + row] : 0.0f;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp) m = fmaxf(m, ms[sp]);
+  float l = 0.0f;
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp) {
+    ms[sp] = sp < p.splits ? exp2f(ms[sp] - m) : 0.0f;  // the split's weight
+    l += ms[sp] * ls[sp];
+  }
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp) {
+    if (sp < p.splits) {
+      const float4* o4 = reinterpret_cast<const float4*>(base + sp * U + row * HD + c0);
+      const float4 a = o4[0], b = o4[1];
+      const float w = ms[sp];
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+  }
+  const float inv = 1.0f / l;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                        (static_cast<int64_t>(z) * p.Tq + qi) * HD + c0);
+  *dst = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                    pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+}
+
+template <int HD>
+cudaError_t launch_merge(const AttnParams& p, int tail, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tail), HD / 8, 1);
+  cfg.blockDim = dim3(QB, 1, 1);
+  cfg.stream = stream;
+  // launched while the attention runs (it releases its dependents at its
+  // start); the kernel waits for the attention's results itself
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, attention_merge_kernel<HD>, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 template <int HD, bool KT>
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
   auto kernel = attention_kernel<HD, KT>;
@@ -407,7 +507,9 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
     if (dev < 64) attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.num_q_blocks), 1, 1);
+  const int64_t q_blocks = static_cast<int64_t>(p.BH) * p.num_q_blocks;
+  const int64_t tail = q_blocks - p.full;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.full + tail * p.splits), 1, 1);
   cfg.blockDim = dim3(ANT, 1, 1);
   cfg.dynamicSmemBytes = ACfg<HD>::SMEM_BYTES;
   cfg.stream = stream;
@@ -422,12 +524,36 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
+AttnSplit attention_split(int64_t q_blocks, int64_t Tk, int hd, int sms) {
+  const int64_t nkb = (Tk + KB - 1) / KB;
+  const int64_t tail = sms > 0 ? q_blocks % sms : 0;
+  AttnSplit a{static_cast<int>(q_blocks), 0, 1, 0};
+  if (tail == 0 || nkb < 2) return a;
+  // the tail's blocks spread over the SMs the last wave leaves idle, at least
+  // one key chunk per split
+  const int64_t splits = std::min<int64_t>(std::min<int64_t>(nkb, sms / tail), kMaxSplits);
+  if (splits < 2) return a;
+  a.full = static_cast<int>(q_blocks - tail);
+  a.tail = static_cast<int>(tail);
+  a.splits = static_cast<int>(splits);
+  a.part_bytes = tail * splits * QB * (hd + 2) * static_cast<int64_t>(sizeof(float));
+  return a;
+}
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, int* launches) {
+  *launches = 0;
   if (p.BH == 0 || p.num_q_blocks == 0) return cudaSuccess;
-  if (p.hd == 64) return p.k_transposed ? launch_attn<64, true>(p, stream) : launch_attn<64, false>(p, stream);
+  cudaError_t err = cudaErrorInvalidValue;
+  if (p.hd == 64) err = p.k_transposed ? launch_attn<64, true>(p, stream) : launch_attn<64, false>(p, stream);
   if (p.hd == 128)
-    return p.k_transposed ? launch_attn<128, true>(p, stream) : launch_attn<128, false>(p, stream);
-  return cudaErrorInvalidValue;
+    err = p.k_transposed ? launch_attn<128, true>(p, stream) : launch_attn<128, false>(p, stream);
+  if (err != cudaSuccess) return err;
+  *launches = 1;
+  const int tail = p.BH * p.num_q_blocks - p.full;
+  if (tail == 0 || p.splits < 2) return cudaSuccess;
+  err = p.hd == 64 ? launch_merge<64>(p, tail, stream) : launch_merge<128>(p, tail, stream);
+  if (err == cudaSuccess) *launches = 2;
+  return err;
 }
 
 }  // namespace fp

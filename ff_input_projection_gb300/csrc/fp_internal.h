@@ -160,7 +160,23 @@ struct AttnParams {
   int* status;
   uint64_t wait_limit_ns;
   int launch_tag;
+  // Query blocks (BH * num_q_blocks of them, in (z, block) order) are split
+  // between whole blocks and a split tail: the first `full` run over all keys
+  // in one CTA each; each remaining block is spread over `splits` CTAs, one
+  // contiguous range of key chunks each, which write unnormalised fp32 partial
+  // results to `part` ([tail block][split] slots of 128 x (hd + 2) floats:
+  // O rows, then m, then l, m in log2 units) for the merge kernel.
+  int full, splits;
+  float* part;
 };
+
+// How a launch spreads its query blocks over the SMs: the blocks past the
+// last whole wave are split along the keys when that fills the wave better.
+struct AttnSplit {
+  int full, tail, splits;
+  int64_t part_bytes;  // partial-result scratch the split tail needs (0 when none)
+};
+AttnSplit attention_split(int64_t q_blocks, int64_t Tk, int hd, int sms);
 
 // Launchers (defined in the .cu files). Return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float2* cs, const int32_t* pos, int64_t T, int half, int n_elem,
@@ -174,7 +190,9 @@ cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream
 cudaError_t launch_bwd_gemm(const BwdGemmParams& p, bool a_mn_major, int num_ctas,
                             cudaStream_t stream);
 cudaError_t launch_bwd_gather(const BwdGatherParams& p, cudaStream_t stream);
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+// One launch, or two when the tail is split (the second merges the partials);
+// *launches receives the count.
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, int* launches);
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kSimtBM = 128, kSimtBN = 128;

@@ -302,8 +302,15 @@ fp_status fp_forward_noalloc(const fp_config* config, const void* x, const fp_la
  * head_dim must be 64 or 128 (else FP_ERR_UNSUPPORTED_LAYOUT); with
  * pre-transposed k, T_k must be a multiple of 8 (its rows are TMA strides).
  * All pointers 16-byte aligned. Uses the plan's status word (device-side
- * timeouts surface through fp_get_device_status) and allocates only as
- * fp_forward does on a plan's first use. Returns FP_OK once enqueued.
+ * timeouts surface through fp_get_device_status). Returns FP_OK once enqueued.
+ * Work split: one CTA per 128-query block while whole waves of SMs fill; the
+ * blocks past the last whole wave have their keys split over up to 16 CTAs
+ * each, and a second launch merges those partial results (fp_last_launch_count
+ * then reports 2). The partial results live in plan scratch, grown in stream
+ * order like the rotary table (128 * (head_dim + 2) floats per split; freed by
+ * fp_reserve or fp_destroy once replaced). Calls on one plan that overlap on
+ * the GPU (different streams without ordering) share that scratch and must be
+ * serialised by the caller.
  */
 fp_status fp_attention(fp_plan* plan, const void* q, const void* k, const void* v, void* out,
                        int64_t batch, int64_t T_q, int64_t T_k, float scale, void* stream);

@@ -5,8 +5,11 @@ head_dim] layout of memory-efficient-attention issue #7. Small cases compare
 every output element (one and several key chunks, ragged chunk tails, both k
 layouts, head_dim 64 and 128, grouped-query heads, peaky softmax rows); the
 UNet attention configuration (4096 tokens, 5 heads, batch 2) is fed by
-fp_forward with k emitted pre-transposed and compared in full. Tolerance: the
-bf16 rule, |d| <= max(1e-2 |ref|, 2e-2 rms(ref)).
+fp_forward with k emitted pre-transposed and compared in full. Launches whose
+query blocks leave the last wave of SMs partly idle split those blocks' keys
+over several CTAs and merge the partial results in a second launch; one case
+fills exactly one wave and is not split. Tolerance: the bf16 rule,
+|d| <= max(1e-2 |ref|, 2e-2 rms(ref)).
 """
 import numpy as np
 import pytest
@@ -31,6 +34,9 @@ CASES = [
     ("grouped_query", 2, 4, 2, 64, 100, 136, True, 1.0, 0.0),
     ("peaky_rows", 1, 2, 2, 64, 128, 640, True, 6.0, 0.0),
     ("custom_scale", 1, 1, 1, 64, 96, 256, False, 1.0, 0.5),
+    # one block over 8 key chunks, the last ragged: 8 splits of one chunk each
+    ("many_splits_ragged", 1, 1, 1, 64, 128, 1000, True, 1.0, 0.0),
+    ("many_splits_hd128", 1, 1, 1, 128, 70, 904, False, 2.0, 0.0),
 ]
 
 
@@ -58,6 +64,29 @@ def test_attention_small_full_compare(case, cuda_ok):
                            dtype="bf16", k_transposed=kt, scale=scale if scale > 0 else None,
                            q_chunk=37, kv_chunk=50)
     assert_close(host(out), ref, "bf16", name)
+    nkb = (Tk + 127) // 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    blocks = B * H * ((Tq + 127) // 128)
+    split = blocks % sms != 0 and nkb >= 2 and min(nkb, sms // (blocks % sms)) >= 2
+    assert proj.last_launch_count == (2 if split else 1)
+
+
+def test_attention_whole_wave_is_not_split(cuda_ok):
+    """As many query blocks as SMs: one wave, every block over all its keys in
+    one CTA (one launch), against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, hd, Tq, Tk = 1, sms, 64, 100, 384
+    q = _bits((B * H, Tq, hd), 301, 1)
+    k = _bits((B * H, hd, Tk), 301, 2)
+    v = _bits((B * H, Tk, hd), 301, 3)
+    proj = fpx.FusedProjection(H * hd, 0, H, hd, "none", 0.0, 0, 0, True)
+    out = torch.full((B * H, Tq, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    proj.attention(*(to_device(a, "bf16") for a in (q, k, v)), batch=B, out=out)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK, fpx.fp_last_error()
+    assert proj.last_launch_count == 1
+    ref = oracle.attention(q, k, v, dtype="bf16", k_transposed=True, q_chunk=64, kv_chunk=100)
+    assert_close(host(out), ref, "bf16", "whole wave")
 
 
 def test_attention_on_unet_projection_outputs(cuda_ok):
