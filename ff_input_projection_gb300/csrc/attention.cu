@@ -15,8 +15,13 @@
 // tokens, head_dim]. z' is the k/v head of query head z: grouped-query
 // layouts share one k/v head among heads / kv_heads query heads.
 //
-// Structure (one CTA per 128-query chunk, 8 warps):
-//   warp 0     TMA producer: the q chunk once, then k and v chunks into
+// Work: 128-query blocks of one (batch, head) each; the blocks past the last
+// whole wave of SMs are split along the keys (up to 16 ranges each, partial
+// results merged by a second kernel). The kernel is persistent: one CTA per SM
+// (8 warps) walks its units in turn, its pipelines running on across unit
+// boundaries.
+// Structure:
+//   warp 0     TMA producer: a unit's q chunk once, then k and v chunks into
 //              rings of 4 stages (head_dim 64) or 2 (head_dim 128)
 //   warp 1     MMA issuer (one thread): S = q k^T into one of two TMEM score
 //              buffers (M 128, N 128, K head_dim), then O += P v into the TMEM
@@ -62,16 +67,52 @@ struct ACfg {
   static constexpr int K_BYTES = KB * HD * 2;
   static constexpr int V_BYTES = KB * HD * 2;
   static constexpr int P_BYTES = QB * KB * 2;  // one P buffer; there are two
-  // q_full; k full/empty and v full/empty per stage; s full/empty per score
-  // buffer; p full and P v done per P buffer; drain
-  static constexpr int NUM_BARS = 1 + 4 * RING + 4 + 4 + 1;
+  // q full/empty; k full/empty and v full/empty per stage; s full/empty per
+  // score buffer; p full and P v done per P buffer; output empty per output
+  // buffer; drain
+  static constexpr int NUM_BARS = 2 + 4 * RING + 4 + 4 + 2 + 1;
   static_assert(RING <= 4, "armed-barrier bit masks hold 1 + 2 * RING slots");
   static constexpr int SMEM_BYTES =
       1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + 2 * P_BYTES + NUM_BARS * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static constexpr int O_COL = 2 * KB;  // TMEM: scores in [0, 256), output in [256, 256 + HD)
+  // TMEM: scores in [0, 256), the two output buffers in [256, 256 + 2 HD)
+  static constexpr int O_COL = 2 * KB;
+  static_assert(O_COL + 2 * HD <= 512, "TMEM holds 512 columns");
 };
 
+// One work unit: a whole 128-query block (units [0, full)), or one key range
+// of a block of the split tail (chunks [j0, j0 + nkb) of its keys, partial
+// results into slot `slot`).
+struct Unit {
+  int z, zkv, q0, j0, nkb, slot;
+};
+
+__device__ __forceinline__ Unit unit_of(const AttnParams& p, int u, int nkb_all) {
+  Unit w;
+  int qb = u;
+  w.j0 = 0;
+  w.nkb = nkb_all;
+  w.slot = -1;
+  if (qb >= p.full) {
+    const int r = (qb - p.full) / p.splits, sp = qb - p.full - r * p.splits;
+    w.j0 = static_cast<int>(static_cast<int64_t>(sp) * nkb_all / p.splits);
+    w.nkb = static_cast<int>(static_cast<int64_t>(sp + 1) * nkb_all / p.splits) - w.j0;
+    w.slot = r * p.splits + sp;
+    qb = p.full + r;
+  }
+  w.z = qb / p.num_q_blocks;
+  w.q0 = (qb - w.z * p.num_q_blocks) * QB;
+  const int qpk = p.heads / p.kv_heads;
+  w.zkv = (w.z / p.heads) * p.kv_heads + (w.z % p.heads) / qpk;
+  return w;
+}
+
+// Persistent: one CTA per SM walks units u = blockIdx.x, + gridDim.x, ...
+// Every role counts the key chunks it has passed over all its units (g): the
+// k/v ring stage and phase, the score and P buffer (g & 1) and their phases
+// (g >> 1) follow from it, so the pipelines run on across unit boundaries.
+// Unit i of a CTA accumulates into output buffer i & 1, so its MMAs can start
+// while the softmax warps still store the output of unit i - 1.
 template <int HD, bool KT>
 __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant__ AttnParams p) {
   using G = ACfg<HD>;
@@ -97,30 +138,19 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   auto p_full = [&](int b) { return bar1 + 8u * (4 + b); };
   auto pv_done = [&](int b) { return bar1 + 8u * (6 + b); };
   const uint32_t drain = bar1 + 8u * 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 9 - sbase));
+  const uint32_t q_empty = bar1 + 8u * 9;                     // the unit's score MMAs read q
+  auto o_empty = [&](int b) { return bar1 + 8u * (10 + b); };  // output buffer b stored
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 12 - sbase));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl wc{p.status, p.wait_limit_ns, p.launch_tag};
-  // this CTA's work: a whole query block, or one key range of a block of the
-  // split tail (chunks [j0, j0 + nkb) of the block's keys, partial results
-  // into slot `slot`)
   const int nkb_all = static_cast<int>((p.Tk + KB - 1) / KB);
-  int qb = static_cast<int>(blockIdx.x), j0 = 0, nkb = nkb_all, slot = -1;
-  if (qb >= p.full) {
-    const int r = (qb - p.full) / p.splits, sp = qb - p.full - r * p.splits;
-    j0 = static_cast<int>(static_cast<int64_t>(sp) * nkb_all / p.splits);
-    nkb = static_cast<int>(static_cast<int64_t>(sp + 1) * nkb_all / p.splits) - j0;
-    slot = r * p.splits + sp;
-    qb = p.full + r;
-  }
-  const int z = qb / p.num_q_blocks;
-  const int q0 = (qb - z * p.num_q_blocks) * QB;
-  const int qpk = p.heads / p.kv_heads;
-  const int zkv = (z / p.heads) * p.kv_heads + (z % p.heads) / qpk;
+  const int n_units = p.full + (p.BH * p.num_q_blocks - p.full) * p.splits;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < RING; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -130,10 +160,9 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), 4);  // the four softmax warps
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(p_full(b), 4);
       mbar_init(pv_done(b), 1);
+      mbar_init(o_empty(b), 4);
     }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -164,42 +193,57 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         armed |= 1u << slot;
         armed_par = (armed_par & ~(1u << slot)) | (par << slot);
       };
-      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
+      bool aborted = false;
+      int g = 0, ui = 0;  // chunks and units this CTA has passed
+      for (int u = static_cast<int>(blockIdx.x); u < n_units && !aborted;
+           u += static_cast<int>(gridDim.x), ++ui) {
+        const Unit w = unit_of(p, u, nkb_all);
+        // the q buffer is free once the previous unit's score MMAs have read it
+        if (ui > 0 && !wait_bounded(q_empty, (ui - 1) & 1, wc, true)) break;
+        mbar_arrive_expect_tx(q_full, G::Q_BYTES);
 #pragma unroll
-      for (int a = 0; a < HD / 64; ++a) tma_load_3d(q_s + a * ATOM, &p.tmap_q, q_full, 64 * a, q0, z);
-      arm(0, 0);
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j % RING;
-        const uint32_t ph = (j / RING) & 1;
-        const int key0 = (j0 + j) * KB;
-        if (!wait_bounded(k_empty(s), ph ^ 1u, wc, true)) break;
-        mbar_arrive_expect_tx(k_full(s), G::K_BYTES);
-        const uint32_t kd = k_s + s * G::K_BYTES;
-        if (KT) {
-          // [hd][Tk] rows of the head: chunk (h, n) holds hd rows 64h.. and keys 64n..
+        for (int a = 0; a < HD / 64; ++a)
+          tma_load_3d(q_s + a * ATOM, &p.tmap_q, q_full, 64 * a, w.q0, w.z);
+        arm(0, ui & 1);
+        for (int j = 0; j < w.nkb; ++j, ++g) {
+          const int s = g % RING;
+          const uint32_t ph = (g / RING) & 1;
+          const int key0 = (w.j0 + j) * KB;
+          if (!wait_bounded(k_empty(s), ph ^ 1u, wc, true)) {
+            aborted = true;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full(s), G::K_BYTES);
+          const uint32_t kd = k_s + s * G::K_BYTES;
+          if (KT) {
+            // [hd][Tk] rows of the head: chunk (h, n) holds hd rows 64h.. and keys 64n..
 #pragma unroll
-          for (int h = 0; h < HD / 64; ++h)
+            for (int h = 0; h < HD / 64; ++h)
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
-              tma_load_3d(kd + (h * 2 + n) * CHUNK, &p.tmap_k, k_full(s), key0 + 64 * n, 64 * h,
-                          zkv);
-        } else {
+              for (int n = 0; n < 2; ++n)
+                tma_load_3d(kd + (h * 2 + n) * CHUNK, &p.tmap_k, k_full(s), key0 + 64 * n, 64 * h,
+                            w.zkv);
+          } else {
 #pragma unroll
-          for (int a = 0; a < HD / 64; ++a)
-            tma_load_3d(kd + a * ATOM, &p.tmap_k, k_full(s), 64 * a, key0, zkv);
+            for (int a = 0; a < HD / 64; ++a)
+              tma_load_3d(kd + a * ATOM, &p.tmap_k, k_full(s), 64 * a, key0, w.zkv);
+          }
+          arm(1 + s, ph);
+          if (!wait_bounded(v_empty(s), ph ^ 1u, wc, true)) {
+            aborted = true;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full(s), G::V_BYTES);
+          const uint32_t vd = v_s + s * G::V_BYTES;
+          // chunk (h, n) holds keys 64h.. and head lanes 64n..
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int n = 0; n < HD / 64; ++n)
+              tma_load_3d(vd + (h * (HD / 64) + n) * CHUNK, &p.tmap_v, v_full(s), 64 * n,
+                          key0 + 64 * h, w.zkv);
+          arm(1 + RING + s, ph);
         }
-        arm(1 + s, ph);
-        if (!wait_bounded(v_empty(s), ph ^ 1u, wc, true)) break;
-        mbar_arrive_expect_tx(v_full(s), G::V_BYTES);
-        const uint32_t vd = v_s + s * G::V_BYTES;
-        // chunk (h, n) holds keys 64h.. and head lanes 64n..
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int n = 0; n < HD / 64; ++n)
-            tma_load_3d(vd + (h * (HD / 64) + n) * CHUNK, &p.tmap_v, v_full(s), 64 * n,
-                        key0 + 64 * h, zkv);
-        arm(1 + RING + s, ph);
       }
       // no copy may still be landing in shared memory when the CTA exits
       const WaitCtl dc{wc.status, wc.limit_ns < 10000000ull ? wc.limit_ns : 10000000ull,
@@ -216,46 +260,70 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc(false, KT, QB, KB);
       const uint32_t idesc_o = make_idesc(false, true, QB, HD);
-      bool issued = false, ok = wait_bounded(q_full, 0, wc, true);
-      tc_fence_after();
-      auto issue_scores = [&](int j) -> bool {
-        const int s = j % RING, b = j & 1;
-        if (!wait_bounded(k_full(s), (j / RING) & 1, wc, true)) return false;
-        if (!wait_bounded(s_empty(b), ((j >> 1) & 1) ^ 1u, wc, true)) return false;
+      bool issued = false, ok = true;
+      int g = 0, ui = 0;  // chunks and units this CTA has passed
+      for (int u = static_cast<int>(blockIdx.x); ok && u < n_units;
+           u += static_cast<int>(gridDim.x), ++ui) {
+        const Unit w = unit_of(p, u, nkb_all);
+        const int ob = ui & 1;  // this unit's output buffer
+        ok = wait_bounded(q_full, ui & 1, wc, true);
         tc_fence_after();
-        const uint32_t kd = k_s + s * G::K_BYTES;
+        // S for the unit's chunk j (global chunk g0 + j) into score buffer (g0 + j) & 1;
+        // the unit's last one releases the q buffer
+        const int g0 = g;
+        auto issue_scores = [&](int j) -> bool {
+          const int gj = g0 + j;
+          const int s = gj % RING, b = gj & 1;
+          if (!wait_bounded(k_full(s), (gj / RING) & 1, wc, true)) return false;
+          if (!wait_bounded(s_empty(b), ((gj >> 1) & 1) ^ 1u, wc, true)) return false;
+          tc_fence_after();
+          const uint32_t kd = k_s + s * G::K_BYTES;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t a_desc = sw128_desc(q_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
-          // pre-transposed k: MN-major B, two 64-key chunks per 64 head lanes;
-          // else K-major B, like q
-          const uint64_t b_desc = KT ? sw128_desc(kd + (k / 4) * 2 * CHUNK + (k % 4) * 2048, CHUNK, 1024)
-                                     : sw128_desc(kd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
-          umma_bf16<1>(tmem + b * KB, a_desc, b_desc, idesc_s, k > 0 ? 1u : 0u);
-        }
-        umma_commit<1>(s_full(b));
-        umma_commit<1>(k_empty(s));
-        issued = true;
-        return true;
-      };
-      if (ok && nkb > 0) ok = issue_scores(0);
-      for (int j = 0; ok && j < nkb; ++j) {
-        if (j + 1 < nkb && !issue_scores(j + 1)) break;
-        const int s = j % RING, pb = j & 1;
-        if (!wait_bounded(p_full(pb), (j >> 1) & 1, wc, true)) break;
-        if (!wait_bounded(v_full(s), (j / RING) & 1, wc, true)) break;
-        tc_fence_after();
-        const uint32_t vd = v_s + s * G::V_BYTES;
-        const uint32_t pd = p_s + pb * G::P_BYTES;
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t a_desc = sw128_desc(q_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+            // pre-transposed k: MN-major B, two 64-key chunks per 64 head lanes;
+            // else K-major B, like q
+            const uint64_t b_desc = KT ? sw128_desc(kd + (k / 4) * 2 * CHUNK + (k % 4) * 2048, CHUNK, 1024)
+                                       : sw128_desc(kd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+            umma_bf16<1>(tmem + b * KB, a_desc, b_desc, idesc_s, k > 0 ? 1u : 0u);
+          }
+          umma_commit<1>(s_full(b));
+          umma_commit<1>(k_empty(s));
+          if (j == w.nkb - 1) umma_commit<1>(q_empty);
+          issued = true;
+          return true;
+        };
+        if (ok) ok = issue_scores(0);
+        // the output buffer is free once the softmax stored the unit two back
+        if (ok && ui >= 2) ok = wait_bounded(o_empty(ob), ((ui >> 1) & 1) ^ 1u, wc, true);
+        for (int j = 0; ok && j < w.nkb; ++j) {
+          // the next chunk's scores go in before this chunk's P v, so the
+          // tensor core works while the softmax runs
+          if (j + 1 < w.nkb && !issue_scores(j + 1)) {
+            ok = false;
+            break;
+          }
+          const int gj = g0 + j;
+          const int s = gj % RING, pb = gj & 1;
+          if (!wait_bounded(p_full(pb), (gj >> 1) & 1, wc, true) ||
+              !wait_bounded(v_full(s), (gj / RING) & 1, wc, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vd = v_s + s * G::V_BYTES;
+          const uint32_t pd = p_s + pb * G::P_BYTES;
 #pragma unroll
-        for (int k = 0; k < KB / 16; ++k) {
-          const uint64_t a_desc = sw128_desc(pd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
-          const uint64_t b_desc =
-              sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
-          umma_bf16<1>(tmem + G::O_COL, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < KB / 16; ++k) {
+            const uint64_t a_desc = sw128_desc(pd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+            const uint64_t b_desc =
+                sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
+            umma_bf16<1>(tmem + G::O_COL + ob * HD, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
+          }
+          umma_commit<1>(pv_done(pb));
+          umma_commit<1>(v_empty(s));
         }
-        umma_commit<1>(pv_done(pb));
-        umma_commit<1>(v_empty(s));
+        g = g0 + w.nkb;
       }
       if (issued) {
         umma_commit<1>(drain);  // every MMA retired before TMEM is freed
@@ -268,11 +336,18 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = p.scale_log2e;
-    float m_ref = -INFINITY, l_run = 0.0f;
     bool alive = true;
-    for (int j = 0; j < nkb; ++j) {
-      const int b = j & 1;
-      if (!__all_sync(0xFFFFFFFFu, wait_bounded(s_full(b), (j >> 1) & 1, wc, true) ? 1 : 0)) {
+    int g = 0, ui = 0;  // chunks and units this CTA has passed
+    for (int u = static_cast<int>(blockIdx.x); alive && u < n_units;
+         u += static_cast<int>(gridDim.x), ++ui) {
+    const Unit w = unit_of(p, u, nkb_all);
+    const int ob = ui & 1;
+    const int g0 = g;
+    float m_ref = -INFINITY, l_run = 0.0f;
+    for (int j = 0; j < w.nkb; ++j) {
+      const int gj = g0 + j;
+      const int b = gj & 1;
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(s_full(b), (gj >> 1) & 1, wc, true) ? 1 : 0)) {
         alive = false;
         break;
       }
@@ -288,7 +363,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       // keys past Tk masked out (only the last chunk can hold any); the maxima
       // are taken on the raw scores (the scale c is positive), eight
       // independent partial maxima and sums keep the dependency chains short
-      const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(j0 + j) * KB);
+      const int valid = static_cast<int>(p.Tk - static_cast<int64_t>(w.j0 + j) * KB);
       if (valid < KB) {
 #pragma unroll
         for (int i = 0; i < KB; ++i)
@@ -326,11 +401,11 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_run = l_run * alpha + sum;
       m_ref = m_new;
-      const int pb = j & 1;
-      if (j >= 2) {
+      const int pb = b;
+      if (gj >= 2) {
         // this P buffer is free once the P v of two chunks ago has read it
         if (!__all_sync(0xFFFFFFFFu,
-                        wait_bounded(pv_done(pb), ((j - 2) >> 1) & 1, wc, true) ? 1 : 0)) {
+                        wait_bounded(pv_done(pb), ((gj - 2) >> 1) & 1, wc, true) ? 1 : 0)) {
           alive = false;
           break;
         }
@@ -350,7 +425,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         // a raised maximum: the output accumulated so far is scaled once the
         // previous chunk's P v has landed in it
         if (!__all_sync(0xFFFFFFFFu,
-                        wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
+                        wait_bounded(pv_done((gj - 1) & 1), ((gj - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
           alive = false;
           break;
         }
@@ -358,11 +433,11 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
 #pragma unroll
         for (int q = 0; q < HD / 32; ++q) {
           uint32_t o[32];
-          tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+          tmem_ld32(t_lane + G::O_COL + ob * HD + 32 * q, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(t_lane + G::O_COL + 32 * q, o);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(t_lane + G::O_COL + ob * HD + 32 * q, o);
         }
         tmem_wait_st();
       }
@@ -371,45 +446,56 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(pb));
     }
-    if (alive && nkb > 0 &&
-        __all_sync(0xFFFFFFFFu,
-                   wait_bounded(pv_done((nkb - 1) & 1), ((nkb - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
+    g = g0 + w.nkb;
+    if (!alive) break;
+    const int gl = g - 1;  // the unit's last chunk
+    if (!__all_sync(0xFFFFFFFFu,
+                    wait_bounded(pv_done(gl & 1), (gl >> 1) & 1, wc, true) ? 1 : 0)) {
+      alive = false;
+      break;
+    }
+    {
       tc_fence_after();
-      if (slot >= 0) {
+      if (w.slot >= 0) {
         // a split: unnormalised O, m and l for the merge (every row, also past Tq)
-        float* pp = p.part + static_cast<int64_t>(slot) * (QB * (HD + 2));
+        float* pp = p.part + static_cast<int64_t>(w.slot) * (QB * (HD + 2));
 #pragma unroll
         for (int q = 0; q < HD / 32; ++q) {
           uint32_t o[32];
-          tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+          tmem_ld32(t_lane + G::O_COL + ob * HD + 32 * q, o);
           tmem_wait_ld();
           float4* d4 = reinterpret_cast<float4*>(pp + row * HD + 32 * q);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          for (int e = 0; e < 8; ++e)
+            d4[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
         }
         pp[QB * HD + row] = m_ref;
         pp[QB * HD + QB + row] = l_run;
       }
       const float inv = 1.0f / l_run;
-      const int64_t qi = slot >= 0 ? p.Tq : q0 + row;  // a split stores no output itself
-      uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(z) * p.Tq + qi) * HD;
+      const int64_t qi = w.slot >= 0 ? p.Tq : w.q0 + row;  // a split stores no output itself
+      uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(w.z) * p.Tq + qi) * HD;
 #pragma unroll
       for (int q = 0; q < HD / 32; ++q) {
         uint32_t o[32];
-        tmem_ld32(t_lane + G::O_COL + 32 * q, o);
+        tmem_ld32(t_lane + G::O_COL + ob * HD + 32 * q, o);
         tmem_wait_ld();
-        uint32_t w[16];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
         if (qi < p.Tq) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
+      // the output buffer may take the unit after next
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty(ob));
+    }
     }
   }
 
@@ -509,7 +595,12 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   const int64_t q_blocks = static_cast<int64_t>(p.BH) * p.num_q_blocks;
   const int64_t tail = q_blocks - p.full;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.full + tail * p.splits), 1, 1);
+  // persistent: at most one CTA per SM, walking the units
+  int sms = 0;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int64_t units = p.full + tail * p.splits;
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(units, std::max(sms, 1))), 1, 1);
   cfg.blockDim = dim3(ANT, 1, 1);
   cfg.dynamicSmemBytes = ACfg<HD>::SMEM_BYTES;
   cfg.stream = stream;
