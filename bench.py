@@ -40,11 +40,17 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GB300 data-sheet figures: dense bf16 tensor throughput and HBM3e bandwidth
 NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
-KERNEL_SOURCES = ["ff_input_projection_gb300/csrc/gemm_tc.cu",
+# the sources each kind of ncu summary under profiles/ was taken on: a summary
+# whose recorded hash no longer matches is stale and its traffic is not used
+KERNEL_SOURCES = {
+    "gemm": ["ff_input_projection_gb300/csrc/gemm_tc.cu",
+             "ff_input_projection_gb300/csrc/epilogue.cuh",
+             "ff_input_projection_gb300/csrc/tc_ptx.cuh",
+             "ff_input_projection_gb300/csrc/gemm_simt.cu"],
+    "attention": ["ff_input_projection_gb300/csrc/attention.cu",
                   "ff_input_projection_gb300/csrc/epilogue.cuh",
-                  "ff_input_projection_gb300/csrc/tc_ptx.cuh",
-                  "ff_input_projection_gb300/csrc/gemm_simt.cu",
-                  "ff_input_projection_gb300/csrc/attention.cu"]
+                  "ff_input_projection_gb300/csrc/tc_ptx.cuh"],
+}
 
 
 def parse():
@@ -88,9 +94,9 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kind: str = "gemm") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -100,16 +106,16 @@ def recorded_traffic(workload: str):
     """DRAM bytes per launch of the workload's dominant kernel from a committed
     ncu summary (tensor-core GEMM, FFMA GEMM or attention), if it was taken on
     the current kernel sources (else None)."""
-    paths = [os.path.join(ROOT, "profiles", f"{k}_{workload}.md")
-             for k in ("tc_gemm", "simt_gemm", "attention")]
-    paths = [q for q in paths if os.path.exists(q)]
+    paths = [(os.path.join(ROOT, "profiles", f"{k}_{workload}.md"), kind)
+             for k, kind in (("tc_gemm", "gemm"), ("simt_gemm", "gemm"), ("attention", "attention"))]
+    paths = [q for q in paths if os.path.exists(q[0])]
     if not paths:
         return None
-    path = paths[0]
+    path, kind = paths[0]
     text = open(path).read()
     mh = re.search(r"kernel_hash:\s*([0-9a-f]+)", text)
     mt = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != kernel_hash():
+    if not mh or not mt or mh.group(1) != kernel_hash(kind):
         return None
     return float(mt.group(1))
 
