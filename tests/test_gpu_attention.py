@@ -123,3 +123,22 @@ def test_attention_rejects_on_host(cuda_ok):
     st = fpx.fp_attention(proj2.plan, u.data_ptr(), u.data_ptr(), u.data_ptr(), u.data_ptr(),
                           1, 16, 16, 0.0, None)
     assert st == fpx.FP_ERR_INVALID_ARG  # out overlaps the inputs
+
+
+@pytest.mark.parametrize("hd,kt", [(128, False), (64, True)])
+def test_attention_persistent_many_units(hd, kt, cuda_ok):
+    """320 query blocks (B 2 x 5 heads x 4096 queries) on one CTA per SM: each
+    CTA walks several whole blocks (alternating TMEM output buffers, the q
+    buffer refilled between units) and then key ranges of the split tail;
+    every element against the oracle."""
+    B, H, Tq, Tk = 2, 5, 4096, 512
+    q = _bits((B * H, Tq, hd), 320 + hd, 1)
+    k = _bits((B * H, hd, Tk) if kt else (B * H, Tk, hd), 320 + hd, 2)
+    v = _bits((B * H, Tk, hd), 320 + hd, 3)
+    proj = fpx.FusedProjection(H * hd, 0, H, hd, "none", 0.0, 0, 0, kt)
+    out = torch.full((B * H, Tq, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    proj.attention(*(to_device(a, "bf16") for a in (q, k, v)), batch=B, out=out)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK, fpx.fp_last_error()
+    ref = oracle.attention(q, k, v, dtype="bf16", k_transposed=kt, q_chunk=1024, kv_chunk=256)
+    assert_close(host(out), ref, "bf16", f"persistent hd{hd}")
