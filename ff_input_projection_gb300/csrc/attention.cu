@@ -24,21 +24,22 @@
 //   warp 0     TMA producer: a unit's q chunk once, then k and v chunks into
 //              rings of 4 stages (head_dim 64) or 2 (head_dim 128)
 //   warp 1     MMA issuer (one thread): S = q k^T into one of two TMEM score
-//              buffers (M 128, N 128, K head_dim), then O += P v into the TMEM
-//              output accumulator (M 128, N head_dim, K 128); the next chunk's
-//              scores are issued before this chunk's P v, so the tensor core
-//              works while the softmax runs
+//              buffers (M 128, N 128, K head_dim), then O += P v into the
+//              unit's TMEM output accumulator (M 128, N head_dim, K 128) with
+//              P read from tensor memory; the next chunk's scores are issued
+//              before this chunk's P v, so the tensor core works while the
+//              softmax runs
 //   warps 4-7  softmax, one query row per thread (TMEM lane = row): scores
 //              from TMEM, a reference maximum m and the sum l, P = 2^(s c - m)
-//              rounded to bf16 into one of two shared-memory buffers (the A
-//              operand of P v), so the next chunk's P is written while the
-//              tensor core still reads this one. m is raised only when a
-//              chunk's maximum exceeds it by more than 8 (log2 units): P then
-//              stays below 2^8, and the output accumulator is rescaled in TMEM
-//              only at those rare steps. At the end O / l is rounded to bf16
-//              and stored.
-// Shared-memory operands use the 128-byte swizzle TMA writes and the MMA reads;
-// P is written by the softmax threads in the same swizzled K-major layout.
+//              rounded to bf16 and written back over the chunk's scores in
+//              TMEM, two keys per 32-bit column (the A operand of P v: no
+//              shared-memory store and no proxy fence on the chain). m is
+//              raised only when a chunk's maximum exceeds it by more than 8
+//              (log2 units): P then stays below 2^8, and the output
+//              accumulator is rescaled in TMEM only at those rare steps. At the
+//              end of a unit O / l is rounded to bf16 and stored.
+// Shared-memory operands (q, k, v) use the 128-byte swizzle TMA writes and the
+// MMA reads.
 // Every mbarrier wait is bounded: a wait that runs out records a timeout in
 // the status word, tags the launch as aborted, drains its own copies and MMAs
 // and returns, so the GPU stays usable.
@@ -66,14 +67,13 @@ struct ACfg {
   static constexpr int Q_BYTES = QB * HD * 2;
   static constexpr int K_BYTES = KB * HD * 2;
   static constexpr int V_BYTES = KB * HD * 2;
-  static constexpr int P_BYTES = QB * KB * 2;  // one P buffer; there are two
   // q full/empty; k full/empty and v full/empty per stage; s full/empty per
   // score buffer; p full and P v done per P buffer; output empty per output
   // buffer; drain
   static constexpr int NUM_BARS = 2 + 4 * RING + 4 + 4 + 2 + 1;
-  static_assert(RING <= 4, "armed-barrier bit masks hold 1 + 2 * RING slots");
+  static_assert(1 + 2 * RING <= 32, "armed-barrier bit masks hold 1 + 2 * RING slots");
   static constexpr int SMEM_BYTES =
-      1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + 2 * P_BYTES + NUM_BARS * 8 + 16;
+      1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + NUM_BARS * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   // TMEM: scores in [0, 256), the two output buffers in [256, 256 + 2 HD)
   static constexpr int O_COL = 2 * KB;
@@ -124,8 +124,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const uint32_t q_s = sbase;
   const uint32_t k_s = q_s + G::Q_BYTES;                   // RING stages
   const uint32_t v_s = k_s + RING * G::K_BYTES;            // RING stages
-  const uint32_t p_s = v_s + RING * G::V_BYTES;
-  const uint32_t bar0 = p_s + 2 * G::P_BYTES;
+  const uint32_t bar0 = v_s + RING * G::V_BYTES;
   const uint32_t q_full = bar0;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto k_empty = [&](int s) { return bar0 + 8u * (1 + RING + s); };
@@ -134,7 +133,8 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const uint32_t bar1 = bar0 + 8u * (1 + 4 * RING);
   auto s_full = [&](int b) { return bar1 + 8u * b; };
   auto s_empty = [&](int b) { return bar1 + 8u * (2 + b); };
-  // P buffer b: full once the softmax wrote it, done once P v has read it
+  // P of the chunk in score buffer b: written once the softmax stored it over
+  // the scores, read once P v has completed
   auto p_full = [&](int b) { return bar1 + 8u * (4 + b); };
   auto pv_done = [&](int b) { return bar1 + 8u * (6 + b); };
   const uint32_t drain = bar1 + 8u * 8;
@@ -312,13 +312,13 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
           }
           tc_fence_after();
           const uint32_t vd = v_s + s * G::V_BYTES;
-          const uint32_t pd = p_s + pb * G::P_BYTES;
 #pragma unroll
           for (int k = 0; k < KB / 16; ++k) {
-            const uint64_t a_desc = sw128_desc(pd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+            // P from tensor memory: 16 keys are 8 packed columns of the score buffer
             const uint64_t b_desc =
                 sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
-            umma_bf16<1>(tmem + G::O_COL + ob * HD, a_desc, b_desc, idesc_o, (j | k) != 0 ? 1u : 0u);
+            umma_bf16_ts(tmem + G::O_COL + ob * HD, tmem + pb * KB + 8 * k, b_desc, idesc_o,
+                         (j | k) != 0 ? 1u : 0u);
           }
           umma_commit<1>(pv_done(pb));
           umma_commit<1>(v_empty(s));
@@ -401,26 +401,12 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_run = l_run * alpha + sum;
       m_ref = m_new;
-      const int pb = b;
-      if (gj >= 2) {
-        // this P buffer is free once the P v of two chunks ago has read it
-        if (!__all_sync(0xFFFFFFFFu,
-                        wait_bounded(pv_done(pb), ((gj - 2) >> 1) & 1, wc, true) ? 1 : 0)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      // P row into the swizzled K-major atoms: 16-byte chunk ch of row r at ch ^ (r & 7)
-      const uint32_t pd = p_s + pb * G::P_BYTES;
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t addr = pd + a * ATOM + row * 128 + ((ch ^ (row & 7)) << 4);
-          const int w0 = a * 32 + ch * 4;
-          st_shared_v4(addr, pw[w0], pw[w0 + 1], pw[w0 + 2], pw[w0 + 3]);
-        }
+      // P over the chunk's scores in TMEM (they are in registers by now): column
+      // c of a row holds keys 2c and 2c+1, the A operand of P v. The next
+      // scores into this buffer are issued only after this chunk's P v.
+      tmem_st32(t_lane + b * KB, *reinterpret_cast<const uint32_t(*)[32]>(pw));
+      tmem_st32(t_lane + b * KB + 32, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32));
+      tmem_wait_st();
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
         // a raised maximum: the output accumulated so far is scaled once the
         // previous chunk's P v has landed in it
@@ -441,10 +427,9 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         }
         tmem_wait_st();
       }
-      fence_async_shared();  // P visible to the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(pb));
+      if (lane == 0) mbar_arrive(p_full(b));
     }
     g = g0 + w.nkb;
     if (!alive) break;

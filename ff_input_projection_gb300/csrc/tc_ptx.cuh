@@ -252,6 +252,19 @@ __host__ __device__ constexpr uint32_t make_idesc(bool a_mn_major, bool b_mn_maj
 // One MMA. CL == 1: M = 128 on this SM. CL == 2: a 2-SM MMA issued by the even
 // CTA of the pair: A rows come from both CTAs' shared memory (same offsets),
 // B columns half from each, and each CTA's TMEM receives its 128 rows.
+// D (+)= A B on one SM with A read from tensor memory: a_tmem addresses a
+// [128 lanes = rows][K/2 columns] block, 32-bit column c of a row holding its
+// 16-bit elements 2c and 2c+1 (K-major); B from shared memory by descriptor.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int CL>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
