@@ -67,16 +67,19 @@ struct ACfg {
   static constexpr int Q_BYTES = QB * HD * 2;
   static constexpr int K_BYTES = KB * HD * 2;
   static constexpr int V_BYTES = KB * HD * 2;
-  // q full/empty; k full/empty and v full/empty per stage; s full/empty per
-  // score buffer; p full and P v done per P buffer; output empty per output
-  // buffer; drain
-  static constexpr int NUM_BARS = 2 + 4 * RING + 4 + 4 + 2 + 1;
+  // score buffers in TMEM (each also holds its chunk's P): three for
+  // head_dim 64, so the scores can be issued two chunks ahead; two for 128
+  static constexpr int NS = HD == 64 ? 3 : 2;
+  // q full/empty; k full/empty and v full/empty per stage; s full/empty,
+  // p full and P v done per score buffer; output empty per output buffer;
+  // drain
+  static constexpr int NUM_BARS = 2 + 4 * RING + 4 * NS + 2 + 1;
   static_assert(1 + 2 * RING <= 32, "armed-barrier bit masks hold 1 + 2 * RING slots");
   static constexpr int SMEM_BYTES =
       1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + NUM_BARS * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  // TMEM: scores in [0, 256), the two output buffers in [256, 256 + 2 HD)
-  static constexpr int O_COL = 2 * KB;
+  // TMEM: scores in [0, NS * 128), the two output buffers after them
+  static constexpr int O_COL = NS * KB;
   static_assert(O_COL + 2 * HD <= 512, "TMEM holds 512 columns");
 };
 
@@ -109,8 +112,8 @@ __device__ __forceinline__ Unit unit_of(const AttnParams& p, int u, int nkb_all)
 
 // Persistent: one CTA per SM walks units u = blockIdx.x, + gridDim.x, ...
 // Every role counts the key chunks it has passed over all its units (g): the
-// k/v ring stage and phase, the score and P buffer (g & 1) and their phases
-// (g >> 1) follow from it, so the pipelines run on across unit boundaries.
+// k/v ring stage and phase, the score and P buffer (g mod NS) and their phases
+// (g / NS) follow from it, so the pipelines run on across unit boundaries.
 // Unit i of a CTA accumulates into output buffer i & 1, so its MMAs can start
 // while the softmax warps still store the output of unit i - 1.
 template <int HD, bool KT>
@@ -131,16 +134,17 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * RING + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * RING + s); };
   const uint32_t bar1 = bar0 + 8u * (1 + 4 * RING);
+  constexpr int NS = G::NS;
   auto s_full = [&](int b) { return bar1 + 8u * b; };
-  auto s_empty = [&](int b) { return bar1 + 8u * (2 + b); };
+  auto s_empty = [&](int b) { return bar1 + 8u * (NS + b); };
   // P of the chunk in score buffer b: written once the softmax stored it over
   // the scores, read once P v has completed
-  auto p_full = [&](int b) { return bar1 + 8u * (4 + b); };
-  auto pv_done = [&](int b) { return bar1 + 8u * (6 + b); };
-  const uint32_t drain = bar1 + 8u * 8;
-  const uint32_t q_empty = bar1 + 8u * 9;                     // the unit's score MMAs read q
-  auto o_empty = [&](int b) { return bar1 + 8u * (10 + b); };  // output buffer b stored
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * 12 - sbase));
+  auto p_full = [&](int b) { return bar1 + 8u * (2 * NS + b); };
+  auto pv_done = [&](int b) { return bar1 + 8u * (3 * NS + b); };
+  const uint32_t drain = bar1 + 8u * (4 * NS);
+  const uint32_t q_empty = bar1 + 8u * (4 * NS + 1);  // the unit's score MMAs read q
+  auto o_empty = [&](int b) { return bar1 + 8u * (4 * NS + 2 + b); };  // output buffer b stored
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * (4 * NS + 4) - sbase));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -157,13 +161,13 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NS; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), 4);  // the four softmax warps
       mbar_init(p_full(b), 4);
       mbar_init(pv_done(b), 1);
-      mbar_init(o_empty(b), 4);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(o_empty(b), 4);
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -268,14 +272,14 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         const int ob = ui & 1;  // this unit's output buffer
         ok = wait_bounded(q_full, ui & 1, wc, true);
         tc_fence_after();
-        // S for the unit's chunk j (global chunk g0 + j) into score buffer (g0 + j) & 1;
+        // S for the unit's chunk j (global chunk g0 + j) into score buffer (g0 + j) mod NS;
         // the unit's last one releases the q buffer
         const int g0 = g;
         auto issue_scores = [&](int j) -> bool {
           const int gj = g0 + j;
-          const int s = gj % RING, b = gj & 1;
+          const int s = gj % RING, b = gj % NS;
           if (!wait_bounded(k_full(s), (gj / RING) & 1, wc, true)) return false;
-          if (!wait_bounded(s_empty(b), ((gj >> 1) & 1) ^ 1u, wc, true)) return false;
+          if (!wait_bounded(s_empty(b), ((gj / NS) & 1) ^ 1u, wc, true)) return false;
           tc_fence_after();
           const uint32_t kd = k_s + s * G::K_BYTES;
 #pragma unroll
@@ -293,19 +297,22 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
           issued = true;
           return true;
         };
-        if (ok) ok = issue_scores(0);
+        // scores run NS - 1 chunks ahead of P v: the scores of chunk j + NS - 1
+        // reuse the buffer holding P of chunk j - 1, issued after its P v
+        constexpr int L = NS - 1;
+        for (int j = 0; ok && j < L && j < w.nkb; ++j) ok = issue_scores(j);
         // the output buffer is free once the softmax stored the unit two back
         if (ok && ui >= 2) ok = wait_bounded(o_empty(ob), ((ui >> 1) & 1) ^ 1u, wc, true);
         for (int j = 0; ok && j < w.nkb; ++j) {
-          // the next chunk's scores go in before this chunk's P v, so the
+          // the later chunks' scores go in before this chunk's P v, so the
           // tensor core works while the softmax runs
-          if (j + 1 < w.nkb && !issue_scores(j + 1)) {
+          if (j + L < w.nkb && !issue_scores(j + L)) {
             ok = false;
             break;
           }
           const int gj = g0 + j;
-          const int s = gj % RING, pb = gj & 1;
-          if (!wait_bounded(p_full(pb), (gj >> 1) & 1, wc, true) ||
+          const int s = gj % RING, pb = gj % NS;
+          if (!wait_bounded(p_full(pb), (gj / NS) & 1, wc, true) ||
               !wait_bounded(v_full(s), (gj / RING) & 1, wc, true)) {
             ok = false;
             break;
@@ -346,8 +353,8 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     float m_ref = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < w.nkb; ++j) {
       const int gj = g0 + j;
-      const int b = gj & 1;
-      if (!__all_sync(0xFFFFFFFFu, wait_bounded(s_full(b), (gj >> 1) & 1, wc, true) ? 1 : 0)) {
+      const int b = gj % NS;
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(s_full(b), (gj / NS) & 1, wc, true) ? 1 : 0)) {
         alive = false;
         break;
       }
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
         // a raised maximum: the output accumulated so far is scaled once the
         // previous chunk's P v has landed in it
         if (!__all_sync(0xFFFFFFFFu,
-                        wait_bounded(pv_done((gj - 1) & 1), ((gj - 1) >> 1) & 1, wc, true) ? 1 : 0)) {
+                        wait_bounded(pv_done((gj - 1) % NS), ((gj - 1) / NS) & 1, wc, true) ? 1 : 0)) {
           alive = false;
           break;
         }
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     if (!alive) break;
     const int gl = g - 1;  // the unit's last chunk
     if (!__all_sync(0xFFFFFFFFu,
-                    wait_bounded(pv_done(gl & 1), (gl >> 1) & 1, wc, true) ? 1 : 0)) {
+                    wait_bounded(pv_done(gl % NS), (gl / NS) & 1, wc, true) ? 1 : 0)) {
       alive = false;
       break;
     }
