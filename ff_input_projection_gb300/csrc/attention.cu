@@ -23,12 +23,13 @@
 // Structure:
 //   warp 0     TMA producer: a unit's q chunk once, then k and v chunks into
 //              rings of 4 stages (head_dim 64) or 2 (head_dim 128)
-//   warp 1     MMA issuer (one thread): S = q k^T into one of two TMEM score
-//              buffers (M 128, N 128, K head_dim), then O += P v into the
-//              unit's TMEM output accumulator (M 128, N head_dim, K 128) with
-//              P read from tensor memory; the next chunk's scores are issued
-//              before this chunk's P v, so the tensor core works while the
-//              softmax runs
+//   warp 1     score MMAs (one thread): S = q k^T into one of NS TMEM score
+//              buffers (M 128, N 128, K head_dim), as far ahead as the buffers
+//              allow (a buffer is reused once its previous chunk's P v is done)
+//   warp 2     P v MMAs (one thread): O += P v into the unit's TMEM output
+//              accumulator (M 128, N head_dim, K 128) with P read from tensor
+//              memory. Two issuing threads: one thread issuing both measured
+//              about 100 cycles per instruction of these thin shapes
 //   warps 4-7  softmax, one query row per thread (TMEM lane = row): scores
 //              from TMEM, a reference maximum m and the sum l, P = 2^(s c - m)
 //              rounded to bf16 and written back over the chunk's scores in
@@ -72,8 +73,8 @@ struct ACfg {
   static constexpr int NS = HD == 64 ? 3 : 2;
   // q full/empty; k full/empty and v full/empty per stage; s full/empty,
   // p full and P v done per score buffer; output empty per output buffer;
-  // drain
-  static constexpr int NUM_BARS = 2 + 4 * RING + 4 * NS + 2 + 1;
+  // a drain per MMA-issuing thread
+  static constexpr int NUM_BARS = 2 + 4 * RING + 4 * NS + 2 + 2;
   static_assert(1 + 2 * RING <= 32, "armed-barrier bit masks hold 1 + 2 * RING slots");
   static constexpr int SMEM_BYTES =
       1024 + Q_BYTES + RING * (K_BYTES + V_BYTES) + NUM_BARS * 8 + 16;
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
   const uint32_t drain = bar1 + 8u * (4 * NS);
   const uint32_t q_empty = bar1 + 8u * (4 * NS + 1);  // the unit's score MMAs read q
   auto o_empty = [&](int b) { return bar1 + 8u * (4 * NS + 2 + b); };  // output buffer b stored
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * (4 * NS + 4) - sbase));
+  const uint32_t drain_pv = bar1 + 8u * (4 * NS + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar1 + 8u * (4 * NS + 5) - sbase));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
     }
     for (int b = 0; b < 2; ++b) mbar_init(o_empty(b), 4);
     mbar_init(drain, 1);
+    mbar_init(drain_pv, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     prefetch_tmap(&p.tmap_q);
@@ -259,9 +262,12 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
           wait_bounded(v_full(s), (armed_par >> (1 + RING + s)) & 1u, dc, false);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------ MMA issuers: warp 1 the
+    // scores, warp 2 the P v products (different TMEM accumulators; each
+    // thread's commits track its own MMAs)
     if (lane == 0) {
+      const bool scores = warp == 1;
       const uint32_t idesc_s = make_idesc(false, KT, QB, KB);
       const uint32_t idesc_o = make_idesc(false, true, QB, HD);
       bool issued = false, ok = true;
@@ -269,72 +275,68 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       for (int u = static_cast<int>(blockIdx.x); ok && u < n_units;
            u += static_cast<int>(gridDim.x), ++ui) {
         const Unit w = unit_of(p, u, nkb_all);
-        const int ob = ui & 1;  // this unit's output buffer
-        ok = wait_bounded(q_full, ui & 1, wc, true);
-        tc_fence_after();
-        // S for the unit's chunk j (global chunk g0 + j) into score buffer (g0 + j) mod NS;
-        // the unit's last one releases the q buffer
         const int g0 = g;
-        auto issue_scores = [&](int j) -> bool {
-          const int gj = g0 + j;
-          const int s = gj % RING, b = gj % NS;
-          if (!wait_bounded(k_full(s), (gj / RING) & 1, wc, true)) return false;
-          if (!wait_bounded(s_empty(b), ((gj / NS) & 1) ^ 1u, wc, true)) return false;
+        if (scores) {
+          ok = wait_bounded(q_full, ui & 1, wc, true);
           tc_fence_after();
-          const uint32_t kd = k_s + s * G::K_BYTES;
+          for (int j = 0; ok && j < w.nkb; ++j) {
+            // S for global chunk gj into score buffer gj mod NS, once the
+            // buffer's previous chunk is done with: its scores read by the
+            // softmax and its P read by P v
+            const int gj = g0 + j;
+            const int s = gj % RING, b = gj % NS;
+            ok = wait_bounded(k_full(s), (gj / RING) & 1, wc, true) &&
+                 wait_bounded(s_empty(b), ((gj / NS) & 1) ^ 1u, wc, true) &&
+                 (gj < NS || wait_bounded(pv_done(b), ((gj / NS) - 1) & 1, wc, true));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kd = k_s + s * G::K_BYTES;
 #pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint64_t a_desc = sw128_desc(q_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
-            // pre-transposed k: MN-major B, two 64-key chunks per 64 head lanes;
-            // else K-major B, like q
-            const uint64_t b_desc = KT ? sw128_desc(kd + (k / 4) * 2 * CHUNK + (k % 4) * 2048, CHUNK, 1024)
-                                       : sw128_desc(kd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
-            umma_bf16<1>(tmem + b * KB, a_desc, b_desc, idesc_s, k > 0 ? 1u : 0u);
+            for (int k = 0; k < HD / 16; ++k) {
+              const uint64_t a_desc = sw128_desc(q_s + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+              // pre-transposed k: MN-major B, two 64-key chunks per 64 head lanes;
+              // else K-major B, like q
+              const uint64_t b_desc = KT ? sw128_desc(kd + (k / 4) * 2 * CHUNK + (k % 4) * 2048, CHUNK, 1024)
+                                         : sw128_desc(kd + (k / 4) * ATOM + (k % 4) * 32, 16, 1024);
+              umma_bf16<1>(tmem + b * KB, a_desc, b_desc, idesc_s, k > 0 ? 1u : 0u);
+            }
+            umma_commit<1>(s_full(b));
+            umma_commit<1>(k_empty(s));
+            if (j == w.nkb - 1) umma_commit<1>(q_empty);  // the unit's last read of q
+            issued = true;
           }
-          umma_commit<1>(s_full(b));
-          umma_commit<1>(k_empty(s));
-          if (j == w.nkb - 1) umma_commit<1>(q_empty);
-          issued = true;
-          return true;
-        };
-        // scores run NS - 1 chunks ahead of P v: the scores of chunk j + NS - 1
-        // reuse the buffer holding P of chunk j - 1, issued after its P v
-        constexpr int L = NS - 1;
-        for (int j = 0; ok && j < L && j < w.nkb; ++j) ok = issue_scores(j);
-        // the output buffer is free once the softmax stored the unit two back
-        if (ok && ui >= 2) ok = wait_bounded(o_empty(ob), ((ui >> 1) & 1) ^ 1u, wc, true);
-        for (int j = 0; ok && j < w.nkb; ++j) {
-          // the later chunks' scores go in before this chunk's P v, so the
-          // tensor core works while the softmax runs
-          if (j + L < w.nkb && !issue_scores(j + L)) {
-            ok = false;
-            break;
-          }
-          const int gj = g0 + j;
-          const int s = gj % RING, pb = gj % NS;
-          if (!wait_bounded(p_full(pb), (gj / NS) & 1, wc, true) ||
-              !wait_bounded(v_full(s), (gj / RING) & 1, wc, true)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vd = v_s + s * G::V_BYTES;
+        } else {
+          // the output buffer is free once the softmax stored the unit two back
+          const int ob = ui & 1;
+          if (ui >= 2) ok = wait_bounded(o_empty(ob), ((ui >> 1) & 1) ^ 1u, wc, true);
+          for (int j = 0; ok && j < w.nkb; ++j) {
+            const int gj = g0 + j;
+            const int s = gj % RING, pb = gj % NS;
+            ok = wait_bounded(p_full(pb), (gj / NS) & 1, wc, true) &&
+                 wait_bounded(v_full(s), (gj / RING) & 1, wc, true);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vd = v_s + s * G::V_BYTES;
 #pragma unroll
-          for (int k = 0; k < KB / 16; ++k) {
-            // P from tensor memory: 16 keys are 8 packed columns of the score buffer
-            const uint64_t b_desc =
-                sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
-            umma_bf16_ts(tmem + G::O_COL + ob * HD, tmem + pb * KB + 8 * k, b_desc, idesc_o,
-                         (j | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < KB / 16; ++k) {
+              // P from tensor memory: 16 keys are 8 packed columns of the score buffer
+              const uint64_t b_desc =
+                  sw128_desc(vd + (k / 4) * (HD / 64) * CHUNK + (k % 4) * 2048, CHUNK, 1024);
+              umma_bf16_ts(tmem + G::O_COL + ob * HD, tmem + pb * KB + 8 * k, b_desc, idesc_o,
+                           (j | k) != 0 ? 1u : 0u);
+            }
+            umma_commit<1>(pv_done(pb));
+            umma_commit<1>(v_empty(s));
+            issued = true;
           }
-          umma_commit<1>(pv_done(pb));
-          umma_commit<1>(v_empty(s));
         }
         g = g0 + w.nkb;
       }
       if (issued) {
-        umma_commit<1>(drain);  // every MMA retired before TMEM is freed
-        wait_bounded(drain, 0, wc, false);
+        // every MMA of this thread retired before TMEM is freed
+        const uint32_t dr = scores ? drain : drain_pv;
+        umma_commit<1>(dr);
+        wait_bounded(dr, 0, wc, false);
       }
     }
   } else if (warp >= 4) {
