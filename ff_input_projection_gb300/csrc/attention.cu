@@ -53,6 +53,13 @@
 namespace fp {
 namespace {
 
+// max(a, b, c): one three-input max instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 constexpr int QB = 128;   // queries per CTA: one per softmax thread and TMEM lane
 constexpr int KB = 128;   // keys per chunk: the N of S and the K of P v
 constexpr int ANT = 256;  // 8 warps
@@ -382,7 +389,10 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < KB; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]));
+      for (int i = 0; i < KB; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx[k] = fmax3(mx[k], __uint_as_float(sv[i + k]), __uint_as_float(sv[i + 8 + k]));
       const float m_blk = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       // the reference maximum (log2 units) moves only when this chunk's maximum
@@ -393,9 +403,9 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
       // P = 2^(s c - m) on packed pairs (one fma.f32x2 per two scores), rounded
       // to bf16 for the tensor core; the row sum adds the fp32 values
       uint32_t pw[KB / 2];
-      float ps[8];
+      uint64_t ps2[4];  // partial sums on packed pairs
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ps[k] = 0.0f;
+      for (int k = 0; k < 4; ++k) ps2[k] = 0ull;
       const uint64_t c2 = f2_splat(c), nm2 = f2_splat(-m_new);
 #pragma unroll
       for (int i = 0; i < KB / 2; ++i) {
@@ -405,8 +415,11 @@ __global__ void __launch_bounds__(ANT, 1) attention_kernel(const __grid_constant
                   x0, x1);
         const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
         pw[i] = pack_bf16x2(e0, e1);
-        ps[i & 7] += e0 + e1;
+        ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(e0, e1));
       }
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) f2_unpack(ps2[k], ps[2 * k], ps[2 * k + 1]);
       const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_run = l_run * alpha + sum;
       m_ref = m_new;
