@@ -534,9 +534,11 @@ __global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * ACC_COLS;
       const int cols = min(e.bn_eff, e.N - tc.n0);  // columns this tile owns
-      // A TMA store writes the warp's 32 rows as one block: they must all be
-      // valid and, for the head-major buffers, lie in one batch element
-      // (tokens t .. t+31). Lane 0 issues the stores with its own coordinates.
+      // Block stores (the ff tiles' warp-wide copy out of the staging buffer,
+      // the TMA stores of head tiles and mixed tiles) write the warp's 32 rows
+      // as one block: they must all be valid and, for the head-major buffers,
+      // lie in one batch element (tokens t .. t+31). Lane 0 issues the TMA
+      // stores with its own coordinates.
       const bool tma_ff = p.tma_store && __all_sync(0xFFFFFFFFu, valid);
       // whole heads of the blocked q|k|v order, rotation absent or in 16-lane
       // groups, k not pre-transposed
@@ -624,9 +626,21 @@ __global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
                            w[4 * q + 2], w[4 * q + 3]);
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&p.tmap_ff32, stg, tc.n0 + c, static_cast<int>(m));
-              bulk_commit();
+            // read back and stored by the whole warp: four lanes per 64-byte
+            // row segment, eight rows per instruction (measured faster than a
+            // TMA store of the block: 134.3 -> 129.5 us on a 24576 x 768 x 5376
+            // product, the same bits)
+            {
+              uint16_t* const blk = static_cast<uint16_t*>(e.out_ff) + (m - lane) * e.ff_ld +
+                                    tc.n0 + c;
+              const int ch = lane & 3;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int r = (lane >> 2) + 8 * k;
+                const uint4 v = ld_shared_v4(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+                *reinterpret_cast<uint4*>(blk + static_cast<int64_t>(r) * e.ff_ld + ch * 8) = v;
+              }
+              __syncwarp();
             }
           } else if (valid && store_in_bounds(e, 0, m * e.ff_ld + tc.n0 + c, 32)) {
             uint4* d4 = reinterpret_cast<uint4*>(ff_row + c);
