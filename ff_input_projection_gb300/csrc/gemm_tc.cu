@@ -634,11 +634,23 @@ __global__ void __launch_bounds__(Warps<GRAD>::NT, 1)
               uint16_t* const blk = static_cast<uint16_t*>(e.out_ff) + (m - lane) * e.ff_ld +
                                     tc.n0 + c;
               const int ch = lane & 3;
+              if (!e.bounds_check) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int r = (lane >> 2) + 8 * k;
-                const uint4 v = ld_shared_v4(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
-                *reinterpret_cast<uint4*>(blk + static_cast<int64_t>(r) * e.ff_ld + ch * 8) = v;
+                for (int k = 0; k < 4; ++k) {
+                  const int r = (lane >> 2) + 8 * k;
+                  const uint4 v = ld_shared_v4(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+                  *reinterpret_cast<uint4*>(blk + static_cast<int64_t>(r) * e.ff_ld + ch * 8) = v;
+                }
+              } else {
+                // FP_OPT_BOUNDS_CHECK: each 16-byte piece checked against the extent
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int r = (lane >> 2) + 8 * k;
+                  const uint4 v = ld_shared_v4(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+                  uint16_t* const dst = blk + static_cast<int64_t>(r) * e.ff_ld + ch * 8;
+                  if (store_in_bounds(e, 0, dst - static_cast<uint16_t*>(e.out_ff), 8))
+                    *reinterpret_cast<uint4*>(dst) = v;
+                }
               }
               __syncwarp();
             }

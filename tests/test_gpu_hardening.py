@@ -99,6 +99,11 @@ DIRECT = [
     W_("bc_simt_f32", (3, 50, 48), 2, 1, 48, 96, 3, 16, A.ACT_GELU_ERF, 10000.0, True, "f32", 98,
        k_transposed=True),
 ]
+# tensor-core ff tiles, all rows valid: every store is the kernel-addressed
+# warp-wide block copy out of the staging buffer
+BLOCKS = W_("bc_blocks_tc", (4, 256, 128), 2, 1, 128, 640, 0, 0, A.ACT_GELU_ERF, 0.0, True,
+            "bf16", 99)
+DIRECT.append(BLOCKS)
 SIMT_ONLY = [w for w in DIRECT if w.name.startswith("bc_simt")]
 
 
@@ -119,7 +124,7 @@ def test_bounds_check_passes_correct_stores(w, cuda_ok):
             assert_close(host(out[k]), ref[k], w.dtype, f"{w.name}:{k}")
 
 
-@pytest.mark.parametrize("w", SIMT_ONLY, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SIMT_ONLY + [BLOCKS], ids=lambda w: w.name)
 def test_bounds_check_stops_and_reports_stores_past_the_extent(w, cuda_ok):
     """Test mode: every extent is halved, so stores into the second half of a
     buffer count as out of bounds. They must be skipped (the NaN fill stays)
