@@ -45,8 +45,9 @@ NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 KERNEL_SOURCES = {
     "gemm": ["ff_input_projection_gb300/csrc/gemm_tc.cu",
              "ff_input_projection_gb300/csrc/epilogue.cuh",
-             "ff_input_projection_gb300/csrc/tc_ptx.cuh",
-             "ff_input_projection_gb300/csrc/gemm_simt.cu"],
+             "ff_input_projection_gb300/csrc/tc_ptx.cuh"],
+    "simt": ["ff_input_projection_gb300/csrc/gemm_simt.cu",
+             "ff_input_projection_gb300/csrc/epilogue.cuh"],
     "attention": ["ff_input_projection_gb300/csrc/attention.cu",
                   "ff_input_projection_gb300/csrc/epilogue.cuh",
                   "ff_input_projection_gb300/csrc/tc_ptx.cuh"],
@@ -107,7 +108,7 @@ def recorded_traffic(workload: str):
     ncu summary (tensor-core GEMM, FFMA GEMM or attention), if it was taken on
     the current kernel sources (else None)."""
     paths = [(os.path.join(ROOT, "profiles", f"{k}_{workload}.md"), kind)
-             for k, kind in (("tc_gemm", "gemm"), ("simt_gemm", "gemm"), ("attention", "attention"))]
+             for k, kind in (("tc_gemm", "gemm"), ("simt_gemm", "simt"), ("attention", "attention"))]
     paths = [q for q in paths if os.path.exists(q[0])]
     if not paths:
         return None
@@ -568,7 +569,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, dev)
     roof = roofline(w, ms, pk, pk_src, sm_count)
     roof["traffic"] = recorded_traffic(w.name)
-    roof["kernel_hash"] = kernel_hash()
+    roof["kernel_hash"] = kernel_hash("simt" if w.dtype == "f32" else "gemm")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

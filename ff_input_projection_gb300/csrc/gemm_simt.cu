@@ -10,14 +10,21 @@
 // describe (e.g. an odd spatial extent) or whose block widths are not
 // multiples of 16.
 //
-// Tile: 128 tokens x 128 fused columns, k-steps of 16, 256 threads with an
-// 8x8 register block each (accumulated on packed fp32 pairs) (rows ty*4+{0..3} and 64+ty*4+{0..3}, columns
-// likewise), operands double-buffered in shared memory with a register
-// prefetch of the next k-step. The epilogue stages the fp32 tile in shared
-// memory so a rotary pair (lane i, lane i + half) can be read by whichever
-// thread owns either lane, then adds bias, applies the activation or the
-// rotation, and writes ff token-major and q/k/v head-major with consecutive
-// threads on consecutive lanes.
+// Tile: 128 tokens x 128 fused columns, 256 threads with an 8x8 register
+// block each (accumulated on packed fp32 pairs) (rows ty*4+{0..3} and
+// 64+ty*4+{0..3}, columns likewise). Two main loops:
+//  * general (any strides, bf16 or fp32 storage): k-steps of 16,
+//    double-buffered in shared memory with a register prefetch of the next
+//    k-step;
+//  * fp32 with unit-stride tokens and 16-byte-aligned chunks (channels-first
+//    x such as NCHW): k-steps of 32 copied global -> shared by cp.async, three
+//    in flight, fragments double-buffered in registers.
+// The epilogue stages the fp32 tile in shared memory so a rotary pair (lane i,
+// lane i + half) can be read by whichever thread owns either lane, then adds
+// bias, applies the activation or the rotation, and writes ff token-major and
+// q/k/v head-major with consecutive threads on consecutive lanes. Tiles of the
+// second loop without rotation or transposed k skip the staging and store
+// 16-byte groups straight from registers.
 #include "epilogue.cuh"
 #include "fp_internal.h"
 
@@ -274,6 +281,226 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
   simt_epilogue<T>(p, Cs, o, s0, n0);
 }
 
+// ---- fp32 storage with unit-stride tokens (channels-first x, e.g. NCHW): the
+// operand tiles are copied global -> shared by cp.async in 16-byte chunks (4
+// tokens of one channel; 4 columns of one weight row), kAsyncStages k-steps in
+// flight, so no thread stages operands through registers. Chunks past the
+// last token, channel or column are zero-filled by the copy's source size.
+constexpr int kAsyncBK = 32, kAsyncStages = 3;
+constexpr int kAsyncChunks = kAsyncBK * BM / 4 / NT;  // 16-byte chunks per thread per operand
+constexpr int kAsyncSmem = kAsyncStages * kAsyncBK * (BM + BN) * 4 > kSmemBytes
+                               ? kAsyncStages * kAsyncBK * (BM + BN) * 4
+                               : kSmemBytes;
+static_assert(BM == BN && kAsyncChunks * NT * 4 == kAsyncBK * BM, "chunk split");
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, int src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams p) {
+  const float* X = static_cast<const float*>(p.x);
+  const float* Wt = static_cast<const float*>(p.W);
+  extern __shared__ __align__(16) float smem[];
+  constexpr int SK = kAsyncBK;
+  float* As = smem;                             // [stage][SK][BM]
+  float* Bs = smem + kAsyncStages * SK * BM;    // [stage][SK][BN]
+
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int64_t tile = blockIdx.x;
+  const int n_tile = static_cast<int>(tile % p.num_n_tiles);
+  const int64_t m_tile = tile / p.num_n_tiles;
+  const int64_t o = m_tile / p.m_tiles_per_slab;
+  const int64_t s0 = (m_tile - o * p.m_tiles_per_slab) * BM;
+  const int n0 = n_tile * p.epi.bn_eff;
+  const TokenMap& tk = p.tok;
+  const int C = p.C, N = p.epi.N;
+
+  // This thread's chunks of each operand per stage: chunk c = tid + 256 j
+  // covers row k = c / 32 = ck + 8 j of the stage and elements 4 (c % 32) .. + 3.
+  const int ck = tid >> 5, ce = (tid & 31) * 4;
+  const int64_t rows_left = tk.S_in - s0 - ce;
+  const int a_bytes = rows_left >= 4 ? 16 : rows_left > 0 ? static_cast<int>(rows_left) * 4 : 0;
+  const int b_bytes = n0 + ce < N ? 16 : 0;  // N is a multiple of 4
+  const float* a_src = X + outer_offset(tk, o) + s0 + ce + static_cast<int64_t>(ck) * tk.c_stride;
+  const float* b_src = Wt + static_cast<int64_t>(ck) * N + n0 + ce;
+  const int64_t a_k8 = 8 * tk.c_stride;  // next chunk: 8 channels further
+  auto issue = [&](int kb) {
+    const int st = kb % kAsyncStages;
+    float* a = As + st * SK * BM + ck * BM + ce;
+    float* b = Bs + st * SK * BN + ck * BN + ce;
+    const int k = kb * SK + ck;
+    const int64_t ka = static_cast<int64_t>(kb) * SK * tk.c_stride;
+    const int64_t kw = static_cast<int64_t>(kb) * SK * N;
+#pragma unroll
+    for (int j = 0; j < kAsyncChunks; ++j) {
+      const bool in = k + 8 * j < C;
+      cp_async16(a + j * 8 * BM, in ? a_src + ka + j * a_k8 : X, in ? a_bytes : 0);
+      cp_async16(b + j * 8 * BN, in ? b_src + kw + static_cast<int64_t>(j) * 8 * N : Wt,
+                 in ? b_bytes : 0);
+    }
+  };
+
+  uint64_t acc2[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc2[i][t] = 0ull;
+
+  const int num_k = (C + SK - 1) / SK;
+#pragma unroll
+  for (int s = 0; s < kAsyncStages - 1; ++s) {
+    if (s < num_k) issue(s);
+    cp_async_commit();
+  }
+  for (int kb = 0; kb < num_k; ++kb) {
+    // this thread's copies of step kb have landed; the barrier publishes every
+    // thread's and retires step kb - 1, whose stage the next issue refills
+    cp_async_wait<kAsyncStages - 2>();
+    __syncthreads();
+    if (kb + kAsyncStages - 1 < num_k) issue(kb + kAsyncStages - 1);
+    cp_async_commit();
+    const int st = kb % kAsyncStages;
+    const float* a = As + st * SK * BM;
+    const float* b = Bs + st * SK * BN;
+    // fragments double-buffered in registers: step kk + 1's loads are issued
+    // before step kk's FMAs
+    float4 fa[2][2], fb[2][2];
+    fa[0][0] = *reinterpret_cast<const float4*>(a + ty * 4);
+    fa[0][1] = *reinterpret_cast<const float4*>(a + 64 + ty * 4);
+    fb[0][0] = *reinterpret_cast<const float4*>(b + tx * 4);
+    fb[0][1] = *reinterpret_cast<const float4*>(b + 64 + tx * 4);
+#pragma unroll
+    for (int kk = 0; kk < SK; ++kk) {
+      const int cur = kk & 1, nxt = cur ^ 1;
+      if (kk + 1 < SK) {
+        fa[nxt][0] = *reinterpret_cast<const float4*>(a + (kk + 1) * BM + ty * 4);
+        fa[nxt][1] = *reinterpret_cast<const float4*>(a + (kk + 1) * BM + 64 + ty * 4);
+        fb[nxt][0] = *reinterpret_cast<const float4*>(b + (kk + 1) * BN + tx * 4);
+        fb[nxt][1] = *reinterpret_cast<const float4*>(b + (kk + 1) * BN + 64 + tx * 4);
+      }
+      const float4 a0 = fa[cur][0], a1 = fa[cur][1], b0 = fb[cur][0], b1 = fb[cur][1];
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint64_t bv2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                               f2_pack(b1.z, b1.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t ai = f2_splat(av[i]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc2[i][t] = f2_fma(ai, bv2[t], acc2[i][t]);
+      }
+    }
+  }
+  cp_async_wait<0>();  // only empty groups remain; the epilogue tile overlays the stages
+  __syncthreads();
+
+  const Epilogue& e = p.epi;
+  if (e.rope_half == 0 && !e.k_transposed && (e.heads == 0 || e.hd % 4 == 0)) {
+    // No rotation pairs and no transposed k: each thread stores its own 8 x 8
+    // block from registers, 4 consecutive columns (one head, F and hd being
+    // multiples of 4) per 16-byte store; a warp's store covers 2 rows x 64
+    // columns. Per-row output bases come from shared memory, once per tile.
+    int64_t* row_ff = reinterpret_cast<int64_t*>(smem);  // [BM]
+    int64_t* row_q = row_ff + BM;
+    int64_t* row_kv = row_q + BM;
+    const int nkv = e.groups > 0 ? e.groups : e.heads;
+    if (tid < BM) {
+      const int64_t m = o * tk.S_in + s0 + tid;
+      const int64_t bb = m / e.T, t = m - bb * e.T;
+      row_ff[tid] = m * e.F;
+      row_q[tid] = (bb * e.heads * e.T + t) * e.hd;
+      row_kv[tid] = (bb * nkv * e.T + t) * e.hd;
+    }
+    __syncthreads();
+    const float* bias = static_cast<const float*>(e.bias);
+    const int64_t tile_rows = tk.S_in - s0;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int c0 = h2 * 64 + tx * 4;
+      const int n = n0 + c0;
+      if (c0 >= e.bn_eff || n >= N) continue;
+      const ColInfo ci = decode_col(e, n);
+      const float4 bv = bias ? *reinterpret_cast<const float4*>(bias + n) : make_float4(0, 0, 0, 0);
+      float* const base = static_cast<float*>(out_base(e, ci.seg));
+      const int64_t col_off =
+          ci.seg == 0 ? ci.j : static_cast<int64_t>(ci.head) * e.T * e.hd + ci.j;
+      const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : row_kv;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+        if (r >= tile_rows) continue;
+        float4 v;
+        f2_unpack(acc2[i][2 * h2], v.x, v.y);
+        f2_unpack(acc2[i][2 * h2 + 1], v.z, v.w);
+        v.x += bv.x;
+        v.y += bv.y;
+        v.z += bv.z;
+        v.w += bv.w;
+        if (ci.seg == 0) {
+          v.x = activate(e.act, v.x);
+          v.y = activate(e.act, v.y);
+          v.z = activate(e.act, v.z);
+          v.w = activate(e.act, v.w);
+        }
+        const int64_t off = rb[r] + col_off;
+        if (store_in_bounds(e, ci.seg, off, 4)) *reinterpret_cast<float4*>(base + off) = v;
+      }
+    }
+    return;
+  }
+
+  float* Cs = smem;  // [BM][CS_LD]
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+    float c[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) f2_unpack(acc2[i][t], c[2 * t], c[2 * t + 1]);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + tx * 4) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(Cs + r * CS_LD + 64 + tx * 4) = make_float4(c[4], c[5], c[6], c[7]);
+  }
+  __syncthreads();
+
+  simt_epilogue<float>(p, Cs, o, s0, n0);
+}
+
+// The cp.async kernel's preconditions: fp32 storage, unit-stride tokens, and
+// every chunk 16-byte aligned (x and W 16-byte aligned; the channel stride,
+// every outer stride and N multiples of 4 elements; tiles start at multiples
+// of 128 tokens and columns n0 multiples of 4).
+bool async_ok(const SimtParams& p) {
+  const TokenMap& tk = p.tok;
+  if (tk.s_stride != 1 || tk.c_stride % 4 != 0 || p.epi.N % 4 != 0 || p.epi.bn_eff % 4 != 0)
+    return false;
+  if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0 || reinterpret_cast<uintptr_t>(p.W) % 16 != 0)
+    return false;
+  for (int d = 0; d < tk.n_outer_dims; ++d)
+    if (tk.outer_stride[d] % 4 != 0) return false;
+  return true;
+}
+
+cudaError_t launch_async(const SimtParams& p, int64_t tiles, cudaStream_t stream) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_done[dev]) {
+    err = cudaFuncSetAttribute(simt_gemm_async_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kAsyncSmem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_done[dev] = 1;
+  }
+  simt_gemm_async_kernel<<<static_cast<unsigned>(tiles), NT, kAsyncSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename T, bool K_MAJOR>
 cudaError_t launch_one(const SimtParams& p, int64_t tiles, cudaStream_t stream) {
   static int attr_done[64] = {0};
@@ -296,6 +523,7 @@ cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream
   int64_t tiles = p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const bool k_major = p.tok.c_stride == 1;
+  if (!bf16 && !k_major && async_ok(p)) return launch_async(p, tiles, stream);
   if (bf16)
     return k_major ? launch_one<uint16_t, true>(p, tiles, stream)
                    : launch_one<uint16_t, false>(p, tiles, stream);

@@ -108,6 +108,49 @@ def test_strided_views_read_in_place(cuda_ok):
             assert_close(host(out[k]), ref[k], w.dtype, f"view:{k}")
 
 
+def test_fp32_channels_first_copy_paths(cuda_ok):
+    """fp32 channels-first operands go global -> shared in 16-byte chunks when
+    the channel stride, the outer token strides and N are multiples of 4
+    elements, else through registers. Cases on both sides of that rule: rows of
+    10 tokens at a stride of 12 (the last chunk of each row is half a chunk),
+    rows at a stride of 11 (channel stride 66), and N = 90 (head_dim 10).
+    Tiles without rotation or transposed k store from registers; the others
+    stage the tile in shared memory."""
+    w = next(s for s in SMALL if s.name == "fp32_rope_silu")  # x [2, 24, 6, 10], N 108
+    inp = fpsynth.make_inputs(w)
+    ref = oracle.forward_workload(w, inp)
+    x = to_device(inp["x"], w.dtype)
+    W = to_device(inp["W"], w.dtype)
+    b = to_device(inp["b"], w.dtype)
+    for row in (12, 11):
+        big = torch.zeros((2, 24, 6, row), dtype=x.dtype, device="cuda")
+        big[..., :10] = x
+        proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+        out = proj.forward(big[..., :10], W, b, None, channel_dim=w.channel_dim,
+                           n_batch_dims=w.n_batch_dims)
+        torch.cuda.synchronize()
+        assert proj.device_status() == fpx.FP_OK
+        for k, o in zip(("ff", "q", "k", "v"), out):
+            assert_close(host(o), ref[k], w.dtype, f"row stride {row}:{k}")
+    # N = 90; then two cases without rotation, whose tiles store straight from
+    # registers: GELU ff + bias + heads over ragged token and column tiles, and
+    # grouped-query heads
+    for w2 in (W_("fp32_n90", (2, 20, 6, 10), 1, 1, 20, 30, 2, 10, A.ACT_SILU, 10000.0, True,
+                  "f32", 78),
+               W_("fp32_gelu_heads", (2, 48, 9, 15), 1, 1, 48, 96, 3, 16, A.ACT_GELU_ERF, 0.0,
+                  True, "f32", 79),
+               W_("fp32_gqa", (2, 64, 10, 10), 1, 1, 64, 0, 4, 16, A.ACT_NONE, 0.0, True, "f32",
+                  80, n_query_groups=2)):
+        inp2 = fpsynth.make_inputs(w2)
+        ref2 = oracle.forward_workload(w2, inp2)
+        out2 = run(w2, inp2)
+        for k in ("ff", "q", "k", "v"):
+            if out2[k] is None:
+                assert ref2[k].size == 0
+                continue
+            assert_close(host(out2[k]), ref2[k], w2.dtype, f"{w2.name}:{k}")
+
+
 def test_identity_weight_layout_is_bit_exact(cuda_ok):
     """W = [I | I | I | I], no bias/act/rotation: ff = x and q = k = v = x split
     head-major, exactly, at the full channels-first Walrus shape."""
