@@ -17,8 +17,9 @@
 //    double-buffered in shared memory with a register prefetch of the next
 //    k-step;
 //  * fp32 with unit-stride tokens and 16-byte-aligned chunks (channels-first
-//    x such as NCHW): k-steps of 32 copied global -> shared by cp.async, three
-//    in flight, fragments double-buffered in registers.
+//    x such as NCHW): k-steps of 32 copied global -> shared by cp.async,
+//    fragments double-buffered in registers; tiles of 128 or 64 columns
+//    (4 CTAs of 128 threads per SM), whichever spreads the work more evenly.
 // The epilogue stages the fp32 tile in shared memory so a rotary pair (lane i,
 // lane i + half) can be read by whichever thread owns either lane, then adds
 // bias, applies the activation or the rotation, and writes ff token-major and
@@ -71,9 +72,12 @@ __device__ __forceinline__ void st_elem(uint16_t* p, int64_t i, float v) {
 // Epilogue of one tile, kept out of line so the main loop's register
 // allocation does not carry it. Cs holds the fp32 accumulator tile [BM][CS_LD]
 // followed by room for five [BM] int64 arrays.
-template <typename T>
+// TBN: the tile's column count (the CTA has 2 * TBN threads; the tile's row
+// stride in Cs is TBN + 4).
+template <typename T, int TBN = BN>
 __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64_t o, int64_t s0,
                                            int n0) {
+  constexpr int CSLD = TBN + 4, NTE = 2 * TBN;
   const int tid = threadIdx.x;
   const int64_t S_in = p.tok.S_in;
   const int N = p.epi.N;
@@ -82,7 +86,7 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
   const int half = e.rope_half;
   // Per-row output bases, once per tile (rows of a tile are consecutive tokens
   // of one slab): token index into ff, q and k/v buffers, and the position.
-  int64_t* row_ff = reinterpret_cast<int64_t*>(Cs + BM * CS_LD);  // [BM]
+  int64_t* row_ff = reinterpret_cast<int64_t*>(Cs + BM * CSLD);  // [BM]
   int64_t* row_q = row_ff + BM;
   int64_t* row_kv = row_q + BM;
   int64_t* row_t = row_kv + BM;
@@ -99,7 +103,7 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
   }
   __syncthreads();
   // each thread owns one column of the tile and every other row
-  const int c = tid % BN;
+  const int c = tid % TBN;
   const int n = n0 + c;
   if (c >= e.bn_eff || n >= N) return;
   const ColInfo ci = decode_col(e, n);
@@ -119,19 +123,19 @@ __device__ __noinline__ void simt_epilogue(const SimtParams& p, float* Cs, int64
   const int64_t tile_rows = S_in - s0;
   // rows in batches of 8: every load of a batch (accumulator, rotation partner,
   // cos/sin) is issued before its stores, so table latency is paid once per batch
-  constexpr int kStep = NT / BN, kBatch = 8;
-  for (int r0 = tid / BN; r0 < BM; r0 += kStep * kBatch) {
+  constexpr int kStep = NTE / TBN, kBatch = 8;
+  for (int r0 = tid / TBN; r0 < BM; r0 += kStep * kBatch) {
     float v[kBatch], pv[kBatch], cc[kBatch], ss[kBatch];
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
       const int r = r0 + q * kStep;
       const bool in = r < BM && r < tile_rows;
-      v[q] = in ? Cs[r * CS_LD + c] + bv : 0.0f;
+      v[q] = in ? Cs[r * CSLD + c] + bv : 0.0f;
       pv[q] = 0.0f;
       cc[q] = 1.0f;
       ss[q] = 0.0f;
       if (in && rot) {
-        pv[q] = Cs[r * CS_LD + pc] + pbv;
+        pv[q] = Cs[r * CSLD + pc] + pbv;
         if (e.rope_per_lane) {
           const float4 c4 = e.rope_cs4[static_cast<int64_t>(f) * e.T + row_t[r]];
           cc[q] = lo ? c4.x : c4.z;
@@ -283,15 +287,30 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
 
 // ---- fp32 storage with unit-stride tokens (channels-first x, e.g. NCHW): the
 // operand tiles are copied global -> shared by cp.async in 16-byte chunks (4
-// tokens of one channel; 4 columns of one weight row), kAsyncStages k-steps in
-// flight, so no thread stages operands through registers. Chunks past the
-// last token, channel or column are zero-filled by the copy's source size.
-constexpr int kAsyncBK = 32, kAsyncStages = 3;
-constexpr int kAsyncChunks = kAsyncBK * BM / 4 / NT;  // 16-byte chunks per thread per operand
-constexpr int kAsyncSmem = kAsyncStages * kAsyncBK * (BM + BN) * 4 > kSmemBytes
-                               ? kAsyncStages * kAsyncBK * (BM + BN) * 4
-                               : kSmemBytes;
-static_assert(BM == BN && kAsyncChunks * NT * 4 == kAsyncBK * BM, "chunk split");
+// tokens of one channel; 4 columns of one weight row), so no thread stages
+// operands through registers. Chunks past the last token, channel or column
+// are zero-filled by the copy's source size.
+//
+// Two tile widths, 8x8 register blocks either way (16 row groups x TBN / 8
+// column groups of threads):
+//  * TBN 128: 256 threads, 2 CTAs per SM, k-steps of 32 with three in flight;
+//  * TBN 64: 128 threads, 4 CTAs per SM, k-steps of 32 double-buffered. Twice
+//    as many tiles for the same work: the launcher takes it when that spreads
+//    the work more evenly over the SMs (a smaller largest per-SM share).
+template <int TBN>
+struct AsyncTile {
+  static constexpr int NT = 2 * TBN;
+  static constexpr int SK = 32;
+  static constexpr int STAGES = TBN == 128 ? 3 : 2;
+  static constexpr int MIN_BLOCKS = TBN == 128 ? 2 : 4;
+  static constexpr int CSLD = TBN + 4;
+  static constexpr int A_CHUNKS = SK * BM / 4 / NT;   // 16-byte chunks per thread per stage
+  static constexpr int B_CHUNKS = SK * TBN / 4 / NT;
+  static constexpr int STAGE_BYTES = STAGES * SK * (BM + TBN) * 4;
+  static constexpr int EPI_BYTES = BM * CSLD * 4 + 5 * BM * 8;
+  static constexpr int SMEM = STAGE_BYTES > EPI_BYTES ? STAGE_BYTES : EPI_BYTES;
+  static_assert(A_CHUNKS * NT * 4 == SK * BM && B_CHUNKS * NT * 4 == SK * TBN, "chunk split");
+};
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src, int src_bytes) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -304,16 +323,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams p) {
+template <int TBN>
+__global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS)
+    simt_gemm_async_kernel(const SimtParams p) {
+  using Cfg = AsyncTile<TBN>;
+  constexpr int SK = Cfg::SK, STAGES = Cfg::STAGES, NTH = Cfg::NT, CSLD = Cfg::CSLD;
+  constexpr int HALF = TBN / 2;  // a thread's second column group starts here
   const float* X = static_cast<const float*>(p.x);
   const float* Wt = static_cast<const float*>(p.W);
   extern __shared__ __align__(16) float smem[];
-  constexpr int SK = kAsyncBK;
-  float* As = smem;                             // [stage][SK][BM]
-  float* Bs = smem + kAsyncStages * SK * BM;    // [stage][SK][BN]
+  float* As = smem;                       // [stage][SK][BM]
+  float* Bs = smem + STAGES * SK * BM;    // [stage][SK][TBN]
 
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
+  const int tx = tid % (TBN / 8), ty = tid / (TBN / 8);
   const int64_t tile = blockIdx.x;
   const int n_tile = static_cast<int>(tile % p.num_n_tiles);
   const int64_t m_tile = tile / p.num_n_tiles;
@@ -323,27 +346,35 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams
   const TokenMap& tk = p.tok;
   const int C = p.C, N = p.epi.N;
 
-  // This thread's chunks of each operand per stage: chunk c = tid + 256 j
-  // covers row k = c / 32 = ck + 8 j of the stage and elements 4 (c % 32) .. + 3.
-  const int ck = tid >> 5, ce = (tid & 31) * 4;
-  const int64_t rows_left = tk.S_in - s0 - ce;
+  // This thread's chunks per stage. A: chunk c = tid + NTH j covers k-row
+  // c / 32 (= ak + (NTH / 32) j) and tokens 4 (c % 32) .. + 3. B likewise with
+  // TBN / 4 chunks per k-row.
+  constexpr int A_ROW_CH = BM / 4, B_ROW_CH = TBN / 4;
+  constexpr int A_DK = NTH / A_ROW_CH, B_DK = NTH / B_ROW_CH;  // k-rows between a thread's chunks
+  const int ak = tid / A_ROW_CH, ae = (tid % A_ROW_CH) * 4;
+  const int bk = tid / B_ROW_CH, be = (tid % B_ROW_CH) * 4;
+  const int64_t rows_left = tk.S_in - s0 - ae;
   const int a_bytes = rows_left >= 4 ? 16 : rows_left > 0 ? static_cast<int>(rows_left) * 4 : 0;
-  const int b_bytes = n0 + ce < N ? 16 : 0;  // N is a multiple of 4
-  const float* a_src = X + outer_offset(tk, o) + s0 + ce + static_cast<int64_t>(ck) * tk.c_stride;
-  const float* b_src = Wt + static_cast<int64_t>(ck) * N + n0 + ce;
-  const int64_t a_k8 = 8 * tk.c_stride;  // next chunk: 8 channels further
+  const int b_bytes = n0 + be < N ? 16 : 0;  // N is a multiple of 4
+  const float* a_src = X + outer_offset(tk, o) + s0 + ae + static_cast<int64_t>(ak) * tk.c_stride;
+  const float* b_src = Wt + static_cast<int64_t>(bk) * N + n0 + be;
   auto issue = [&](int kb) {
-    const int st = kb % kAsyncStages;
-    float* a = As + st * SK * BM + ck * BM + ce;
-    float* b = Bs + st * SK * BN + ck * BN + ce;
-    const int k = kb * SK + ck;
-    const int64_t ka = static_cast<int64_t>(kb) * SK * tk.c_stride;
-    const int64_t kw = static_cast<int64_t>(kb) * SK * N;
+    const int st = kb % STAGES;
+    float* a = As + st * SK * BM + ak * BM + ae;
+    float* b = Bs + st * SK * TBN + bk * TBN + be;
+    const int k0 = kb * SK;
+    const int64_t ka = static_cast<int64_t>(k0) * tk.c_stride;
+    const int64_t kw = static_cast<int64_t>(k0) * N;
 #pragma unroll
-    for (int j = 0; j < kAsyncChunks; ++j) {
-      const bool in = k + 8 * j < C;
-      cp_async16(a + j * 8 * BM, in ? a_src + ka + j * a_k8 : X, in ? a_bytes : 0);
-      cp_async16(b + j * 8 * BN, in ? b_src + kw + static_cast<int64_t>(j) * 8 * N : Wt,
+    for (int j = 0; j < Cfg::A_CHUNKS; ++j) {
+      const bool in = k0 + ak + A_DK * j < C;
+      cp_async16(a + j * A_DK * BM, in ? a_src + ka + static_cast<int64_t>(j) * A_DK * tk.c_stride : X,
+                 in ? a_bytes : 0);
+    }
+#pragma unroll
+    for (int j = 0; j < Cfg::B_CHUNKS; ++j) {
+      const bool in = k0 + bk + B_DK * j < C;
+      cp_async16(b + j * B_DK * TBN, in ? b_src + kw + static_cast<int64_t>(j) * B_DK * N : Wt,
                  in ? b_bytes : 0);
     }
   };
@@ -356,35 +387,35 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams
 
   const int num_k = (C + SK - 1) / SK;
 #pragma unroll
-  for (int s = 0; s < kAsyncStages - 1; ++s) {
+  for (int s = 0; s < STAGES - 1; ++s) {
     if (s < num_k) issue(s);
     cp_async_commit();
   }
   for (int kb = 0; kb < num_k; ++kb) {
     // this thread's copies of step kb have landed; the barrier publishes every
     // thread's and retires step kb - 1, whose stage the next issue refills
-    cp_async_wait<kAsyncStages - 2>();
+    cp_async_wait<STAGES - 2>();
     __syncthreads();
-    if (kb + kAsyncStages - 1 < num_k) issue(kb + kAsyncStages - 1);
+    if (kb + STAGES - 1 < num_k) issue(kb + STAGES - 1);
     cp_async_commit();
-    const int st = kb % kAsyncStages;
+    const int st = kb % STAGES;
     const float* a = As + st * SK * BM;
-    const float* b = Bs + st * SK * BN;
+    const float* b = Bs + st * SK * TBN;
     // fragments double-buffered in registers: step kk + 1's loads are issued
     // before step kk's FMAs
     float4 fa[2][2], fb[2][2];
     fa[0][0] = *reinterpret_cast<const float4*>(a + ty * 4);
     fa[0][1] = *reinterpret_cast<const float4*>(a + 64 + ty * 4);
     fb[0][0] = *reinterpret_cast<const float4*>(b + tx * 4);
-    fb[0][1] = *reinterpret_cast<const float4*>(b + 64 + tx * 4);
+    fb[0][1] = *reinterpret_cast<const float4*>(b + HALF + tx * 4);
 #pragma unroll
     for (int kk = 0; kk < SK; ++kk) {
       const int cur = kk & 1, nxt = cur ^ 1;
       if (kk + 1 < SK) {
         fa[nxt][0] = *reinterpret_cast<const float4*>(a + (kk + 1) * BM + ty * 4);
         fa[nxt][1] = *reinterpret_cast<const float4*>(a + (kk + 1) * BM + 64 + ty * 4);
-        fb[nxt][0] = *reinterpret_cast<const float4*>(b + (kk + 1) * BN + tx * 4);
-        fb[nxt][1] = *reinterpret_cast<const float4*>(b + (kk + 1) * BN + 64 + tx * 4);
+        fb[nxt][0] = *reinterpret_cast<const float4*>(b + (kk + 1) * TBN + tx * 4);
+        fb[nxt][1] = *reinterpret_cast<const float4*>(b + (kk + 1) * TBN + HALF + tx * 4);
       }
       const float4 a0 = fa[cur][0], a1 = fa[cur][1], b0 = fb[cur][0], b1 = fb[cur][1];
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -398,32 +429,32 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams
       }
     }
   }
-  cp_async_wait<0>();  // only empty groups remain; the epilogue tile overlays the stages
+  cp_async_wait<0>();  // only empty groups remain; the epilogue overlays the stages
   __syncthreads();
 
   const Epilogue& e = p.epi;
   if (e.rope_half == 0 && !e.k_transposed && (e.heads == 0 || e.hd % 4 == 0)) {
     // No rotation pairs and no transposed k: each thread stores its own 8 x 8
     // block from registers, 4 consecutive columns (one head, F and hd being
-    // multiples of 4) per 16-byte store; a warp's store covers 2 rows x 64
-    // columns. Per-row output bases come from shared memory, once per tile.
+    // multiples of 4) per 16-byte store. Per-row output bases come from shared
+    // memory, once per tile.
     int64_t* row_ff = reinterpret_cast<int64_t*>(smem);  // [BM]
     int64_t* row_q = row_ff + BM;
     int64_t* row_kv = row_q + BM;
     const int nkv = e.groups > 0 ? e.groups : e.heads;
-    if (tid < BM) {
-      const int64_t m = o * tk.S_in + s0 + tid;
+    for (int r = tid; r < BM; r += NTH) {
+      const int64_t m = o * tk.S_in + s0 + r;
       const int64_t bb = m / e.T, t = m - bb * e.T;
-      row_ff[tid] = m * e.F;
-      row_q[tid] = (bb * e.heads * e.T + t) * e.hd;
-      row_kv[tid] = (bb * nkv * e.T + t) * e.hd;
+      row_ff[r] = m * e.F;
+      row_q[r] = (bb * e.heads * e.T + t) * e.hd;
+      row_kv[r] = (bb * nkv * e.T + t) * e.hd;
     }
     __syncthreads();
     const float* bias = static_cast<const float*>(e.bias);
     const int64_t tile_rows = tk.S_in - s0;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
-      const int c0 = h2 * 64 + tx * 4;
+      const int c0 = h2 * HALF + tx * 4;
       const int n = n0 + c0;
       if (c0 >= e.bn_eff || n >= N) continue;
       const ColInfo ci = decode_col(e, n);
@@ -456,19 +487,19 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_async_kernel(const SimtParams
     return;
   }
 
-  float* Cs = smem;  // [BM][CS_LD]
+  float* Cs = smem;  // [BM][CSLD]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
     float c[8];
 #pragma unroll
     for (int t = 0; t < 4; ++t) f2_unpack(acc2[i][t], c[2 * t], c[2 * t + 1]);
-    *reinterpret_cast<float4*>(Cs + r * CS_LD + tx * 4) = make_float4(c[0], c[1], c[2], c[3]);
-    *reinterpret_cast<float4*>(Cs + r * CS_LD + 64 + tx * 4) = make_float4(c[4], c[5], c[6], c[7]);
+    *reinterpret_cast<float4*>(Cs + r * CSLD + tx * 4) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(Cs + r * CSLD + HALF + tx * 4) = make_float4(c[4], c[5], c[6], c[7]);
   }
   __syncthreads();
 
-  simt_epilogue<float>(p, Cs, o, s0, n0);
+  simt_epilogue<float, TBN>(p, Cs, o, s0, n0);
 }
 
 // The cp.async kernel's preconditions: fp32 storage, unit-stride tokens, and
@@ -486,19 +517,47 @@ bool async_ok(const SimtParams& p) {
   return true;
 }
 
-cudaError_t launch_async(const SimtParams& p, int64_t tiles, cudaStream_t stream) {
+template <int TBN>
+cudaError_t launch_async_tiles(const SimtParams& p, int dev, cudaStream_t stream) {
   static int attr_done[64] = {0};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_done[dev]) {
-    err = cudaFuncSetAttribute(simt_gemm_async_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kAsyncSmem);
+    cudaError_t err = cudaFuncSetAttribute(simt_gemm_async_kernel<TBN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           AsyncTile<TBN>::SMEM);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
-  simt_gemm_async_kernel<<<static_cast<unsigned>(tiles), NT, kAsyncSmem, stream>>>(p);
+  const int64_t tiles = p.num_m_tiles * p.num_n_tiles;
+  simt_gemm_async_kernel<TBN>
+      <<<static_cast<unsigned>(tiles), AsyncTile<TBN>::NT, AsyncTile<TBN>::SMEM, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Tile width: 64 columns when that lowers the largest per-SM share of the work
+// (in 128 x 128 tile units, with tiles dealt evenly over the SMs), else 128.
+// Narrow tiles need an N-tile of whole heads under rotation (head_dim <= 64).
+cudaError_t launch_async(const SimtParams& p, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const Epilogue& e = p.epi;
+  const int half = e.rope_half > 0;
+  const int bn_narrow = half ? (64 / e.hd) * e.hd : 64;
+  if (bn_narrow > 0 && bn_narrow % 4 == 0 && sms > 0) {
+    const int64_t n_narrow = (e.N + bn_narrow - 1) / bn_narrow;
+    const int64_t wide = p.num_m_tiles * p.num_n_tiles, narrow = p.num_m_tiles * n_narrow;
+    const int64_t share_wide = 2 * ((wide + sms - 1) / sms);  // in half-tile units
+    const int64_t share_narrow = (narrow + sms - 1) / sms;
+    if (share_narrow < share_wide) {
+      SimtParams q = p;
+      q.epi.bn_eff = bn_narrow;
+      q.num_n_tiles = static_cast<int>(n_narrow);
+      return launch_async_tiles<64>(q, dev, stream);
+    }
+  }
+  return launch_async_tiles<128>(p, dev, stream);
 }
 
 template <typename T, bool K_MAJOR>
@@ -523,7 +582,7 @@ cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream
   int64_t tiles = p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const bool k_major = p.tok.c_stride == 1;
-  if (!bf16 && !k_major && async_ok(p)) return launch_async(p, tiles, stream);
+  if (!bf16 && !k_major && async_ok(p)) return launch_async(p, stream);
   if (bf16)
     return k_major ? launch_one<uint16_t, true>(p, tiles, stream)
                    : launch_one<uint16_t, false>(p, tiles, stream);

@@ -115,7 +115,8 @@ def test_fp32_channels_first_copy_paths(cuda_ok):
     10 tokens at a stride of 12 (the last chunk of each row is half a chunk),
     rows at a stride of 11 (channel stride 66), and N = 90 (head_dim 10).
     Tiles without rotation or transposed k store from registers; the others
-    stage the tile in shared memory."""
+    stage the tile in shared memory. Small problems take 64-column tiles (4
+    CTAs per SM), two larger ones 128-column tiles."""
     w = next(s for s in SMALL if s.name == "fp32_rope_silu")  # x [2, 24, 6, 10], N 108
     inp = fpsynth.make_inputs(w)
     ref = oracle.forward_workload(w, inp)
@@ -140,7 +141,13 @@ def test_fp32_channels_first_copy_paths(cuda_ok):
                W_("fp32_gelu_heads", (2, 48, 9, 15), 1, 1, 48, 96, 3, 16, A.ACT_GELU_ERF, 0.0,
                   True, "f32", 79),
                W_("fp32_gqa", (2, 64, 10, 10), 1, 1, 64, 0, 4, 16, A.ACT_NONE, 0.0, True, "f32",
-                  80, n_query_groups=2)):
+                  80, n_query_groups=2),
+               # on 152 SMs these two keep 128-column tiles (narrower ones would not
+               # lower the largest per-SM share): register stores, then rotation
+               W_("fp32_wide_tiles", (2, 320, 32, 32), 1, 1, 320, 0, 5, 64, A.ACT_NONE, 0.0,
+                  True, "f32", 82),
+               W_("fp32_wide_rope", (2, 128, 34, 64), 1, 1, 128, 0, 2, 64, A.ACT_NONE, 10000.0,
+                  True, "f32", 83)):
         inp2 = fpsynth.make_inputs(w2)
         ref2 = oracle.forward_workload(w2, inp2)
         out2 = run(w2, inp2)
