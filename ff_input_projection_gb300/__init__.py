@@ -38,7 +38,7 @@ FP_OPT_BOUNDS_CHECK = 6
 FP_OPT_TILE_N = 7
 
 # the C ABI's entry points, as declared in include/fp.h
-EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_rope_table",
+EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_host", "fp_forward_rope_table",
            "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward", "fp_attention",
            "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
@@ -92,6 +92,8 @@ def load():
     lib.fp_create_ex.restype = I
     lib.fp_forward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
     lib.fp_forward.restype = I
+    lib.fp_forward_host.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P]
+    lib.fp_forward_host.restype = I
     lib.fp_forward_rope_table.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P,
                                           ctypes.POINTER(fp_rope_table), P, P, P, P, P]
     lib.fp_forward_rope_table.restype = I
@@ -154,6 +156,14 @@ def fp_forward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int], p
                out_v: Optional[int], stream: Optional[int]) -> int:
     return load().fp_forward(plan, x, ctypes.byref(layout), W, b, pos, out_ff, out_q, out_k, out_v,
                              stream)
+
+
+def fp_forward_host(plan: int, x_host: int, layout: fp_layout, W: int, b: Optional[int],
+                    pos: Optional[int], out_ff: Optional[int], out_q: Optional[int],
+                    out_k: Optional[int], out_v: Optional[int], stream: Optional[int]) -> int:
+    """fp_forward on page-locked host x and outputs (copies pipelined in the library)."""
+    return load().fp_forward_host(plan, x_host, ctypes.byref(layout), W, b, pos, out_ff, out_q,
+                                  out_k, out_v, stream)
 
 
 def fp_forward_rope_table(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
@@ -352,6 +362,53 @@ class FusedProjection:
         else:
             st = fp_forward(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
                             ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
+        check(st)
+        return out
+
+    def forward_host(self, x, W, b=None, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
+                     out=None, stream=None, device=None):
+        """The projection of a page-locked host x into page-locked host outputs
+        (allocated here when out is None); W, b and pos live on the GPU. The
+        library moves x and the outputs through device staging in chunks,
+        overlapping the copies with the compute. Returns (ff, q, k, v) host
+        tensors, complete once `stream` reaches the end of the call's work."""
+        import torch
+        if x.device.type != "cpu" or not x.is_pinned():
+            raise ValueError("x must be a page-locked (pinned) CPU tensor")
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
+        dev = W.device if device is None else torch.device(device)
+        dt = FP_BF16 if x.dtype == torch.bfloat16 else FP_F32
+        Bb, T = self.out_shapes(x.shape, channel_dim, n_batch_dims)
+        M = Bb * T
+        if tuple(W.shape) != (self.C, self.N) or not W.is_contiguous() or W.dtype != x.dtype \
+                or W.device.type != "cuda":
+            raise ValueError(f"W must be a contiguous [{self.C}, {self.N}] {x.dtype} CUDA tensor")
+        if b is not None and (tuple(b.shape) != (self.N,) or not b.is_contiguous()
+                              or b.dtype != x.dtype or b.device != W.device):
+            raise ValueError(f"b must be a contiguous [{self.N}] {x.dtype} tensor on W's device")
+        if pos is not None and (tuple(pos.shape) != (T,) or pos.dtype != torch.int32
+                                or not pos.is_contiguous() or pos.device != W.device):
+            raise ValueError(f"pos must be a contiguous int32 [{T}] tensor on W's device")
+        want = [(M, self.F) if self.F else None] + \
+               [self._head_shape(Bb, nh, T, kt) if self.heads else None
+                for nh, kt in ((self.heads, False), (self.kv_heads, self.k_transposed),
+                               (self.kv_heads, False))]
+        if out is None:
+            out = tuple(None if shp is None else torch.empty(shp, dtype=x.dtype, pin_memory=True)
+                        for shp in want)
+        for o, shp in zip(out, want):
+            if (o is None) != (shp is None) or (o is not None and (
+                    tuple(o.shape) != shp or not o.is_contiguous() or o.dtype != x.dtype
+                    or o.device.type != "cpu" or not o.is_pinned())):
+                raise ValueError(f"output buffers must be contiguous pinned CPU tensors {want}")
+        L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, dt)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        if stream is None:
+            stream = torch.cuda.current_stream(dev).cuda_stream
+        with torch.cuda.device(dev):
+            st = fp_forward_host(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
+                                 ptr(out[0]), ptr(out[1]), ptr(out[2]), ptr(out[3]), stream)
         check(st)
         return out
 

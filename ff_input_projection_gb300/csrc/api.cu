@@ -56,6 +56,16 @@ struct fp_plan {
   cudaEvent_t scratch_ready;
   bool scratch_pending;
   std::vector<void*> retired;
+  // fp_forward_host: device staging for two chunks in flight, the upload and
+  // download streams, and per-slot events (upload done, compute done,
+  // download done) plus the fork event recorded on the caller's stream
+  void* d_host_stage = nullptr;
+  int64_t host_stage_cap = 0;  // bytes
+  cudaStream_t up_stream = nullptr, down_stream = nullptr;
+  cudaEvent_t ev_host_fork = nullptr;
+  cudaEvent_t ev_up[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr},
+              ev_down[2] = {nullptr, nullptr};
+  int host_last = 0;  // slot of the previous host call's last download
 };
 
 namespace {
@@ -768,7 +778,7 @@ fp_status fp_create(fp_plan** plan, int C, int ff_hidden, int heads, int head_di
 
 void fp_destroy(fp_plan* plan) {
   if (!plan) return;
-  if (plan->d_status || plan->d_table || plan->d_attn) {
+  if (plan->d_status || plan->d_table || plan->d_attn || plan->d_host_stage || plan->up_stream) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (plan->device >= 0) cudaSetDevice(plan->device);
@@ -777,8 +787,14 @@ void fp_destroy(fp_plan* plan) {
     if (plan->d_status) cudaFreeAsync(plan->d_status, nullptr);
     if (plan->d_table) cudaFreeAsync(plan->d_table, nullptr);
     if (plan->d_attn) cudaFreeAsync(plan->d_attn, nullptr);
+    if (plan->d_host_stage) cudaFreeAsync(plan->d_host_stage, nullptr);
     for (void* q : plan->retired) cudaFreeAsync(q, nullptr);
     cudaStreamSynchronize(nullptr);
+    for (cudaEvent_t e : {plan->ev_host_fork, plan->ev_up[0], plan->ev_up[1], plan->ev_comp[0],
+                          plan->ev_comp[1], plan->ev_down[0], plan->ev_down[1]})
+      if (e) cudaEventDestroy(e);
+    if (plan->up_stream) cudaStreamDestroy(plan->up_stream);
+    if (plan->down_stream) cudaStreamDestroy(plan->down_stream);
     if (plan->table_ready) cudaEventDestroy(plan->table_ready);
     if (plan->scratch_ready) cudaEventDestroy(plan->scratch_ready);
     if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
@@ -903,6 +919,177 @@ fp_status fp_forward(fp_plan* p, const void* x, const fp_layout* xl, const void*
     p->table_stream = stream;
     p->table_T = pos ? -1 : pr.ta.T;
   }
+  p->last_launches = launches;
+  return ok();
+}
+
+namespace {
+
+// A host pointer the copy engines can reach asynchronously: page-locked host
+// memory (cudaHostAlloc or cudaHostRegister).
+bool page_locked(const void* q) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+    cudaGetLastError();  // an unregistered pointer is an answer, not an error
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+constexpr int kHostChunks = 4;
+constexpr int64_t kStageAlign = 256;
+
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, const void* W,
+                          const void* b, const int32_t* pos, void* ff_h, void* q_h, void* k_h,
+                          void* v_h, void* stream_v) {
+  const NvtxRange range("fp_forward_host");
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (!xl) return fail(FP_ERR_INVALID_ARG, "x_layout is NULL");
+  // shapes, strides and outputs exactly as fp_forward sees them
+  {
+    const Args full{x_host, xl, W, b, pos, ff_h, q_h, k_h, v_h};
+    Prepared pr;
+    const fp_status st = prepare(*p, full, pr);
+    if (st != FP_OK) return st;
+    if (pr.ta.M == 0) {
+      p->last_launches = 0;
+      return ok();
+    }
+  }
+  void* const outs_h[4] = {ff_h, q_h, k_h, v_h};
+  if (!page_locked(x_host)) return fail(FP_ERR_INVALID_ARG, "x_host is not page-locked host memory");
+  for (void* q : outs_h)
+    if (q && !page_locked(q))
+      return fail(FP_ERR_INVALID_ARG, "output buffers must be page-locked host memory");
+  const fp_layout L = *xl;
+  const int64_t esz = L.dtype == FP_BF16 ? 2 : 4;
+  const TokAxes ta = analyse_tokens(L);
+  // dense row-major x: every axis of size > 1 has the stride of the axes inside it
+  bool dense = true;
+  int64_t numel = 1;
+  for (int d = L.ndim - 1; d >= 0; --d) {
+    if (L.sizes[d] > 1 && L.strides[d] != numel) dense = false;
+    numel *= L.sizes[d];
+  }
+  const bool chunked = dense && L.channel_dim != 0 && L.n_batch_dims >= 1 && L.sizes[0] > 1;
+  const int64_t span = chunked ? L.sizes[0] : 1;  // units along axis 0
+  const int64_t per_chunk = (span + kHostChunks - 1) / kHostChunks;
+  const int n_chunks = static_cast<int>((span + per_chunk - 1) / per_chunk);
+  // elements of x and of each output per unit of axis 0 (the whole call when not chunked)
+  const int nkv = p->groups > 0 ? p->groups : p->heads;
+  const int64_t m_unit = ta.M / span;
+  int64_t x_unit = 0;
+  if (chunked) {
+    x_unit = numel / span;
+  } else {
+    x_unit = 1;  // span of the strided x, in elements
+    for (int d = 0; d < L.ndim; ++d) x_unit += (L.sizes[d] - 1) * L.strides[d];
+  }
+  const int64_t out_unit[4] = {m_unit * p->F, m_unit * p->heads * p->hd, m_unit * nkv * p->hd,
+                               m_unit * nkv * p->hd};
+  // one staging slot: x, then ff, q, k, v, each 256-byte aligned
+  int64_t off[5], slot = 0;
+  off[0] = 0;
+  slot = align_up(per_chunk * x_unit * esz, kStageAlign);
+  for (int i = 0; i < 4; ++i) {
+    off[i + 1] = slot;
+    slot += outs_h[i] ? align_up(per_chunk * out_unit[i] * esz, kStageAlign) : 0;
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  if (p->d_status && p->device != dev)
+    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
+                p->device, dev);
+  if (!p->up_stream) {
+    if (cudaStreamCreateWithFlags(&p->up_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->down_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "copy stream creation failed");
+    for (cudaEvent_t* e : {&p->ev_host_fork, &p->ev_up[0], &p->ev_up[1], &p->ev_comp[0],
+                           &p->ev_comp[1], &p->ev_down[0], &p->ev_down[1]})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "event creation failed");
+  }
+  if (2 * slot > p->host_stage_cap) {
+    void* q = nullptr;
+    if (cudaMallocAsync(&q, static_cast<size_t>(2 * slot), stream) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "host-call staging allocation (%lld bytes) failed",
+                  static_cast<long long>(2 * slot));
+    if (p->d_host_stage) p->retired.push_back(p->d_host_stage);  // queued copies may use it
+    p->d_host_stage = q;
+    p->host_stage_cap = 2 * slot;
+  }
+  unsigned char* const stage = static_cast<unsigned char*>(p->d_host_stage);
+  auto chunk_layout = [&](int64_t units) {
+    fp_layout c = L;
+    if (chunked) c.sizes[0] = units;
+    return c;
+  };
+  auto dev_out = [&](int s, int i) -> void* {
+    return outs_h[i] ? stage + s * slot + off[i + 1] : nullptr;
+  };
+  // every fp_forward check, on the first chunk's staging pointers, before any copy
+  {
+    const fp_layout c0 = chunk_layout(std::min<int64_t>(per_chunk, span));
+    const Args a0{stage, &c0, W, b, pos, dev_out(0, 0), dev_out(0, 1), dev_out(0, 2),
+                  dev_out(0, 3)};
+    Prepared pr;
+    const fp_status st = prepare(*p, a0, pr);
+    if (st != FP_OK) return st;
+  }
+  // calls on one plan run one after another, whichever streams they are on:
+  // this call starts after the previous call's last download (which follows
+  // all of that call's uploads and compute)
+  if (wait_event(stream, p->ev_down[p->host_last]) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "stream wait on the previous host call failed");
+  if (cudaEventRecord(p->ev_host_fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(p->up_stream, p->ev_host_fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->down_stream, p->ev_host_fork, 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "forking the copy streams failed");
+  const unsigned char* const xh = static_cast<const unsigned char*>(x_host);
+  int launches = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int s = c & 1;
+    const int64_t u0 = c * per_chunk, units = std::min(per_chunk, span - u0);
+    // upload: slot s's x is free once chunk c - 2 has been computed
+    if (c >= 2 && cudaStreamWaitEvent(p->up_stream, p->ev_comp[s], 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "upload stream wait failed");
+    if (cudaMemcpyAsync(stage + s * slot, xh + u0 * x_unit * esz,
+                        static_cast<size_t>(units * x_unit * esz), cudaMemcpyHostToDevice,
+                        p->up_stream) != cudaSuccess ||
+        cudaEventRecord(p->ev_up[s], p->up_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "upload of chunk %d failed", c);
+    // compute: after the upload, and once chunk c - 2's outputs have left slot s
+    if (cudaStreamWaitEvent(stream, p->ev_up[s], 0) != cudaSuccess ||
+        (c >= 2 && cudaStreamWaitEvent(stream, p->ev_down[s], 0) != cudaSuccess))
+      return fail(FP_ERR_CUDA, "compute stream wait failed");
+    const fp_layout cl = chunk_layout(units);
+    const fp_status st = fp_forward(p, stage + s * slot, &cl, W, b, pos, dev_out(s, 0),
+                                    dev_out(s, 1), dev_out(s, 2), dev_out(s, 3), stream);
+    if (st != FP_OK) return st;
+    launches += p->last_launches;
+    if (cudaEventRecord(p->ev_comp[s], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(p->down_stream, p->ev_comp[s], 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "compute event failed");
+    // download
+    for (int i = 0; i < 4; ++i) {
+      if (!outs_h[i]) continue;
+      unsigned char* dst = static_cast<unsigned char*>(outs_h[i]) + u0 * out_unit[i] * esz;
+      if (cudaMemcpyAsync(dst, dev_out(s, i), static_cast<size_t>(units * out_unit[i] * esz),
+                          cudaMemcpyDeviceToHost, p->down_stream) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "download of chunk %d failed", c);
+    }
+    if (cudaEventRecord(p->ev_down[s], p->down_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "download event failed");
+  }
+  // the download stream runs in order: its last event covers every chunk
+  p->host_last = (n_chunks - 1) & 1;
+  if (cudaStreamWaitEvent(stream, p->ev_down[p->host_last], 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "joining the download stream failed");
   p->last_launches = launches;
   return ok();
 }

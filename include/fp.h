@@ -29,6 +29,8 @@
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers on the current CUDA device, owned
  *    by the caller; the library keeps no reference after a call returns.
+ *    fp_forward_host is the one exception: its x and outputs are page-locked
+ *    host memory.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). fp_forward only enqueues work: it never synchronises.
  *  - Argument checks run on the host before any launch; a rejected call
@@ -174,6 +176,41 @@ fp_status fp_create_ex(fp_plan** plan, const fp_config* config);
 fp_status fp_forward(fp_plan* plan, const void* x, const fp_layout* x_layout, const void* W,
                      const void* b, const int32_t* pos, void* out_ff, void* out_q, void* out_k,
                      void* out_v, void* stream);
+
+/*
+ * fp_forward_host — fp_forward for an activation and outputs in host memory.
+ * It is the same projection, with the host <-> device copies pipelined against
+ * the compute.
+ *   x_host                 host pointer to x, page-locked (cudaHostAlloc or
+ *                          cudaHostRegister), layout `x_layout`
+ *   W, b, pos              device pointers, as fp_forward
+ *   out_*_host             page-locked host pointers, shapes as fp_forward's
+ *                          outputs (NULL where fp_forward takes NULL)
+ * When x is dense (row-major strides over its sizes) and its first axis is a
+ * batch axis (channel_dim != 0, n_batch_dims >= 1), the call splits that axis
+ * into up to 4 chunks. Each chunk is a contiguous range of x and of every
+ * output. For chunk c: its x bytes are uploaded on the plan's upload stream,
+ * projected on `stream` by fp_forward into device staging, and its outputs
+ * downloaded on the plan's download stream. Two staging slots alternate, so
+ * chunk c + 1's upload and compute overlap chunk c's download. Otherwise the
+ * whole call is one chunk.
+ * Staging (two chunks of x and of every output) is plan-owned device memory. It
+ * is grown in stream order on `stream` (cudaMallocAsync) and freed by fp_reserve
+ * or fp_destroy. Both side streams are forked from `stream` by an event, and
+ * `stream` waits for the last download, so the work completes in `stream`
+ * order. The host buffers must stay valid and unmodified until then. Host
+ * calls on one plan run one after another: each starts after the previous
+ * one's last download, whatever streams they are on. Inside a stream capture
+ * only after a first call has sized the staging.
+ * Errors: FP_ERR_INVALID_ARG for host buffers that are not page-locked host
+ * memory, and every error of fp_forward (checked on the first chunk's staging
+ * pointers before any copy is enqueued). Rotary positions: as fp_forward; with
+ * caller positions the table is rebuilt per chunk. Returns FP_OK once the work
+ * is enqueued; fp_last_launch_count counts the kernels of every chunk.
+ */
+fp_status fp_forward_host(fp_plan* plan, const void* x_host, const fp_layout* x_layout,
+                          const void* W, const void* b, const int32_t* pos, void* out_ff_host,
+                          void* out_q_host, void* out_k_host, void* out_v_host, void* stream);
 
 /*
  * fp_forward_rope_table — fp_forward with caller-given rotary tables instead
