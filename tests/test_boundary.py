@@ -101,6 +101,30 @@ def test_forward_rejects_on_host(lib):
     fpx.fp_destroy(h)
 
 
+def test_forward_host_rejects_on_host(lib):
+    """The host-buffer entry point runs fp_forward's argument checks on the
+    caller's pointers first, and takes only page-locked host memory: plain
+    addresses (here, with no GPU, nothing is page-locked) are refused before
+    any copy or launch."""
+    h = _plan()
+    L = _cf_layout()
+    host = lambda **kw: fpx.fp_forward_host(h, kw.get("x", X), kw.get("L", L), WP, BP, None,
+                                            kw.get("ff", O1), O2, O3, O4, None)
+    assert fpx.fp_forward_host(None, X, L, WP, BP, None, O1, O2, O3, O4, None) == \
+        fpx.FP_ERR_INVALID_ARG
+    assert host(x=None) == fpx.FP_ERR_INVALID_ARG
+    assert host(ff=None) == fpx.FP_ERR_INVALID_ARG     # F > 0 needs out_ff
+    assert host(x=X + 2) == fpx.FP_ERR_MISALIGNED
+    assert host(ff=X) == fpx.FP_ERR_INVALID_ARG        # output aliases input
+    assert host(L=_cf_layout(C=32)) == fpx.FP_ERR_INVALID_ARG
+    assert host() == fpx.FP_ERR_INVALID_ARG            # not page-locked host memory
+    assert "page-locked" in fpx.fp_last_error()
+    E = fpx.make_layout([0, 64, 8, 8], [4096, 64, 8, 1], 1, 1, fpx.FP_BF16)
+    assert host(L=E) == fpx.FP_OK                      # no tokens: nothing to copy
+    assert fpx.fp_last_launch_count(h) == 0
+    fpx.fp_destroy(h)
+
+
 @pytest.mark.parametrize("kw", [
     dict(n_query_groups=3),                 # heads % groups
     dict(rope_n_elem=5),                    # odd
