@@ -732,7 +732,8 @@ def main_backward(args, rank, world, local):
     value = flops * world / (ms * 1e-3) / 1e12
     proj, stream, dx, ws = run.proj, run.stream, run.dx, run.ws
 
-    # end to end: upstream gradients and x from pinned host memory, dx, dW, db back
+    # end to end: upstream gradients and x from pinned host memory, dx, dW, db
+    # back, one fp_backward_host call per step (copies pipelined in chunks)
     x0, W0, b0, g0 = run.sets[0]
     hx = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True)
     hx.copy_(x0.cpu())
@@ -740,8 +741,6 @@ def main_backward(args, rank, world, local):
     for h, g in zip(hg, g0):
         if h is not None:
             h.copy_(g.cpu())
-    dxx = torch.empty_like(x0)
-    dg = [None if g is None else torch.empty_like(g) for g in g0]
     hdx = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True)
     hdW = torch.empty((w.C, w.N), dtype=torch.float32, pin_memory=True)
     hdb = torch.empty((w.N,), dtype=torch.float32, pin_memory=True) if w.bias else None
@@ -750,17 +749,9 @@ def main_backward(args, rank, world, local):
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        dxx.copy_(hx, non_blocking=True)
-        for d, h in zip(dg, hg):
-            if d is not None:
-                d.copy_(h, non_blocking=True)
-        ddx, ddW, ddb = proj.backward(dxx, W0, b0, tuple(dg), None, channel_dim=w.channel_dim,
-                                      n_batch_dims=w.n_batch_dims, dx=dx, workspace=ws,
-                                      stream=stream.cuda_stream)
-        hdx.copy_(ddx, non_blocking=True)
-        hdW.copy_(ddW, non_blocking=True)
-        if hdb is not None:
-            hdb.copy_(ddb, non_blocking=True)
+        proj.backward_host(hx, W0, b0, tuple(hg), None, channel_dim=w.channel_dim,
+                           n_batch_dims=w.n_batch_dims, out=(hdx, hdW, hdb),
+                           stream=stream.cuda_stream)
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -799,7 +790,8 @@ def main_backward(args, rank, world, local):
         "roofline": roof,
         "clocks": run.clocks,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "call": "fp_backward_host"},
     }
     if not args.no_cpu_baseline and world == 1:
         import oracle

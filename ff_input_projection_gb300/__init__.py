@@ -39,7 +39,8 @@ FP_OPT_TILE_N = 7
 
 # the C ABI's entry points, as declared in include/fp.h
 EXPORTS = ("fp_create", "fp_create_ex", "fp_forward", "fp_forward_host", "fp_forward_rope_table",
-           "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward", "fp_attention",
+           "fp_forward_noalloc", "fp_backward_workspace_size", "fp_backward", "fp_backward_host",
+           "fp_attention",
            "fp_reserve", "fp_get_device_status",
            "fp_last_launch_count", "fp_status_string", "fp_last_error", "fp_set_option",
            "fp_destroy")
@@ -106,6 +107,9 @@ def load():
     lib.fp_backward.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P, P, P, P,
                                 ctypes.c_size_t, P]
     lib.fp_backward.restype = I
+    lib.fp_backward_host.argtypes = [P, P, ctypes.POINTER(fp_layout), P, P, P, P, P, P, P, P, P,
+                                     P, P]
+    lib.fp_backward_host.restype = I
     lib.fp_attention.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, P]
     lib.fp_attention.restype = I
     lib.fp_reserve.argtypes = [P, I64]
@@ -194,6 +198,15 @@ def fp_backward(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
                 workspace_bytes: int, stream: Optional[int]) -> int:
     return load().fp_backward(plan, x, ctypes.byref(layout), W, b, pos, g_ff, g_q, g_k, g_v, dx,
                               dW, db, workspace, workspace_bytes, stream)
+
+
+def fp_backward_host(plan: int, x: int, layout: fp_layout, W: int, b: Optional[int],
+                     pos: Optional[int], g_ff: Optional[int], g_q: Optional[int],
+                     g_k: Optional[int], g_v: Optional[int], dx: int, dW: int,
+                     db: Optional[int], stream: Optional[int]) -> int:
+    """fp_backward on page-locked host x, gradients and results (copies pipelined)."""
+    return load().fp_backward_host(plan, x, ctypes.byref(layout), W, b, pos, g_ff, g_q, g_k, g_v,
+                                   dx, dW, db, stream)
 
 
 def fp_attention(plan: int, q: int, k: int, v: int, out: int, batch: int, T_q: int, T_k: int,
@@ -486,5 +499,58 @@ class FusedProjection:
                           ptr(grads[1]), ptr(grads[2]), ptr(grads[3]), dx.data_ptr(), dW.data_ptr(),
                           ptr(db), workspace.data_ptr(),
                           workspace.numel() * workspace.element_size(), stream))
+        return dx, dW, db
+
+    def backward_host(self, x, W, b, grads, pos=None, *, channel_dim: int, n_batch_dims: int = 1,
+                      out=None, stream=None):
+        """``backward`` on a page-locked host x and host gradients: returns host
+        ``(dx, dW, db)`` (page-locked; allocated here when out is None). W, b and
+        pos live on the GPU; x must be dense. The library moves the data in batch
+        chunks, overlapping the copies with the compute."""
+        import torch
+        if x.device.type != "cpu" or not x.is_pinned() or not x.is_contiguous():
+            raise ValueError("x must be a contiguous page-locked (pinned) CPU tensor")
+        if x.dtype != torch.bfloat16:
+            raise TypeError("the backward takes bfloat16 activations")
+        Bb, T = self.out_shapes(x.shape, channel_dim, n_batch_dims)
+        M = Bb * T
+        if tuple(W.shape) != (self.C, self.N) or not W.is_contiguous() or W.dtype != x.dtype \
+                or W.device.type != "cuda":
+            raise ValueError(f"W must be a contiguous [{self.C}, {self.N}] {x.dtype} CUDA tensor")
+        if b is not None and (tuple(b.shape) != (self.N,) or not b.is_contiguous()
+                              or b.dtype != x.dtype or b.device != W.device):
+            raise ValueError(f"b must be a contiguous [{self.N}] {x.dtype} tensor on W's device")
+        if pos is not None and (tuple(pos.shape) != (T,) or pos.dtype != torch.int32
+                                or not pos.is_contiguous() or pos.device != W.device):
+            raise ValueError(f"pos must be a contiguous int32 [{T}] tensor on W's device")
+        want = [(M, self.F) if self.F else None] + \
+               [self._head_shape(Bb, nh, T, kt) if self.heads else None
+                for nh, kt in ((self.heads, False), (self.kv_heads, self.k_transposed),
+                               (self.kv_heads, False))]
+        grads = tuple(grads)
+        for g, shp in zip(grads, want):
+            if (g is None) != (shp is None) or (g is not None and (
+                    tuple(g.shape) != shp or not g.is_contiguous() or g.dtype != x.dtype
+                    or g.device.type != "cpu" or not g.is_pinned())):
+                raise ValueError(f"gradients must be contiguous pinned CPU tensors {want}")
+        if out is None:
+            out = (torch.empty_like(x).pin_memory(),
+                   torch.empty((self.C, self.N), dtype=torch.float32).pin_memory(),
+                   torch.empty((self.N,), dtype=torch.float32).pin_memory()
+                   if b is not None else None)
+        dx, dW, db = out
+        for t, shp, dt in ((dx, tuple(x.shape), x.dtype), (dW, (self.C, self.N), torch.float32),
+                           (db, (self.N,), torch.float32)):
+            if t is not None and (tuple(t.shape) != shp or t.dtype != dt or not t.is_contiguous()
+                                  or t.device.type != "cpu" or not t.is_pinned()):
+                raise ValueError("dx, dW and db must be contiguous pinned CPU tensors")
+        L = make_layout(x.shape, x.stride(), channel_dim, n_batch_dims, FP_BF16)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        if stream is None:
+            stream = torch.cuda.current_stream(W.device).cuda_stream
+        with torch.cuda.device(W.device):
+            check(fp_backward_host(self.plan, x.data_ptr(), L, W.data_ptr(), ptr(b), ptr(pos),
+                                   ptr(grads[0]), ptr(grads[1]), ptr(grads[2]), ptr(grads[3]),
+                                   dx.data_ptr(), dW.data_ptr(), ptr(db), stream))
         return dx, dW, db
 

@@ -1234,10 +1234,14 @@ fp_status fp_backward_workspace_size(const fp_plan* p, const fp_layout* x_layout
   return ok();
 }
 
-fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
-                      const int32_t* pos, const void* g_ff, const void* g_q, const void* g_k,
-                      const void* g_v, void* dx, float* dW, float* db, void* workspace,
-                      size_t workspace_bytes, void* stream_v) {
+// fp_backward's body. `accumulate`: add this call's dW and db into the
+// buffers instead of overwriting them (the host entry point's later chunks);
+// the kernels add into dW and db in either case, so only the clearing differs.
+static fp_status backward_impl(fp_plan* p, const void* x, const fp_layout* xl, const void* W,
+                               const void* b, const int32_t* pos, const void* g_ff,
+                               const void* g_q, const void* g_k, const void* g_v, void* dx,
+                               float* dW, float* db, void* workspace, size_t workspace_bytes,
+                               void* stream_v, bool accumulate) {
   const NvtxRange range("fp_backward");
   if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
   // the upstream gradients have the forward outputs' shapes: reuse its checks
@@ -1263,8 +1267,9 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
   if (M == 0) {
     // no tokens: the gradients of W and b are zero, dx is empty
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    if (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
-        (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess))
+    if (!accumulate &&
+        (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
+         (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess)))
       return fail(FP_ERR_CUDA, "clearing dW / db failed");
     p->last_launches = 0;
     return ok();
@@ -1295,8 +1300,9 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
     p->table_stream = stream;
     p->table_T = pos ? -1 : pr.ta.T;
   }
-  if (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
-      (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess))
+  if (!accumulate &&
+      (cudaMemsetAsync(dW, 0, static_cast<size_t>(C) * N * sizeof(float), stream) != cudaSuccess ||
+       (db && cudaMemsetAsync(db, 0, static_cast<size_t>(N) * sizeof(float), stream) != cudaSuccess)))
     return fail(FP_ERR_CUDA, "clearing dW / db failed");
 
   p->launch_seq = p->launch_seq % 0x7FFFFFFEu + 1u;
@@ -1564,6 +1570,175 @@ fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void
 }
 
 // ---------------------------------------------------------------- attention over the outputs
+
+fp_status fp_backward(fp_plan* p, const void* x, const fp_layout* xl, const void* W, const void* b,
+                      const int32_t* pos, const void* g_ff, const void* g_q, const void* g_k,
+                      const void* g_v, void* dx, float* dW, float* db, void* workspace,
+                      size_t workspace_bytes, void* stream_v) {
+  return backward_impl(p, x, xl, W, b, pos, g_ff, g_q, g_k, g_v, dx, dW, db, workspace,
+                       workspace_bytes, stream_v, false);
+}
+
+fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, const void* W,
+                           const void* b, const int32_t* pos, const void* gff_h,
+                           const void* gq_h, const void* gk_h, const void* gv_h, void* dx_h,
+                           float* dW_h, float* db_h, void* stream_v) {
+  const NvtxRange range("fp_backward_host");
+  if (!p) return fail(FP_ERR_INVALID_ARG, "plan is NULL");
+  if (!xl) return fail(FP_ERR_INVALID_ARG, "x_layout is NULL");
+  const void* const g_h[4] = {gff_h, gq_h, gk_h, gv_h};
+  {
+    // the forward's checks on x and the gradients (they have the outputs' shapes)
+    const Args full{x_host, xl, W, b, pos, const_cast<void*>(gff_h), const_cast<void*>(gq_h),
+                    const_cast<void*>(gk_h), const_cast<void*>(gv_h)};
+    Prepared pr;
+    const fp_status st = prepare(*p, full, pr);
+    if (st != FP_OK) return st;
+    if (xl->dtype != FP_BF16)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT, "the backward takes bf16 activations");
+    if (pr.ta.M > 0 && !pr.tc_path)
+      return fail(FP_ERR_UNSUPPORTED_LAYOUT,
+                  "the backward runs on the tensor-core path only (bf16, head_dim and ff_hidden "
+                  "multiples of 16, x addressable by TMA)");
+  }
+  if (!dW_h || !dx_h) return fail(FP_ERR_INVALID_ARG, "dx and dW are required");
+  const fp_layout L = *xl;
+  bool dense = true;
+  int64_t numel = 1;
+  for (int d = L.ndim - 1; d >= 0; --d) {
+    if (L.sizes[d] > 1 && L.strides[d] != numel) dense = false;
+    numel *= L.sizes[d];
+  }
+  // dx comes back as whole byte ranges: a strided x's gaps would be overwritten
+  if (!dense)
+    return fail(FP_ERR_UNSUPPORTED_LAYOUT, "fp_backward_host needs a dense (row-major) x");
+  const void* const host_ptrs[] = {x_host, gff_h, gq_h, gk_h, gv_h, dx_h, dW_h, db_h};
+  for (const void* q : host_ptrs)
+    if (q && !page_locked(q))
+      return fail(FP_ERR_INVALID_ARG, "host buffers must be page-locked host memory");
+  const int64_t esz = 2;
+  const TokAxes ta = analyse_tokens(L);
+  const int N = n_total(p), C = p->C;
+  const bool chunked = L.channel_dim != 0 && L.n_batch_dims >= 1 && L.sizes[0] > 1;
+  const int64_t span = chunked ? L.sizes[0] : 1;
+  const int64_t per_chunk = (span + kHostChunks - 1) / kHostChunks;
+  const int n_chunks = static_cast<int>((span + per_chunk - 1) / per_chunk);
+  const int nkv = p->groups > 0 ? p->groups : p->heads;
+  const int64_t m_unit = ta.M / span, x_unit = numel / span;
+  const int64_t g_unit[4] = {m_unit * p->F, m_unit * p->heads * p->hd, m_unit * nkv * p->hd,
+                             m_unit * nkv * p->hd};
+  // one slot: x, g_ff, g_q, g_k, g_v, dx; then, shared by the slots, the G
+  // workspace of one chunk, dW and db
+  int64_t off[6], slot = 0;
+  off[0] = 0;
+  slot = align_up(per_chunk * x_unit * esz, kStageAlign);
+  for (int i = 0; i < 4; ++i) {
+    off[i + 1] = slot;
+    slot += g_h[i] ? align_up(per_chunk * g_unit[i] * esz, kStageAlign) : 0;
+  }
+  off[5] = slot;
+  slot += align_up(per_chunk * x_unit * esz, kStageAlign);
+  const int64_t ws_bytes =
+      align_up(static_cast<int64_t>(backward_workspace_bytes(per_chunk * m_unit, N)), kStageAlign);
+  const int64_t dw_bytes = align_up(static_cast<int64_t>(C) * N * 4, kStageAlign);
+  const int64_t db_bytes = align_up(static_cast<int64_t>(N) * 4, kStageAlign);
+  const int64_t total = 2 * slot + ws_bytes + dw_bytes + db_bytes;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  if (p->d_status && p->device != dev)
+    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
+                p->device, dev);
+  if (!p->up_stream) {
+    if (cudaStreamCreateWithFlags(&p->up_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->down_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "copy stream creation failed");
+    for (cudaEvent_t* e : {&p->ev_host_fork, &p->ev_up[0], &p->ev_up[1], &p->ev_comp[0],
+                           &p->ev_comp[1], &p->ev_down[0], &p->ev_down[1]})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "event creation failed");
+  }
+  if (total > p->host_stage_cap) {
+    void* q = nullptr;
+    if (cudaMallocAsync(&q, static_cast<size_t>(total), stream) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "host-call staging allocation (%lld bytes) failed",
+                  static_cast<long long>(total));
+    if (p->d_host_stage) p->retired.push_back(p->d_host_stage);
+    p->d_host_stage = q;
+    p->host_stage_cap = total;
+  }
+  unsigned char* const stage = static_cast<unsigned char*>(p->d_host_stage);
+  void* const ws = stage + 2 * slot;
+  float* const dW = reinterpret_cast<float*>(stage + 2 * slot + ws_bytes);
+  float* const db = db_h ? reinterpret_cast<float*>(stage + 2 * slot + ws_bytes + dw_bytes) : nullptr;
+  auto chunk_layout = [&](int64_t units) {
+    fp_layout c = L;
+    if (chunked) c.sizes[0] = units;
+    return c;
+  };
+  auto dev_g = [&](int s, int i) -> const void* {
+    return g_h[i] ? stage + s * slot + off[i + 1] : nullptr;
+  };
+  if (wait_event(stream, p->ev_down[p->host_last]) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "stream wait on the previous host call failed");
+  if (cudaEventRecord(p->ev_host_fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(p->up_stream, p->ev_host_fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->down_stream, p->ev_host_fork, 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "forking the copy streams failed");
+  int launches = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int s = c & 1;
+    const int64_t u0 = c * per_chunk, units = std::min(per_chunk, span - u0);
+    // upload x and the four gradients; slot s is free once chunk c - 2 is computed
+    if (c >= 2 && cudaStreamWaitEvent(p->up_stream, p->ev_comp[s], 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "upload stream wait failed");
+    if (cudaMemcpyAsync(stage + s * slot, static_cast<const unsigned char*>(x_host) + u0 * x_unit * esz,
+                        static_cast<size_t>(units * x_unit * esz), cudaMemcpyHostToDevice,
+                        p->up_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "upload of chunk %d failed", c);
+    for (int i = 0; i < 4; ++i) {
+      if (!g_h[i]) continue;
+      if (cudaMemcpyAsync(const_cast<void*>(dev_g(s, i)),
+                          static_cast<const unsigned char*>(g_h[i]) + u0 * g_unit[i] * esz,
+                          static_cast<size_t>(units * g_unit[i] * esz), cudaMemcpyHostToDevice,
+                          p->up_stream) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "upload of chunk %d failed", c);
+    }
+    if (cudaEventRecord(p->ev_up[s], p->up_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "upload event failed");
+    // gradients of the chunk; dW and db summed over the chunks
+    if (cudaStreamWaitEvent(stream, p->ev_up[s], 0) != cudaSuccess ||
+        (c >= 2 && cudaStreamWaitEvent(stream, p->ev_down[s], 0) != cudaSuccess))
+      return fail(FP_ERR_CUDA, "compute stream wait failed");
+    const fp_layout cl = chunk_layout(units);
+    const fp_status st = backward_impl(p, stage + s * slot, &cl, W, b, pos, dev_g(s, 0),
+                                       dev_g(s, 1), dev_g(s, 2), dev_g(s, 3),
+                                       stage + s * slot + off[5], dW, db, ws,
+                                       static_cast<size_t>(ws_bytes), stream, c > 0);
+    if (st != FP_OK) return st;
+    launches += p->last_launches;
+    if (cudaEventRecord(p->ev_comp[s], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(p->down_stream, p->ev_comp[s], 0) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "compute event failed");
+    if (cudaMemcpyAsync(static_cast<unsigned char*>(dx_h) + u0 * x_unit * esz,
+                        stage + s * slot + off[5], static_cast<size_t>(units * x_unit * esz),
+                        cudaMemcpyDeviceToHost, p->down_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "download of chunk %d failed", c);
+    if (c == n_chunks - 1 &&
+        (cudaMemcpyAsync(dW_h, dW, static_cast<size_t>(C) * N * 4, cudaMemcpyDeviceToHost,
+                         p->down_stream) != cudaSuccess ||
+         (db_h && cudaMemcpyAsync(db_h, db, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
+                                  p->down_stream) != cudaSuccess)))
+      return fail(FP_ERR_CUDA, "download of dW / db failed");
+    if (cudaEventRecord(p->ev_down[s], p->down_stream) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "download event failed");
+  }
+  p->host_last = (n_chunks - 1) & 1;
+  if (cudaStreamWaitEvent(stream, p->ev_down[p->host_last], 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "joining the download stream failed");
+  p->last_launches = launches;
+  return ok();
+}
 
 extern "C" fp_status fp_attention(fp_plan* p, const void* q, const void* k, const void* v,
                                   void* out, int64_t batch, int64_t T_q, int64_t T_k, float scale,

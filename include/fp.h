@@ -29,8 +29,8 @@
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers on the current CUDA device, owned
  *    by the caller; the library keeps no reference after a call returns.
- *    fp_forward_host is the one exception: its x and outputs are page-locked
- *    host memory.
+ *    fp_forward_host and fp_backward_host are the exceptions: their
+ *    activation, gradient and result buffers are page-locked host memory.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). fp_forward only enqueues work: it never synchronises.
  *  - Argument checks run on the host before any launch; a rejected call
@@ -284,6 +284,36 @@ fp_status fp_backward(fp_plan* plan, const void* x, const fp_layout* x_layout, c
                       const void* b, const int32_t* pos, const void* g_ff, const void* g_q,
                       const void* g_k, const void* g_v, void* dx, float* dW, float* db,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fp_backward_host — fp_backward for an activation, upstream gradients and
+ * results in host memory, with the copies pipelined against the compute as in
+ * fp_forward_host.
+ *   x_host, g_*_host   page-locked host memory, layouts as fp_backward's x and
+ *                      gradients (NULL exactly where fp_backward takes NULL)
+ *   dx_host            page-locked host memory laid out like x
+ *   dW_host, db_host   page-locked host float32 [C, N] and [N] (db_host NULL to
+ *                      skip), overwritten
+ *   W, b, pos          device pointers, as fp_backward
+ * x must be dense (row-major strides over its sizes): dx comes back as whole
+ * byte ranges. When the first axis is a batch axis (channel_dim != 0,
+ * n_batch_dims >= 1) it is split into up to 4 chunks. For each chunk, x and
+ * the gradients are uploaded on the plan's upload stream. The chunk's
+ * gradients are computed on `stream`: dW and db are summed into plan-owned
+ * device accumulators, cleared by the first chunk. dx is downloaded on the
+ * plan's download stream, and dW and db after the last chunk. The staging,
+ * the G workspace and the accumulators are plan-owned device memory, grown
+ * and ordered as for fp_forward_host (shared with it). Errors: those of
+ * fp_backward, FP_ERR_UNSUPPORTED_LAYOUT for a strided x, and
+ * FP_ERR_INVALID_ARG for host buffers that are not page-locked. All are
+ * checked before anything is enqueued. dW and db are sums whose order varies
+ * between runs, as fp_backward's. Returns FP_OK once the work is enqueued.
+ */
+fp_status fp_backward_host(fp_plan* plan, const void* x_host, const fp_layout* x_layout,
+                           const void* W, const void* b, const int32_t* pos,
+                           const void* g_ff_host, const void* g_q_host, const void* g_k_host,
+                           const void* g_v_host, void* dx_host, float* dW_host, float* db_host,
+                           void* stream);
 
 /*
  * fp_forward_noalloc — fp_forward for callers that may not allocate device

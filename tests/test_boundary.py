@@ -125,6 +125,29 @@ def test_forward_host_rejects_on_host(lib):
     fpx.fp_destroy(h)
 
 
+def test_backward_host_rejects_on_host(lib):
+    """fp_backward_host: fp_backward's checks first, then a dense x and
+    page-locked host memory, all before anything is enqueued."""
+    h = _plan()
+    L = _cf_layout()
+    G = (O1, O2, O3, O4)
+    DX, DW, DB = 0x30000000, 0x31000000, 0x32000000
+    bh = lambda **kw: fpx.fp_backward_host(h, kw.get("x", X), kw.get("L", L), WP, BP, None,
+                                           *kw.get("g", G), kw.get("dx", DX), kw.get("dW", DW),
+                                           DB, None)
+    assert fpx.fp_backward_host(None, X, L, WP, BP, None, *G, DX, DW, DB, None) == \
+        fpx.FP_ERR_INVALID_ARG
+    assert bh(x=None) == fpx.FP_ERR_INVALID_ARG
+    assert bh(g=(None, O2, O3, O4)) == fpx.FP_ERR_INVALID_ARG   # F > 0 needs g_ff
+    assert bh(dW=None) == fpx.FP_ERR_INVALID_ARG
+    assert bh(L=_cf_layout(dtype=fpx.FP_F32)) == fpx.FP_ERR_UNSUPPORTED_LAYOUT
+    padded = fpx.make_layout([2, 64, 8, 8], [64 * 80, 80, 8, 1], 1, 1, fpx.FP_BF16)
+    assert bh(L=padded) == fpx.FP_ERR_UNSUPPORTED_LAYOUT        # not dense
+    assert bh() == fpx.FP_ERR_INVALID_ARG                       # not page-locked
+    assert "page-locked" in fpx.fp_last_error()
+    fpx.fp_destroy(h)
+
+
 @pytest.mark.parametrize("kw", [
     dict(n_query_groups=3),                 # heads % groups
     dict(rope_n_elem=5),                    # odd

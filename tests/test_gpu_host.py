@@ -150,3 +150,72 @@ def test_host_entry_rejects_pageable_memory(cuda_ok):
     assert st == fpx.FP_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         proj.forward_host(x, W, b, None, channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims)
+
+
+BWD_CASES = [
+    # channels-first, 2 chunks (dxᵀ kernel), GELU ff + rotated heads
+    W_("bwd_host_walrus_small", (2, 3, 64, 16, 16, 1), 2, 1, 64, 128, 2, 32, A.ACT_GELU_ERF,
+       10000.0, True, "bf16", 96),
+    # token-major, 5 batch elements in chunks of 2, 2 and 1 (dx kernel), no ff block
+    W_("bwd_host_uneven", (5, 77, 192), 2, 1, 192, 0, 3, 64, A.ACT_NONE, 0.0, True, "bf16", 97),
+]
+
+
+@pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: w.name)
+def test_backward_host_matches_oracle_and_device_path(w, cuda_ok):
+    """dx, dW and db of the host entry point against the oracle; dx bit for bit
+    against fp_backward (each chunk computes its rows exactly as the whole call
+    does); dW and db, summed over the chunks in another order, within the f32
+    rule of fp_backward's."""
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+    ref = oracle.backward_workload(w, inp, grads)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    W = to_device(inp["W"], w.dtype)
+    b = to_device(inp["b"], w.dtype)
+    hg = tuple(None if grads[k] is None else pinned(grads[k], w.dtype)
+               for k in ("ff", "q", "k", "v"))
+    dx, dW, db = proj.backward_host(pinned(inp["x"], w.dtype), W, b, hg,
+                                    channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK
+    assert dx.device.type == "cpu" and dW.device.type == "cpu"
+    ddx, ddW, ddb = proj.backward(to_device(inp["x"], w.dtype), W, b,
+                                  tuple(None if g is None else g.cuda() for g in hg),
+                                  channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, ddx.cpu()), "dx differs from fp_backward"
+    perm = [a for a in range(dx.dim()) if a != w.channel_dim] + [w.channel_dim]
+    assert_close(host(dx.permute(*perm).reshape(-1, w.C)), ref["dx"], "bf16", f"{w.name}:dx")
+    assert_close(dW.double().numpy(), ref["dW"], "bf16", f"{w.name}:dW")
+    assert_close(dW.double().numpy(), ddW.double().cpu().numpy(), "f32", f"{w.name}:dW vs device")
+    assert_close(db.double().numpy(), ref["db"], "f32", f"{w.name}:db")
+    assert_close(db.double().numpy(), ddb.double().cpu().numpy(), "f32", f"{w.name}:db vs device")
+
+
+def test_backward_host_rejects(cuda_ok):
+    """A strided x (dx would overwrite its gaps) and pageable gradients."""
+    w = BWD_CASES[0]
+    inp = fpsynth.make_inputs(w)
+    grads = fpsynth.make_grads(w)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    W = to_device(inp["W"], w.dtype)
+    b = to_device(inp["b"], w.dtype)
+    hg = [pinned(grads[k], w.dtype) for k in ("ff", "q", "k", "v")]
+    x = pinned(inp["x"], w.dtype)
+    dx = torch.empty_like(x).pin_memory()
+    dW = torch.empty((w.C, w.N), dtype=torch.float32).pin_memory()
+    db = torch.empty((w.N,), dtype=torch.float32).pin_memory()
+    big = torch.zeros((2, 4, 64, 16, 16, 1), dtype=x.dtype).pin_memory()
+    big[:, :3] = x
+    xs = big[:, :3]
+    Ls = fpx.make_layout(xs.shape, xs.stride(), w.channel_dim, w.n_batch_dims, fpx.FP_BF16)
+    call = lambda xt, L, gs: fpx.fp_backward_host(
+        proj.plan, xt.data_ptr(), L, W.data_ptr(), b.data_ptr(), None,
+        *[g.data_ptr() for g in gs], dx.data_ptr(), dW.data_ptr(), db.data_ptr(), None)
+    assert call(xs, Ls, hg) == fpx.FP_ERR_UNSUPPORTED_LAYOUT
+    L = fpx.make_layout(x.shape, x.stride(), w.channel_dim, w.n_batch_dims, fpx.FP_BF16)
+    pageable = [hg[0].clone()] + hg[1:]  # clone() of a pinned tensor is pageable
+    assert not pageable[0].is_pinned()
+    assert call(x, L, pageable) == fpx.FP_ERR_INVALID_ARG
+    assert "page-locked" in fpx.fp_last_error()
