@@ -16,10 +16,11 @@
 //  * general (any strides, bf16 or fp32 storage): k-steps of 16,
 //    double-buffered in shared memory with a register prefetch of the next
 //    k-step;
-//  * fp32 with unit-stride tokens and 16-byte-aligned chunks (channels-first
-//    x such as NCHW): k-steps of 32 copied global -> shared by cp.async,
-//    fragments double-buffered in registers; tiles of 128 or 64 columns
-//    (4 CTAs of 128 threads per SM), whichever spreads the work more evenly.
+//  * fp32 with 16-byte-aligned chunks, either unit-stride tokens
+//    (channels-first x such as NCHW) or unit-stride channels (row-major x):
+//    k-steps of 32 copied global -> shared by cp.async; tiles of 128 or 64
+//    columns (4 CTAs of 128 threads per SM), whichever spreads the work more
+//    evenly.
 // The epilogue stages the fp32 tile in shared memory so a rotary pair (lane i,
 // lane i + half) can be read by whichever thread owns either lane, then adds
 // bias, applies the activation or the rotation, and writes ff token-major and
@@ -297,16 +298,22 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(const SimtParams p) {
 //  * TBN 64: 128 threads, 4 CTAs per SM, k-steps of 32 double-buffered. Twice
 //    as many tiles for the same work: the launcher takes it when that spreads
 //    the work more evenly over the SMs (a smaller largest per-SM share).
-template <int TBN>
+// Row-major x with unit-stride channels (AK, K-major A) takes the same loop
+// with A held per token: [BM][SK + 4] (the 4-float pad spreads the rows over
+// the banks), copied as 4 channels of one token per chunk. A thread then owns
+// rows ty + 16 i, and one 8-byte load per row gives two k-steps.
+template <int TBN, bool AK>
 struct AsyncTile {
   static constexpr int NT = 2 * TBN;
   static constexpr int SK = 32;
+  static constexpr int SKP = SK + 4;  // A row stride when K-major
   static constexpr int STAGES = TBN == 128 ? 3 : 2;
   static constexpr int MIN_BLOCKS = TBN == 128 ? 2 : 4;
   static constexpr int CSLD = TBN + 4;
   static constexpr int A_CHUNKS = SK * BM / 4 / NT;   // 16-byte chunks per thread per stage
   static constexpr int B_CHUNKS = SK * TBN / 4 / NT;
-  static constexpr int STAGE_BYTES = STAGES * SK * (BM + TBN) * 4;
+  static constexpr int A_STAGE = AK ? BM * SKP : SK * BM;  // floats
+  static constexpr int STAGE_BYTES = STAGES * (A_STAGE + SK * TBN) * 4;
   static constexpr int EPI_BYTES = BM * CSLD * 4 + 5 * BM * 8;
   static constexpr int SMEM = STAGE_BYTES > EPI_BYTES ? STAGE_BYTES : EPI_BYTES;
   static_assert(A_CHUNKS * NT * 4 == SK * BM && B_CHUNKS * NT * 4 == SK * TBN, "chunk split");
@@ -323,17 +330,18 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int TBN>
-__global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS)
+template <int TBN, bool AK>
+__global__ void __launch_bounds__(AsyncTile<TBN, AK>::NT, AsyncTile<TBN, AK>::MIN_BLOCKS)
     simt_gemm_async_kernel(const SimtParams p) {
-  using Cfg = AsyncTile<TBN>;
+  using Cfg = AsyncTile<TBN, AK>;
   constexpr int SK = Cfg::SK, STAGES = Cfg::STAGES, NTH = Cfg::NT, CSLD = Cfg::CSLD;
   constexpr int HALF = TBN / 2;  // a thread's second column group starts here
   const float* X = static_cast<const float*>(p.x);
   const float* Wt = static_cast<const float*>(p.W);
   extern __shared__ __align__(16) float smem[];
-  float* As = smem;                       // [stage][SK][BM]
-  float* Bs = smem + STAGES * SK * BM;    // [stage][SK][TBN]
+  constexpr int SKP = Cfg::SKP;
+  float* As = smem;                       // [stage][SK][BM], K-major: [stage][BM][SKP]
+  float* Bs = smem + STAGES * Cfg::A_STAGE;  // [stage][SK][TBN]
 
   const int tid = threadIdx.x;
   const int tx = tid % (TBN / 8), ty = tid / (TBN / 8);
@@ -345,6 +353,8 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
   const int n0 = n_tile * p.epi.bn_eff;
   const TokenMap& tk = p.tok;
   const int C = p.C, N = p.epi.N;
+  // accumulator row i of this thread within the tile
+  auto row_of = [&](int i) { return AK ? ty + 16 * i : (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4)); };
 
   // This thread's chunks per stage. A: chunk c = tid + NTH j covers k-row
   // c / 32 (= ak + (NTH / 32) j) and tokens 4 (c % 32) .. + 3. B likewise with
@@ -358,18 +368,39 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
   const int b_bytes = n0 + be < N ? 16 : 0;  // N is a multiple of 4
   const float* a_src = X + outer_offset(tk, o) + s0 + ae + static_cast<int64_t>(ak) * tk.c_stride;
   const float* b_src = Wt + static_cast<int64_t>(bk) * N + n0 + be;
+  // K-major A: chunk c = tid + NTH j covers token row c / (SK / 4) (= kr +
+  // (NTH * 4 / SK) j) and channels 4 (c % (SK / 4)) .. + 3 of the k-step
+  constexpr int K_ROW_CH = SK / 4, K_DR = NTH / K_ROW_CH;
+  const int kr = tid / K_ROW_CH, kq = (tid % K_ROW_CH) * 4;
+  const float* ak_src = X + outer_offset(tk, o) + (s0 + kr) * tk.s_stride + kq;
+  const int64_t ak_step = K_DR * tk.s_stride;     // between a thread's chunks
+  const int64_t ak_rows = tk.S_in - s0 - kr;      // its chunk j exists while K_DR j < ak_rows
   auto issue = [&](int kb) {
     const int st = kb % STAGES;
-    float* a = As + st * SK * BM + ak * BM + ae;
     float* b = Bs + st * SK * TBN + bk * TBN + be;
     const int k0 = kb * SK;
-    const int64_t ka = static_cast<int64_t>(k0) * tk.c_stride;
     const int64_t kw = static_cast<int64_t>(k0) * N;
+    if constexpr (AK) {
+      float* a = As + st * Cfg::A_STAGE + kr * SKP + kq;
+      const int k_left = C - k0 - kq;
+      const int kbytes = k_left >= 4 ? 16 : k_left > 0 ? 4 * k_left : 0;
+      const float* src = ak_src + k0;
 #pragma unroll
-    for (int j = 0; j < Cfg::A_CHUNKS; ++j) {
-      const bool in = k0 + ak + A_DK * j < C;
-      cp_async16(a + j * A_DK * BM, in ? a_src + ka + static_cast<int64_t>(j) * A_DK * tk.c_stride : X,
-                 in ? a_bytes : 0);
+      for (int j = 0; j < Cfg::A_CHUNKS; ++j) {
+        const bool in = K_DR * j < ak_rows && kbytes > 0;
+        cp_async16(a + j * K_DR * SKP, in ? src : X, in ? kbytes : 0);
+        src += ak_step;
+      }
+    } else {
+      float* a = As + st * SK * BM + ak * BM + ae;
+      const int64_t ka = static_cast<int64_t>(k0) * tk.c_stride;
+#pragma unroll
+      for (int j = 0; j < Cfg::A_CHUNKS; ++j) {
+        const bool in = k0 + ak + A_DK * j < C;
+        cp_async16(a + j * A_DK * BM,
+                   in ? a_src + ka + static_cast<int64_t>(j) * A_DK * tk.c_stride : X,
+                   in ? a_bytes : 0);
+      }
     }
 #pragma unroll
     for (int j = 0; j < Cfg::B_CHUNKS; ++j) {
@@ -399,8 +430,32 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
     if (kb + STAGES - 1 < num_k) issue(kb + STAGES - 1);
     cp_async_commit();
     const int st = kb % STAGES;
-    const float* a = As + st * SK * BM;
+    const float* a = As + st * Cfg::A_STAGE;
     const float* b = Bs + st * SK * TBN;
+    if constexpr (AK) {
+      // two k-steps per pass: one 8-byte load per owned row, B for both steps
+#pragma unroll 2
+      for (int kk = 0; kk < SK; kk += 2) {
+        float2 a2[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          a2[i] = *reinterpret_cast<const float2*>(a + row_of(i) * SKP + kk);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float4 b0 = *reinterpret_cast<const float4*>(b + (kk + h) * TBN + tx * 4);
+          const float4 b1 = *reinterpret_cast<const float4*>(b + (kk + h) * TBN + HALF + tx * 4);
+          const uint64_t bv2[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                                   f2_pack(b1.z, b1.w)};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint64_t ai = f2_splat(h ? a2[i].y : a2[i].x);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) acc2[i][t] = f2_fma(ai, bv2[t], acc2[i][t]);
+          }
+        }
+      }
+      continue;
+    }
     // fragments double-buffered in registers: step kk + 1's loads are issued
     // before step kk's FMAs
     float4 fa[2][2], fb[2][2];
@@ -465,7 +520,7 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
       const int64_t* const rb = ci.seg == 0 ? row_ff : ci.seg == 1 ? row_q : row_kv;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+        const int r = row_of(i);
         if (r >= tile_rows) continue;
         float4 v;
         f2_unpack(acc2[i][2 * h2], v.x, v.y);
@@ -490,7 +545,7 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
   float* Cs = smem;  // [BM][CSLD]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+    const int r = row_of(i);
     float c[8];
 #pragma unroll
     for (int t = 0; t < 4; ++t) f2_unpack(acc2[i][t], c[2 * t], c[2 * t + 1]);
@@ -502,40 +557,43 @@ __global__ void __launch_bounds__(AsyncTile<TBN>::NT, AsyncTile<TBN>::MIN_BLOCKS
   simt_epilogue<float, TBN>(p, Cs, o, s0, n0);
 }
 
-// The cp.async kernel's preconditions: fp32 storage, unit-stride tokens, and
-// every chunk 16-byte aligned (x and W 16-byte aligned; the channel stride,
-// every outer stride and N multiples of 4 elements; tiles start at multiples
-// of 128 tokens and columns n0 multiples of 4).
-bool async_ok(const SimtParams& p) {
+// The cp.async kernel's preconditions: fp32 storage and every chunk 16-byte
+// aligned (x and W 16-byte aligned; every outer stride and N multiples of 4
+// elements; tiles start at multiples of 128 tokens and columns n0 multiples
+// of 4), with either unit-stride tokens and a channel stride that is a
+// multiple of 4 (returns 1: MN-major A) or unit-stride channels and a token
+// stride that is a multiple of 4 (returns 2: K-major A); else 0.
+int async_form(const SimtParams& p) {
   const TokenMap& tk = p.tok;
-  if (tk.s_stride != 1 || tk.c_stride % 4 != 0 || p.epi.N % 4 != 0 || p.epi.bn_eff % 4 != 0)
-    return false;
+  if (p.epi.N % 4 != 0 || p.epi.bn_eff % 4 != 0) return 0;
   if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0 || reinterpret_cast<uintptr_t>(p.W) % 16 != 0)
-    return false;
+    return 0;
   for (int d = 0; d < tk.n_outer_dims; ++d)
-    if (tk.outer_stride[d] % 4 != 0) return false;
-  return true;
+    if (tk.outer_stride[d] % 4 != 0) return 0;
+  if (tk.s_stride == 1 && tk.c_stride % 4 == 0) return 1;
+  if (tk.c_stride == 1 && tk.s_stride % 4 == 0) return 2;
+  return 0;
 }
 
-template <int TBN>
+template <int TBN, bool AK>
 cudaError_t launch_async_tiles(const SimtParams& p, int dev, cudaStream_t stream) {
+  using Cfg = AsyncTile<TBN, AK>;
   static int attr_done[64] = {0};
   if (dev >= 64 || !attr_done[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(simt_gemm_async_kernel<TBN>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           AsyncTile<TBN>::SMEM);
+    cudaError_t err = cudaFuncSetAttribute(simt_gemm_async_kernel<TBN, AK>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_done[dev] = 1;
   }
   const int64_t tiles = p.num_m_tiles * p.num_n_tiles;
-  simt_gemm_async_kernel<TBN>
-      <<<static_cast<unsigned>(tiles), AsyncTile<TBN>::NT, AsyncTile<TBN>::SMEM, stream>>>(p);
+  simt_gemm_async_kernel<TBN, AK><<<static_cast<unsigned>(tiles), Cfg::NT, Cfg::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
 // Tile width: 64 columns when that lowers the largest per-SM share of the work
 // (in 128 x 128 tile units, with tiles dealt evenly over the SMs), else 128.
 // Narrow tiles need an N-tile of whole heads under rotation (head_dim <= 64).
+template <bool AK>
 cudaError_t launch_async(const SimtParams& p, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -554,10 +612,10 @@ cudaError_t launch_async(const SimtParams& p, cudaStream_t stream) {
       SimtParams q = p;
       q.epi.bn_eff = bn_narrow;
       q.num_n_tiles = static_cast<int>(n_narrow);
-      return launch_async_tiles<64>(q, dev, stream);
+      return launch_async_tiles<64, AK>(q, dev, stream);
     }
   }
-  return launch_async_tiles<128>(p, dev, stream);
+  return launch_async_tiles<128, AK>(p, dev, stream);
 }
 
 template <typename T, bool K_MAJOR>
@@ -582,7 +640,9 @@ cudaError_t launch_simt_gemm(const SimtParams& p, bool bf16, cudaStream_t stream
   int64_t tiles = p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const bool k_major = p.tok.c_stride == 1;
-  if (!bf16 && !k_major && async_ok(p)) return launch_async(p, stream);
+  const int form = bf16 ? 0 : async_form(p);
+  if (form == 1) return launch_async<false>(p, stream);
+  if (form == 2) return launch_async<true>(p, stream);
   if (bf16)
     return k_major ? launch_one<uint16_t, true>(p, tiles, stream)
                    : launch_one<uint16_t, false>(p, tiles, stream);

@@ -158,6 +158,41 @@ def test_fp32_channels_first_copy_paths(cuda_ok):
             assert_close(host(out2[k]), ref2[k], w2.dtype, f"{w2.name}:{k}")
 
 
+def test_fp32_row_major_copy_paths(cuda_ok):
+    """fp32 row-major x (unit-stride channels) goes global -> shared in 16-byte
+    chunks of 4 channels of one token when the token stride and N are
+    multiples of 4 elements, else through registers. Cases: several row and
+    column tiles with rotation, on 64- and on 128-column tiles; rows padded to
+    44 with C = 42 (each token's last chunk holds 2 channels); rows padded to
+    37 (register path)."""
+    cases = [
+        (W_("fp32_km_tiles", (4, 300, 64), 2, 1, 64, 128, 4, 16, A.ACT_SILU, 10000.0, True, "f32",
+            84), None),
+        # 32 row tiles: on 152 SMs 128-column tiles (96 of them) keep the per-SM share
+        (W_("fp32_km_wide", (4, 1000, 64), 2, 1, 64, 128, 4, 16, A.ACT_SILU, 10000.0, True, "f32",
+            87), None),
+        (W_("fp32_km_c42", (2, 30, 42), 2, 1, 42, 14, 3, 14, A.ACT_GELU_ERF, 0.0, True, "f32", 85),
+         44),
+        (W_("fp32_km_odd_stride", (2, 30, 36), 2, 1, 36, 0, 3, 12, A.ACT_NONE, 10000.0, True,
+            "f32", 86), 37),
+    ]
+    for w, row in cases:
+        inp = fpsynth.make_inputs(w)
+        ref = oracle.forward_workload(w, inp)
+        view = None
+        if row is not None:
+            x = to_device(inp["x"], w.dtype)
+            big = torch.zeros(x.shape[:-1] + (row,), dtype=x.dtype, device="cuda")
+            big[..., :w.C] = x
+            view = big[..., :w.C]
+        out = run(w, inp, x_dev=view)
+        for k in ("ff", "q", "k", "v"):
+            if out[k] is None:
+                assert ref[k].size == 0
+                continue
+            assert_close(host(out[k]), ref[k], w.dtype, f"{w.name}:{k}")
+
+
 def test_identity_weight_layout_is_bit_exact(cuda_ok):
     """W = [I | I | I | I], no bias/act/rotation: ff = x and q = k = v = x split
     head-major, exactly, at the full channels-first Walrus shape."""
