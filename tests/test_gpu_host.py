@@ -36,6 +36,10 @@ CASES = [
     # channel axis first: not chunked, one copy of the whole x
     W_("host_channel_first_axis", (64, 2, 50), 0, 1, 64, 64, 2, 32, A.ACT_GELU_TANH, 10000.0,
        True, "bf16", 94),
+    # grouped-query heads, partial rotary and k pre-transposed: 4 chunks whose
+    # k/v ranges follow the group count
+    W_("host_gqa_kt", (4, 130, 256), 2, 1, 256, 0, 8, 32, A.ACT_NONE, 10000.0, False, "bf16", 98,
+       rope_n_elem=8, n_query_groups=2, k_transposed=True),
 ]
 
 
@@ -69,6 +73,22 @@ def test_host_entry_matches_oracle_and_device_path(w, cuda_ok):
         assert out[k].device.type == "cpu"
         assert_close(host(out[k]), ref[k], w.dtype, f"{w.name}:{k}")
         assert torch.equal(out[k], dev[k].cpu()), f"{w.name}:{k} differs from fp_forward"
+
+
+def test_host_entry_caller_positions(cuda_ok):
+    """Caller positions: each chunk rebuilds the rotary table from them."""
+    w = CASES[0]
+    inp = fpsynth.make_inputs(w)
+    pos = ((np.arange(w.T) * 37) % 1000 + 3).astype(np.int32)
+    ref = oracle.forward_workload(w, {**inp, "pos": pos})
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    out = proj.forward_host(pinned(inp["x"], w.dtype), to_device(inp["W"], w.dtype),
+                            to_device(inp["b"], w.dtype), torch.from_numpy(pos).cuda(),
+                            channel_dim=w.channel_dim, n_batch_dims=w.n_batch_dims)
+    torch.cuda.synchronize()
+    assert proj.device_status() == fpx.FP_OK
+    for k, o in zip(("ff", "q", "k", "v"), out):
+        assert_close(host(o), ref[k], w.dtype, f"pos:{k}")
 
 
 def test_host_entry_launch_count(cuda_ok):
@@ -158,6 +178,9 @@ BWD_CASES = [
        10000.0, True, "bf16", 96),
     # token-major, 5 batch elements in chunks of 2, 2 and 1 (dx kernel), no ff block
     W_("bwd_host_uneven", (5, 77, 192), 2, 1, 192, 0, 3, 64, A.ACT_NONE, 0.0, True, "bf16", 97),
+    # grouped-query heads with partial rotary: the gradients' k/v chunks follow the groups
+    W_("bwd_host_gqa", (2, 200, 256), 2, 1, 256, 0, 8, 32, A.ACT_NONE, 10000.0, True, "bf16", 99,
+       rope_n_elem=16, n_query_groups=2),
 ]
 
 
@@ -170,7 +193,8 @@ def test_backward_host_matches_oracle_and_device_path(w, cuda_ok):
     inp = fpsynth.make_inputs(w)
     grads = fpsynth.make_grads(w)
     ref = oracle.backward_workload(w, inp, grads)
-    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base)
+    proj = fpx.FusedProjection(w.C, w.F, w.heads, w.head_dim, w.act, w.rope_base,
+                               w.n_query_groups, w.rope_n_elem, w.k_transposed)
     W = to_device(inp["W"], w.dtype)
     b = to_device(inp["b"], w.dtype)
     hg = tuple(None if grads[k] is None else pinned(grads[k], w.dtype)
