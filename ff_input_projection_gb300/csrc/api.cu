@@ -941,6 +941,83 @@ constexpr int64_t kStageAlign = 256;
 
 int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
+// How a host entry point splits x: along axis 0 when x is dense (row-major
+// strides over its sizes) and axis 0 is a batch axis, in up to kHostChunks
+// chunks of `per_chunk` units; else one chunk of one unit (the whole call).
+struct HostChunks {
+  bool dense, chunked;
+  int64_t numel, span, per_chunk;
+  int n_chunks;
+};
+
+HostChunks host_chunks(const fp_layout& L) {
+  HostChunks h{};
+  h.dense = true;
+  h.numel = 1;
+  for (int d = L.ndim - 1; d >= 0; --d) {
+    if (L.sizes[d] > 1 && L.strides[d] != h.numel) h.dense = false;
+    h.numel *= L.sizes[d];
+  }
+  h.chunked = h.dense && L.channel_dim != 0 && L.n_batch_dims >= 1 && L.sizes[0] > 1;
+  h.span = h.chunked ? L.sizes[0] : 1;
+  h.per_chunk = (h.span + kHostChunks - 1) / kHostChunks;
+  h.n_chunks = static_cast<int>((h.span + h.per_chunk - 1) / h.per_chunk);
+  return h;
+}
+
+// The host entry points' copy streams and events (created on first use) and
+// device staging of at least `bytes` (grown in `stream` order; a replaced
+// buffer may still be read by queued copies, so it is retired).
+fp_status host_pipeline_setup(fp_plan* p, int64_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
+  if (p->d_status && p->device != dev)
+    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
+                p->device, dev);
+  if (!p->up_stream) {
+    if (cudaStreamCreateWithFlags(&p->up_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->down_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(FP_ERR_CUDA, "copy stream creation failed");
+    for (cudaEvent_t* e : {&p->ev_host_fork, &p->ev_up[0], &p->ev_up[1], &p->ev_comp[0],
+                           &p->ev_comp[1], &p->ev_down[0], &p->ev_down[1]})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
+        return fail(FP_ERR_CUDA, "event creation failed");
+  }
+  if (bytes > p->host_stage_cap) {
+    void* q = nullptr;
+    if (cudaMallocAsync(&q, static_cast<size_t>(bytes), stream) != cudaSuccess)
+      return fail(FP_ERR_OUT_OF_MEMORY, "host-call staging allocation (%lld bytes) failed",
+                  static_cast<long long>(bytes));
+    if (p->d_host_stage) p->retired.push_back(p->d_host_stage);
+    p->d_host_stage = q;
+    p->host_stage_cap = bytes;
+  }
+  return FP_OK;
+}
+
+// Host calls on one plan run one after another, whichever streams they are
+// on: the call starts after the previous call's last download (which follows
+// all of that call's uploads and compute), and both copy streams start after
+// `stream`'s work so far.
+fp_status host_pipeline_fork(fp_plan* p, cudaStream_t stream) {
+  if (wait_event(stream, p->ev_down[p->host_last]) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "stream wait on the previous host call failed");
+  if (cudaEventRecord(p->ev_host_fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(p->up_stream, p->ev_host_fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->down_stream, p->ev_host_fork, 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "forking the copy streams failed");
+  return FP_OK;
+}
+
+// `stream` waits for the last download; the download stream runs in order,
+// so its last event covers every chunk.
+fp_status host_pipeline_join(fp_plan* p, int n_chunks, cudaStream_t stream) {
+  p->host_last = (n_chunks - 1) & 1;
+  if (cudaStreamWaitEvent(stream, p->ev_down[p->host_last], 0) != cudaSuccess)
+    return fail(FP_ERR_CUDA, "joining the download stream failed");
+  return FP_OK;
+}
+
 }  // namespace
 
 fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, const void* W,
@@ -968,17 +1045,10 @@ fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, c
   const fp_layout L = *xl;
   const int64_t esz = L.dtype == FP_BF16 ? 2 : 4;
   const TokAxes ta = analyse_tokens(L);
-  // dense row-major x: every axis of size > 1 has the stride of the axes inside it
-  bool dense = true;
-  int64_t numel = 1;
-  for (int d = L.ndim - 1; d >= 0; --d) {
-    if (L.sizes[d] > 1 && L.strides[d] != numel) dense = false;
-    numel *= L.sizes[d];
-  }
-  const bool chunked = dense && L.channel_dim != 0 && L.n_batch_dims >= 1 && L.sizes[0] > 1;
-  const int64_t span = chunked ? L.sizes[0] : 1;  // units along axis 0
-  const int64_t per_chunk = (span + kHostChunks - 1) / kHostChunks;
-  const int n_chunks = static_cast<int>((span + per_chunk - 1) / per_chunk);
+  const HostChunks hc = host_chunks(L);
+  const bool chunked = hc.chunked;
+  const int64_t span = hc.span, per_chunk = hc.per_chunk, numel = hc.numel;
+  const int n_chunks = hc.n_chunks;
   // elements of x and of each output per unit of axis 0 (the whole call when not chunked)
   const int nkv = p->groups > 0 ? p->groups : p->heads;
   const int64_t m_unit = ta.M / span;
@@ -1000,29 +1070,8 @@ fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, c
     slot += outs_h[i] ? align_up(per_chunk * out_unit[i] * esz, kStageAlign) : 0;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
-  if (p->d_status && p->device != dev)
-    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
-                p->device, dev);
-  if (!p->up_stream) {
-    if (cudaStreamCreateWithFlags(&p->up_stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&p->down_stream, cudaStreamNonBlocking) != cudaSuccess)
-      return fail(FP_ERR_CUDA, "copy stream creation failed");
-    for (cudaEvent_t* e : {&p->ev_host_fork, &p->ev_up[0], &p->ev_up[1], &p->ev_comp[0],
-                           &p->ev_comp[1], &p->ev_down[0], &p->ev_down[1]})
-      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
-        return fail(FP_ERR_CUDA, "event creation failed");
-  }
-  if (2 * slot > p->host_stage_cap) {
-    void* q = nullptr;
-    if (cudaMallocAsync(&q, static_cast<size_t>(2 * slot), stream) != cudaSuccess)
-      return fail(FP_ERR_OUT_OF_MEMORY, "host-call staging allocation (%lld bytes) failed",
-                  static_cast<long long>(2 * slot));
-    if (p->d_host_stage) p->retired.push_back(p->d_host_stage);  // queued copies may use it
-    p->d_host_stage = q;
-    p->host_stage_cap = 2 * slot;
-  }
+  fp_status st0 = host_pipeline_setup(p, 2 * slot, stream);
+  if (st0 != FP_OK) return st0;
   unsigned char* const stage = static_cast<unsigned char*>(p->d_host_stage);
   auto chunk_layout = [&](int64_t units) {
     fp_layout c = L;
@@ -1041,15 +1090,8 @@ fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, c
     const fp_status st = prepare(*p, a0, pr);
     if (st != FP_OK) return st;
   }
-  // calls on one plan run one after another, whichever streams they are on:
-  // this call starts after the previous call's last download (which follows
-  // all of that call's uploads and compute)
-  if (wait_event(stream, p->ev_down[p->host_last]) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "stream wait on the previous host call failed");
-  if (cudaEventRecord(p->ev_host_fork, stream) != cudaSuccess ||
-      cudaStreamWaitEvent(p->up_stream, p->ev_host_fork, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->down_stream, p->ev_host_fork, 0) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "forking the copy streams failed");
+  st0 = host_pipeline_fork(p, stream);
+  if (st0 != FP_OK) return st0;
   const unsigned char* const xh = static_cast<const unsigned char*>(x_host);
   int launches = 0;
   for (int c = 0; c < n_chunks; ++c) {
@@ -1086,10 +1128,8 @@ fp_status fp_forward_host(fp_plan* p, const void* x_host, const fp_layout* xl, c
     if (cudaEventRecord(p->ev_down[s], p->down_stream) != cudaSuccess)
       return fail(FP_ERR_CUDA, "download event failed");
   }
-  // the download stream runs in order: its last event covers every chunk
-  p->host_last = (n_chunks - 1) & 1;
-  if (cudaStreamWaitEvent(stream, p->ev_down[p->host_last], 0) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "joining the download stream failed");
+  st0 = host_pipeline_join(p, n_chunks, stream);
+  if (st0 != FP_OK) return st0;
   p->last_launches = launches;
   return ok();
 }
@@ -1603,14 +1643,9 @@ fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, 
   }
   if (!dW_h || !dx_h) return fail(FP_ERR_INVALID_ARG, "dx and dW are required");
   const fp_layout L = *xl;
-  bool dense = true;
-  int64_t numel = 1;
-  for (int d = L.ndim - 1; d >= 0; --d) {
-    if (L.sizes[d] > 1 && L.strides[d] != numel) dense = false;
-    numel *= L.sizes[d];
-  }
+  const HostChunks hc = host_chunks(L);
   // dx comes back as whole byte ranges: a strided x's gaps would be overwritten
-  if (!dense)
+  if (!hc.dense)
     return fail(FP_ERR_UNSUPPORTED_LAYOUT, "fp_backward_host needs a dense (row-major) x");
   const void* const host_ptrs[] = {x_host, gff_h, gq_h, gk_h, gv_h, dx_h, dW_h, db_h};
   for (const void* q : host_ptrs)
@@ -1619,10 +1654,9 @@ fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, 
   const int64_t esz = 2;
   const TokAxes ta = analyse_tokens(L);
   const int N = n_total(p), C = p->C;
-  const bool chunked = L.channel_dim != 0 && L.n_batch_dims >= 1 && L.sizes[0] > 1;
-  const int64_t span = chunked ? L.sizes[0] : 1;
-  const int64_t per_chunk = (span + kHostChunks - 1) / kHostChunks;
-  const int n_chunks = static_cast<int>((span + per_chunk - 1) / per_chunk);
+  const bool chunked = hc.chunked;
+  const int64_t span = hc.span, per_chunk = hc.per_chunk, numel = hc.numel;
+  const int n_chunks = hc.n_chunks;
   const int nkv = p->groups > 0 ? p->groups : p->heads;
   const int64_t m_unit = ta.M / span, x_unit = numel / span;
   const int64_t g_unit[4] = {m_unit * p->F, m_unit * p->heads * p->hd, m_unit * nkv * p->hd,
@@ -1644,29 +1678,8 @@ fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, 
   const int64_t db_bytes = align_up(static_cast<int64_t>(N) * 4, kStageAlign);
   const int64_t total = 2 * slot + ws_bytes + dw_bytes + db_bytes;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP_ERR_CUDA, "cudaGetDevice failed");
-  if (p->d_status && p->device != dev)
-    return fail(FP_ERR_INVALID_ARG, "plan was first used on device %d, now on device %d",
-                p->device, dev);
-  if (!p->up_stream) {
-    if (cudaStreamCreateWithFlags(&p->up_stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&p->down_stream, cudaStreamNonBlocking) != cudaSuccess)
-      return fail(FP_ERR_CUDA, "copy stream creation failed");
-    for (cudaEvent_t* e : {&p->ev_host_fork, &p->ev_up[0], &p->ev_up[1], &p->ev_comp[0],
-                           &p->ev_comp[1], &p->ev_down[0], &p->ev_down[1]})
-      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
-        return fail(FP_ERR_CUDA, "event creation failed");
-  }
-  if (total > p->host_stage_cap) {
-    void* q = nullptr;
-    if (cudaMallocAsync(&q, static_cast<size_t>(total), stream) != cudaSuccess)
-      return fail(FP_ERR_OUT_OF_MEMORY, "host-call staging allocation (%lld bytes) failed",
-                  static_cast<long long>(total));
-    if (p->d_host_stage) p->retired.push_back(p->d_host_stage);
-    p->d_host_stage = q;
-    p->host_stage_cap = total;
-  }
+  fp_status st0 = host_pipeline_setup(p, total, stream);
+  if (st0 != FP_OK) return st0;
   unsigned char* const stage = static_cast<unsigned char*>(p->d_host_stage);
   void* const ws = stage + 2 * slot;
   float* const dW = reinterpret_cast<float*>(stage + 2 * slot + ws_bytes);
@@ -1679,12 +1692,8 @@ fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, 
   auto dev_g = [&](int s, int i) -> const void* {
     return g_h[i] ? stage + s * slot + off[i + 1] : nullptr;
   };
-  if (wait_event(stream, p->ev_down[p->host_last]) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "stream wait on the previous host call failed");
-  if (cudaEventRecord(p->ev_host_fork, stream) != cudaSuccess ||
-      cudaStreamWaitEvent(p->up_stream, p->ev_host_fork, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->down_stream, p->ev_host_fork, 0) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "forking the copy streams failed");
+  st0 = host_pipeline_fork(p, stream);
+  if (st0 != FP_OK) return st0;
   int launches = 0;
   for (int c = 0; c < n_chunks; ++c) {
     const int s = c & 1;
@@ -1733,9 +1742,8 @@ fp_status fp_backward_host(fp_plan* p, const void* x_host, const fp_layout* xl, 
     if (cudaEventRecord(p->ev_down[s], p->down_stream) != cudaSuccess)
       return fail(FP_ERR_CUDA, "download event failed");
   }
-  p->host_last = (n_chunks - 1) & 1;
-  if (cudaStreamWaitEvent(stream, p->ev_down[p->host_last], 0) != cudaSuccess)
-    return fail(FP_ERR_CUDA, "joining the download stream failed");
+  st0 = host_pipeline_join(p, n_chunks, stream);
+  if (st0 != FP_OK) return st0;
   p->last_launches = launches;
   return ok();
 }
