@@ -255,3 +255,23 @@ def test_wrapper_checks_buffer_sizes(lib):
     with pytest.raises(ValueError):
         proj.forward(x, W.float(), None, None, channel_dim=2)
     proj.close()
+
+
+def test_host_wrappers_check_buffers(lib):
+    """The host-buffer wrappers take only page-locked CPU activations,
+    gradients and results, contiguous where the library copies byte ranges,
+    and a weight on the GPU; each mismatch raises before the C ABI is called
+    (without a GPU nothing here can be page-locked or on the device)."""
+    import torch
+    proj = fpx.FusedProjection(64, 64, 4, 16, "gelu", 0.0)
+    x = torch.zeros((2, 8, 64), dtype=torch.bfloat16)           # pageable
+    W = torch.zeros((64, 256), dtype=torch.bfloat16)            # CPU, not CUDA
+    with pytest.raises(ValueError):
+        proj.forward_host(x, W, None, None, channel_dim=2)
+    grads = (torch.zeros((16, 64), dtype=torch.bfloat16),) + \
+        tuple(torch.zeros((8, 8, 16), dtype=torch.bfloat16) for _ in range(3))
+    with pytest.raises(ValueError):
+        proj.backward_host(x, W, None, grads, channel_dim=2)
+    with pytest.raises(ValueError):
+        proj.backward_host(x.transpose(1, 2), W, None, grads, channel_dim=1)
+    proj.close()
